@@ -1,0 +1,109 @@
+"""The oracle's pins must catch plausible mistakes (CPU only).
+
+Each case copies the oracle source, plants one mistake in the copy, builds it
+with gcc into a temporary directory and runs the pin suite against it; at least
+one pin must fail.  The committed oracle is never modified.
+"""
+import os
+import subprocess
+import tempfile
+
+import pytest
+
+import oracle
+from tests import test_oracle_codecs as codecs
+from tests import test_oracle_gemm as gemm
+from tests import test_oracle_quantize as quant
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "nvfp4_oracle.c")
+
+# (name, text to find, replacement)
+MUTATIONS = [
+    ("tensor scale constant", "a / 2688.0f", "a / 2560.0f"),
+    ("nibble order", "if ((k & 1) == 0)\n                *byte", "if ((k & 1) == 1)\n                *byte"),
+    ("ties away from even", "(d == bd && (c & 1) == 0)", "(d == bd && (c & 1) == 1)"),
+    ("E2M1 exponent bias", "ldexp(1.0 + 0.5 * m, e - 1)", "ldexp(1.0 + 0.5 * m, e - 2)"),
+    ("E4M3 subnormal exponent", "ldexp((double)m, -9)", "ldexp((double)m, -10)"),
+    ("E4M3 mantissa width", "ldexp(1.0 + m / 8.0, e - 7)", "ldexp(1.0 + m / 16.0, e - 7)"),
+    ("no saturation", "if (!(x_abs < grid[n - 1]))\n        return n - 1;", ""),
+    ("block amax without abs", "float v = fabsf(orc_bf16_to_f32(row[b * 16 + i]));",
+     "float v = orc_bf16_to_f32(row[b * 16 + i]);"),
+    ("block scale from 4 instead of 6", "float d = 6.0f * c->s_t;", "float d = 4.0f * c->s_t;"),
+    ("sign of code dropped", "return (signbit(x) ? 8 : 0) | mag;", "return mag;"),
+    ("noise ignored", "float p = orc_bf16_to_f32(b) * z[k];", "float p = orc_bf16_to_f32(b);"),
+    ("noisy input not rounded to bf16", "b = orc_f32_to_bf16(p);",
+     "b = orc_f32_to_bf16(orc_bf16_to_f32(b) * (1.0f + (z[k] - 1.0f) * 0.5f));"),
+    ("LoRA scale dropped", "acc + c->s * lora", "acc + lora"),
+    ("LoRA B transposed", "c->B[n * c->r + j]", "c->B[j * c->N + n]"),
+    ("wrong block index in GEMM", "c->scales[n * (c->K / 16) + k / 16]", "c->scales[n * (c->K / 16) + k / 32]"),
+    ("tensor scale dropped in GEMM", "* c->s_t;\n            acc", ";\n            acc"),
+    ("dequant drops tensor scale", "float v = vd * s_t;", "float v = vd;"),
+    ("scale update divides wrong way", "p / s_t;", "p * s_t;"),
+    ("reciprocal instead of division", "float x = orc_bf16_to_f32(row[b * 16 + i]) / S_b;",
+     "float x = orc_bf16_to_f32(row[b * 16 + i]) * (1.0f / S_b);"),
+]
+
+PINS = [
+    codecs.test_e2m1_grid_matches_golden,
+    codecs.test_e2m1_ties_match_golden,
+    codecs.test_e2m1_encoder_vs_thresholds,
+    codecs.test_e4m3_decode_all_bytes_vs_torch,
+    codecs.test_e4m3_encoder_vs_torch_in_range,
+    codecs.test_e4m3_encoder_saturates,
+    quant.test_worked_example,
+    lambda o: quant.test_grid_round_trip(o, False),
+    lambda o: quant.test_grid_round_trip(o, True),
+    lambda o: quant.test_error_bound(o, "normal_outliers"),
+    lambda o: quant.test_error_bound(o, "student_t"),
+    quant.test_subnormal_scale_blocks_saturate,
+    quant.test_exact_ties_resolve_to_even_code_at_every_scale,
+    quant.test_scale_only_update_merge_is_bit_identical,
+    quant.test_round_scales_edge_values,
+    lambda o: gemm.test_gemm_vs_exact_rationals(o, 3, 5, 32, 2),
+    lambda o: gemm.test_gemm_vs_exact_rationals(o, 2, 8, 48, 4),
+    gemm.test_gemm_dyadic_is_exact,
+    gemm.test_power_of_two_noise_equals_prescaled_input_and_scaled_weight,
+    gemm.test_degenerate_cases,
+]
+
+
+def _build_mutant(text, tmp):
+    path = os.path.join(tmp, "mutant.c")
+    with open(path, "w") as f:
+        f.write(text)
+    so = os.path.join(tmp, "libmutant.so")
+    subprocess.check_call(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared",
+                           "-pthread", path, "-o", so, "-lm"])
+    return so
+
+
+def _first_failing_pin():
+    for pin in PINS:
+        try:
+            pin(oracle)
+        except (AssertionError, ValueError):
+            return pin
+    return None
+
+
+def test_unmutated_copy_passes_every_pin():
+    with tempfile.TemporaryDirectory() as tmp:
+        so = _build_mutant(open(SRC).read(), tmp)
+        prev = oracle.use_library(so)
+        try:
+            assert _first_failing_pin() is None
+        finally:
+            oracle.use_library(None)
+
+
+@pytest.mark.parametrize("name,find,repl", MUTATIONS, ids=[m[0] for m in MUTATIONS])
+def test_mutation_is_caught(name, find, repl):
+    src = open(SRC).read()
+    assert src.count(find) == 1, f"mutation site for '{name}' not unique"
+    with tempfile.TemporaryDirectory() as tmp:
+        so = _build_mutant(src.replace(find, repl), tmp)
+        oracle.use_library(so)
+        try:
+            assert _first_failing_pin() is not None, f"no pin catches: {name}"
+        finally:
+            oracle.use_library(None)
