@@ -1,0 +1,528 @@
+"""Benchmark of the NVFP4 weight path on one GB300 (or N replicas).
+
+One step = one pass of every operation of the path over the Qwen2.5-7B-shaped
+decode workload (MLP up 18944 x 3584 and down 3584 x 18944, bf16 weights
+~N(0, 0.02^2) with 0.1% outliers x20, LoRA r = 32, noise sigma 5e-4):
+  1. quantise both weight matrices with a dynamic (amax) tensor scale;
+  2. decode GEMM Y = s_t X' deq(W)^T + s (X' A^T) B^T for M = 1, 4, 8, 16 on
+     both matrices (8 GEMMs), FP32 output;
+  3. scale-only update (round trained block-scale parameters to E4M3) for
+     both matrices.
+Inputs are resident in HBM before the timed region; the GEMMs read quantised
+weights from a ring of replicas (>4x L2 in total) so that no GEMM reads
+codes another operation just wrote to L2, and the bf16 weights (272 MB) are
+larger than L2.
+
+value  = algorithmic bytes of the step / device time of the step (GB/s).
+e2e    = the same through the public API with pinned host inputs copied in
+         and the outputs copied back inside the timed region.
+--impl reference times the CPU oracle on a bounded sample of the same step.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+MS = (1, 4, 8, 16)
+R_LORA = 32
+SIGMA = 5e-4
+LORA_SCALE = 2.0
+UP = (18944, 3584)
+DOWN = (3584, 18944)
+WORKLOAD = "qwen2.5-7b-mlp-decode"
+
+
+# ----------------------------------------------------------------- byte counts
+def quant_bytes(N, K):
+    return 2.5625 * N * K + 4
+
+
+def gemm_bytes(M, N, K, r):
+    return N * K * 0.5625 + 2 * M * K + 4 * M * N + 2 * r * K + 2 * N * r + 4 * K + 4
+
+
+def gemm_flops(M, N, K, r):
+    return 2.0 * M * N * K + 2.0 * M * r * (K + N)
+
+
+def round_bytes(N, K):
+    return 5.0 * N * K / 16 + 4
+
+
+def step_bytes():
+    b = sum(quant_bytes(*s) for s in (UP, DOWN))
+    b += sum(gemm_bytes(M, *s, R_LORA) for M in MS for s in (UP, DOWN))
+    b += sum(round_bytes(*s) for s in (UP, DOWN))
+    return b
+
+
+# ----------------------------------------------------------------- helpers
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d.get("hbm_gbs", 6800.0), d.get("bf16_tflops", 1900.0), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+def source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "nvfp4_weight_only_02_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def traffic_record(kernel):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel sources."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    rec = d.get(kernel)
+    if not rec or rec.get("source_hash") != source_hash():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid):
+        self.uuid = uuid
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.uuid, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, ValueError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------- GPU arm
+class Workload:
+    def __init__(self, torch, nv, synth, device, replicas):
+        self.torch = torch
+        self.nv = nv
+        dev = device
+        t = torch
+
+        def to_dev(bits):
+            return t.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(t.bfloat16).to(dev)
+
+        self.host = {}
+        self.w = {}
+        self.lora = {}
+        self.z = {}
+        self.x = {}
+        for name, shape, seed in (("up", UP, 0), ("down", DOWN, 100)):
+            wb = synth.normal_weight(shape, 0.02, seed, outlier_frac=1e-3, outlier_mult=20.0)
+            a, b = synth.lora_pair(shape[0], shape[1], R_LORA, 0.01, seed + 2)
+            z = synth.noise_vector(shape[1], SIGMA, seed + 3)
+            self.host[name] = (wb, a, b, z)
+            self.w[name] = to_dev(wb)
+            self.lora[name] = (to_dev(a), to_dev(b))
+            self.z[name] = t.from_numpy(z).to(dev)
+            for M in MS:
+                self.x[(name, M)] = to_dev(synth.activations(M, shape[1], seed + 10 + M))
+        self.ws = nv.new_workspace(max(nv.nvfp4_workspace_bytes(16, *s, R_LORA) for s in (UP, DOWN)), dev)
+        # replicas of the quantised weights for the GEMMs
+        self.rep = []
+        for i in range(replicas):
+            self.rep.append({n: nv.quantize(self.w[n], workspace=self.ws) for n in ("up", "down")})
+        self.y = {(n, M): t.empty((M, (UP if n == "up" else DOWN)[0]), dtype=t.float32, device=dev)
+                  for n in ("up", "down") for M in MS}
+        # trained block-scale parameters for the scale-only update
+        self.param = {}
+        for n in ("up", "down"):
+            q = self.rep[0][n]
+            dec = q.scales.view(t.float8_e4m3fn).float()
+            g = t.Generator(device="cpu").manual_seed(7)
+            jitter = (t.rand(dec.shape, generator=g) * 0.2 - 0.1).to(dev)
+            self.param[n] = (dec * q.tensor_scale * (1 + jitter)).contiguous()
+        self.new_scales = {n: t.empty_like(self.rep[0][n].scales) for n in ("up", "down")}
+        self.qbuf = {n: (t.empty_like(self.rep[0][n].codes), t.empty_like(self.rep[0][n].scales),
+                         t.zeros(1, dtype=t.float32, device=dev)) for n in ("up", "down")}
+        self.launches_per_step = 2 * 2 + len(MS) * 2 + 2
+
+    def step(self, i, ev=None):
+        """One pass of the path.  ev: optional dict of (start, end) event lists
+        per kernel kind for per-launch timing."""
+        nv, t = self.nv, self.torch
+
+        def timed(kind, fn):
+            if ev is None:
+                fn()
+                return
+            s = t.cuda.Event(enable_timing=True)
+            e = t.cuda.Event(enable_timing=True)
+            s.record()
+            fn()
+            e.record()
+            ev.setdefault(kind, []).append((s, e))
+
+        for n in ("up", "down"):
+            codes, scales, ts = self.qbuf[n]
+            timed("quantize", lambda: nv.nvfp4_quantize(self.w[n], codes, scales, ts, False, self.ws))
+        R = len(self.rep)
+        j = 0
+        for M in MS:
+            for n in ("up", "down"):
+                q = self.rep[(i * 8 + j) % R][n]
+                j += 1
+                a, b = self.lora[n]
+                timed(f"gemm_M{M}", lambda: nv.nvfp4_w4a16_lora_gemm(
+                    self.x[(n, M)], q.codes, q.scales, q.tensor_scale, a, b, LORA_SCALE, self.z[n],
+                    self.y[(n, M)], self.ws))
+        for n in ("up", "down"):
+            q = self.rep[0][n]
+            timed("round_scales", lambda: nv.nvfp4_round_scales(self.param[n], q.tensor_scale,
+                                                                self.new_scales[n], self.ws))
+
+
+def kernel_breakdown(ev):
+    out = {}
+    for kind, pairs in ev.items():
+        ms = [s.elapsed_time(e) for s, e in pairs]
+        out[kind] = {"launches": len(ms), "mean_us": 1e3 * sum(ms) / len(ms), "total_ms": sum(ms)}
+    return out
+
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    from nvfp4_weight_only_02_gb300 import binding as nv
+    from nvfp4_weight_only_02_gb300 import synth
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    nv.load()
+    wl = Workload(torch, nv, synth, dev, replicas=9)
+    torch.cuda.synchronize()
+
+    for i in range(args.warmup):
+        wl.step(i)
+    torch.cuda.synchronize()
+    st = nv.nvfp4_get_device_status(wl.ws)
+    if st != nv.OK:
+        raise RuntimeError(f"device status after warm-up: {nv.status_string(st)}")
+
+    props = torch.cuda.get_device_properties(dev)
+    uuid = "GPU-" + str(props.uuid) if not str(props.uuid).startswith("GPU-") else str(props.uuid)
+    sampler = ClockSampler(uuid)
+    sampler.start()
+    time.sleep(0.3)
+
+    # timed region: K steps, device time by events on the launch stream
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record()
+    for i in range(args.steps):
+        wl.step(args.warmup + i)
+    end.record()
+    torch.cuda.synchronize()
+    total_ms = start.elapsed_time(end)
+    if world > 1:
+        tt = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    clocks = sampler.stop()
+
+    # per-launch timing pass (separate, so that the event records do not
+    # perturb the timed region)
+    ev = {}
+    for i in range(args.steps):
+        wl.step(args.warmup + args.steps + i, ev)
+    torch.cuda.synchronize()
+    kb = kernel_breakdown(ev)
+    st = nv.nvfp4_get_device_status(wl.ws)
+    if st != nv.OK:
+        raise RuntimeError(f"device status after timing: {nv.status_string(st)}")
+
+    # end-to-end: pinned host inputs in, outputs back, through the public API
+    e2e = run_e2e(torch, nv, wl, dev, args)
+
+    bytes_step = step_bytes()
+    ms_step = total_ms / args.steps
+    value = world * bytes_step / (ms_step * 1e-3) / 1e9
+    peak_hbm, peak_tf, peak_kind = load_peaks()
+
+    # roofline of the dominant kernel kind
+    gemm_kinds = [k for k in kb if k.startswith("gemm_")]
+    gemm_total = sum(kb[k]["total_ms"] for k in gemm_kinds)
+    quant_total = kb["quantize"]["total_ms"]
+    if gemm_total >= quant_total:
+        launches = sum(kb[k]["launches"] for k in gemm_kinds)
+        alg = sum(gemm_bytes(M, *s, R_LORA) for M in MS for s in (UP, DOWN)) / (2 * len(MS))
+        dur = gemm_total / launches * 1e-3
+        kern = "decode_gemm"
+    else:
+        launches = kb["quantize"]["launches"]
+        alg = sum(quant_bytes(*s) for s in (UP, DOWN)) / 2
+        dur = quant_total / launches * 1e-3
+        kern = "quantize"
+    achieved = alg / dur / 1e9
+    roof = {"kernel": kern, "bound": "hbm", "achieved": round(achieved, 1), "peak": peak_hbm,
+            "peak_source": peak_kind, "unit": "GB/s", "frac": round(achieved / peak_hbm, 4),
+            "traffic": traffic_record(kern), "alg_bytes_per_launch": alg}
+
+    per_kernel = {}
+    for M in MS:
+        k = f"gemm_M{M}"
+        if k in kb:
+            b = sum(gemm_bytes(M, *s, R_LORA) for s in (UP, DOWN)) / 2
+            f = sum(gemm_flops(M, *s, R_LORA) for s in (UP, DOWN)) / 2
+            us = kb[k]["mean_us"]
+            per_kernel[k] = {"mean_us": round(us, 2), "GB/s": round(b / us / 1e3, 1),
+                             "TFLOP/s": round(f / us / 1e6, 2),
+                             "frac_hbm": round(b / us / 1e3 / peak_hbm, 4)}
+    q_us = kb["quantize"]["mean_us"]
+    qb = sum(quant_bytes(*s) for s in (UP, DOWN)) / 2
+    per_kernel["quantize"] = {"mean_us": round(q_us, 2), "GB/s": round(qb / q_us / 1e3, 1),
+                              "frac_hbm": round(qb / q_us / 1e3 / peak_hbm, 4)}
+    r_us = kb["round_scales"]["mean_us"]
+    rb = sum(round_bytes(*s) for s in (UP, DOWN)) / 2
+    per_kernel["round_scales"] = {"mean_us": round(r_us, 2), "GB/s": round(rb / r_us / 1e3, 1)}
+
+    line = {
+        "metric": "nvfp4 weight path: quantise + W4A16+LoRA decode GEMM + scale update, algorithmic HBM bytes per second",
+        "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "e2m1/e4m3 weights, bf16->f16 activations, f32 accumulate",
+        "data": "synthetic (seeded Qwen2.5-7B-shaped weights and activations)",
+        "config": {"workload": WORKLOAD, "layers": {"up": list(UP), "down": list(DOWN)}, "M": list(MS),
+                   "lora_rank": R_LORA, "noise_sigma": SIGMA, "bytes_per_step": bytes_step,
+                   "l2": "inputs larger than L2 (272 MB bf16 weights; GEMMs read a 9-replica ring, 0.69 GB)",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": roof, "kernels": per_kernel, "clocks": clocks, "e2e": e2e,
+        "gpu_launches": wl.launches_per_step * args.steps,
+    }
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(seconds=args.cpu_seconds)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def run_e2e(torch, nv, wl, dev, args):
+    """Public-API step with host buffers: pinned inputs copied in, outputs back."""
+    t = torch
+    host_in = {}
+    for n in ("up", "down"):
+        wb, a, b, z = wl.host[n]
+        host_in[("w", n)] = t.from_numpy(wb.view(np.int16)).view(t.bfloat16).pin_memory()
+        host_in[("p", n)] = wl.param[n].cpu().pin_memory()
+        for M in MS:
+            host_in[("x", n, M)] = wl.x[(n, M)].cpu().pin_memory()
+        host_in[("z", n)] = wl.z[n].cpu().pin_memory()
+        host_in[("a", n)] = wl.lora[n][0].cpu().pin_memory()
+        host_in[("b", n)] = wl.lora[n][1].cpu().pin_memory()
+    dev_in = {k: t.empty_like(v, device=dev) for k, v in host_in.items()}
+    host_out = {k: t.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in wl.y.items()}
+    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+    d2h = sum(v.numel() * v.element_size() for v in host_out.values())
+    steps = max(1, args.steps)
+
+    def one(i):
+        for k, v in host_in.items():
+            dev_in[k].copy_(v, non_blocking=True)
+        for n in ("up", "down"):
+            codes, scales, ts = wl.qbuf[n]
+            nv.nvfp4_quantize(dev_in[("w", n)], codes, scales, ts, False, wl.ws)
+        R = len(wl.rep)
+        j = 0
+        for M in MS:
+            for n in ("up", "down"):
+                q = wl.rep[(i * 8 + j) % R][n]
+                j += 1
+                nv.nvfp4_w4a16_lora_gemm(dev_in[("x", n, M)], q.codes, q.scales, q.tensor_scale,
+                                         dev_in[("a", n)], dev_in[("b", n)], LORA_SCALE,
+                                         dev_in[("z", n)], wl.y[(n, M)], wl.ws)
+        for n in ("up", "down"):
+            nv.nvfp4_round_scales(dev_in[("p", n)], wl.rep[0][n].tensor_scale, wl.new_scales[n], wl.ws)
+        for k, v in wl.y.items():
+            host_out[k].copy_(v, non_blocking=True)
+
+    one(0)
+    torch.cuda.synchronize()
+    s = t.cuda.Event(enable_timing=True)
+    e = t.cuda.Event(enable_timing=True)
+    s.record()
+    for i in range(steps):
+        one(i + 1)
+    e.record()
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e) / steps
+    return {"value": round(step_bytes() / (ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+            "ms_per_step": round(ms, 4), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+
+# ----------------------------------------------------------------- CPU oracle
+def oracle_sample_inputs(synth, rows_up, rows_down):
+    """Seeded inputs of the step restricted to a sample of weight rows."""
+    out = []
+    for shape, rows, seed in ((UP, rows_up, 0), (DOWN, rows_down, 100)):
+        N, K = shape
+        wb = synth.normal_weight((rows, K), 0.02, seed, outlier_frac=1e-3, outlier_mult=20.0)
+        a, b = synth.lora_pair(rows, K, R_LORA, 0.01, seed + 2)
+        z = synth.noise_vector(K, SIGMA, seed + 3)
+        xs = {M: synth.activations(M, K, seed + 10 + M) for M in MS}
+        out.append((rows, K, wb, a, b, z, xs))
+    return out
+
+
+def oracle_sample_step(oracle, inputs, nthreads):
+    """The step on a row sample: quantise the sampled rows of each matrix,
+    GEMM at every M on them, scale update on them.  Returns algorithmic bytes."""
+    total = 0.0
+    for rows, K, wb, a, b, z, xs in inputs:
+        rc, codes, scales, st = oracle.quantize(wb, nthreads=nthreads)
+        total += quant_bytes(rows, K)
+        for M in MS:
+            oracle.gemm(xs[M], codes, scales, st, a, b, LORA_SCALE, z, nthreads=nthreads)
+            total += gemm_bytes(M, rows, K, R_LORA)
+        param = (np.float32(st) * np.ones(scales.shape, np.float32)).astype(np.float32)
+        oracle.round_scales(param, st)
+        total += round_bytes(rows, K)
+    return total
+
+
+def cpu_baseline(seconds=15.0):
+    import oracle
+    from nvfp4_weight_only_02_gb300 import synth
+    oracle.build()
+    cores = os.cpu_count() or 1
+    # calibrate on a small sample, then size the sample to about `seconds`
+    small = oracle_sample_inputs(synth, 64, 12)
+    t0 = time.perf_counter()
+    oracle_sample_step(oracle, small, cores)
+    dt = time.perf_counter() - t0
+    scale = max(1, int(seconds / max(dt, 1e-3)))
+    rows_up, rows_down = min(UP[0], 64 * scale), min(DOWN[0], 12 * scale)
+    inputs = oracle_sample_inputs(synth, rows_up, rows_down)
+    t0 = time.perf_counter()
+    b = oracle_sample_step(oracle, inputs, cores)
+    dt = time.perf_counter() - t0
+    return {"value": round(b / dt / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "seconds": round(dt, 2),
+            "sample": f"every step operation on {rows_up} of {UP[0]} up rows and {rows_down} of "
+                      f"{DOWN[0]} down rows (all M, same K, r, noise)"}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    from nvfp4_weight_only_02_gb300 import synth
+    oracle.build()
+    cores = os.cpu_count() or 1
+    rows_up, rows_down = 256, 48
+    inputs = oracle_sample_inputs(synth, rows_up, rows_down)
+    for _ in range(args.warmup):
+        oracle_sample_step(oracle, inputs, cores)
+    t0 = time.perf_counter()
+    b = 0.0
+    for _ in range(args.steps):
+        b += oracle_sample_step(oracle, inputs, cores)
+    dt = time.perf_counter() - t0
+    value = b / dt / 1e9
+    sample = (f"every step operation on {rows_up} of {UP[0]} up rows and {rows_down} of {DOWN[0]} "
+              f"down rows per step")
+    line = {
+        "impl": "reference",
+        "metric": "nvfp4 weight path: quantise + W4A16+LoRA decode GEMM + scale update, algorithmic HBM bytes per second",
+        "value": round(value, 4), "unit": "GB/s", "n_gpus": int(os.environ.get("WORLD_SIZE", "1")),
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
+        "data": "synthetic (seeded Qwen2.5-7B-shaped weights and activations)",
+        "config": {"workload": WORKLOAD, "layers": {"up": list(UP), "down": list(DOWN)}, "M": list(MS),
+                   "lora_rank": R_LORA, "noise_sigma": SIGMA},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,157 @@
+/*
+ * nvfp4.h -- C ABI of libnvfp4.so: the NVFP4 weight path on one GB300 (sm_103a).
+ *
+ * Two operations make up the path:
+ *   1. Weight-only block quantisation of bf16 weights into NVFP4 (activations
+ *      stay 16-bit: "RL with NVFP4 + LoRA" post, tggo.me/sberlogasci/42740,
+ *      section "Метод").  Each weight becomes an E2M1 code plus the scale of
+ *      its block ("Scale-QLoRA", rit.work, format paragraph).  Format: blocks
+ *      of 16 consecutive elements of a row, one E4M3 scale byte per block, one
+ *      FP32 tensor scale, E2M1 grid {0,.5,1,1.5,2,3,4,6}, round to nearest
+ *      even, two codes per byte (even element in the low nibble).
+ *   2. The memory-bound W4A16 GEMM used for rollouts ("Marlin-like kernel",
+ *      same post, section "Эксперименты") with the parallel LoRA branch (as in
+ *      QLoRA, section "Метод") and multiplicative noise applied through the
+ *      RMSNorm gain before the projection (section "Метод"):
+ *          X' = bf16(X * z),   Y = s_t * X' deq(W)^T + s * (X' A^T) B^T.
+ *
+ * Conventions for every entry point:
+ *   - Pointers are DEVICE pointers owned by the caller, except where a
+ *     comment says otherwise.  Arrays are row-major and contiguous; every
+ *     pointer must be 16-byte aligned.  The library never allocates device
+ *     memory on these paths; scratch space is the caller's workspace.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Calls are asynchronous on that stream, except the host-side
+ *     argument checks, which run before anything is launched: when a call
+ *     returns an error from the host checks, nothing was launched.
+ *   - The current CUDA device must be an sm_103 GPU (GB300); otherwise
+ *     NVFP4_ERR_UNSUPPORTED_DEVICE.
+ *   - Data-dependent failures (non-finite weights or scales, a device wait
+ *     that gave up) never trap: kernels record them in a status word inside
+ *     the workspace, read with nvfp4_get_device_status().  Outputs of a call
+ *     that recorded such a status are unspecified.
+ *   - A workspace must be zero-filled once before its first use (e.g. with
+ *     cudaMemsetAsync); every call leaves its counters at zero again.  One
+ *     workspace serves one call at a time: calls that share a workspace must
+ *     be ordered on one stream.
+ *
+ * Shapes: W is N x K (out x in, the PyTorch Linear layout); codes are N x K/2
+ * bytes; scales are N x K/16 bytes; X is M x K; Y is M x N; LoRA A is r x K,
+ * LoRA B is N x r; the noise vector z has K floats.  K must be a multiple of
+ * 16 (no partial blocks); M, N >= 1; 0 <= r <= 256.
+ */
+#ifndef NVFP4_H
+#define NVFP4_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum nvfp4_status {
+    NVFP4_OK = 0,
+    NVFP4_ERR_INVALID_ARG = 1,        /* null pointer, bad enum value        */
+    NVFP4_ERR_SHAPE = 2,              /* K % 16 != 0, M/N < 1, r out of range */
+    NVFP4_ERR_ALIGNMENT = 3,          /* a pointer is not 16-byte aligned    */
+    NVFP4_ERR_WORKSPACE = 4,          /* workspace missing or too small      */
+    NVFP4_ERR_UNSUPPORTED_DEVICE = 5, /* current device is not sm_103        */
+    NVFP4_ERR_CUDA = 6,               /* a CUDA runtime call or launch failed */
+    NVFP4_ERR_NONFINITE = 7,          /* device: non-finite weight or scale  */
+    NVFP4_ERR_TIMEOUT = 8             /* device: a bounded wait gave up      */
+} nvfp4_status;
+
+typedef enum nvfp4_dtype {
+    NVFP4_OUT_BF16 = 0,
+    NVFP4_OUT_FP32 = 1
+} nvfp4_dtype;
+
+/* Bytes of workspace needed by nvfp4_w4a16_lora_gemm for these sizes; also
+ * enough for nvfp4_quantize and nvfp4_round_scales (which need only the
+ * 256-byte control block at its start).  Returns 0 for invalid sizes. */
+size_t nvfp4_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t r);
+
+/* Quantise a bf16 weight matrix W (N x K) into NVFP4.
+ *   use_given_tensor_scale == 0 ("dynamic", Nemotron NVFP4/QAD page, section
+ *     03 "Dynamic Scale QAD": scales recomputed from the current tensor):
+ *     s_t = amax|W| / 2688 (2688 = 6 * 448) is computed on the device and
+ *     written to *tensor_scale.
+ *   use_given_tensor_scale != 0 ("frozen", same section, "Frozen Scale QAD"):
+ *     *tensor_scale is read and used as is; it must be finite and >= 0.
+ * Per block b of 16 elements: e_b = E4M3_RNE(amax_b / (6 s_t)) (saturating at
+ * 448; 0 when s_t == 0), S_b = fl32(dec(e_b) * s_t); each code is
+ * E2M1_RNE(fl32(w / S_b)) with the sign of w, and 0 for the whole block when
+ * S_b == 0.  Codes and scales are bit-identical to the CPU definition.
+ * Non-finite weights (or a bad frozen scale) record NVFP4_ERR_NONFINITE.
+ * Outputs: codes (N x K/2 bytes), scales_e4m3 (N x K/16 bytes),
+ * tensor_scale (1 float, device).  workspace: >= 256 bytes. */
+nvfp4_status nvfp4_quantize(const void *w_bf16, int64_t N, int64_t K,
+                            uint8_t *codes, uint8_t *scales_e4m3, float *tensor_scale,
+                            int use_given_tensor_scale, void *workspace, size_t ws_bytes,
+                            void *stream);
+
+/* Dequantise: out[n][k] = fl32(fl32(v(q) * dec(e_b)) * s_t) (the inner
+ * product is exact), written as FP32 or rounded to bf16 (RNE). */
+nvfp4_status nvfp4_dequantize(const uint8_t *codes, const uint8_t *scales_e4m3,
+                              const float *tensor_scale, int64_t N, int64_t K,
+                              void *out, nvfp4_dtype out_dtype, void *stream);
+
+/* Y = s_t * X' deq(W)^T + lora_scale * (X' A^T) B^T, X' = bf16(X * z).
+ *   x_bf16: M x K; noise_fp32: K floats or NULL (then X' = X);
+ *   lora_a_bf16: r x K, lora_b_bf16: N x r (both NULL or r == 0: no LoRA);
+ *   y: M x N, FP32 or bf16 (RNE of the FP32 result).
+ * Accumulation is FP32.  M <= 16 takes the HBM-streaming decode kernel;
+ * larger M takes the tensor-core (tcgen05) prefill kernel.
+ * workspace: nvfp4_workspace_bytes(M, N, K, r) bytes. */
+nvfp4_status nvfp4_w4a16_lora_gemm(const void *x_bf16, int64_t M, int64_t N, int64_t K,
+                                   const uint8_t *codes, const uint8_t *scales_e4m3,
+                                   const float *tensor_scale,
+                                   const void *lora_a_bf16, const void *lora_b_bf16,
+                                   int64_t r, float lora_scale, const float *noise_fp32,
+                                   void *y, nvfp4_dtype y_dtype,
+                                   void *workspace, size_t ws_bytes, void *stream);
+
+/* Scale-only update (Scale-QLoRA page: codes frozen, trained block-scale
+ * corrections rounded onto the target scale grid; the merge writes only the
+ * scale bytes, so merged weights are bit-identical to the training forward;
+ * the guarantee holds while format, scale grid, blocking and codes are
+ * unchanged).  scales_e4m3[i] = E4M3_RNE(scale_param[i] / s_t), saturating;
+ * 0 for a parameter <= 0 or for s_t == 0.  scale_param holds the effective
+ * block scale in weight units (N x K/16 floats).  Codes are not an argument.
+ * A non-finite parameter records NVFP4_ERR_NONFINITE and gives byte 0. */
+nvfp4_status nvfp4_round_scales(const float *scale_param, const float *tensor_scale,
+                                int64_t N, int64_t K, uint8_t *scales_e4m3,
+                                void *workspace, size_t ws_bytes, void *stream);
+
+/* Synchronises `stream`, returns the device status recorded in `workspace`
+ * since the last read (NVFP4_OK if none) and clears it. */
+nvfp4_status nvfp4_get_device_status(void *workspace, void *stream);
+
+/* Static description of a status code. */
+const char *nvfp4_status_string(nvfp4_status s);
+
+/* Diagnostics (no counterpart on the pages): run the device's scalar
+ * encoders on n device floats x and write one byte per input:
+ *   which == 0: the E2M1 code of x (magnitude code 0..7, sign in bit 3);
+ *   which == 1: the E4M3 byte of x (x >= 0, round to nearest even,
+ *               saturating at 448).
+ * Lets the tests compare the device encoders with the CPU definition over
+ * large input sets. */
+nvfp4_status nvfp4_encode_debug(const float *x, int64_t n, int which, uint8_t *out,
+                                void *stream);
+
+/* Diagnostics (no counterpart on the pages): the quantiser forms w / S_b
+ * without a division per element (one correctly rounded reciprocal per block
+ * and a fused remainder correction).  This sweeps every bf16 significand w
+ * against every fp32 significand of S in [sig_lo, sig_hi) (23-bit values),
+ * for quotient exponents -3..3, and adds to *mismatches (device u64) the
+ * number of pairs where that quotient differs from IEEE division. */
+nvfp4_status nvfp4_quotient_check(uint32_t sig_lo, uint32_t sig_hi,
+                                  unsigned long long *mismatches, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NVFP4_H */

@@ -1,0 +1,221 @@
+// api.cu -- the extern "C" entry points declared in include/nvfp4.h: argument
+// checks on the host, then launches on the caller's stream.  Nothing here
+// computes; no entry point allocates device memory.
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace nvfp4 {
+
+static std::mutex g_dev_mu;
+static DeviceInfo g_dev[64];
+
+const DeviceInfo *device_info(nvfp4_status *st)
+{
+    int d = -1;
+    if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= 64) {
+        *st = NVFP4_ERR_CUDA;
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    DeviceInfo &di = g_dev[d];
+    if (di.device != d) {
+        cudaDeviceProp prop;
+        if (cudaGetDeviceProperties(&prop, d) != cudaSuccess) {
+            *st = NVFP4_ERR_CUDA;
+            return nullptr;
+        }
+        di.cc_major = prop.major;
+        di.cc_minor = prop.minor;
+        di.num_sms = prop.multiProcessorCount;
+        if (!(prop.major == 10 && prop.minor == 3)) {
+            *st = NVFP4_ERR_UNSUPPORTED_DEVICE;
+            return nullptr;
+        }
+        query_decode_occupancy(di);
+        di.device = d;
+    }
+    *st = NVFP4_OK;
+    return &di;
+}
+
+static bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+}  // namespace nvfp4
+
+using namespace nvfp4;
+
+#define NVFP4_TRY_DEVICE(devp)                 \
+    nvfp4_status _st;                          \
+    const DeviceInfo *devp = device_info(&_st); \
+    if (!devp)                                 \
+        return _st;
+
+static nvfp4_status from_cuda(cudaError_t e) { return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA; }
+
+extern "C" {
+
+size_t nvfp4_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t r)
+{
+    if (M < 1 || N < 1 || K < 16 || K % 16 != 0 || r < 0 || r > 256 || N > (1LL << 30) ||
+        K > (1LL << 30))
+        return 0;
+    nvfp4_status st;
+    const DeviceInfo *dev = device_info(&st);
+    if (!dev)
+        return 0;
+    size_t g = decode_workspace_bytes(M, N, K, r, *dev);
+    return g < kCtlBytes ? kCtlBytes : g;
+}
+
+nvfp4_status nvfp4_quantize(const void *w_bf16, int64_t N, int64_t K, uint8_t *codes,
+                            uint8_t *scales_e4m3, float *tensor_scale, int use_given_tensor_scale,
+                            void *workspace, size_t ws_bytes, void *stream)
+{
+    if (!w_bf16 || !codes || !scales_e4m3 || !tensor_scale || !workspace)
+        return NVFP4_ERR_INVALID_ARG;
+    if (N < 1 || K < 16 || K % 16 != 0 || N > (1LL << 40) / K)
+        return NVFP4_ERR_SHAPE;
+    if (!aligned16(w_bf16) || !aligned16(codes) || !aligned16(scales_e4m3) || !aligned16(tensor_scale) ||
+        !aligned16(workspace))
+        return NVFP4_ERR_ALIGNMENT;
+    if (ws_bytes < kCtlBytes)
+        return NVFP4_ERR_WORKSPACE;
+    NVFP4_TRY_DEVICE(dev);
+    return from_cuda(launch_quantize(w_bf16, N, K, codes, scales_e4m3, tensor_scale,
+                                     use_given_tensor_scale != 0, (uint32_t *)workspace,
+                                     (cudaStream_t)stream, *dev));
+}
+
+nvfp4_status nvfp4_dequantize(const uint8_t *codes, const uint8_t *scales_e4m3,
+                              const float *tensor_scale, int64_t N, int64_t K, void *out,
+                              nvfp4_dtype out_dtype, void *stream)
+{
+    if (!codes || !scales_e4m3 || !tensor_scale || !out)
+        return NVFP4_ERR_INVALID_ARG;
+    if (out_dtype != NVFP4_OUT_BF16 && out_dtype != NVFP4_OUT_FP32)
+        return NVFP4_ERR_INVALID_ARG;
+    if (N < 1 || K < 16 || K % 16 != 0 || N > (1LL << 40) / K)
+        return NVFP4_ERR_SHAPE;
+    if (!aligned16(codes) || !aligned16(scales_e4m3) || !aligned16(tensor_scale) || !aligned16(out))
+        return NVFP4_ERR_ALIGNMENT;
+    NVFP4_TRY_DEVICE(dev);
+    return from_cuda(launch_dequantize(codes, scales_e4m3, tensor_scale, N, K, out,
+                                       out_dtype == NVFP4_OUT_FP32, (cudaStream_t)stream, *dev));
+}
+
+nvfp4_status nvfp4_w4a16_lora_gemm(const void *x_bf16, int64_t M, int64_t N, int64_t K,
+                                   const uint8_t *codes, const uint8_t *scales_e4m3,
+                                   const float *tensor_scale, const void *lora_a_bf16,
+                                   const void *lora_b_bf16, int64_t r, float lora_scale,
+                                   const float *noise_fp32, void *y, nvfp4_dtype y_dtype,
+                                   void *workspace, size_t ws_bytes, void *stream)
+{
+    if (!x_bf16 || !codes || !scales_e4m3 || !tensor_scale || !y || !workspace)
+        return NVFP4_ERR_INVALID_ARG;
+    if (y_dtype != NVFP4_OUT_BF16 && y_dtype != NVFP4_OUT_FP32)
+        return NVFP4_ERR_INVALID_ARG;
+    if (M < 1 || N < 1 || K < 16 || K % 16 != 0 || r < 0 || r > 256 || N > (1LL << 30) ||
+        K > (1LL << 30) || M > (1LL << 31) / 1)
+        return NVFP4_ERR_SHAPE;
+    const bool lora = r > 0 && lora_a_bf16 && lora_b_bf16;
+    if (r > 0 && (!lora_a_bf16) != (!lora_b_bf16))
+        return NVFP4_ERR_INVALID_ARG;
+    if (!aligned16(x_bf16) || !aligned16(codes) || !aligned16(scales_e4m3) || !aligned16(tensor_scale) ||
+        !aligned16(y) || !aligned16(workspace) || (noise_fp32 && !aligned16(noise_fp32)) ||
+        (lora && (!aligned16(lora_a_bf16) || !aligned16(lora_b_bf16))))
+        return NVFP4_ERR_ALIGNMENT;
+    NVFP4_TRY_DEVICE(dev);
+    const size_t need = decode_workspace_bytes(M, N, K, lora ? r : 0, *dev);
+    if (need == 0)
+        return NVFP4_ERR_UNSUPPORTED_DEVICE;
+    if (ws_bytes < need)
+        return NVFP4_ERR_WORKSPACE;
+    GemmArgs a;
+    a.x = (const uint16_t *)x_bf16;
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.r = lora ? r : 0;
+    a.codes = codes;
+    a.scales = scales_e4m3;
+    a.tensor_scale = tensor_scale;
+    a.lora_a = lora ? (const uint16_t *)lora_a_bf16 : nullptr;
+    a.lora_b = lora ? (const uint16_t *)lora_b_bf16 : nullptr;
+    a.lora_scale = lora ? lora_scale : 0.0f;
+    a.noise = noise_fp32;
+    a.y = y;
+    a.y_fp32 = y_dtype == NVFP4_OUT_FP32;
+    a.ws = (uint8_t *)workspace;
+    a.ws_bytes = ws_bytes;
+    return from_cuda(launch_decode_gemm(a, (cudaStream_t)stream, *dev));
+}
+
+nvfp4_status nvfp4_round_scales(const float *scale_param, const float *tensor_scale, int64_t N,
+                                int64_t K, uint8_t *scales_e4m3, void *workspace, size_t ws_bytes,
+                                void *stream)
+{
+    if (!scale_param || !tensor_scale || !scales_e4m3 || !workspace)
+        return NVFP4_ERR_INVALID_ARG;
+    if (N < 1 || K < 16 || K % 16 != 0 || N > (1LL << 40) / K)
+        return NVFP4_ERR_SHAPE;
+    if (!aligned16(scale_param) || !aligned16(tensor_scale) || !aligned16(scales_e4m3) ||
+        !aligned16(workspace))
+        return NVFP4_ERR_ALIGNMENT;
+    if (ws_bytes < kCtlBytes)
+        return NVFP4_ERR_WORKSPACE;
+    NVFP4_TRY_DEVICE(dev);
+    return from_cuda(launch_round_scales(scale_param, tensor_scale, N * (K / 16), scales_e4m3,
+                                         (uint32_t *)workspace, (cudaStream_t)stream, *dev));
+}
+
+nvfp4_status nvfp4_get_device_status(void *workspace, void *stream)
+{
+    if (!workspace)
+        return NVFP4_ERR_INVALID_ARG;
+    cudaStream_t s = (cudaStream_t)stream;
+    uint32_t word = 0;
+    if (cudaMemcpyAsync(&word, workspace, 4, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaMemsetAsync(workspace, 0, 4, s) != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess)
+        return NVFP4_ERR_CUDA;
+    return (nvfp4_status)word;
+}
+
+const char *nvfp4_status_string(nvfp4_status s)
+{
+    switch (s) {
+    case NVFP4_OK: return "ok";
+    case NVFP4_ERR_INVALID_ARG: return "invalid argument";
+    case NVFP4_ERR_SHAPE: return "unsupported shape (K must be a positive multiple of 16; M, N >= 1; 0 <= r <= 256)";
+    case NVFP4_ERR_ALIGNMENT: return "pointer not 16-byte aligned";
+    case NVFP4_ERR_WORKSPACE: return "workspace missing or too small";
+    case NVFP4_ERR_UNSUPPORTED_DEVICE: return "current CUDA device is not an sm_103 GPU";
+    case NVFP4_ERR_CUDA: return "CUDA runtime error";
+    case NVFP4_ERR_NONFINITE: return "non-finite weight, tensor scale or scale parameter";
+    case NVFP4_ERR_TIMEOUT: return "a bounded device-side wait gave up";
+    }
+    return "unknown status";
+}
+
+nvfp4_status nvfp4_encode_debug(const float *x, int64_t n, int which, uint8_t *out, void *stream)
+{
+    if (!x || !out || (which != 0 && which != 1))
+        return NVFP4_ERR_INVALID_ARG;
+    if (n < 1)
+        return NVFP4_ERR_SHAPE;
+    NVFP4_TRY_DEVICE(dev);
+    return from_cuda(launch_encode_debug(x, n, which, out, (cudaStream_t)stream, *dev));
+}
+
+nvfp4_status nvfp4_quotient_check(uint32_t sig_lo, uint32_t sig_hi, unsigned long long *mismatches,
+                                  void *stream)
+{
+    if (!mismatches || sig_hi > (1u << 23) || sig_lo > sig_hi)
+        return NVFP4_ERR_INVALID_ARG;
+    NVFP4_TRY_DEVICE(dev);
+    (void)dev;
+    return from_cuda(launch_quotient_check(sig_lo, sig_hi, mismatches, (cudaStream_t)stream));
+}
+
+}  // extern "C"

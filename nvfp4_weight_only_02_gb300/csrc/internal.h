@@ -1,0 +1,54 @@
+// internal.h -- host-side declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/nvfp4.h"
+
+namespace nvfp4 {
+
+struct DeviceInfo {
+    int device = -1;
+    int num_sms = 0;
+    int cc_major = 0, cc_minor = 0;
+    int decode_blocks_per_sm[2] = {0, 0};  // cooperative residency of the decode kernel (MP 8, 16)
+};
+
+// Cached per-device facts; nullptr (and *st set) when the device is unusable.
+const DeviceInfo *device_info(nvfp4_status *st);
+
+cudaError_t launch_quantize(const void *w, int64_t N, int64_t K, uint8_t *codes, uint8_t *scales,
+                            float *tensor_scale, bool given, uint32_t *ctl, cudaStream_t s,
+                            const DeviceInfo &dev);
+cudaError_t launch_dequantize(const uint8_t *codes, const uint8_t *scales, const float *tensor_scale,
+                              int64_t N, int64_t K, void *out, bool fp32, cudaStream_t s,
+                              const DeviceInfo &dev);
+cudaError_t launch_round_scales(const float *param, const float *tensor_scale, int64_t n,
+                                uint8_t *out, uint32_t *ctl, cudaStream_t s, const DeviceInfo &dev);
+cudaError_t launch_encode_debug(const float *x, int64_t n, int which, uint8_t *out, cudaStream_t s,
+                                const DeviceInfo &dev);
+cudaError_t launch_quotient_check(uint32_t lo, uint32_t hi, unsigned long long *mismatches,
+                                  cudaStream_t s);
+
+struct GemmArgs {
+    const uint16_t *x;  // M x K bf16
+    int64_t M, N, K, r;
+    const uint8_t *codes, *scales;
+    const float *tensor_scale;
+    const uint16_t *lora_a, *lora_b;  // r x K, N x r (bf16) or null
+    float lora_scale;
+    const float *noise;  // K or null
+    void *y;
+    bool y_fp32;
+    uint8_t *ws;
+    size_t ws_bytes;
+};
+
+// Occupancy of the decode kernels; called once per device by device_info().
+void query_decode_occupancy(DeviceInfo &dev);
+
+size_t decode_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t r, const DeviceInfo &dev);
+cudaError_t launch_decode_gemm(const GemmArgs &a, cudaStream_t s, const DeviceInfo &dev);
+
+}  // namespace nvfp4

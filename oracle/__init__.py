@@ -62,6 +62,8 @@ def _configure(lib):
     lib.orc_round_scales.argtypes = [P, ctypes.c_float, i64, P]
     lib.orc_noisy_input.restype = None
     lib.orc_noisy_input.argtypes = [P, P, i64, i64, P]
+    lib.orc_encode_array.restype = None
+    lib.orc_encode_array.argtypes = [P, i64, ctypes.c_int, P, ctypes.c_int]
     lib.orc_gemm.restype = ctypes.c_int
     lib.orc_gemm.argtypes = [P, i64, i64, i64, P, P, ctypes.c_float, P, P, i64,
                              ctypes.c_float, P, P, ctypes.c_int]
@@ -128,6 +130,14 @@ def e2m1_encode(x: float) -> int:
 
 def e4m3_encode(x: float) -> int:
     return _load().orc_e4m3_encode_nonneg(float(np.float32(x)))
+
+
+def encode_array(x, which, nthreads=None):
+    """which 0: E2M1 codes (sign in bit 3); which 1: E4M3 bytes of x >= 0."""
+    x = _c(x, np.float32).ravel()
+    out = np.zeros(x.size, np.uint8)
+    _load().orc_encode_array(_ptr(x), x.size, int(which), _ptr(out), nthreads or default_threads())
+    return out
 
 
 # ---------------------------------------------------------------- tensors

@@ -403,3 +403,31 @@ int orc_gemm(const uint16_t *x, int64_t M, int64_t N, int64_t K,
     free(T);
     return ORC_OK;
 }
+
+/* ------------------------------------------------------------------ */
+/* Array forms of the scalar encoders (used to sweep the device        */
+/* encoders over large input sets)                                     */
+/* ------------------------------------------------------------------ */
+
+struct enc_ctx {
+    const float *x;
+    uint8_t *out;
+    int64_t n, per;
+    int which;
+};
+
+static void enc_row(void *p, int64_t r)
+{
+    struct enc_ctx *c = (struct enc_ctx *)p;
+    int64_t lo = r * c->per, hi = lo + c->per < c->n ? lo + c->per : c->n;
+    for (int64_t i = lo; i < hi; i++)
+        c->out[i] = (uint8_t)(c->which == 0 ? orc_e2m1_encode(c->x[i]) : orc_e4m3_encode_nonneg(c->x[i]));
+}
+
+/* which == 0: E2M1 code of x (sign in bit 3); which == 1: E4M3 byte of x >= 0 */
+void orc_encode_array(const float *x, int64_t n, int which, uint8_t *out, int nthreads)
+{
+    grids();
+    struct enc_ctx c = {x, out, n, 1 << 16, which};
+    for_rows((n + c.per - 1) / c.per, nthreads, enc_row, &c);
+}

@@ -18,3 +18,14 @@ def orc():
     import oracle
     oracle.build()
     return oracle
+
+
+@pytest.fixture(scope="session")
+def nv():
+    """The CUDA binding, built and loaded; skips when no GPU is present."""
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    from nvfp4_weight_only_02_gb300 import binding
+    binding.load()
+    return binding

@@ -1,0 +1,78 @@
+"""The C ABI library builds, loads and exports every declared symbol (CPU).
+
+Also checks the host-side argument validation, which runs before any CUDA
+call and so needs no GPU.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+from nvfp4_weight_only_02_gb300 import binding, build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "nvfp4.h")
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(nvfp4_[a-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.load()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared()
+    assert "nvfp4_quantize" in names and "nvfp4_w4a16_lora_gemm" in names
+    for n in names:
+        assert hasattr(lib, n), n
+    assert sorted(binding.EXPORTS) == names
+
+
+def test_status_strings(lib):
+    for s in range(9):
+        assert binding.status_string(s)
+    assert "16" in binding.status_string(binding.ERR_SHAPE)
+
+
+def test_host_checks_reject_before_launch(lib):
+    P = ctypes.c_void_p
+    good = P(4096)  # never dereferenced: the checks below fail first
+    bad_align = P(4096 + 4)
+    null = None
+    # null pointer
+    assert lib.nvfp4_quantize(null, 16, 32, good, good, good, 0, good, 256, null) == binding.ERR_INVALID_ARG
+    # K not a multiple of 16, N < 1
+    assert lib.nvfp4_quantize(good, 16, 24, good, good, good, 0, good, 256, null) == binding.ERR_SHAPE
+    assert lib.nvfp4_quantize(good, 0, 32, good, good, good, 0, good, 256, null) == binding.ERR_SHAPE
+    # misaligned pointer
+    assert lib.nvfp4_quantize(bad_align, 16, 32, good, good, good, 0, good, 256, null) == binding.ERR_ALIGNMENT
+    # workspace too small
+    assert lib.nvfp4_quantize(good, 16, 32, good, good, good, 0, good, 64, null) == binding.ERR_WORKSPACE
+    # gemm: bad dtype enum, r out of range, half a LoRA pair
+    assert lib.nvfp4_w4a16_lora_gemm(good, 1, 16, 32, good, good, good, null, null, 0, 0.0, null, good,
+                                     7, good, 1 << 20, null) == binding.ERR_INVALID_ARG
+    assert lib.nvfp4_w4a16_lora_gemm(good, 1, 16, 32, good, good, good, good, good, 300, 1.0, null, good,
+                                     0, good, 1 << 20, null) == binding.ERR_SHAPE
+    assert lib.nvfp4_w4a16_lora_gemm(good, 1, 16, 32, good, good, good, good, null, 4, 1.0, null, good,
+                                     0, good, 1 << 20, null) == binding.ERR_INVALID_ARG
+    assert lib.nvfp4_w4a16_lora_gemm(good, 1, 16, 30, good, good, good, null, null, 0, 0.0, null, good,
+                                     0, good, 1 << 20, null) == binding.ERR_SHAPE
+    assert lib.nvfp4_dequantize(good, good, good, 4, 32, bad_align, 1, null) == binding.ERR_ALIGNMENT
+    assert lib.nvfp4_round_scales(good, good, 4, 31, good, good, 256, null) == binding.ERR_SHAPE
+    assert lib.nvfp4_workspace_bytes(1, 16, 30, 0) == 0
+    assert lib.nvfp4_encode_debug(good, 8, 5, good, null) == binding.ERR_INVALID_ARG
+    assert lib.nvfp4_quotient_check(0, (1 << 23) + 1, good, null) == binding.ERR_INVALID_ARG
+
+
+def test_library_does_not_link_the_oracle():
+    # the product library and the oracle share no code: no oracle symbol in it
+    out = os.popen(f"nm -D --defined-only {build.LIB}").read()
+    assert "orc_" not in out
+    exported = set(re.findall(r"\b(nvfp4_[a-z0-9_]+)\b", out))
+    assert exported == set(_declared())
