@@ -507,8 +507,44 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_kernel_case(case, reps):
+    """One operation, repeated: a small, self-contained target for ncu."""
+    import torch
+
+    from nvfp4_weight_only_02_gb300 import binding as nv
+    from nvfp4_weight_only_02_gb300 import synth
+    nv.load()
+    kind, which, M = case.split("_") if case.startswith("gemm") else (case.split("_") + [0])[:3]
+    shape = UP if which == "up" else DOWN
+    dev = lambda b: torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(torch.bfloat16).cuda()
+    wb = synth.normal_weight(shape, 0.02, 0, outlier_frac=1e-3, outlier_mult=20.0)
+    w = dev(wb)
+    ws = nv.new_workspace(nv.nvfp4_workspace_bytes(16, *shape, R_LORA))
+    q = nv.quantize(w, workspace=ws)
+    if kind == "quantize":
+        for _ in range(reps):
+            nv.nvfp4_quantize(w, q.codes, q.scales, q.tensor_scale, False, ws)
+    else:
+        M = int(M[1:])
+        a, b = synth.lora_pair(shape[0], shape[1], R_LORA, 0.01, 2)
+        z = torch.from_numpy(synth.noise_vector(shape[1], SIGMA, 3)).cuda()
+        x = dev(synth.activations(M, shape[1], 10))
+        y = torch.empty((M, shape[0]), dtype=torch.float32, device="cuda")
+        for _ in range(reps):
+            nv.nvfp4_w4a16_lora_gemm(x, q.codes, q.scales, q.tensor_scale, dev(a), dev(b), LORA_SCALE,
+                                     z, y, ws)
+    torch.cuda.synchronize()
+    st = nv.nvfp4_get_device_status(ws)
+    if st != nv.OK:
+        raise RuntimeError(nv.status_string(st))
+    print(f"kernel case {case}: {reps} reps ok")
+
+
 def main():
     ap = argparse.ArgumentParser()
+    ap.add_argument("--kernel-case", default=None,
+                    help="run one operation repeatedly (quantize_up, gemm_up_M8, gemm_down_M16, ...)")
+    ap.add_argument("--reps", type=int, default=3)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
@@ -518,7 +554,9 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    if args.impl == "reference":
+    if args.kernel_case:
+        run_kernel_case(args.kernel_case, args.reps)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_gpu(args)
