@@ -112,6 +112,34 @@ nvfp4_status nvfp4_w4a16_lora_gemm(const void *x_bf16, int64_t M, int64_t N, int
                                    void *y, nvfp4_dtype y_dtype,
                                    void *workspace, size_t ws_bytes, void *stream);
 
+/* nvfp4_w4a16_lora_gemm without a workspace argument, for callers that
+ * cannot allocate device memory: code running inside a host framework that
+ * owns every device allocation and hands its plugins no scratch, or a
+ * latency-critical loop that cannot afford cudaMalloc's implicit device-wide
+ * synchronisation.  (No counterpart on the pages.)
+ *   - Scratch is a fixed 8 MiB array inside the library (a file-scope
+ *     __device__ array), held on every GPU that loads the library until the
+ *     process exits.  Problems whose workspace (nvfp4_workspace_bytes) exceeds
+ *     8 MiB are rejected with NVFP4_ERR_WORKSPACE; every Qwen2.5-7B and -32B
+ *     projection at M <= 16 fits.
+ *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ *     The caller still passes inputs and outputs as for the workspace variant.
+ *   - The first call on a device looks up the array's device address (once per
+ *     device, with that device current) and caches it; make that first call
+ *     before any stream capture.
+ *   - All calls share the one array.  Each call clears its control words
+ *     (an asynchronous memset on `stream`) before launching; two calls whose
+ *     executions overlap on the GPU (different streams, no ordering) race on
+ *     the array and give wrong results.
+ *   - The device status word lives in the shared array and is cleared by the
+ *     next call; this variant does not report device-side statuses. */
+nvfp4_status nvfp4_w4a16_lora_gemm_static(const void *x_bf16, int64_t M, int64_t N, int64_t K,
+                                          const uint8_t *codes, const uint8_t *scales_e4m3,
+                                          const float *tensor_scale,
+                                          const void *lora_a_bf16, const void *lora_b_bf16,
+                                          int64_t r, float lora_scale, const float *noise_fp32,
+                                          void *y, nvfp4_dtype y_dtype, void *stream);
+
 /* Scale-only update (Scale-QLoRA page: codes frozen, trained block-scale
  * corrections rounded onto the target scale grid; the merge writes only the
  * scale bytes, so merged weights are bit-identical to the training forward;

@@ -25,7 +25,7 @@ OUT_BF16, OUT_FP32 = 0, 1
 EXPORTS = [
     "nvfp4_workspace_bytes", "nvfp4_quantize", "nvfp4_dequantize", "nvfp4_w4a16_lora_gemm",
     "nvfp4_round_scales", "nvfp4_get_device_status", "nvfp4_status_string", "nvfp4_encode_debug",
-    "nvfp4_quotient_check",
+    "nvfp4_quotient_check", "nvfp4_w4a16_lora_gemm_static",
 ]
 
 
@@ -64,6 +64,8 @@ def load(build_if_missing: bool = True):
             "nvfp4_status_string": (ctypes.c_char_p, [st]),
             "nvfp4_encode_debug": (st, [P, i64, ctypes.c_int, P, P]),
             "nvfp4_quotient_check": (st, [u32, u32, P, P]),
+            "nvfp4_w4a16_lora_gemm_static": (st, [P, i64, i64, i64, P, P, P, P, P, i64, ctypes.c_float,
+                                                  P, P, ctypes.c_int, P]),
         }
         for name, (res, args) in sig.items():
             f = getattr(lib, name)

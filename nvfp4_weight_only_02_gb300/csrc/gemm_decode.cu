@@ -37,6 +37,7 @@
 // All blocks are co-resident (cooperative launch); both grid barriers have a
 // bounded wait and report NVFP4_ERR_TIMEOUT instead of hanging.
 #include <algorithm>
+#include <mutex>
 
 #include "common.cuh"
 #include "internal.h"
@@ -523,3 +524,61 @@ cudaError_t launch_decode_gemm(const GemmArgs &a, cudaStream_t s, const DeviceIn
 }
 
 }  // namespace nvfp4
+
+// ---------------------------------------------------------------- fixed scratch
+// Scratch for callers that cannot allocate device memory: one file-scope
+// device array, loaded with the library and held by every GPU that loads it
+// until the process exits.  kStaticWsBytes covers the decode GEMM of every
+// Qwen2.5-7B and -32B projection at M <= 16; larger problems are rejected.
+namespace nvfp4 {
+
+constexpr size_t kStaticWsBytes = size_t(8) << 20;
+static __device__ __align__(256) uint8_t g_static_ws[kStaticWsBytes];
+
+static std::mutex g_static_mu;
+static void *g_static_ptr[64];
+
+// Device address of g_static_ws on the current device.  In host code the
+// array's name is only a host-side stand-in, so its device address is looked
+// up once per device (with that device current) and cached.
+static cudaError_t static_workspace(void **out)
+{
+    int d = -1;
+    cudaError_t e = cudaGetDevice(&d);
+    if (e != cudaSuccess)
+        return e;
+    if (d < 0 || d >= 64)
+        return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lk(g_static_mu);
+    if (!g_static_ptr[d]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_static_ws);
+        if (e != cudaSuccess)
+            return e;
+        g_static_ptr[d] = p;
+    }
+    *out = g_static_ptr[d];
+    return cudaSuccess;
+}
+
+}  // namespace nvfp4
+
+extern "C" nvfp4_status nvfp4_w4a16_lora_gemm_static(
+    const void *x_bf16, int64_t M, int64_t N, int64_t K, const uint8_t *codes,
+    const uint8_t *scales_e4m3, const float *tensor_scale, const void *lora_a_bf16,
+    const void *lora_b_bf16, int64_t r, float lora_scale, const float *noise_fp32, void *y,
+    nvfp4_dtype y_dtype, void *stream)
+{
+    void *ws = nullptr;
+    if (nvfp4::static_workspace(&ws) != cudaSuccess)
+        return NVFP4_ERR_CUDA;
+    const size_t need = nvfp4_workspace_bytes(M, N, K, (lora_a_bf16 && lora_b_bf16) ? r : 0);
+    if (need > nvfp4::kStaticWsBytes)
+        return NVFP4_ERR_WORKSPACE;  // beyond the fixed scratch size
+    // every call shares the array: its control words must start at zero
+    if (cudaMemsetAsync(ws, 0, nvfp4::kCtlBytes, (cudaStream_t)stream) != cudaSuccess)
+        return NVFP4_ERR_CUDA;
+    return nvfp4_w4a16_lora_gemm(x_bf16, M, N, K, codes, scales_e4m3, tensor_scale, lora_a_bf16,
+                                 lora_b_bf16, r, lora_scale, noise_fp32, y, y_dtype, ws,
+                                 nvfp4::kStaticWsBytes, stream);
+}
