@@ -68,15 +68,6 @@ __device__ __forceinline__ uint32_t e4m3_encode_nonneg(float x)
     return r & 0xFF;
 }
 
-// Two non-negative floats -> byte of two E2M1 magnitude codes (lo in bits 0..3,
-// hi in bits 4..7), round to nearest even, saturating at 6.
-__device__ __forceinline__ uint32_t e2m1x2_encode_nonneg(float lo, float hi)
-{
-    uint16_t r;
-    asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u16.u8 %0, t;\n\t}"
-        : "=h"(r) : "f"(hi), "f"(lo));
-    return r & 0xFF;
-}
 
 // Byte with two E2M1 codes -> f16x2 (low nibble -> low half), exact.
 __device__ __forceinline__ uint32_t e2m1x2_to_h2(uint32_t byte_in_low8)

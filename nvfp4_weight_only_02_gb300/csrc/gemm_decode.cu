@@ -49,7 +49,11 @@ constexpr int kWarps = 8;
 constexpr int kTileRows = 256;  // rows of W per stream-K tile (8 warps x 32)
 constexpr int kStep = 64;       // columns of W per stream-K unit
 constexpr int kChunk = 512;     // columns per X' scaling chunk
-constexpr int kDepth = 4;       // register prefetch depth (steps in flight)
+constexpr int kStepsPerChunk = kChunk / kStep;
+constexpr int kDepth = 4;       // register prefetch depth (units in flight per warp)
+constexpr int kMaxUnitsPerBlock = 24;  // X' staging capacity in shared memory
+constexpr int kLoraSteps = 4;   // k16 steps per LoRA down-projection unit
+constexpr int kMaxR = 256;
 
 struct DecodeParams {
     const uint16_t *x;
@@ -67,13 +71,13 @@ struct DecodeParams {
     float *tpart;  // [NS][MP][r]
     float *tfin;   // [MP][r]
     float *part;   // [R][maxseg][MP][256]
-    int S, NC, R, NS, NJG, KSL, maxseg;
-    long long U;
+    int S, NC, R, NS, NJG, maxseg;
+    int U;
 };
 
-__device__ __forceinline__ int owner_of(long long u, long long U, int P)
+__device__ __forceinline__ int owner_of(int u, int U, int P)
 {
-    return (int)(((u + 1) * (long long)P - 1) / U);
+    return (int)(((long long)(u + 1) * P - 1) / U);
 }
 
 __device__ __forceinline__ float bf16_round(float v)
@@ -82,68 +86,64 @@ __device__ __forceinline__ float bf16_round(float v)
 }
 
 // ---------------------------------------------------------------- phase 0a
+// One warp converts one (token, 512-column chunk): X' = bf16(X z), its max,
+// the power of two 2^p that puts the max in [2^14, 2^15), and X' 2^-p as
+// f16 in fragment order.  Each lane handles one 16-column block.
 template <int MP>
-__device__ void convert_chunk(const DecodeParams &p, int c)
+__device__ void convert_unit(const DecodeParams &p, int m, int c)
 {
-    constexpr int TPT = kThreads / MP;  // threads per token
-    constexpr int EPT = kChunk / TPT;   // consecutive columns per thread (16 or 32)
-    const int m = threadIdx.x / TPT;
-    const int part = threadIdx.x % TPT;
-    const int k0 = c * kChunk + part * EPT;
-    float v[EPT];
+    const int lane = threadIdx.x & 31;
+    const int k0 = c * kChunk + lane * 16;
+    float v[16];
     float mx = 0.0f;
+    if (m < p.M && k0 < p.K) {
+        const uint4 *xs = reinterpret_cast<const uint4 *>(p.x + (size_t)m * p.K + k0);
+        const uint4 xa = xs[0], xb = xs[1];
+        const uint32_t xw[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+        float zz[16];
+        if (p.noise) {
+            const float4 *zs = reinterpret_cast<const float4 *>(p.noise + k0);
 #pragma unroll
-    for (int q = 0; q < EPT / 8; q++) {
-        const int k = k0 + 8 * q;
-        if (m < p.M && k < p.K) {
-            const uint4 xb = *reinterpret_cast<const uint4 *>(p.x + (size_t)m * p.K + k);
-            const uint32_t xw[4] = {xb.x, xb.y, xb.z, xb.w};
-            float zz[8];
-            if (p.noise) {
-                const float4 z0 = *reinterpret_cast<const float4 *>(p.noise + k);
-                const float4 z1 = *reinterpret_cast<const float4 *>(p.noise + k + 4);
-                zz[0] = z0.x; zz[1] = z0.y; zz[2] = z0.z; zz[3] = z0.w;
-                zz[4] = z1.x; zz[5] = z1.y; zz[6] = z1.z; zz[7] = z1.w;
+            for (int q = 0; q < 4; q++) {
+                const float4 z4 = zs[q];
+                zz[4 * q] = z4.x; zz[4 * q + 1] = z4.y; zz[4 * q + 2] = z4.z; zz[4 * q + 3] = z4.w;
             }
-#pragma unroll
-            for (int i = 0; i < 8; i++) {
-                float f = bf16_bits_to_f32((xw[i / 2] >> (16 * (i & 1))) & 0xFFFFu);
-                if (p.noise)
-                    f = bf16_round(__fmul_rn(f, zz[i]));
-                v[8 * q + i] = f;
-                mx = fmaxf(mx, fabsf(f));
-            }
-        } else {
-#pragma unroll
-            for (int i = 0; i < 8; i++)
-                v[8 * q + i] = 0.0f;
         }
+#pragma unroll
+        for (int i = 0; i < 16; i++) {
+            float f = bf16_bits_to_f32((xw[i / 2] >> (16 * (i & 1))) & 0xFFFFu);
+            if (p.noise)
+                f = bf16_round(__fmul_rn(f, zz[i]));
+            v[i] = f;
+            mx = fmaxf(mx, fabsf(f));
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 16; i++)
+            v[i] = 0.0f;
     }
 #pragma unroll
-    for (int off = TPT / 2; off >= 1; off >>= 1)
+    for (int off = 16; off >= 1; off >>= 1)
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-    // exponent e = floor(log2 mx); the chunk is scaled by 2^-(e-14)
     int pexp = 0;
     if (mx > 0.0f) {
         const uint32_t b = __float_as_uint(mx);
         const int e = (b >> 23) ? (int)(b >> 23) - 127 : (31 - __clz(b)) - 149;
         pexp = e - 14;
     }
+    const int s = k0 / kStep, tt = (k0 % kStep) / 16;
 #pragma unroll
-    for (int q = 0; q < EPT / 8; q++) {
-        const int k = k0 + 8 * q;
+    for (int hh = 0; hh < 2; hh++) {
         uint32_t hw[4];
 #pragma unroll
         for (int i = 0; i < 4; i++) {
-            __half2 h2 = __halves2half2(__float2half_rn(scale_pow2(v[8 * q + 2 * i], -pexp)),
-                                        __float2half_rn(scale_pow2(v[8 * q + 2 * i + 1], -pexp)));
+            __half2 h2 = __halves2half2(__float2half_rn(scale_pow2(v[8 * hh + 2 * i], -pexp)),
+                                        __float2half_rn(scale_pow2(v[8 * hh + 2 * i + 1], -pexp)));
             hw[i] = *reinterpret_cast<uint32_t *>(&h2);
         }
-        const int s = k / kStep, within = k % kStep;
-        const int tt = within / 16, hh = (within % 16) / 8;
         p.xh[((size_t)(s * 2 + hh) * MP + m) * 4 + tt] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
     }
-    if (part == 0)
+    if (lane == 0)
         p.fac[c * MP + m] = exp2i(pexp);
 }
 
@@ -161,29 +161,34 @@ __device__ __forceinline__ uint32_t xprime_pair(const DecodeParams &p, int m, in
     return *reinterpret_cast<uint32_t *>(&o);
 }
 
+// One warp: T partial for 8 LoRA columns over kLoraSteps*16 input columns
+// (bf16 mma.sync, tokens as the 16-row M dimension).  All loads first.
 template <int MP>
 __device__ void lora_down_unit(const DecodeParams &p, int unit)
 {
     const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
     const int jg = unit % p.NJG, sl = unit / p.NJG;
-    const int j0 = jg * 8;
-    const int ka = sl * p.KSL, kb = min(p.K, ka + p.KSL);
-    float c[4] = {0.f, 0.f, 0.f, 0.f};
-    const int jrow = j0 + g;
-    const uint16_t *arow = p.lora_a + (size_t)jrow * p.K;
-    for (int k0 = ka; k0 < kb; k0 += 16) {
-        uint32_t a[4];
-        a[0] = xprime_pair(p, g, k0 + 2 * t);
-        a[1] = MP > 8 ? xprime_pair(p, g + 8, k0 + 2 * t) : 0u;
-        a[2] = xprime_pair(p, g, k0 + 2 * t + 8);
-        a[3] = MP > 8 ? xprime_pair(p, g + 8, k0 + 2 * t + 8) : 0u;
-        uint32_t b0 = 0, b1 = 0;
-        if (jrow < p.r) {
-            b0 = *reinterpret_cast<const uint32_t *>(arow + k0 + 2 * t);
-            b1 = *reinterpret_cast<const uint32_t *>(arow + k0 + 2 * t + 8);
+    const int j0 = jg * 8, jrow = j0 + g;
+    const int ka = sl * kLoraSteps * 16;
+    uint32_t a[kLoraSteps][4], b[kLoraSteps][2];
+#pragma unroll
+    for (int q = 0; q < kLoraSteps; q++) {
+        const int k0 = ka + 16 * q;
+        a[q][0] = xprime_pair(p, g, k0 + 2 * t);
+        a[q][1] = MP > 8 ? xprime_pair(p, g + 8, k0 + 2 * t) : 0u;
+        a[q][2] = xprime_pair(p, g, k0 + 2 * t + 8);
+        a[q][3] = MP > 8 ? xprime_pair(p, g + 8, k0 + 2 * t + 8) : 0u;
+        b[q][0] = b[q][1] = 0u;
+        if (jrow < p.r && k0 < p.K) {
+            const uint16_t *arow = p.lora_a + (size_t)jrow * p.K;
+            b[q][0] = *reinterpret_cast<const uint32_t *>(arow + k0 + 2 * t);
+            b[q][1] = *reinterpret_cast<const uint32_t *>(arow + k0 + 2 * t + 8);
         }
-        mma_bf16_16816(c, a, b0, b1);
     }
+    float c[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int q = 0; q < kLoraSteps; q++)
+        mma_bf16_16816(c, a[q], b[q][0], b[q][1]);
     float *dst = p.tpart + (size_t)sl * MP * p.r;
     const int j = j0 + 2 * t;
     if (j < p.r) {
@@ -204,10 +209,11 @@ struct Stage {
     uint32_t sc[2][2];  // matching block-scale bytes
 };
 
-template <int MP>
-__device__ __forceinline__ void load_stage(const DecodeParams &p, Stage &st, int row_base, int s)
+__device__ __forceinline__ void load_stage(const DecodeParams &p, Stage &st, int u)
 {
     const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    const int rt = u / p.S, s = u - rt * p.S;
+    const int row_base = rt * kTileRows + (threadIdx.x >> 5) * 32;
     const int kcol = s * kStep + 16 * t;
 #pragma unroll
     for (int i = 0; i < 2; i++)
@@ -225,17 +231,11 @@ __device__ __forceinline__ void load_stage(const DecodeParams &p, Stage &st, int
 }
 
 template <int MP>
-__device__ __forceinline__ void compute_stage(const DecodeParams &p, const Stage &st, int s,
+__device__ __forceinline__ void compute_stage(const Stage &st, const uint4 *xs,
                                               float (&cacc)[2][MP / 8][4])
 {
     constexpr int NT = MP / 8;
     const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-    uint4 xf[NT][2];
-#pragma unroll
-    for (int nt = 0; nt < NT; nt++)
-#pragma unroll
-        for (int h = 0; h < 2; h++)
-            xf[nt][h] = p.xh[((size_t)(s * 2 + h) * MP + g + 8 * nt) * 4 + t];
 #pragma unroll
     for (int i = 0; i < 2; i++) {
         const uint32_t sc0 = e4m3_to_h2_dup(st.sc[i][0]);
@@ -246,18 +246,22 @@ __device__ __forceinline__ void compute_stage(const DecodeParams &p, const Stage
         e2m1x8_to_h2x4(st.c[i][1].x, w1);
         e2m1x8_to_h2x4(st.c[i][1].y, w1 + 4);
 #pragma unroll
-        for (int j = 0; j < 4; j++) {
-            uint32_t a[4];
-            a[0] = hmul2_u32(w0[2 * j], sc0);
-            a[1] = hmul2_u32(w1[2 * j], sc1);
-            a[2] = hmul2_u32(w0[2 * j + 1], sc0);
-            a[3] = hmul2_u32(w1[2 * j + 1], sc1);
+        for (int h = 0; h < 2; h++) {
+            uint4 xf[NT];
 #pragma unroll
-            for (int nt = 0; nt < NT; nt++) {
-                const uint4 &v = xf[nt][j >> 1];
-                const uint32_t b0 = (j & 1) ? v.z : v.x;
-                const uint32_t b1 = (j & 1) ? v.w : v.y;
-                mma_f16_16816(cacc[i][nt], a, b0, b1);
+            for (int nt = 0; nt < NT; nt++)
+                xf[nt] = xs[(h * MP + g + 8 * nt) * 4 + t];
+#pragma unroll
+            for (int jj = 0; jj < 2; jj++) {
+                const int j = 2 * h + jj;
+                uint32_t a[4];
+                a[0] = hmul2_u32(w0[2 * j], sc0);
+                a[1] = hmul2_u32(w1[2 * j], sc1);
+                a[2] = hmul2_u32(w0[2 * j + 1], sc0);
+                a[3] = hmul2_u32(w1[2 * j + 1], sc1);
+#pragma unroll
+                for (int nt = 0; nt < NT; nt++)
+                    mma_f16_16816(cacc[i][nt], a, jj ? xf[nt].z : xf[nt].x, jj ? xf[nt].w : xf[nt].y);
             }
         }
     }
@@ -284,39 +288,11 @@ __device__ __forceinline__ void flush_chunk(const DecodeParams &p, int chunk, fl
 }
 
 template <int MP>
-__device__ void process_segment(const DecodeParams &p, int rt, int sa, int sb, int slot)
+__device__ __forceinline__ void write_partial(const DecodeParams &p, int rt, int slot,
+                                              float (&acc)[2][MP / 8][4])
 {
     constexpr int NT = MP / 8;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-    const int row_base = rt * kTileRows + warp * 32;
-    float acc[2][NT][4], cacc[2][NT][4];
-#pragma unroll
-    for (int i = 0; i < 2; i++)
-#pragma unroll
-        for (int nt = 0; nt < NT; nt++)
-#pragma unroll
-            for (int q = 0; q < 4; q++)
-                acc[i][nt][q] = cacc[i][nt][q] = 0.0f;
-
-    Stage st[kDepth];
-#pragma unroll
-    for (int d = 0; d < kDepth; d++)
-        if (sa + d < sb)
-            load_stage<MP>(p, st[d], row_base, sa + d);
-    for (int s0 = sa; s0 < sb; s0 += kDepth) {
-#pragma unroll
-        for (int d = 0; d < kDepth; d++) {
-            const int s = s0 + d;
-            if (s < sb) {
-                compute_stage<MP>(p, st[d], s, cacc);
-                if (s + kDepth < sb)
-                    load_stage<MP>(p, st[d], row_base, s + kDepth);
-                if ((s % (kChunk / kStep)) == (kChunk / kStep) - 1 || s == sb - 1)
-                    flush_chunk<MP>(p, s / (kChunk / kStep), acc, cacc);
-            }
-        }
-    }
-    // partial tile, stored token-major so that phase 2 reads rows contiguously
     float *dst = p.part + ((size_t)(rt * p.maxseg + slot) * MP) * kTileRows;
 #pragma unroll
     for (int i = 0; i < 2; i++)
@@ -327,6 +303,7 @@ __device__ void process_segment(const DecodeParams &p, int rt, int sa, int sb, i
                 const int row = warp * 32 + 16 * i + g + 8 * (q >> 1);
                 const int tok = nt * 8 + 2 * t + (q & 1);
                 dst[tok * kTileRows + row] = acc[i][nt][q];
+                acc[i][nt][q] = 0.0f;
             }
 }
 
@@ -334,69 +311,128 @@ __device__ void process_segment(const DecodeParams &p, int rt, int sa, int sb, i
 template <int MP>
 __global__ void __launch_bounds__(kThreads, 2) decode_gemm_kernel(DecodeParams p)
 {
+    constexpr int NT = MP / 8;
+    __shared__ __align__(16) uint4 s_x[kMaxUnitsPerBlock * 2 * MP * 4];  // X' of this block's steps
+    __shared__ float s_t_lora[MP * kMaxR / 4];                            // T (phase 2), r <= 64 here
     const int P = gridDim.x, bid = blockIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int gwarp = bid * kWarps + warp, nwarps = P * kWarps;
+    const int u_begin = (int)((long long)bid * p.U / P), u_end = (int)((long long)(bid + 1) * p.U / P);
 
-    // phase 0a: X' -> scaled f16, fragment order
-    for (int c = bid; c < p.NC; c += P)
-        convert_chunk<MP>(p, c);
-    // phase 0b: LoRA down-projection partial sums
-    if (p.r > 0) {
-        const int warp = threadIdx.x >> 5;
-        for (int unit = bid * kWarps + warp; unit < p.NJG * p.NS; unit += P * kWarps)
+    // start streaming this block's first weight units before anything else
+    Stage st[kDepth];
+#pragma unroll
+    for (int d = 0; d < kDepth; d++)
+        if (u_begin + d < u_end)
+            load_stage(p, st[d], u_begin + d);
+
+    // phase 0: X' -> scaled f16 in fragment order; LoRA down partial sums
+    for (int unit = gwarp; unit < MP * p.NC; unit += nwarps)
+        convert_unit<MP>(p, unit % MP, unit / MP);
+    if (p.r > 0)
+        for (int unit = nwarps - 1 - gwarp; unit < p.NJG * p.NS; unit += nwarps)
             lora_down_unit<MP>(p, unit);
-    }
     if (!grid_barrier(p.ctl, P))
         return;
 
-    // phase 1: stream-K over (row tile, 64-column step) units
-    const long long u_begin = (long long)bid * p.U / P, u_end = (long long)(bid + 1) * p.U / P;
-    for (long long u = u_begin; u < u_end;) {
-        const int rt = (int)(u / p.S);
-        const int sa = (int)(u % p.S);
-        const long long seg_end = min(u_end, (long long)(rt + 1) * p.S);
-        const int sb = sa + (int)(seg_end - u);
-        const int slot = bid - owner_of((long long)rt * p.S, p.U, P);
-        process_segment<MP>(p, rt, sa, sb, slot);
-        u = seg_end;
+    // phase 1: stage X' for this block's units (when they fit), then stream W
+    const bool staged = u_end - u_begin <= kMaxUnitsPerBlock;
+    if (staged) {
+        const int nu = u_end - u_begin;
+        for (int i = threadIdx.x; i < nu * 2 * MP * 4; i += kThreads) {
+            const int uo = i / (2 * MP * 4), rem = i % (2 * MP * 4);
+            const int u = u_begin + uo;
+            const int s = u % p.S;
+            s_x[i] = p.xh[(size_t)s * 2 * MP * 4 + rem];
+        }
+        __syncthreads();
     }
-    // reduce the T partial sums (fixed order); this block's share
-    if (p.r > 0) {
-        const int total = MP * p.r;
-        const int per = (total + P - 1) / P;
-        for (int el = threadIdx.x; el < per; el += kThreads) {
-            const int e = bid * per + el;
-            if (e < total) {
-                float s = 0.0f;
-                for (int sl = 0; sl < p.NS; sl++)
-                    s += p.tpart[(size_t)sl * total + e];
-                p.tfin[e] = s;
+    float acc[2][NT][4], cacc[2][NT][4];
+#pragma unroll
+    for (int i = 0; i < 2; i++)
+#pragma unroll
+        for (int nt = 0; nt < NT; nt++)
+#pragma unroll
+            for (int q = 0; q < 4; q++)
+                acc[i][nt][q] = cacc[i][nt][q] = 0.0f;
+    for (int u0 = u_begin; u0 < u_end; u0 += kDepth) {
+#pragma unroll
+        for (int d = 0; d < kDepth; d++) {
+            const int u = u0 + d;
+            if (u < u_end) {
+                const int rt = u / p.S, s = u - rt * p.S;
+                const uint4 *xs = staged ? s_x + (size_t)(u - u_begin) * 2 * MP * 4
+                                         : p.xh + (size_t)s * 2 * MP * 4;
+                compute_stage<MP>(st[d], xs, cacc);
+                if (u + kDepth < u_end)
+                    load_stage(p, st[d], u + kDepth);
+                const bool seg_end = (s == p.S - 1) || (u == u_end - 1);
+                if ((s % kStepsPerChunk) == kStepsPerChunk - 1 || seg_end)
+                    flush_chunk<MP>(p, s / kStepsPerChunk, acc, cacc);
+                if (seg_end)
+                    write_partial<MP>(p, rt, bid - owner_of(rt * p.S, p.U, P), acc);
             }
         }
     }
+    // T = sum of the LoRA partial sums: one warp per element, fixed order
+    if (p.r > 0) {
+        const int total = MP * p.r;
+        for (int e = gwarp; e < total; e += nwarps) {
+            float s = 0.0f;
+            for (int sl = lane; sl < p.NS; sl += 32)
+                s += p.tpart[(size_t)sl * total + e];
+#pragma unroll
+            for (int off = 16; off >= 1; off >>= 1)
+                s += __shfl_xor_sync(0xffffffffu, s, off);
+            if (lane == 0)
+                p.tfin[e] = s;
+        }
+    }
     if (!grid_barrier(p.ctl, P))
         return;
 
-    // phase 2: split-K reduction in fixed order + epilogue
-    const float s_t = *p.tensor_scale;
+    // phase 2: split-K reduction in fixed order + epilogue, one thread per output
     const int r = p.r;
+    float *sT = s_t_lora;
+    const bool t_in_smem = MP * r <= MP * kMaxR / 4;
+    if (r > 0 && t_in_smem) {
+        for (int i = threadIdx.x; i < MP * r; i += kThreads)
+            sT[i] = p.tfin[i];
+        __syncthreads();
+    }
+    const float *T = t_in_smem ? sT : p.tfin;
+    const float s_t = *p.tensor_scale;
     const long long total = (long long)p.M * p.N;
     for (long long o = (long long)bid * kThreads + threadIdx.x; o < total; o += (long long)P * kThreads) {
-        const int m = (int)(o / p.N), n = (int)(o % p.N);
+        const int m = (int)(o / p.N), n = (int)(o - (long long)m * p.N);
         const int rt = n / kTileRows, row = n % kTileRows;
-        const int first = owner_of((long long)rt * p.S, p.U, P);
-        const int last = owner_of((long long)rt * p.S + p.S - 1, p.U, P);
-        float acc = 0.0f;
+        const int nseg = owner_of(rt * p.S + p.S - 1, p.U, P) - owner_of(rt * p.S, p.U, P) + 1;
         const float *src = p.part + ((size_t)(rt * p.maxseg) * MP + m) * kTileRows + row;
-        for (int j = 0; j <= last - first; j++)
-            acc += src[(size_t)j * MP * kTileRows];
+        float acc1 = 0.0f;
+#pragma unroll 8
+        for (int j = 0; j < nseg; j++)
+            acc1 += src[(size_t)j * MP * kTileRows];
         float lora = 0.0f;
         if (r > 0) {
-            const uint16_t *brow = p.lora_b + (size_t)n * r;
-            const float *trow = p.tfin + m * r;
-            for (int jj = 0; jj < r; jj++)
-                lora = __fmaf_rn(trow[jj], bf16_bits_to_f32(brow[jj]), lora);
+            const float *trow = T + m * r;
+            if ((r & 7) == 0) {
+                const uint4 *brow = reinterpret_cast<const uint4 *>(p.lora_b + (size_t)n * r);
+                for (int jj = 0; jj < r / 8; jj++) {
+                    const uint4 bv = brow[jj];
+                    const uint32_t bw[4] = {bv.x, bv.y, bv.z, bv.w};
+#pragma unroll
+                    for (int q = 0; q < 4; q++) {
+                        lora = __fmaf_rn(trow[8 * jj + 2 * q], bf16_bits_to_f32(bw[q] & 0xFFFFu), lora);
+                        lora = __fmaf_rn(trow[8 * jj + 2 * q + 1], bf16_bits_to_f32(bw[q] >> 16), lora);
+                    }
+                }
+            } else {
+                const uint16_t *brow = p.lora_b + (size_t)n * r;
+                for (int jj = 0; jj < r; jj++)
+                    lora = __fmaf_rn(trow[jj], bf16_bits_to_f32(brow[jj]), lora);
+            }
         }
-        const float yv = __fmaf_rn(s_t, acc, p.lora_scale * lora);
+        const float yv = __fmaf_rn(s_t, acc1, p.lora_scale * lora);
         if (p.y_fp32)
             reinterpret_cast<float *>(p.y)[o] = yv;
         else
@@ -406,14 +442,13 @@ __global__ void __launch_bounds__(kThreads, 2) decode_gemm_kernel(DecodeParams p
 
 // ---------------------------------------------------------------- host side
 struct DecodePlan {
-    int MP, P, S, NC, R, NS, NJG, KSL, maxseg;
-    long long U;
+    int MP, P, S, NC, R, NS, NJG, maxseg, U;
     size_t off_xh, off_fac, off_tpart, off_tfin, off_part, total;
 };
 
 static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-static int host_owner(long long u, long long U, int P) { return (int)(((u + 1) * (long long)P - 1) / U); }
+static int host_owner(int u, int U, int P) { return (int)(((long long)(u + 1) * P - 1) / U); }
 
 static bool make_plan(int64_t M, int64_t N, int64_t K, int64_t r, const DeviceInfo &dev, DecodePlan &pl)
 {
@@ -424,23 +459,23 @@ static bool make_plan(int64_t M, int64_t N, int64_t K, int64_t r, const DeviceIn
     pl.S = (int)((K + kStep - 1) / kStep);
     pl.NC = (int)((K + kChunk - 1) / kChunk);
     pl.R = (int)((N + kTileRows - 1) / kTileRows);
-    pl.U = (long long)pl.R * pl.S;
+    const long long U = (long long)pl.R * pl.S;
+    if (U > (1LL << 30))
+        return false;
+    pl.U = (int)U;
     // every block gets at least one unit, so every partial slot is written
-    pl.P = (int)std::min<long long>((long long)dev.num_sms * bps, pl.U);
-    const int k16 = (int)(K / 16);
-    pl.NS = std::max(1, std::min(32, k16 / 8));
-    pl.KSL = ((k16 + pl.NS - 1) / pl.NS) * 16;
-    pl.NS = (int)((K + pl.KSL - 1) / pl.KSL);
+    pl.P = (int)std::min<long long>((long long)dev.num_sms * bps, U);
+    pl.NS = (int)((K + kLoraSteps * 16 - 1) / (kLoraSteps * 16));
     pl.NJG = (int)((r + 7) / 8);
     pl.maxseg = 1;
     for (int rt = 0; rt < pl.R; rt++) {
-        const int a = host_owner((long long)rt * pl.S, pl.U, pl.P);
-        const int b = host_owner((long long)rt * pl.S + pl.S - 1, pl.U, pl.P);
+        const int a = host_owner(rt * pl.S, pl.U, pl.P);
+        const int b = host_owner(rt * pl.S + pl.S - 1, pl.U, pl.P);
         pl.maxseg = std::max(pl.maxseg, b - a + 1);
     }
     size_t off = kCtlBytes;
     pl.off_xh = off;
-    off = align_up(off + (size_t)pl.NC * (kChunk / kStep) * pl.MP * kStep * 2, 256);
+    off = align_up(off + (size_t)pl.NC * kStepsPerChunk * pl.MP * kStep * 2, 256);
     pl.off_fac = off;
     off = align_up(off + (size_t)pl.NC * pl.MP * 4, 256);
     pl.off_tpart = off;
@@ -506,7 +541,6 @@ cudaError_t launch_decode_gemm(const GemmArgs &a, cudaStream_t s, const DeviceIn
         p.R = pl.R;
         p.NS = pl.NS;
         p.NJG = pl.NJG;
-        p.KSL = pl.KSL;
         p.maxseg = pl.maxseg;
         p.U = pl.U;
         void *args[] = {&p};

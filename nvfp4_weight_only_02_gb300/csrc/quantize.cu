@@ -20,6 +20,16 @@
 namespace nvfp4 {
 
 // ------------------------------------------------------------------ amax
+__device__ __forceinline__ uint32_t absmax8(uint4 a, uint4 b)
+{
+    // per-halfword max of the bf16 magnitude bits of 16 elements
+    const uint32_t m = 0x7FFF7FFFu;
+    uint32_t x = __vimax3_u16x2(a.x & m, a.y & m, a.z & m);
+    uint32_t y = __vimax3_u16x2(a.w & m, b.x & m, b.y & m);
+    uint32_t z = __vimax3_u16x2(b.z & m, b.w & m, x);
+    return __vmaxu2(y, z);
+}
+
 // Pass 1 of the dynamic mode: a = max |w| over the tensor, exact (integer max
 // of bf16 magnitude bits; NaN/inf patterns sort above every finite value and
 // are reported).  The last block to finish turns a into s_t = a / 2688 and
@@ -31,18 +41,16 @@ __global__ void __launch_bounds__(256) amax_kernel(const uint4 *__restrict__ w, 
     uint32_t m = 0;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    for (; i + stride < nvec; i += 2 * stride) {  // two loads in flight per thread
+    for (; i + 3 * stride < nvec; i += 4 * stride) {  // four 16-byte loads in flight
         uint4 a = ld_stream_u4(w + i);
         uint4 b = ld_stream_u4(w + i + stride);
-        m = __vmaxu2(m, __vmaxu2(__vmaxu2(a.x & 0x7FFF7FFFu, a.y & 0x7FFF7FFFu),
-                                 __vmaxu2(a.z & 0x7FFF7FFFu, a.w & 0x7FFF7FFFu)));
-        m = __vmaxu2(m, __vmaxu2(__vmaxu2(b.x & 0x7FFF7FFFu, b.y & 0x7FFF7FFFu),
-                                 __vmaxu2(b.z & 0x7FFF7FFFu, b.w & 0x7FFF7FFFu)));
+        uint4 c = ld_stream_u4(w + i + 2 * stride);
+        uint4 d = ld_stream_u4(w + i + 3 * stride);
+        m = __vmaxu2(m, __vmaxu2(absmax8(a, b), absmax8(c, d)));
     }
-    if (i < nvec) {
+    for (; i < nvec; i += stride) {
         uint4 a = ld_stream_u4(w + i);
-        m = __vmaxu2(m, __vmaxu2(__vmaxu2(a.x & 0x7FFF7FFFu, a.y & 0x7FFF7FFFu),
-                                 __vmaxu2(a.z & 0x7FFF7FFFu, a.w & 0x7FFF7FFFu)));
+        m = __vmaxu2(m, absmax8(a, make_uint4(0, 0, 0, 0)));
     }
     m = max(m & 0xFFFFu, m >> 16);
     m = __reduce_max_sync(0xffffffffu, m);
@@ -75,16 +83,20 @@ __global__ void __launch_bounds__(256) amax_kernel(const uint4 *__restrict__ w, 
 }
 
 // ------------------------------------------------------------------ quantise
-// x / S for 0 <= x <= 8 S, S in [2^-96, 2^96], r = RN(1/S): one product, an
-// exact FMA remainder and one FMA correction (Markstein's correction step,
-// P. Markstein, IBM J. Res. Dev. 34(1), 1990).  The kernel only needs the
-// E2M1 code of the quotient; nvfp4_quotient_check compares this quotient
-// with IEEE division over every significand pair of the domain.
+// x / S without a division: with r = RN(1/S), q0 = RN(x r) is within two ulps
+// of x/S, the remainder q0 S - x is exact in one FMA, and one FMA correction
+// q0 - rem r gives the correctly rounded quotient (Markstein's correction
+// step, P. Markstein, IBM J. Res. Dev. 34(1), 1990).  Written so that the
+// sign of a zero quotient follows x.  Used for S in [2^-96, 2^96] and
+// |x / S| < 2^20 (no overflow or underflow in the steps); nvfp4_quotient_check
+// compares it with IEEE division for every fp32 significand of S, every bf16
+// significand of x, both signs and quotient exponents -13 .. 9, which covers
+// every quotient whose E2M1 or E4M3 rounding it decides.
 __device__ __forceinline__ float quotient(float x, float S, float r)
 {
-    float q0 = __fmul_rn(x, r);
-    float rem = __fmaf_rn(-q0, S, x);
-    return __fmaf_rn(rem, r, q0);
+    const float q0 = __fmul_rn(x, r);
+    const float rem = __fmaf_rn(q0, S, -x);
+    return __fmaf_rn(-rem, r, q0);
 }
 
 __device__ __forceinline__ bool fast_quotient_domain(float S)
@@ -92,90 +104,103 @@ __device__ __forceinline__ bool fast_quotient_domain(float S)
     return S >= 0x1p-96f && S <= 0x1p96f;
 }
 
-// Sign bits of the 8 bf16 elements of a half-block, moved to bit 3 of their
-// nibble in the packed code word.
-__device__ __forceinline__ uint32_t nibble_signs(uint4 v)
+// Four packed E2M1 bytes from eight signed quotients (element 2i in the low
+// nibble of byte i); round to nearest even, saturating, sign kept (-0 -> 0x8).
+__device__ __forceinline__ uint32_t e2m1x8_pack(const float q[8])
 {
-    return ((v.x >> 12) & 0x8u) | ((v.x >> 24) & 0x80u) | ((v.y >> 4) & 0x800u) |
-           ((v.y >> 16) & 0x8000u) | ((v.z << 4) & 0x80000u) | ((v.z >> 8) & 0x800000u) |
-           ((v.w << 12) & 0x8000000u) | (v.w & 0x80000000u);
+    uint32_t w;
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+        "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+        : "=r"(w)
+        : "f"(q[0]), "f"(q[1]), "f"(q[2]), "f"(q[3]), "f"(q[4]), "f"(q[5]), "f"(q[6]), "f"(q[7]));
+    return w;
 }
 
-// Codes of one half-block (8 elements) with effective block scale S > 0.
-__device__ __forceinline__ uint32_t encode_half(uint4 v, float S)
+// Codes of 8 elements (4 bf16 pairs) with block scale S > 0.
+__device__ __forceinline__ uint32_t encode8(uint4 v, float S, float r, bool fast)
 {
-    float q[8];
     const uint32_t words[4] = {v.x, v.y, v.z, v.w};
-    const float S8 = __fmul_rn(8.0f, S);  // beyond 8 S every code is 6
-    if (fast_quotient_domain(S)) {
-        const float r = __frcp_rn(S);
+    float q[8];
+    if (fast) {
 #pragma unroll
         for (int i = 0; i < 4; i++) {
-            float lo = fminf(bf16_bits_to_f32(words[i] & 0x7FFFu), S8);
-            float hi = fminf(bf16_bits_to_f32((words[i] >> 16) & 0x7FFFu), S8);
-            q[2 * i] = quotient(lo, S, r);
-            q[2 * i + 1] = quotient(hi, S, r);
+            q[2 * i] = quotient(__uint_as_float(words[i] << 16), S, r);
+            q[2 * i + 1] = quotient(__uint_as_float(words[i] & 0xFFFF0000u), S, r);
         }
     } else {
+        // rare: scale outside the fast domain, or quotients beyond 2^20
+        const float S8 = __fmul_rn(8.0f, S);
 #pragma unroll
         for (int i = 0; i < 4; i++) {
-            float lo = fminf(bf16_bits_to_f32(words[i] & 0x7FFFu), S8);
-            float hi = fminf(bf16_bits_to_f32((words[i] >> 16) & 0x7FFFu), S8);
-            q[2 * i] = __fdiv_rn(lo, S);
-            q[2 * i + 1] = __fdiv_rn(hi, S);
+            const float lo = __uint_as_float(words[i] << 16);
+            const float hi = __uint_as_float(words[i] & 0xFFFF0000u);
+            q[2 * i] = copysignf(__fdiv_rn(fminf(fabsf(lo), S8), S), lo);
+            q[2 * i + 1] = copysignf(__fdiv_rn(fminf(fabsf(hi), S8), S), hi);
         }
     }
-    uint32_t out = 0;
-#pragma unroll
-    for (int i = 0; i < 4; i++)
-        out |= e2m1x2_encode_nonneg(q[2 * i], q[2 * i + 1]) << (8 * i);
-    return out | nibble_signs(v);
+    return e2m1x8_pack(q);
 }
 
-// Pass 2: two threads per 16-element block (8 elements each, one 16-byte
-// load).  The block amax is the max of the pair (one shuffle); both threads
-// derive the same scale; each writes its 4 code bytes; the second writes the
-// scale byte.  Blocks are visited from the end of the tensor towards the
-// start, so that the tail that pass 1 left in L2 is re-read first.
-__global__ void __launch_bounds__(256) quantize_kernel(const uint4 *__restrict__ w, int64_t nhalves,
+// Pass 2: one thread per 16-element block (two 16-byte loads).  Every block
+// scale byte e has a fixed S = fl32(dec(e) s_t) and RN(1/S) for the whole
+// tensor, so both are tabulated once per CTA in shared memory.  Blocks are
+// visited from the end of the tensor towards the start, so that the tail
+// pass 1 left in L2 is re-read first.
+__global__ void __launch_bounds__(256) quantize_kernel(const uint4 *__restrict__ w, int64_t nblocks,
                                                        const float *__restrict__ tensor_scale,
-                                                       uint32_t *__restrict__ codes,
+                                                       uint2 *__restrict__ codes,
                                                        uint8_t *__restrict__ scales,
                                                        uint32_t *__restrict__ ctl)
 {
+    __shared__ float s_S[128], s_R[128];
     float s_t = *tensor_scale;
     if (!(s_t >= 0.0f && s_t <= FLT_MAX)) {  // NaN, inf or negative frozen scale
         if (blockIdx.x == 0 && threadIdx.x == 0)
             record_status(ctl, NVFP4_ERR_NONFINITE);
         s_t = 0.0f;
     }
+    for (int e = threadIdx.x; e < 128; e += blockDim.x) {
+        const float S = __fmul_rn(e4m3_to_f32((uint32_t)e), s_t);
+        s_S[e] = S;
+        s_R[e] = fast_quotient_domain(S) ? __frcp_rn(S) : 0.0f;
+    }
     const float d = __fmul_rn(6.0f, s_t);
+    const bool d_fast = fast_quotient_domain(d);
+    const float rd = d_fast ? __frcp_rn(d) : 0.0f;
+    __syncthreads();
+
     const int64_t nthreads = (int64_t)gridDim.x * blockDim.x;
-    const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    const int64_t iters = (nhalves + nthreads - 1) / nthreads;
-    for (int64_t it = 0; it < iters; it++) {
-        const int64_t h = nhalves - 1 - tid - it * nthreads;
-        const bool valid = h >= 0;
-        uint4 v = valid ? ld_stream_u4(w + h) : make_uint4(0, 0, 0, 0);
-        uint32_t m = __vmaxu2(__vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu),
-                              __vmaxu2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
+    for (int64_t b = nblocks - 1 - ((int64_t)blockIdx.x * blockDim.x + threadIdx.x); b >= 0; b -= nthreads) {
+        const uint4 v0 = ld_stream_u4(w + 2 * b);
+        const uint4 v1 = ld_stream_u4(w + 2 * b + 1);
+        uint32_t m = absmax8(v0, v1);
         m = max(m & 0xFFFFu, m >> 16);
-        m = max(m, __shfl_xor_sync(0xffffffffu, m, 1));
-        if (!valid)
-            continue;
-        uint32_t e = 0, cw = 0;
+        uint32_t e = 0;
+        uint2 cw = make_uint2(0u, 0u);
         if (m >= 0x7F80u) {
             record_status(ctl, NVFP4_ERR_NONFINITE);
         } else if (s_t != 0.0f) {
-            const float e_f = __fdiv_rn(bf16_bits_to_f32(m), d);
-            e = e4m3_encode_nonneg(e_f);
-            const float S = __fmul_rn(e4m3_to_f32(e), s_t);
-            if (S != 0.0f)
-                cw = encode_half(v, S);
+            const float a_b = bf16_bits_to_f32(m);
+            if (!d_fast)
+                e = e4m3_encode_nonneg(__fdiv_rn(a_b, d));
+            else if (__fmul_rn(a_b, rd) >= 1024.0f)
+                e = 0x7E;  // far beyond 448: saturates
+            else
+                e = e4m3_encode_nonneg(quotient(a_b, d, rd));
+            const float S = s_S[e];
+            if (S != 0.0f) {
+                const float r = s_R[e];
+                const bool fast = r != 0.0f && __fmul_rn(a_b, r) < 0x1p20f;
+                cw.x = encode8(v0, S, r, fast);
+                cw.y = encode8(v1, S, r, fast);
+            }
         }
-        codes[h] = cw;
-        if (h & 1)
-            scales[h >> 1] = (uint8_t)e;
+        codes[b] = cw;
+        scales[b] = (uint8_t)e;
     }
 }
 
@@ -246,8 +271,8 @@ __global__ void encode_debug_kernel(const float *__restrict__ x, int64_t n, int 
         const float v = x[i];
         uint32_t b;
         if (which == 0) {
-            b = e2m1x2_encode_nonneg(fminf(fabsf(v), 8.0f), 0.0f) & 0xFu;
-            b |= (__float_as_uint(v) >> 28) & 0x8u;
+            const float q[8] = {v, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            b = e2m1x8_pack(q) & 0xFu;
         } else {
             b = e4m3_encode_nonneg(v);
         }
@@ -263,11 +288,12 @@ __global__ void quotient_check_kernel(uint32_t sig_lo, uint32_t sig_hi,
         return;
     const float S = __uint_as_float((127u << 23) | sig);  // [1, 2)
     const float r = __frcp_rn(S);
-    const float S8 = __fmul_rn(8.0f, S);
     unsigned long long bad = 0;
-    for (int e = -3; e <= 3; e++)
-        for (uint32_t ws = 0; ws < 128; ws++) {
-            const float x = fminf(__uint_as_float(((uint32_t)(127 + e) << 23) | (ws << 16)), S8);
+    for (int e = -13; e <= 9; e++)
+        for (uint32_t ws = 0; ws < 256; ws++) {
+            // bf16 significand (7 bits) with both signs
+            const uint32_t bits = ((ws & 128u) << 24) | ((uint32_t)(127 + e) << 23) | ((ws & 127u) << 16);
+            const float x = __uint_as_float(bits);
             bad += __float_as_uint(quotient(x, S, r)) != __float_as_uint(__fdiv_rn(x, S));
         }
     if (bad)
@@ -290,13 +316,13 @@ cudaError_t launch_quantize(const void *w, int64_t N, int64_t K, uint8_t *codes,
     const int64_t nelem = N * K;
     if (!given) {
         const int64_t nvec = nelem / 8;
-        amax_kernel<<<grid_for(nvec, 256 * 2, dev.num_sms * 8), 256, 0, s>>>(
+        amax_kernel<<<grid_for(nvec, 256 * 4, dev.num_sms * 8), 256, 0, s>>>(
             reinterpret_cast<const uint4 *>(w), nvec, tensor_scale, ctl);
     }
-    const int64_t nhalves = nelem / 8;
-    quantize_kernel<<<grid_for(nhalves, 256, dev.num_sms * 8), 256, 0, s>>>(
-        reinterpret_cast<const uint4 *>(w), nhalves, tensor_scale,
-        reinterpret_cast<uint32_t *>(codes), scales, ctl);
+    const int64_t nblocks = nelem / 16;
+    quantize_kernel<<<grid_for(nblocks, 256, dev.num_sms * 8), 256, 0, s>>>(
+        reinterpret_cast<const uint4 *>(w), nblocks, tensor_scale,
+        reinterpret_cast<uint2 *>(codes), scales, ctl);
     return cudaGetLastError();
 }
 

@@ -10,9 +10,10 @@ def _sweep(lo_bits, hi_bits):
     return np.arange(lo_bits, hi_bits, dtype=np.uint32).view(np.float32)
 
 
-def test_e2m1_encoder_exhaustive_over_decision_range(nv, orc):
-    # every fp32 in [2^-4, 8): all thresholds 0.25 .. 5 and saturation at 6
-    x = _sweep(0x3D800000, 0x41000000)
+@pytest.mark.parametrize("sign", [1.0, -1.0])
+def test_e2m1_encoder_exhaustive_over_decision_range(nv, orc, sign):
+    # every fp32 in +-[2^-4, 8): all thresholds 0.25 .. 5 and saturation at 6
+    x = _sweep(0x3D800000, 0x41000000) * np.float32(sign)
     got = nv.nvfp4_encode_debug(torch.from_numpy(x).cuda(), 0).cpu().numpy()
     exp = orc.encode_array(x, 0)
     bad = np.nonzero(got != exp)[0]
@@ -52,6 +53,6 @@ def test_e4m3_encoder_extremes(nv, orc):
 
 
 def test_fast_quotient_equals_ieee_division_everywhere(nv):
-    # all 2^23 fp32 significands of the block scale x all 128 bf16 significands
-    # x quotient exponents -3..3
+    # all 2^23 fp32 significands of the divisor x all 128 bf16 significands of
+    # the dividend x both signs x quotient exponents -13..9
     assert nv.nvfp4_quotient_check(0, 1 << 23) == 0
