@@ -65,7 +65,7 @@ size_t nvfp4_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t r)
     const DeviceInfo *dev = device_info(&st);
     if (!dev)
         return 0;
-    size_t g = decode_workspace_bytes(M, N, K, r, *dev);
+    size_t g = gemm_workspace_bytes(M, N, K, r, *dev);
     return g < kCtlBytes ? kCtlBytes : g;
 }
 
@@ -127,7 +127,7 @@ nvfp4_status nvfp4_w4a16_lora_gemm(const void *x_bf16, int64_t M, int64_t N, int
         (lora && (!aligned16(lora_a_bf16) || !aligned16(lora_b_bf16))))
         return NVFP4_ERR_ALIGNMENT;
     NVFP4_TRY_DEVICE(dev);
-    const size_t need = decode_workspace_bytes(M, N, K, lora ? r : 0, *dev);
+    const size_t need = gemm_workspace_bytes(M, N, K, lora ? r : 0, *dev);
     if (need == 0)
         return NVFP4_ERR_UNSUPPORTED_DEVICE;
     if (ws_bytes < need)
@@ -149,6 +149,8 @@ nvfp4_status nvfp4_w4a16_lora_gemm(const void *x_bf16, int64_t M, int64_t N, int
     a.y_fp32 = y_dtype == NVFP4_OUT_FP32;
     a.ws = (uint8_t *)workspace;
     a.ws_bytes = ws_bytes;
+    if (prefill_supported(M, N, K, a.r))
+        return from_cuda(launch_prefill_gemm(a, (cudaStream_t)stream, *dev));
     return from_cuda(launch_decode_gemm(a, (cudaStream_t)stream, *dev));
 }
 

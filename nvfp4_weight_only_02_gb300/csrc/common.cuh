@@ -28,6 +28,11 @@ enum CtlWord : int {
     CTL_RS_COUNT = 5,     // reserved
 };
 constexpr size_t kCtlBytes = 256;
+// After the control block: arrival counters at a fixed place, so that calls
+// of any shape find them at zero (every kernel that counts resets its
+// counters before it returns).  Per-call scratch starts after them.
+constexpr int kCounterWords = 8192;
+constexpr size_t kWsHeaderBytes = kCtlBytes + 4 * (size_t)kCounterWords;
 
 // Spin limit of every device-side wait: about a second of polling, after
 // which the kernel records NVFP4_ERR_TIMEOUT and gives up instead of hanging.

@@ -1,5 +1,5 @@
 // gemm_decode.cu -- memory-bound W4A16 decode GEMM with fused LoRA and input
-// noise (M <= 16 tokens), one persistent cooperative kernel on sm_103a.
+// noise (M <= 16 tokens) on sm_103a.
 //
 //   X' = bf16(X * z)                      noise through the RMSNorm gain, which
 //                                         equals multiplicative weight noise
@@ -8,34 +8,32 @@
 // rollouts are memory-bound on the weights, section "Эксперименты").
 //
 // The weight bytes (0.5625 B per weight) are the only large stream, so the
-// kernel is organised around reading them once at full HBM bandwidth:
+// work is organised around reading them once at full HBM bandwidth:
 //
-//  phase 0  (all blocks)  X' is formed once, rounded to bf16 and re-expressed
-//           as f16 times a power of two per token and 512-channel chunk
-//           (f16 holds every bf16 value of the chunk exactly once scaled so
-//           its max lies in [2^14, 2^15); values more than 2^28 below the
-//           chunk max may round); it is written in the order in which the
-//           MMA B fragments are read.  The LoRA down-projection T = X' A^T
-//           is computed as partial sums over K slices with bf16 MMAs.
-//  barrier
-//  phase 1  stream-K main loop: the (256-row tile x 64-column step) units of
-//           W are split evenly over the resident blocks.  Each warp owns 32
-//           rows; every lane loads its codes (8 bytes per row) and block
-//           scales straight into registers, several steps ahead, converts
-//           them with cvt.e2m1x2 -> f16x2 and one f16x2 multiply by the
-//           block scale (both exact: v * dec(e) has at most 6 significant
-//           bits), and feeds mma.sync m16n8k16 with the tokens as the
-//           8-wide N dimension.  Accumulation is FP32; at each 512-column
-//           chunk the chunk's partial sums are scaled back by the chunk's
-//           power of two.  Each block writes one partial tile per row tile
-//           it touched; the T partial sums are reduced.
-//  barrier
-//  phase 2  every output element sums its row tile's partials in a fixed
-//           order (deterministic) and applies the epilogue
-//           Y = s_t * acc + s * T B^T, written as FP32 or bf16.
-//
-// All blocks are co-resident (cooperative launch); both grid barriers have a
-// bounded wait and report NVFP4_ERR_TIMEOUT instead of hanging.
+//  prologue kernel: X' is formed once, rounded to bf16 and re-expressed as
+//      f16 times a power of two per token and 512-column chunk (f16 holds
+//      every bf16 value of the chunk exactly once scaled so its max lies in
+//      [2^14, 2^15); values more than 2^28 below the chunk max may round),
+//      written in the order in which the MMA B fragments are read.  The LoRA
+//      down-projection T = X' A^T is summed in two fixed-order levels (8
+//      warps of a block in shared memory, then the last block of each group
+//      of 8 LoRA columns), so T is deterministic.
+//  main kernel (programmatic dependent launch): each block starts streaming
+//      its first weight units before it waits for the prologue.  Units are
+//      (tile of 32*RG rows, 64 columns), split evenly over the resident blocks
+//      (stream-K).  Inside a block, warp (rg, kl) owns 32 rows and a
+//      contiguous share of the block's columns of each tile; every lane loads
+//      its codes and block scales straight into registers several units
+//      ahead, converts them with cvt.e2m1x2 -> f16x2 and one f16x2 multiply by
+//      the block scale (both exact: v * dec(e) has at most 6 significant bits),
+//      and feeds mma.sync m16n8k16 with the tokens as the 8-wide N dimension.
+//      Accumulation is FP32; at each 512-column chunk the chunk's sums are
+//      scaled back by the chunk's power of two.  Per tile the block reduces
+//      its warps' partial sums in shared memory in a fixed order; a tile that
+//      one block covers entirely is finished on the spot, otherwise the last
+//      of its (few) blocks to arrive sums the partials in slot order and
+//      applies the epilogue Y = s_t * acc + s * T B^T.  Results do not depend
+//      on arrival order.
 #include <algorithm>
 #include <mutex>
 
@@ -46,34 +44,14 @@ namespace nvfp4 {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = 8;
-constexpr int kTileRows = 256;  // rows of W per stream-K tile (8 warps x 32)
-constexpr int kStep = 64;       // columns of W per stream-K unit
-constexpr int kChunk = 512;     // columns per X' scaling chunk
+constexpr int kStep = 64;   // columns of W per stream-K unit
+constexpr int kChunk = 512; // columns per X' scaling chunk
 constexpr int kStepsPerChunk = kChunk / kStep;
-constexpr int kDepth = 4;       // register prefetch depth (units in flight per warp)
-constexpr int kMaxUnitsPerBlock = 24;  // X' staging capacity in shared memory
-constexpr int kLoraSteps = 4;   // k16 steps per LoRA down-projection unit
-constexpr int kMaxR = 256;
-
-struct DecodeParams {
-    const uint16_t *x;
-    int M, N, K, r;
-    const uint8_t *codes, *scales;
-    const float *tensor_scale;
-    const uint16_t *lora_a, *lora_b;
-    float lora_scale;
-    const float *noise;
-    void *y;
-    int y_fp32;
-    uint32_t *ctl;
-    uint4 *xh;     // [S][2][MP][4] x 8 f16
-    float *fac;    // [NC][MP]
-    float *tpart;  // [NS][MP][r]
-    float *tfin;   // [MP][r]
-    float *part;   // [R][maxseg][MP][256]
-    int S, NC, R, NS, NJG, maxseg;
-    int U;
-};
+constexpr int kDepth = 4;   // register prefetch depth (units in flight per warp)
+constexpr int kMaxSeg = 3;  // tiles a block may touch
+constexpr int kStageSteps = 28;  // X' staging capacity (steps) in shared memory
+constexpr int kLoraSlice = 512;  // input columns per LoRA prologue block (8 warps x 64)
+constexpr int kMaxRSmem = 64;
 
 __device__ __forceinline__ int owner_of(int u, int U, int P)
 {
@@ -85,12 +63,35 @@ __device__ __forceinline__ float bf16_round(float v)
     return __bfloat162float(__float2bfloat16_rn(v));
 }
 
-// ---------------------------------------------------------------- phase 0a
+__device__ __forceinline__ void pdl_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void pdl_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// ================================================================ prologue
+struct PrologueParams {
+    const uint16_t *x;
+    int M, K, r;
+    const uint16_t *lora_a;
+    const float *noise;
+    uint4 *xh;       // [S][2][MP][4] x 8 f16
+    float *fac;      // [NC][MP]
+    float *tpart;    // [NS][MP][r]
+    float *tfin;     // [MP][r]
+    uint32_t *jcnt;  // [NJG] arrival counters
+    int NC, NS, NJG, conv_blocks;
+};
+
 // One warp converts one (token, 512-column chunk): X' = bf16(X z), its max,
-// the power of two 2^p that puts the max in [2^14, 2^15), and X' 2^-p as
-// f16 in fragment order.  Each lane handles one 16-column block.
+// the power of two 2^p that puts the max in [2^14, 2^15), and X' 2^-p as f16
+// in fragment order.  Each lane handles one 16-column block.
 template <int MP>
-__device__ void convert_unit(const DecodeParams &p, int m, int c)
+__device__ void convert_unit(const PrologueParams &p, int m, int c)
 {
     const int lane = threadIdx.x & 31;
     const int k0 = c * kChunk + lane * 16;
@@ -147,37 +148,46 @@ __device__ void convert_unit(const DecodeParams &p, int m, int c)
         p.fac[c * MP + m] = exp2i(pexp);
 }
 
-// ---------------------------------------------------------------- phase 0b
-__device__ __forceinline__ uint32_t xprime_pair(const DecodeParams &p, int m, int k)
+__device__ __forceinline__ uint32_t xprime_pair(const uint16_t *x, const float *z, int M, int K, int m, int k)
 {
-    if (m >= p.M || k >= p.K)
+    if (m >= M || k >= K)
         return 0u;
-    const uint32_t xb = *reinterpret_cast<const uint32_t *>(p.x + (size_t)m * p.K + k);
-    if (!p.noise)
+    const uint32_t xb = *reinterpret_cast<const uint32_t *>(x + (size_t)m * K + k);
+    if (!z)
         return xb;
-    const float2 z = *reinterpret_cast<const float2 *>(p.noise + k);
-    __nv_bfloat162 o = __floats2bfloat162_rn(__fmul_rn(bf16_bits_to_f32(xb & 0xFFFFu), z.x),
-                                             __fmul_rn(bf16_bits_to_f32(xb >> 16), z.y));
+    const float2 zz = *reinterpret_cast<const float2 *>(z + k);
+    __nv_bfloat162 o = __floats2bfloat162_rn(__fmul_rn(bf16_bits_to_f32(xb & 0xFFFFu), zz.x),
+                                             __fmul_rn(bf16_bits_to_f32(xb >> 16), zz.y));
     return *reinterpret_cast<uint32_t *>(&o);
 }
 
-// One warp: T partial for 8 LoRA columns over kLoraSteps*16 input columns
-// (bf16 mma.sync, tokens as the 16-row M dimension).  All loads first.
 template <int MP>
-__device__ void lora_down_unit(const DecodeParams &p, int unit)
+__global__ void __launch_bounds__(kThreads) decode_prologue_kernel(PrologueParams p)
 {
-    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-    const int jg = unit % p.NJG, sl = unit / p.NJG;
+    pdl_launch_dependents();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if ((int)blockIdx.x < p.conv_blocks) {
+        const int unit = blockIdx.x * kWarps + warp;
+        if (unit < MP * p.NC)
+            convert_unit<MP>(p, unit % MP, unit / MP);
+        return;
+    }
+    // LoRA down-projection: block (jg, slice) -> 8 columns of T over 512 inputs
+    __shared__ float s_c[kWarps][32][4];
+    __shared__ bool s_last;
+    const int lb = blockIdx.x - p.conv_blocks;
+    const int jg = lb % p.NJG, sl = lb / p.NJG;
+    const int g = lane >> 2, t = lane & 3;
     const int j0 = jg * 8, jrow = j0 + g;
-    const int ka = sl * kLoraSteps * 16;
-    uint32_t a[kLoraSteps][4], b[kLoraSteps][2];
+    const int ka = sl * kLoraSlice + warp * 64;
+    uint32_t a[4][4], b[4][2];
 #pragma unroll
-    for (int q = 0; q < kLoraSteps; q++) {
+    for (int q = 0; q < 4; q++) {
         const int k0 = ka + 16 * q;
-        a[q][0] = xprime_pair(p, g, k0 + 2 * t);
-        a[q][1] = MP > 8 ? xprime_pair(p, g + 8, k0 + 2 * t) : 0u;
-        a[q][2] = xprime_pair(p, g, k0 + 2 * t + 8);
-        a[q][3] = MP > 8 ? xprime_pair(p, g + 8, k0 + 2 * t + 8) : 0u;
+        a[q][0] = xprime_pair(p.x, p.noise, p.M, p.K, g, k0 + 2 * t);
+        a[q][1] = MP > 8 ? xprime_pair(p.x, p.noise, p.M, p.K, g + 8, k0 + 2 * t) : 0u;
+        a[q][2] = xprime_pair(p.x, p.noise, p.M, p.K, g, k0 + 2 * t + 8);
+        a[q][3] = MP > 8 ? xprime_pair(p.x, p.noise, p.M, p.K, g + 8, k0 + 2 * t + 8) : 0u;
         b[q][0] = b[q][1] = 0u;
         if (jrow < p.r && k0 < p.K) {
             const uint16_t *arow = p.lora_a + (size_t)jrow * p.K;
@@ -187,33 +197,74 @@ __device__ void lora_down_unit(const DecodeParams &p, int unit)
     }
     float c[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int q = 0; q < kLoraSteps; q++)
+    for (int q = 0; q < 4; q++)
         mma_bf16_16816(c, a[q], b[q][0], b[q][1]);
-    float *dst = p.tpart + (size_t)sl * MP * p.r;
-    const int j = j0 + 2 * t;
-    if (j < p.r) {
-        dst[g * p.r + j] = c[0];
-        if (MP > 8)
-            dst[(g + 8) * p.r + j] = c[2];
+#pragma unroll
+    for (int q = 0; q < 4; q++)
+        s_c[warp][lane][q] = c[q];
+    __syncthreads();
+    if (warp == 0) {
+        float sum[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int w = 0; w < kWarps; w++)
+#pragma unroll
+            for (int q = 0; q < 4; q++)
+                sum[q] += s_c[w][lane][q];
+        float *dst = p.tpart + (size_t)sl * MP * p.r;
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+            const int m = g + 8 * (q >> 1), j = j0 + 2 * t + (q & 1);
+            if (m < MP && j < p.r)
+                dst[m * p.r + j] = sum[q];
+        }
+        __threadfence();
     }
-    if (j + 1 < p.r) {
-        dst[g * p.r + j + 1] = c[1];
-        if (MP > 8)
-            dst[(g + 8) * p.r + j + 1] = c[3];
+    __syncthreads();
+    if (threadIdx.x == 0)
+        s_last = atomicAdd(&p.jcnt[jg], 1u) == (uint32_t)p.NS - 1;
+    __syncthreads();
+    if (s_last) {
+        __threadfence();
+        for (int e = threadIdx.x; e < MP * 8; e += kThreads) {
+            const int m = e / 8, j = j0 + e % 8;
+            if (j < p.r) {
+                float sum = 0.0f;
+                for (int q = 0; q < p.NS; q++)
+                    sum += __ldcg(p.tpart + ((size_t)q * MP + m) * p.r + j);
+                p.tfin[m * p.r + j] = sum;
+            }
+        }
+        if (threadIdx.x == 0)
+            p.jcnt[jg] = 0;
     }
 }
 
-// ---------------------------------------------------------------- phase 1
+// ================================================================ main kernel
+struct MainParams {
+    int M, N, K, r;
+    const uint8_t *codes, *scales;
+    const float *tensor_scale;
+    const uint16_t *lora_b;
+    float lora_scale;
+    const uint4 *xh;
+    const float *fac;
+    const float *tfin;
+    float *part;        // [R][maxseg][MP][rows]
+    uint32_t *tcnt;     // [R] arrival counters
+    void *y;
+    int y_fp32;
+    int S, R, U, maxseg;
+};
+
 struct Stage {
     uint2 c[2][2];      // [m-tile][row g / row g+8] 8 code bytes (16 columns)
     uint32_t sc[2][2];  // matching block-scale bytes
 };
 
-__device__ __forceinline__ void load_stage(const DecodeParams &p, Stage &st, int u)
+template <int RG>
+__device__ __forceinline__ void load_stage(const MainParams &p, Stage &st, int rt, int s, int rg)
 {
     const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-    const int rt = u / p.S, s = u - rt * p.S;
-    const int row_base = rt * kTileRows + (threadIdx.x >> 5) * 32;
+    const int row_base = rt * (32 * RG) + rg * 32;
     const int kcol = s * kStep + 16 * t;
 #pragma unroll
     for (int i = 0; i < 2; i++)
@@ -231,8 +282,7 @@ __device__ __forceinline__ void load_stage(const DecodeParams &p, Stage &st, int
 }
 
 template <int MP>
-__device__ __forceinline__ void compute_stage(const Stage &st, const uint4 *xs,
-                                              float (&cacc)[2][MP / 8][4])
+__device__ __forceinline__ void compute_stage(const Stage &st, const uint4 *xs, float (&cacc)[2][MP / 8][4])
 {
     constexpr int NT = MP / 8;
     const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
@@ -268,14 +318,14 @@ __device__ __forceinline__ void compute_stage(const Stage &st, const uint4 *xs,
 }
 
 template <int MP>
-__device__ __forceinline__ void flush_chunk(const DecodeParams &p, int chunk, float (&acc)[2][MP / 8][4],
+__device__ __forceinline__ void flush_chunk(const float *fac, int chunk, float (&acc)[2][MP / 8][4],
                                             float (&cacc)[2][MP / 8][4])
 {
     constexpr int NT = MP / 8;
     const int t = threadIdx.x & 3;
 #pragma unroll
     for (int nt = 0; nt < NT; nt++) {
-        const float2 f = *reinterpret_cast<const float2 *>(p.fac + chunk * MP + nt * 8 + 2 * t);
+        const float2 f = *reinterpret_cast<const float2 *>(fac + chunk * MP + nt * 8 + 2 * t);
 #pragma unroll
         for (int i = 0; i < 2; i++) {
             acc[i][nt][0] = __fmaf_rn(cacc[i][nt][0], f.x, acc[i][nt][0]);
@@ -287,66 +337,125 @@ __device__ __forceinline__ void flush_chunk(const DecodeParams &p, int chunk, fl
     }
 }
 
-template <int MP>
-__device__ __forceinline__ void write_partial(const DecodeParams &p, int rt, int slot,
-                                              float (&acc)[2][MP / 8][4])
+// The block's share of the unit range, cut into per-tile segments; warp
+// (rg, kl) takes rows rg*32.. of every tile and the kl-th contiguous part of
+// each segment's columns.
+struct SegCursor {
+    int seg, s, end;  // current segment, step, end step of this warp's part
+};
+
+__device__ __forceinline__ void seg_part(int u_begin, int u_end, int S, int seg, int kl, int KL, int &rt, int &a,
+                                         int &b)
 {
-    constexpr int NT = MP / 8;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-    float *dst = p.part + ((size_t)(rt * p.maxseg + slot) * MP) * kTileRows;
-#pragma unroll
-    for (int i = 0; i < 2; i++)
-#pragma unroll
-        for (int nt = 0; nt < NT; nt++)
-#pragma unroll
-            for (int q = 0; q < 4; q++) {
-                const int row = warp * 32 + 16 * i + g + 8 * (q >> 1);
-                const int tok = nt * 8 + 2 * t + (q & 1);
-                dst[tok * kTileRows + row] = acc[i][nt][q];
-                acc[i][nt][q] = 0.0f;
-            }
+    const int rt0 = u_begin / S;
+    rt = rt0 + seg;
+    const int sa = (seg == 0) ? u_begin - rt0 * S : 0;
+    const int last = (u_end - 1) / S;
+    const int sb = (rt == last) ? (u_end - 1) - last * S + 1 : S;
+    const int L = sb - sa;
+    a = sa + (int)((long long)L * kl / KL);
+    b = sa + (int)((long long)L * (kl + 1) / KL);
 }
 
-// ---------------------------------------------------------------- kernel
 template <int MP>
-__global__ void __launch_bounds__(kThreads, 2) decode_gemm_kernel(DecodeParams p)
+constexpr size_t main_smem_bytes()
+{
+    // X' staging + per-warp partial tiles (KL x ROWS = 256 for every RG) + T
+    return (size_t)kStageSteps * 2 * MP * 4 * 16 + (size_t)kMaxSeg * kThreads * MP * 4 + (size_t)MP * kMaxRSmem * 4;
+}
+
+template <int MP, int RG>
+__device__ __forceinline__ void decode_range(const MainParams &p, int u_begin, int u_end, bool first_range,
+                                             bool &t_loaded)
 {
     constexpr int NT = MP / 8;
-    __shared__ __align__(16) uint4 s_x[kMaxUnitsPerBlock * 2 * MP * 4];  // X' of this block's steps
-    __shared__ float s_t_lora[MP * kMaxR / 4];                            // T (phase 2), r <= 64 here
-    const int P = gridDim.x, bid = blockIdx.x;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int gwarp = bid * kWarps + warp, nwarps = P * kWarps;
-    const int u_begin = (int)((long long)bid * p.U / P), u_end = (int)((long long)(bid + 1) * p.U / P);
+    constexpr int KL = kWarps / RG;
+    constexpr int ROWS = 32 * RG;
+    extern __shared__ __align__(16) uint8_t smem_dyn[];
+    uint4 *s_x = reinterpret_cast<uint4 *>(smem_dyn);  // X' of this block's steps
+    float(*s_red)[KL][MP][ROWS] = reinterpret_cast<float(*)[KL][MP][ROWS]>(
+        smem_dyn + (size_t)kStageSteps * 2 * MP * 4 * 16);  // per-warp partial tiles
+    float *s_T = reinterpret_cast<float *>(smem_dyn + (size_t)kStageSteps * 2 * MP * 4 * 16 +
+                                           (size_t)kMaxSeg * KL * MP * ROWS * 4);
+    __shared__ bool s_flag;
 
-    // start streaming this block's first weight units before anything else
+    const int P = gridDim.x, bid = blockIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    const int rg = warp % RG, kl = warp / RG;
+    const int rt_first = u_begin / p.S, nseg = (u_end - 1) / p.S - rt_first + 1;
+
+    // cursors over this warp's steps: ld runs kDepth steps ahead of cm
+    SegCursor ld{0, 0, 0};
+    {
+        int rt, a, b;
+        seg_part(u_begin, u_end, p.S, 0, kl, KL, rt, a, b);
+        ld = {0, a, b};
+    }
+    auto advance = [&](SegCursor &c) {
+        c.s++;
+        while (c.s >= c.end && c.seg < nseg) {
+            c.seg++;
+            if (c.seg >= nseg)
+                break;
+            int rt, a, b;
+            seg_part(u_begin, u_end, p.S, c.seg, kl, KL, rt, a, b);
+            c.s = a;
+            c.end = b;
+        }
+    };
+    auto normalize = [&](SegCursor &c) {  // skip empty parts at the start
+        while (c.s >= c.end && c.seg < nseg) {
+            c.seg++;
+            if (c.seg >= nseg)
+                break;
+            int rt, a, b;
+            seg_part(u_begin, u_end, p.S, c.seg, kl, KL, rt, a, b);
+            c.s = a;
+            c.end = b;
+        }
+    };
+    normalize(ld);
+    SegCursor cm = ld;
+
+    // start streaming the first weight units before waiting for the prologue
     Stage st[kDepth];
 #pragma unroll
-    for (int d = 0; d < kDepth; d++)
-        if (u_begin + d < u_end)
-            load_stage(p, st[d], u_begin + d);
-
-    // phase 0: X' -> scaled f16 in fragment order; LoRA down partial sums
-    for (int unit = gwarp; unit < MP * p.NC; unit += nwarps)
-        convert_unit<MP>(p, unit % MP, unit / MP);
-    if (p.r > 0)
-        for (int unit = nwarps - 1 - gwarp; unit < p.NJG * p.NS; unit += nwarps)
-            lora_down_unit<MP>(p, unit);
-    if (!grid_barrier(p.ctl, P))
-        return;
-
-    // phase 1: stage X' for this block's units (when they fit), then stream W
-    const bool staged = u_end - u_begin <= kMaxUnitsPerBlock;
-    if (staged) {
-        const int nu = u_end - u_begin;
-        for (int i = threadIdx.x; i < nu * 2 * MP * 4; i += kThreads) {
-            const int uo = i / (2 * MP * 4), rem = i % (2 * MP * 4);
-            const int u = u_begin + uo;
-            const int s = u % p.S;
-            s_x[i] = p.xh[(size_t)s * 2 * MP * 4 + rem];
+    for (int d = 0; d < kDepth; d++) {
+        if (ld.seg < nseg) {
+            load_stage<RG>(p, st[d], rt_first + ld.seg, ld.s, rg);
+            advance(ld);
         }
-        __syncthreads();
     }
+    if (first_range)
+        pdl_wait();
+    __syncthreads();  // shared buffers of the previous range are free
+
+    // X' of the block's steps (all of its segments) into shared memory
+    int nsteps = 0, off0 = 0, off1 = 0, off2 = 0;  // staged index of step s in segment j = off_j + s
+    for (int j = 0; j < nseg && j < kMaxSeg; j++) {
+        int rt, a, b;
+        seg_part(u_begin, u_end, p.S, j, 0, 1, rt, a, b);
+        const int o = nsteps - a;
+        off0 = j == 0 ? o : off0;
+        off1 = j == 1 ? o : off1;
+        off2 = j == 2 ? o : off2;
+        nsteps += b - a;
+    }
+    const bool staged = nsteps <= kStageSteps;
+    if (staged) {
+        for (int j = 0, base = 0; j < nseg; j++) {
+            int rt, a, b;
+            seg_part(u_begin, u_end, p.S, j, 0, 1, rt, a, b);
+            const int n = (b - a) * 2 * MP * 4;
+            for (int i = threadIdx.x; i < n; i += kThreads)
+                s_x[base * 2 * MP * 4 + i] = p.xh[(size_t)a * 2 * MP * 4 + i];
+            base += b - a;
+        }
+    }
+    for (int i = threadIdx.x; i < kMaxSeg * KL * MP * ROWS; i += kThreads)
+        (&s_red[0][0][0][0])[i] = 0.0f;  // warps with an empty share leave zeros
+    __syncthreads();
+
     float acc[2][NT][4], cacc[2][NT][4];
 #pragma unroll
     for (int i = 0; i < 2; i++)
@@ -355,100 +464,167 @@ __global__ void __launch_bounds__(kThreads, 2) decode_gemm_kernel(DecodeParams p
 #pragma unroll
             for (int q = 0; q < 4; q++)
                 acc[i][nt][q] = cacc[i][nt][q] = 0.0f;
-    for (int u0 = u_begin; u0 < u_end; u0 += kDepth) {
+
+    auto store_warp_partial = [&](int seg) {
+#pragma unroll
+        for (int i = 0; i < 2; i++)
+#pragma unroll
+            for (int nt = 0; nt < NT; nt++)
+#pragma unroll
+                for (int q = 0; q < 4; q++) {
+                    const int row = rg * 32 + 16 * i + g + 8 * (q >> 1);
+                    const int tok = nt * 8 + 2 * t + (q & 1);
+                    s_red[seg][kl][tok][row] = acc[i][nt][q];
+                    acc[i][nt][q] = 0.0f;
+                }
+    };
+
+    // main loop over this warp's steps, kDepth at a time (static register indices)
+    while (cm.seg < nseg) {
 #pragma unroll
         for (int d = 0; d < kDepth; d++) {
-            const int u = u0 + d;
-            if (u < u_end) {
-                const int rt = u / p.S, s = u - rt * p.S;
-                const uint4 *xs = staged ? s_x + (size_t)(u - u_begin) * 2 * MP * 4
+            if (cm.seg < nseg) {
+                const int seg = cm.seg, s = cm.s;
+                const int soff = seg == 0 ? off0 : (seg == 1 ? off1 : off2);
+                const uint4 *xs = staged ? s_x + (size_t)(soff + s) * 2 * MP * 4
                                          : p.xh + (size_t)s * 2 * MP * 4;
                 compute_stage<MP>(st[d], xs, cacc);
-                if (u + kDepth < u_end)
-                    load_stage(p, st[d], u + kDepth);
-                const bool seg_end = (s == p.S - 1) || (u == u_end - 1);
-                if ((s % kStepsPerChunk) == kStepsPerChunk - 1 || seg_end)
-                    flush_chunk<MP>(p, s / kStepsPerChunk, acc, cacc);
-                if (seg_end)
-                    write_partial<MP>(p, rt, bid - owner_of(rt * p.S, p.U, P), acc);
-            }
-        }
-    }
-    // T = sum of the LoRA partial sums: one warp per element, fixed order
-    if (p.r > 0) {
-        const int total = MP * p.r;
-        for (int e = gwarp; e < total; e += nwarps) {
-            float s = 0.0f;
-            for (int sl = lane; sl < p.NS; sl += 32)
-                s += p.tpart[(size_t)sl * total + e];
-#pragma unroll
-            for (int off = 16; off >= 1; off >>= 1)
-                s += __shfl_xor_sync(0xffffffffu, s, off);
-            if (lane == 0)
-                p.tfin[e] = s;
-        }
-    }
-    if (!grid_barrier(p.ctl, P))
-        return;
-
-    // phase 2: split-K reduction in fixed order + epilogue, one thread per output
-    const int r = p.r;
-    float *sT = s_t_lora;
-    const bool t_in_smem = MP * r <= MP * kMaxR / 4;
-    if (r > 0 && t_in_smem) {
-        for (int i = threadIdx.x; i < MP * r; i += kThreads)
-            sT[i] = p.tfin[i];
-        __syncthreads();
-    }
-    const float *T = t_in_smem ? sT : p.tfin;
-    const float s_t = *p.tensor_scale;
-    const long long total = (long long)p.M * p.N;
-    for (long long o = (long long)bid * kThreads + threadIdx.x; o < total; o += (long long)P * kThreads) {
-        const int m = (int)(o / p.N), n = (int)(o - (long long)m * p.N);
-        const int rt = n / kTileRows, row = n % kTileRows;
-        const int nseg = owner_of(rt * p.S + p.S - 1, p.U, P) - owner_of(rt * p.S, p.U, P) + 1;
-        const float *src = p.part + ((size_t)(rt * p.maxseg) * MP + m) * kTileRows + row;
-        float acc1 = 0.0f;
-#pragma unroll 8
-        for (int j = 0; j < nseg; j++)
-            acc1 += src[(size_t)j * MP * kTileRows];
-        float lora = 0.0f;
-        if (r > 0) {
-            const float *trow = T + m * r;
-            if ((r & 7) == 0) {
-                const uint4 *brow = reinterpret_cast<const uint4 *>(p.lora_b + (size_t)n * r);
-                for (int jj = 0; jj < r / 8; jj++) {
-                    const uint4 bv = brow[jj];
-                    const uint32_t bw[4] = {bv.x, bv.y, bv.z, bv.w};
-#pragma unroll
-                    for (int q = 0; q < 4; q++) {
-                        lora = __fmaf_rn(trow[8 * jj + 2 * q], bf16_bits_to_f32(bw[q] & 0xFFFFu), lora);
-                        lora = __fmaf_rn(trow[8 * jj + 2 * q + 1], bf16_bits_to_f32(bw[q] >> 16), lora);
-                    }
+                if (ld.seg < nseg) {
+                    load_stage<RG>(p, st[d], rt_first + ld.seg, ld.s, rg);
+                    advance(ld);
                 }
-            } else {
-                const uint16_t *brow = p.lora_b + (size_t)n * r;
-                for (int jj = 0; jj < r; jj++)
-                    lora = __fmaf_rn(trow[jj], bf16_bits_to_f32(brow[jj]), lora);
+                advance(cm);
+                const bool seg_end = cm.seg != seg;
+                if ((s % kStepsPerChunk) == kStepsPerChunk - 1 || seg_end)
+                    flush_chunk<MP>(p.fac, s / kStepsPerChunk, acc, cacc);
+                if (seg_end && seg < kMaxSeg)
+                    store_warp_partial(seg);
             }
         }
-        const float yv = __fmaf_rn(s_t, acc1, p.lora_scale * lora);
-        if (p.y_fp32)
-            reinterpret_cast<float *>(p.y)[o] = yv;
-        else
-            reinterpret_cast<__nv_bfloat16 *>(p.y)[o] = __float2bfloat16_rn(yv);
+    }
+    __syncthreads();
+
+    // per tile: sum the warps' partials (fixed order); finish or hand over
+    const float s_t = *p.tensor_scale;
+    const int r = p.r;
+    for (int j = 0; j < nseg && j < kMaxSeg; j++) {
+        const int rt = rt_first + j;
+        const int first = owner_of(rt * p.S, p.U, P), last = owner_of(rt * p.S + p.S - 1, p.U, P);
+        const int cover = last - first + 1;
+        // this block's partial tile (token-major) -> registers of threads (tok, row)
+        if (cover > 1) {
+            float *dst = p.part + ((size_t)(rt * p.maxseg + (bid - first)) * MP) * ROWS;
+            for (int e = threadIdx.x; e < MP * ROWS; e += kThreads) {
+                const int tok = e / ROWS, row = e % ROWS;
+                float v = 0.0f;
+#pragma unroll
+                for (int k = 0; k < KL; k++)
+                    v += s_red[j][k][tok][row];
+                dst[e] = v;
+            }
+            __threadfence();
+            __syncthreads();
+            if (threadIdx.x == 0)
+                s_flag = atomicAdd(&p.tcnt[rt], 1u) == (uint32_t)cover - 1;
+            __syncthreads();
+            if (!s_flag)
+                continue;
+            __threadfence();
+        }
+        // epilogue for tile rt: Y = s_t * acc + s * T B^T
+        if (!t_loaded && r > 0 && r <= kMaxRSmem) {
+            for (int e = threadIdx.x; e < MP * r; e += kThreads)
+                s_T[e] = p.tfin[e];
+            __syncthreads();
+            t_loaded = true;
+        }
+        const float *T = r <= kMaxRSmem ? s_T : p.tfin;
+        for (int e = threadIdx.x; e < p.M * ROWS; e += kThreads) {
+            const int m = e / ROWS, row = e % ROWS;
+            const int n = rt * ROWS + row;
+            if (n >= p.N)
+                continue;
+            float a1 = 0.0f;
+            if (cover > 1) {
+                const float *src = p.part + ((size_t)(rt * p.maxseg) * MP + m) * ROWS + row;
+                for (int k = 0; k < cover; k++)
+                    a1 += __ldcg(src + (size_t)k * MP * ROWS);
+            } else {
+#pragma unroll
+                for (int k = 0; k < KL; k++)
+                    a1 += s_red[j][k][m][row];
+            }
+            float lora = 0.0f;
+            if (r > 0) {
+                const float *trow = T + m * r;
+                if ((r & 7) == 0) {
+                    const uint4 *brow = reinterpret_cast<const uint4 *>(p.lora_b + (size_t)n * r);
+                    for (int jj = 0; jj < r / 8; jj++) {
+                        const uint4 bv = brow[jj];
+                        const uint32_t bw[4] = {bv.x, bv.y, bv.z, bv.w};
+#pragma unroll
+                        for (int q = 0; q < 4; q++) {
+                            lora = __fmaf_rn(trow[8 * jj + 2 * q], bf16_bits_to_f32(bw[q] & 0xFFFFu), lora);
+                            lora = __fmaf_rn(trow[8 * jj + 2 * q + 1], bf16_bits_to_f32(bw[q] >> 16), lora);
+                        }
+                    }
+                } else {
+                    const uint16_t *brow = p.lora_b + (size_t)n * r;
+                    for (int jj = 0; jj < r; jj++)
+                        lora = __fmaf_rn(trow[jj], bf16_bits_to_f32(brow[jj]), lora);
+                }
+            }
+            const float yv = __fmaf_rn(s_t, a1, p.lora_scale * lora);
+            const size_t o = (size_t)m * p.N + n;
+            if (p.y_fp32)
+                reinterpret_cast<float *>(p.y)[o] = yv;
+            else
+                reinterpret_cast<__nv_bfloat16 *>(p.y)[o] = __float2bfloat16_rn(yv);
+        }
+        if (cover > 1 && threadIdx.x == 0)
+            p.tcnt[rt] = 0;
     }
 }
 
-// ---------------------------------------------------------------- host side
+template <int MP, int RG>
+__global__ void __launch_bounds__(kThreads, 2) decode_main_kernel(MainParams p)
+{
+    const int P = gridDim.x, bid = blockIdx.x;
+    const int u_begin = (int)((long long)bid * p.U / P), u_end = (int)((long long)(bid + 1) * p.U / P);
+    bool t_loaded = false;
+    // a block whose share touches more than kMaxSeg tiles works through it
+    // in ranges of at most kMaxSeg tiles
+    for (int ub = u_begin; ub < u_end;) {
+        const int ue = min(u_end, (ub / p.S + kMaxSeg) * p.S);
+        decode_range<MP, RG>(p, ub, ue, ub == u_begin, t_loaded);
+        ub = ue;
+    }
+}
+
+// ================================================================ host side
 struct DecodePlan {
-    int MP, P, S, NC, R, NS, NJG, maxseg, U;
-    size_t off_xh, off_fac, off_tpart, off_tfin, off_part, total;
+    int MP, RG, P, S, NC, R, NS, NJG, maxseg, U, conv_blocks;
+    size_t off_xh, off_fac, off_tpart, off_tfin, off_jcnt, off_tcnt, off_part, total;
 };
 
 static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 static int host_owner(int u, int U, int P) { return (int)(((long long)(u + 1) * P - 1) / U); }
+
+// Tiles a block touches at most, and the deepest split of a tile over blocks.
+static void split_stats(int R, int S, int P, int &max_tiles, int &max_cover)
+{
+    const long long U = (long long)R * S;
+    max_tiles = 0;
+    max_cover = 0;
+    for (int b = 0; b < P; b++) {
+        const int ub = (int)(b * U / P), ue = (int)((b + 1) * U / P);
+        if (ue > ub)
+            max_tiles = std::max(max_tiles, (ue - 1) / S - ub / S + 1);
+    }
+    for (int rt = 0; rt < R; rt++)
+        max_cover = std::max(max_cover, host_owner(rt * S + S - 1, (int)U, P) - host_owner(rt * S, (int)U, P) + 1);
+}
 
 static bool make_plan(int64_t M, int64_t N, int64_t K, int64_t r, const DeviceInfo &dev, DecodePlan &pl)
 {
@@ -458,22 +634,42 @@ static bool make_plan(int64_t M, int64_t N, int64_t K, int64_t r, const DeviceIn
         return false;
     pl.S = (int)((K + kStep - 1) / kStep);
     pl.NC = (int)((K + kChunk - 1) / kChunk);
-    pl.R = (int)((N + kTileRows - 1) / kTileRows);
-    const long long U = (long long)pl.R * pl.S;
-    if (U > (1LL << 30))
-        return false;
-    pl.U = (int)U;
-    // every block gets at least one unit, so every partial slot is written
-    pl.P = (int)std::min<long long>((long long)dev.num_sms * bps, U);
-    pl.NS = (int)((K + kLoraSteps * 16 - 1) / (kLoraSteps * 16));
-    pl.NJG = (int)((r + 7) / 8);
-    pl.maxseg = 1;
-    for (int rt = 0; rt < pl.R; rt++) {
-        const int a = host_owner(rt * pl.S, pl.U, pl.P);
-        const int b = host_owner(rt * pl.S + pl.S - 1, pl.U, pl.P);
-        pl.maxseg = std::max(pl.maxseg, b - a + 1);
+    // tile height 32*RG: the tallest tile whose split over blocks stays <= 3
+    // (less X' traffic per weight), else the shortest (cheapest reduction)
+    pl.RG = 0;
+    int fallback = 0;
+    for (int rg : {8, 4, 2}) {
+        const int R = (int)((N + 32 * rg - 1) / (32 * rg));
+        const long long U = (long long)R * pl.S;
+        if (U > (1LL << 30))
+            continue;
+        const int P = (int)std::min<long long>((long long)dev.num_sms * bps, U);
+        int max_tiles, max_cover;
+        split_stats(R, pl.S, P, max_tiles, max_cover);
+        fallback = rg;
+        if (max_cover <= 3) {
+            pl.RG = rg;
+            break;
+        }
     }
-    size_t off = kCtlBytes;
+    if (!pl.RG)
+        pl.RG = fallback;
+    if (!pl.RG)
+        return false;
+    const int rows = 32 * pl.RG;
+    pl.R = (int)((N + rows - 1) / rows);
+    pl.U = (int)((long long)pl.R * pl.S);
+    pl.P = (int)std::min<long long>((long long)dev.num_sms * bps, pl.U);
+    int max_tiles;
+    split_stats(pl.R, pl.S, pl.P, max_tiles, pl.maxseg);
+    pl.NS = (int)((K + kLoraSlice - 1) / kLoraSlice);
+    pl.NJG = (int)((r + 7) / 8);
+    pl.conv_blocks = (pl.MP * pl.NC + kWarps - 1) / kWarps;
+    if (pl.NJG + pl.R > kCounterWords)
+        return false;
+    pl.off_jcnt = kCtlBytes;
+    pl.off_tcnt = kCtlBytes + 4 * (size_t)pl.NJG;
+    size_t off = kWsHeaderBytes;
     pl.off_xh = off;
     off = align_up(off + (size_t)pl.NC * kStepsPerChunk * pl.MP * kStep * 2, 256);
     pl.off_fac = off;
@@ -483,20 +679,41 @@ static bool make_plan(int64_t M, int64_t N, int64_t K, int64_t r, const DeviceIn
     pl.off_tfin = off;
     off = align_up(off + (size_t)pl.MP * std::max<int64_t>(r, 1) * 4, 256);
     pl.off_part = off;
-    off = align_up(off + (size_t)pl.R * pl.maxseg * pl.MP * kTileRows * 4, 256);
+    off = align_up(off + (size_t)pl.R * pl.maxseg * pl.MP * rows * 4, 256);
     pl.total = off;
     return true;
 }
 
+template <int MP>
+static const void *main_kernel(int RG)
+{
+    switch (RG) {
+    case 8: return (const void *)decode_main_kernel<MP, 8>;
+    case 4: return (const void *)decode_main_kernel<MP, 4>;
+    default: return (const void *)decode_main_kernel<MP, 2>;
+    }
+}
+
 void query_decode_occupancy(DeviceInfo &dev)
 {
-    int b8 = 0, b16 = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b8, decode_gemm_kernel<8>, kThreads, 0) != cudaSuccess)
-        b8 = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b16, decode_gemm_kernel<16>, kThreads, 0) != cudaSuccess)
-        b16 = 0;
-    dev.decode_blocks_per_sm[0] = std::min(b8, 2);
-    dev.decode_blocks_per_sm[1] = std::min(b16, 2);
+    int lo8 = 2, lo16 = 2;
+    for (int rg : {8, 4, 2}) {
+        int b8 = 0, b16 = 0;
+        if (cudaFuncSetAttribute(main_kernel<8>(rg), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)main_smem_bytes<8>()) != cudaSuccess ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b8, main_kernel<8>(rg), kThreads,
+                                                          main_smem_bytes<8>()) != cudaSuccess)
+            b8 = 0;
+        if (cudaFuncSetAttribute(main_kernel<16>(rg), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)main_smem_bytes<16>()) != cudaSuccess ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b16, main_kernel<16>(rg), kThreads,
+                                                          main_smem_bytes<16>()) != cudaSuccess)
+            b16 = 0;
+        lo8 = std::min(lo8, b8);
+        lo16 = std::min(lo16, b16);
+    }
+    dev.decode_blocks_per_sm[0] = lo8;
+    dev.decode_blocks_per_sm[1] = lo16;
 }
 
 size_t decode_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t r, const DeviceInfo &dev)
@@ -515,8 +732,32 @@ cudaError_t launch_decode_gemm(const GemmArgs &a, cudaStream_t s, const DeviceIn
         DecodePlan pl;
         if (!make_plan(Mg, a.N, a.K, a.r, dev, pl))
             return cudaErrorInvalidConfiguration;
-        DecodeParams p;
-        p.x = a.x + m0 * a.K;
+        PrologueParams pp;
+        pp.x = a.x + m0 * a.K;
+        pp.M = (int)Mg;
+        pp.K = (int)a.K;
+        pp.r = (int)a.r;
+        pp.lora_a = a.lora_a;
+        pp.noise = a.noise;
+        pp.xh = reinterpret_cast<uint4 *>(a.ws + pl.off_xh);
+        pp.fac = reinterpret_cast<float *>(a.ws + pl.off_fac);
+        pp.tpart = reinterpret_cast<float *>(a.ws + pl.off_tpart);
+        pp.tfin = reinterpret_cast<float *>(a.ws + pl.off_tfin);
+        pp.jcnt = reinterpret_cast<uint32_t *>(a.ws + pl.off_jcnt);
+        pp.NC = pl.NC;
+        pp.NS = pl.NS;
+        pp.NJG = pl.NJG;
+        pp.conv_blocks = pl.conv_blocks;
+        const int pro_blocks = pl.conv_blocks + (a.r > 0 ? pl.NJG * pl.NS : 0);
+        if (pl.MP == 8)
+            decode_prologue_kernel<8><<<pro_blocks, kThreads, 0, s>>>(pp);
+        else
+            decode_prologue_kernel<16><<<pro_blocks, kThreads, 0, s>>>(pp);
+        cudaError_t err = cudaGetLastError();
+        if (err != cudaSuccess)
+            return err;
+
+        MainParams p;
         p.M = (int)Mg;
         p.N = (int)a.N;
         p.K = (int)a.K;
@@ -524,33 +765,32 @@ cudaError_t launch_decode_gemm(const GemmArgs &a, cudaStream_t s, const DeviceIn
         p.codes = a.codes;
         p.scales = a.scales;
         p.tensor_scale = a.tensor_scale;
-        p.lora_a = a.lora_a;
         p.lora_b = a.lora_b;
         p.lora_scale = a.lora_scale;
-        p.noise = a.noise;
+        p.xh = pp.xh;
+        p.fac = pp.fac;
+        p.tfin = pp.tfin;
+        p.part = reinterpret_cast<float *>(a.ws + pl.off_part);
+        p.tcnt = reinterpret_cast<uint32_t *>(a.ws + pl.off_tcnt);
         p.y = a.y_fp32 ? (void *)((float *)a.y + m0 * a.N) : (void *)((uint16_t *)a.y + m0 * a.N);
         p.y_fp32 = a.y_fp32 ? 1 : 0;
-        p.ctl = reinterpret_cast<uint32_t *>(a.ws);
-        p.xh = reinterpret_cast<uint4 *>(a.ws + pl.off_xh);
-        p.fac = reinterpret_cast<float *>(a.ws + pl.off_fac);
-        p.tpart = reinterpret_cast<float *>(a.ws + pl.off_tpart);
-        p.tfin = reinterpret_cast<float *>(a.ws + pl.off_tfin);
-        p.part = reinterpret_cast<float *>(a.ws + pl.off_part);
         p.S = pl.S;
-        p.NC = pl.NC;
         p.R = pl.R;
-        p.NS = pl.NS;
-        p.NJG = pl.NJG;
-        p.maxseg = pl.maxseg;
         p.U = pl.U;
+        p.maxseg = pl.maxseg;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(pl.P);
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = pl.MP == 8 ? main_smem_bytes<8>() : main_smem_bytes<16>();
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
         void *args[] = {&p};
-        cudaError_t err;
-        if (pl.MP == 8)
-            err = cudaLaunchCooperativeKernel((const void *)decode_gemm_kernel<8>, dim3(pl.P), dim3(kThreads),
-                                              args, 0, s);
-        else
-            err = cudaLaunchCooperativeKernel((const void *)decode_gemm_kernel<16>, dim3(pl.P),
-                                              dim3(kThreads), args, 0, s);
+        const void *fn = pl.MP == 8 ? main_kernel<8>(pl.RG) : main_kernel<16>(pl.RG);
+        err = cudaLaunchKernelExC(&cfg, fn, args);
         if (err != cudaSuccess)
             return err;
     }
@@ -609,8 +849,8 @@ extern "C" nvfp4_status nvfp4_w4a16_lora_gemm_static(
     const size_t need = nvfp4_workspace_bytes(M, N, K, (lora_a_bf16 && lora_b_bf16) ? r : 0);
     if (need > nvfp4::kStaticWsBytes)
         return NVFP4_ERR_WORKSPACE;  // beyond the fixed scratch size
-    // every call shares the array: its control words must start at zero
-    if (cudaMemsetAsync(ws, 0, nvfp4::kCtlBytes, (cudaStream_t)stream) != cudaSuccess)
+    // every call shares the array: its control words and counters must start at zero
+    if (cudaMemsetAsync(ws, 0, nvfp4::kWsHeaderBytes, (cudaStream_t)stream) != cudaSuccess)
         return NVFP4_ERR_CUDA;
     return nvfp4_w4a16_lora_gemm(x_bf16, M, N, K, codes, scales_e4m3, tensor_scale, lora_a_bf16,
                                  lora_b_bf16, r, lora_scale, noise_fp32, y, y_dtype, ws,

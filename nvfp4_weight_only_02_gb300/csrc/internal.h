@@ -51,4 +51,17 @@ void query_decode_occupancy(DeviceInfo &dev);
 size_t decode_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t r, const DeviceInfo &dev);
 cudaError_t launch_decode_gemm(const GemmArgs &a, cudaStream_t s, const DeviceInfo &dev);
 
+// Tensor-core (tcgen05) path for many tokens; smaller M uses the decode kernel.
+constexpr int64_t kPrefillMinM = 64;
+bool prefill_supported(int64_t M, int64_t N, int64_t K, int64_t r);
+size_t prefill_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t r);
+cudaError_t launch_prefill_gemm(const GemmArgs &a, cudaStream_t s, const DeviceInfo &dev);
+
+// Workspace of nvfp4_w4a16_lora_gemm for these sizes (0: unsupported).
+inline size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t r, const DeviceInfo &dev)
+{
+    return prefill_supported(M, N, K, r) ? prefill_workspace_bytes(M, N, K, r)
+                                         : decode_workspace_bytes(M, N, K, r, dev);
+}
+
 }  // namespace nvfp4
