@@ -508,36 +508,52 @@ def run_reference(args):
 
 
 def run_kernel_case(case, reps):
-    """One operation, repeated: a small, self-contained target for ncu."""
+    """One operation, repeated and timed with CUDA events: a small,
+    self-contained target for ncu (quantize_up, gemm_up_M8, gemm_down_M16,
+    prefill, ...)."""
     import torch
 
     from nvfp4_weight_only_02_gb300 import binding as nv
     from nvfp4_weight_only_02_gb300 import synth
     nv.load()
-    kind, which, M = case.split("_") if case.startswith("gemm") else (case.split("_") + [0])[:3]
+    parts = case.split("_")
+    kind = parts[0]
+    which = parts[1] if len(parts) > 1 else "up"
     shape = UP if which == "up" else DOWN
     dev = lambda b: torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(torch.bfloat16).cuda()
     wb = synth.normal_weight(shape, 0.02, 0, outlier_frac=1e-3, outlier_mult=20.0)
     w = dev(wb)
-    ws = nv.new_workspace(nv.nvfp4_workspace_bytes(16, *shape, R_LORA))
+    M = int(parts[2][1:]) if kind == "gemm" else (16384 if kind == "prefill" else 0)
+    ws = nv.new_workspace(nv.nvfp4_workspace_bytes(max(M, 1), *shape, R_LORA))
     q = nv.quantize(w, workspace=ws)
     if kind == "quantize":
-        for _ in range(reps):
-            nv.nvfp4_quantize(w, q.codes, q.scales, q.tensor_scale, False, ws)
+        frozen = len(parts) > 2 and parts[2] == "frozen"
+        op = lambda: nv.nvfp4_quantize(w, q.codes, q.scales, q.tensor_scale, frozen, ws)
+        nbytes, flops = quant_bytes(*shape), 0.0
     else:
-        M = int(M[1:])
         a, b = synth.lora_pair(shape[0], shape[1], R_LORA, 0.01, 2)
+        a, b = dev(a), dev(b)
         z = torch.from_numpy(synth.noise_vector(shape[1], SIGMA, 3)).cuda()
         x = dev(synth.activations(M, shape[1], 10))
-        y = torch.empty((M, shape[0]), dtype=torch.float32, device="cuda")
-        for _ in range(reps):
-            nv.nvfp4_w4a16_lora_gemm(x, q.codes, q.scales, q.tensor_scale, dev(a), dev(b), LORA_SCALE,
-                                     z, y, ws)
+        ydt = torch.bfloat16 if kind == "prefill" else torch.float32
+        y = torch.empty((M, shape[0]), dtype=ydt, device="cuda")
+        op = lambda: nv.nvfp4_w4a16_lora_gemm(x, q.codes, q.scales, q.tensor_scale, a, b, LORA_SCALE, z, y, ws)
+        nbytes, flops = gemm_bytes(M, *shape, R_LORA), gemm_flops(M, *shape, R_LORA)
+    op()
     torch.cuda.synchronize()
+    s = torch.cuda.Event(enable_timing=True)
+    e = torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(reps):
+        op()
+    e.record()
+    torch.cuda.synchronize()
+    us = s.elapsed_time(e) * 1e3 / reps
     st = nv.nvfp4_get_device_status(ws)
     if st != nv.OK:
         raise RuntimeError(nv.status_string(st))
-    print(f"kernel case {case}: {reps} reps ok")
+    print(f"kernel case {case}: {reps} reps, {us:.2f} us/call, {nbytes / us / 1e3:.1f} GB/s, "
+          f"{flops / us / 1e6:.1f} TFLOP/s")
 
 
 def main():

@@ -112,6 +112,15 @@ nvfp4_status nvfp4_w4a16_lora_gemm(const void *x_bf16, int64_t M, int64_t N, int
                                    void *y, nvfp4_dtype y_dtype,
                                    void *workspace, size_t ws_bytes, void *stream);
 
+/* Diagnostics (no counterpart on the pages): make one of the library's
+ * bounded device-side waits run out on purpose -- which == 0: an mbarrier
+ * wait that no arrival completes; which == 1: a grid barrier expecting one
+ * block more than are launched.  The wait gives up after about two seconds
+ * and records NVFP4_ERR_TIMEOUT in the workspace status word (read it with
+ * nvfp4_get_device_status); the context stays usable.  workspace: >= 256
+ * bytes, zero-filled. */
+nvfp4_status nvfp4_wait_selftest(void *workspace, int which, void *stream);
+
 /* nvfp4_w4a16_lora_gemm without a workspace argument, for callers that
  * cannot allocate device memory: code running inside a host framework that
  * owns every device allocation and hands its plugins no scratch, or a

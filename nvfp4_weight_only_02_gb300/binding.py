@@ -25,7 +25,7 @@ OUT_BF16, OUT_FP32 = 0, 1
 EXPORTS = [
     "nvfp4_workspace_bytes", "nvfp4_quantize", "nvfp4_dequantize", "nvfp4_w4a16_lora_gemm",
     "nvfp4_round_scales", "nvfp4_get_device_status", "nvfp4_status_string", "nvfp4_encode_debug",
-    "nvfp4_quotient_check", "nvfp4_w4a16_lora_gemm_static",
+    "nvfp4_quotient_check", "nvfp4_w4a16_lora_gemm_static", "nvfp4_wait_selftest",
 ]
 
 
@@ -66,6 +66,7 @@ def load(build_if_missing: bool = True):
             "nvfp4_quotient_check": (st, [u32, u32, P, P]),
             "nvfp4_w4a16_lora_gemm_static": (st, [P, i64, i64, i64, P, P, P, P, P, i64, ctypes.c_float,
                                                   P, P, ctypes.c_int, P]),
+            "nvfp4_wait_selftest": (st, [P, ctypes.c_int, P]),
         }
         for name, (res, args) in sig.items():
             f = getattr(lib, name)
@@ -190,6 +191,10 @@ def nvfp4_encode_debug(x: torch.Tensor, which: int) -> torch.Tensor:
     st = load().nvfp4_encode_debug(_ptr(x), x.numel(), int(which), _ptr(out), _stream())
     _check(st, "nvfp4_encode_debug")
     return out
+
+
+def nvfp4_wait_selftest(workspace: torch.Tensor, which: int):
+    _check(load().nvfp4_wait_selftest(_ptr(workspace), int(which), _stream()), "nvfp4_wait_selftest")
 
 
 def nvfp4_quotient_check(sig_lo: int, sig_hi: int) -> int:

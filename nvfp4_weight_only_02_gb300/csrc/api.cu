@@ -34,6 +34,7 @@ const DeviceInfo *device_info(nvfp4_status *st)
             return nullptr;
         }
         query_decode_occupancy(di);
+        query_quantize_occupancy(di);
         di.device = d;
     }
     *st = NVFP4_OK;

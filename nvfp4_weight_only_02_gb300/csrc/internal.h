@@ -12,7 +12,8 @@ struct DeviceInfo {
     int device = -1;
     int num_sms = 0;
     int cc_major = 0, cc_minor = 0;
-    int decode_blocks_per_sm[2] = {0, 0};  // cooperative residency of the decode kernel (MP 8, 16)
+    int decode_blocks_per_sm[2] = {0, 0};  // residency of the decode main kernel (MP 8, 16)
+    int fused_quant_blocks = 0;            // grid of the fused dynamic quantiser (0: unavailable)
 };
 
 // Cached per-device facts; nullptr (and *st set) when the device is unusable.
@@ -44,6 +45,9 @@ struct GemmArgs {
     uint8_t *ws;
     size_t ws_bytes;
 };
+
+// Occupancy of the fused quantiser; called once per device by device_info().
+void query_quantize_occupancy(DeviceInfo &dev);
 
 // Occupancy of the decode kernels; called once per device by device_info().
 void query_decode_occupancy(DeviceInfo &dev);

@@ -204,6 +204,149 @@ __global__ void __launch_bounds__(256) quantize_kernel(const uint4 *__restrict__
     }
 }
 
+// ------------------------------------------------------------------ fused dynamic quantise
+// Dynamic mode in one persistent cooperative kernel: pass 1 reads the block's
+// contiguous share of W once for the tensor amax and keeps the last
+// kFusedCacheBlocks 16-element blocks of the share in shared memory; after
+// one grid barrier, pass 2 quantises the share from its end backwards, so it
+// starts with the blocks held in shared memory and continues with those
+// pass 1 read last, which are the ones still in L2.
+constexpr int kFusedThreads = 1024;
+constexpr int kFusedCacheBlocks = 6144;  // 192 KB of bf16 per block
+
+__device__ __forceinline__ void quantize_block(uint4 v0, uint4 v1, float s_t, float d, bool d_fast, float rd,
+                                               const float *s_S, const float *s_R, uint2 &cw_out,
+                                               uint32_t &e_out, uint32_t *ctl)
+{
+    uint32_t m = absmax8(v0, v1);
+    m = max(m & 0xFFFFu, m >> 16);
+    uint32_t e = 0;
+    uint2 cw = make_uint2(0u, 0u);
+    if (m >= 0x7F80u) {
+        record_status(ctl, NVFP4_ERR_NONFINITE);
+    } else if (s_t != 0.0f) {
+        const float a_b = bf16_bits_to_f32(m);
+        if (!d_fast)
+            e = e4m3_encode_nonneg(__fdiv_rn(a_b, d));
+        else if (__fmul_rn(a_b, rd) >= 1024.0f)
+            e = 0x7E;
+        else
+            e = e4m3_encode_nonneg(quotient(a_b, d, rd));
+        const float S = s_S[e];
+        if (S != 0.0f) {
+            const float r = s_R[e];
+            const bool fast = r != 0.0f && __fmul_rn(a_b, r) < 0x1p20f;
+            cw.x = encode8(v0, S, r, fast);
+            cw.y = encode8(v1, S, r, fast);
+        }
+    }
+    cw_out = cw;
+    e_out = e;
+}
+
+__global__ void __launch_bounds__(kFusedThreads, 1)
+    quantize_fused_kernel(const uint4 *__restrict__ w, int64_t nblocks, float *__restrict__ tensor_scale,
+                          uint2 *__restrict__ codes, uint8_t *__restrict__ scales, uint32_t *__restrict__ ctl)
+{
+    extern __shared__ __align__(16) uint4 s_cache[];  // [kFusedCacheBlocks][2]
+    __shared__ float s_S[128], s_R[128];
+    __shared__ uint32_t s_m[kFusedThreads / 32];
+    __shared__ bool s_last;
+    const int P = gridDim.x, bid = blockIdx.x, tid = threadIdx.x;
+    const int64_t b0 = (int64_t)bid * nblocks / P, b1 = (int64_t)(bid + 1) * nblocks / P;
+    const int64_t cache_from = max(b0, b1 - (int64_t)kFusedCacheBlocks);
+
+    // pass 1: amax of the share; keep its tail in shared memory
+    uint32_t m = 0;
+    int64_t b = b0 + tid;
+    for (; b + kFusedThreads < b1; b += 2 * kFusedThreads) {
+        const uint4 a0 = ld_stream_u4(w + 2 * b), a1 = ld_stream_u4(w + 2 * b + 1);
+        const uint4 c0 = ld_stream_u4(w + 2 * (b + kFusedThreads)), c1 = ld_stream_u4(w + 2 * (b + kFusedThreads) + 1);
+        m = __vmaxu2(m, __vmaxu2(absmax8(a0, a1), absmax8(c0, c1)));
+        if (b >= cache_from) {
+            s_cache[2 * (b - cache_from)] = a0;
+            s_cache[2 * (b - cache_from) + 1] = a1;
+        }
+        if (b + kFusedThreads >= cache_from) {
+            s_cache[2 * (b + kFusedThreads - cache_from)] = c0;
+            s_cache[2 * (b + kFusedThreads - cache_from) + 1] = c1;
+        }
+    }
+    for (; b < b1; b += kFusedThreads) {
+        const uint4 a0 = ld_stream_u4(w + 2 * b), a1 = ld_stream_u4(w + 2 * b + 1);
+        m = __vmaxu2(m, absmax8(a0, a1));
+        if (b >= cache_from) {
+            s_cache[2 * (b - cache_from)] = a0;
+            s_cache[2 * (b - cache_from) + 1] = a1;
+        }
+    }
+    m = max(m & 0xFFFFu, m >> 16);
+    m = __reduce_max_sync(0xffffffffu, m);
+    if ((tid & 31) == 0)
+        s_m[tid >> 5] = m;
+    __syncthreads();
+    if (tid == 0) {
+        uint32_t bm = 0;
+        for (int k = 0; k < kFusedThreads / 32; k++)
+            bm = max(bm, s_m[k]);
+        atomicMax(&ctl[CTL_AMAX], bm);
+    }
+    if (!grid_barrier(ctl, P))
+        return;
+
+    // s_t = amax / 2688, identical in every block
+    const uint32_t a_bits = *(volatile uint32_t *)&ctl[CTL_AMAX];
+    float s_t;
+    if (a_bits >= 0x7F80u) {
+        if (bid == 0 && tid == 0) {
+            record_status(ctl, NVFP4_ERR_NONFINITE);
+            *tensor_scale = __uint_as_float(0x7FC00000u);
+        }
+        s_t = 0.0f;
+    } else {
+        s_t = __fdiv_rn(bf16_bits_to_f32(a_bits), 2688.0f);
+        if (bid == 0 && tid == 0)
+            *tensor_scale = s_t;
+    }
+    for (int e = tid; e < 128; e += kFusedThreads) {
+        const float S = __fmul_rn(e4m3_to_f32((uint32_t)e), s_t);
+        s_S[e] = S;
+        s_R[e] = fast_quotient_domain(S) ? __frcp_rn(S) : 0.0f;
+    }
+    const float d = __fmul_rn(6.0f, s_t);
+    const bool d_fast = fast_quotient_domain(d);
+    const float rd = d_fast ? __frcp_rn(d) : 0.0f;
+    __syncthreads();
+
+    // pass 2: from the end of the share backwards
+    for (int64_t bb = b1 - 1 - tid; bb >= b0; bb -= kFusedThreads) {
+        uint4 v0, v1;
+        if (bb >= cache_from) {
+            v0 = s_cache[2 * (bb - cache_from)];
+            v1 = s_cache[2 * (bb - cache_from) + 1];
+        } else {
+            v0 = ld_stream_u4(w + 2 * bb);
+            v1 = ld_stream_u4(w + 2 * bb + 1);
+        }
+        uint2 cw;
+        uint32_t e;
+        quantize_block(v0, v1, s_t, d, d_fast, rd, s_S, s_R, cw, e, ctl);
+        codes[bb] = cw;
+        scales[bb] = (uint8_t)e;
+    }
+
+    // the last block out leaves the amax word at zero for the next call
+    __syncthreads();
+    if (tid == 0) {
+        __threadfence();
+        s_last = atomicAdd(&ctl[CTL_AMAX_COUNT], 1u) == (uint32_t)P - 1;
+        if (s_last) {
+            ctl[CTL_AMAX] = 0;
+            ctl[CTL_AMAX_COUNT] = 0;
+        }
+    }
+}
+
 // ------------------------------------------------------------------ dequantise
 __global__ void __launch_bounds__(256) dequantize_kernel(const uint32_t *__restrict__ codes,
                                                          const uint8_t *__restrict__ scales,
@@ -314,6 +457,17 @@ cudaError_t launch_quantize(const void *w, int64_t N, int64_t K, uint8_t *codes,
                             const DeviceInfo &dev)
 {
     const int64_t nelem = N * K;
+    if (!given && dev.fused_quant_blocks > 0) {
+        const uint4 *wp = reinterpret_cast<const uint4 *>(w);
+        int64_t nblocks = nelem / 16;
+        float *tsp = tensor_scale;
+        uint2 *cp = reinterpret_cast<uint2 *>(codes);
+        uint8_t *sp = scales;
+        uint32_t *ctlp = ctl;
+        void *args[] = {&wp, &nblocks, &tsp, &cp, &sp, &ctlp};
+        return cudaLaunchCooperativeKernel((const void *)quantize_fused_kernel, dim3(dev.fused_quant_blocks),
+                                           dim3(kFusedThreads), args, kFusedCacheBlocks * 32, s);
+    }
     if (!given) {
         const int64_t nvec = nelem / 8;
         amax_kernel<<<grid_for(nvec, 256 * 4, dev.num_sms * 8), 256, 0, s>>>(
@@ -324,6 +478,17 @@ cudaError_t launch_quantize(const void *w, int64_t N, int64_t K, uint8_t *codes,
         reinterpret_cast<const uint4 *>(w), nblocks, tensor_scale,
         reinterpret_cast<uint2 *>(codes), scales, ctl);
     return cudaGetLastError();
+}
+
+void query_quantize_occupancy(DeviceInfo &dev)
+{
+    int b = 0;
+    if (cudaFuncSetAttribute(quantize_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kFusedCacheBlocks * 32) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, quantize_fused_kernel, kFusedThreads,
+                                                      kFusedCacheBlocks * 32) != cudaSuccess)
+        b = 0;
+    dev.fused_quant_blocks = b >= 1 ? dev.num_sms : 0;
 }
 
 cudaError_t launch_dequantize(const uint8_t *codes, const uint8_t *scales, const float *tensor_scale,
