@@ -43,8 +43,9 @@ def _assert_parity(nv, orc, bits, tensor_scale=None):
     assert bad_s.size == 0, f"{len(bad_s)} scale bytes differ, first {bad_s[:4].tolist()}"
     bad_c = np.argwhere(c_gpu != c_ref)
     assert bad_c.size == 0, f"{len(bad_c)} code bytes differ, first {bad_c[:4].tolist()}"
-    # control words are left at zero for the next call
-    assert not ws[:256].any()
+    # status, amax and arrival counters are left at zero for the next call
+    # (word 4, the grid-barrier generation, only ever counts up)
+    assert not ws[:16].any()
     return codes, scales, ts
 
 
