@@ -138,6 +138,13 @@ __device__ __forceinline__ uint2 ld_stream_u2(const void *p)
     return v;
 }
 
+__device__ __forceinline__ uint32_t ld_stream_u32(const void *p)
+{
+    uint32_t v;
+    asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+}
+
 __device__ __forceinline__ uint32_t ld_stream_u8(const void *p)
 {
     uint32_t v;

@@ -14,26 +14,30 @@
 //      f16 times a power of two per token and 512-column chunk (f16 holds
 //      every bf16 value of the chunk exactly once scaled so its max lies in
 //      [2^14, 2^15); values more than 2^28 below the chunk max may round),
-//      written in the order in which the MMA B fragments are read.  The LoRA
-//      down-projection T = X' A^T is summed in two fixed-order levels (8
-//      warps of a block in shared memory, then the last block of each group
-//      of 8 LoRA columns), so T is deterministic.
-//  main kernel (programmatic dependent launch): each block starts streaming
-//      its first weight units before it waits for the prologue.  Units are
-//      (tile of 32*RG rows, 64 columns), split evenly over the resident blocks
+//      written in the (swizzled) order in which the MMA B fragments are read.
+//      The LoRA down-projection T = X' A^T is written as fixed-order partial
+//      sums over 512-column slices (bf16 mma.sync, 8 warps per slice summed
+//      in shared memory).
+//  main kernel (programmatic dependent launch): units are (tile of 32*RG
+//      rows, stage of 256 columns), split evenly over the resident blocks
 //      (stream-K).  Inside a block, warp (rg, kl) owns 32 rows and a
-//      contiguous share of the block's columns of each tile; every lane loads
-//      its codes and block scales straight into registers several units
-//      ahead, converts them with cvt.e2m1x2 -> f16x2 and one f16x2 multiply by
-//      the block scale (both exact: v * dec(e) has at most 6 significant bits),
-//      and feeds mma.sync m16n8k16 with the tokens as the 8-wide N dimension.
-//      Accumulation is FP32; at each 512-column chunk the chunk's sums are
-//      scaled back by the chunk's power of two.  Per tile the block reduces
-//      its warps' partial sums in shared memory in a fixed order; a tile that
-//      one block covers entirely is finished on the spot, otherwise the last
-//      of its (few) blocks to arrive sums the partials in slot order and
-//      applies the epilogue Y = s_t * acc + s * T B^T.  Results do not depend
-//      on arrival order.
+//      contiguous share of the block's stages of each tile.  Lane t of a
+//      4-lane group owns 64 consecutive columns (4 scale blocks) of its 4 rows
+//      in every stage, so each stage costs it two 16-byte code loads and one
+//      4-byte scale load per row, issued two stages ahead into registers
+//      (the first ones before the block waits for the prologue).  Codes are
+//      converted with cvt.e2m1x2 -> f16x2 and one f16x2 multiply by the block
+//      scale (both exact: v * dec(e) has at most 6 significant bits) and fed
+//      to mma.sync m16n8k16 with the tokens as the 8-wide N dimension; the MMA
+//      k index is permuted so that these lane-contiguous columns line up with
+//      the X' fragments.  Accumulation is FP32; at each 512-column chunk the
+//      chunk's sums are scaled back by the chunk's power of two.  Per tile the
+//      block reduces its warps' partial sums in shared memory in a fixed
+//      order; a tile that one block covers entirely is finished on the spot,
+//      otherwise the last of its (few) blocks to arrive sums the partials in
+//      slot order and applies the epilogue Y = s_t * acc + s * T B^T (T summed
+//      over its slices in fixed order).  Results do not depend on arrival
+//      order.
 #include <algorithm>
 #include <mutex>
 
@@ -44,12 +48,12 @@ namespace nvfp4 {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = 8;
-constexpr int kStep = 64;   // columns of W per stream-K unit
-constexpr int kChunk = 512; // columns per X' scaling chunk
-constexpr int kStepsPerChunk = kChunk / kStep;
-constexpr int kDepth = 4;   // register prefetch depth (units in flight per warp)
-constexpr int kMaxSeg = 3;  // tiles a block may touch
-constexpr int kStageSteps = 28;  // X' staging capacity (steps) in shared memory
+constexpr int kStage = 256;  // columns of W per stream-K unit
+constexpr int kChunk = 512;  // columns per X' scaling chunk
+constexpr int kStagesPerChunk = kChunk / kStage;
+constexpr int kDepth = 2;        // register prefetch depth (stages in flight per warp)
+constexpr int kMaxSeg = 2;       // tiles a block range may touch (longer ranges are cut)
+constexpr int kStageUnits = 8;   // X' staging capacity (units) in shared memory
 constexpr int kLoraSlice = 512;  // input columns per LoRA prologue block (8 warps x 64)
 constexpr int kMaxRSmem = 64;
 
@@ -73,23 +77,30 @@ __device__ __forceinline__ void pdl_wait()
     asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
+// X' f16 layout, in 16-byte chunks: stage s (256 columns), token n, lane
+// slot t (64 columns), chunk q (8 columns), with the chunk index XORed by
+// (4n + t) mod 8 so that the B-fragment loads of a quarter warp hit 8
+// different bank groups.
+__device__ __forceinline__ size_t xh_index(int MP, int s, int n, int t, int q)
+{
+    return (((size_t)s * MP + n) * 4 + t) * 8 + (q ^ ((n * 4 + t) & 7));
+}
+
 // ================================================================ prologue
 struct PrologueParams {
     const uint16_t *x;
     int M, K, r;
     const uint16_t *lora_a;
     const float *noise;
-    uint4 *xh;       // [S][2][MP][4] x 8 f16
-    float *fac;      // [NC][MP]
-    float *tpart;    // [NS][MP][r]
-    float *tfin;     // [MP][r]
-    uint32_t *jcnt;  // [NJG] arrival counters
+    uint4 *xh;     // see xh_index
+    float *fac;    // [NC][MP]
+    float *tpart;  // [NS][MP][r]
     int NC, NS, NJG, conv_blocks;
 };
 
 // One warp converts one (token, 512-column chunk): X' = bf16(X z), its max,
-// the power of two 2^p that puts the max in [2^14, 2^15), and X' 2^-p as f16
-// in fragment order.  Each lane handles one 16-column block.
+// the power of two 2^p that puts the max in [2^14, 2^15), and X' 2^-p as f16.
+// Each lane handles 16 consecutive columns.
 template <int MP>
 __device__ void convert_unit(const PrologueParams &p, int m, int c)
 {
@@ -132,7 +143,8 @@ __device__ void convert_unit(const PrologueParams &p, int m, int c)
         const int e = (b >> 23) ? (int)(b >> 23) - 127 : (31 - __clz(b)) - 149;
         pexp = e - 14;
     }
-    const int s = k0 / kStep, tt = (k0 % kStep) / 16;
+    const int s = k0 / kStage, col = k0 % kStage;
+    const int t = col / 64, q0 = (col % 64) / 8;
 #pragma unroll
     for (int hh = 0; hh < 2; hh++) {
         uint32_t hw[4];
@@ -142,7 +154,7 @@ __device__ void convert_unit(const PrologueParams &p, int m, int c)
                                         __float2half_rn(scale_pow2(v[8 * hh + 2 * i + 1], -pexp)));
             hw[i] = *reinterpret_cast<uint32_t *>(&h2);
         }
-        p.xh[((size_t)(s * 2 + hh) * MP + m) * 4 + tt] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+        p.xh[xh_index(MP, s, m, t, q0 + hh)] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
     }
     if (lane == 0)
         p.fac[c * MP + m] = exp2i(pexp);
@@ -174,7 +186,6 @@ __global__ void __launch_bounds__(kThreads) decode_prologue_kernel(PrologueParam
     }
     // LoRA down-projection: block (jg, slice) -> 8 columns of T over 512 inputs
     __shared__ float s_c[kWarps][32][4];
-    __shared__ bool s_last;
     const int lb = blockIdx.x - p.conv_blocks;
     const int jg = lb % p.NJG, sl = lb / p.NJG;
     const int g = lane >> 2, t = lane & 3;
@@ -216,25 +227,6 @@ __global__ void __launch_bounds__(kThreads) decode_prologue_kernel(PrologueParam
             if (m < MP && j < p.r)
                 dst[m * p.r + j] = sum[q];
         }
-        __threadfence();
-    }
-    __syncthreads();
-    if (threadIdx.x == 0)
-        s_last = atomicAdd(&p.jcnt[jg], 1u) == (uint32_t)p.NS - 1;
-    __syncthreads();
-    if (s_last) {
-        __threadfence();
-        for (int e = threadIdx.x; e < MP * 8; e += kThreads) {
-            const int m = e / 8, j = j0 + e % 8;
-            if (j < p.r) {
-                float sum = 0.0f;
-                for (int q = 0; q < p.NS; q++)
-                    sum += __ldcg(p.tpart + ((size_t)q * MP + m) * p.r + j);
-                p.tfin[m * p.r + j] = sum;
-            }
-        }
-        if (threadIdx.x == 0)
-            p.jcnt[jg] = 0;
     }
 }
 
@@ -247,68 +239,112 @@ struct MainParams {
     float lora_scale;
     const uint4 *xh;
     const float *fac;
-    const float *tfin;
-    float *part;        // [R][maxseg][MP][rows]
-    uint32_t *tcnt;     // [R] arrival counters
+    const float *tpart;  // [NS][MP][r]
+    float *part;         // [R][maxseg][MP][rows]
+    uint32_t *tcnt;      // [R] arrival counters
     void *y;
     int y_fp32;
-    int S, R, U, maxseg;
+    int S, R, U, maxseg, NS;
+    int fast;  // K % 64 == 0: 16-byte code loads
 };
 
+// m-tiles (16 rows) per warp: two when the tokens fit one MMA N tile, else one
+template <int MP>
+__host__ __device__ constexpr int mt_of()
+{
+    return MP == 8 ? 2 : 1;
+}
+
+template <int MT>
 struct Stage {
-    uint2 c[2][2];      // [m-tile][row g / row g+8] 8 code bytes (16 columns)
-    uint32_t sc[2][2];  // matching block-scale bytes
+    uint4 c[MT][2][2];   // [m-tile][row g / g+8][half]: 32 code bytes = 64 columns
+    uint32_t sc[MT][2];  // 4 block-scale bytes
 };
 
-template <int RG>
-__device__ __forceinline__ void load_stage(const MainParams &p, Stage &st, int rt, int s, int rg)
+template <int MT, int RG>
+__device__ __forceinline__ void load_stage(const MainParams &p, Stage<MT> &st, int rt, int s, int rg)
 {
     const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-    const int row_base = rt * (32 * RG) + rg * 32;
-    const int kcol = s * kStep + 16 * t;
+    const int row_base = rt * (16 * MT * RG) + rg * 16 * MT;
+    const int kcol = s * kStage + 64 * t;  // first column of this lane's slice
 #pragma unroll
-    for (int i = 0; i < 2; i++)
+    for (int i = 0; i < MT; i++)
 #pragma unroll
         for (int h = 0; h < 2; h++) {
             const int row = row_base + 16 * i + g + 8 * h;
+            uint4 c0 = make_uint4(0, 0, 0, 0), c1 = c0;
+            uint32_t sw = 0;
             if (row < p.N && kcol < p.K) {
-                st.c[i][h] = ld_stream_u2(p.codes + (size_t)row * (p.K / 2) + kcol / 2);
-                st.sc[i][h] = ld_stream_u8(p.scales + (size_t)row * (p.K / 16) + kcol / 16);
-            } else {
-                st.c[i][h] = make_uint2(0u, 0u);
-                st.sc[i][h] = 0u;
+                const uint8_t *cp = p.codes + (size_t)row * (p.K / 2) + kcol / 2;
+                const uint8_t *sp = p.scales + (size_t)row * (p.K / 16) + kcol / 16;
+                if (p.fast) {
+                    c0 = ld_stream_u4(cp);
+                    c1 = ld_stream_u4(cp + 16);
+                    sw = ld_stream_u32(sp);
+                } else {
+                    // K % 64 != 0: 16-column blocks one by one, up to K
+                    uint32_t w[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+#pragma unroll
+                    for (int b = 0; b < 4; b++)
+                        if (kcol + 16 * b < p.K) {
+                            const uint2 v = ld_stream_u2(cp + 8 * b);
+                            w[2 * b] = v.x;
+                            w[2 * b + 1] = v.y;
+                            sw |= ld_stream_u8(sp + b) << (8 * b);
+                        }
+                    c0 = make_uint4(w[0], w[1], w[2], w[3]);
+                    c1 = make_uint4(w[4], w[5], w[6], w[7]);
+                }
             }
+            st.c[i][h][0] = c0;
+            st.c[i][h][1] = c1;
+            st.sc[i][h] = sw;
         }
 }
 
+// 16 MMA k-steps over the stage.  Step j uses, in lane slot t, columns
+// 64t + 4j .. 64t + 4j + 3: code bytes 2j, 2j+1 of the slice and scale
+// byte j/4; X' chunk j/2 (halves by parity of j).
 template <int MP>
-__device__ __forceinline__ void compute_stage(const Stage &st, const uint4 *xs, float (&cacc)[2][MP / 8][4])
+__device__ __forceinline__ void compute_stage(const Stage<mt_of<MP>()> &st, const uint4 *xs,
+                                              float (&cacc)[mt_of<MP>()][MP / 8][4])
 {
     constexpr int NT = MP / 8;
+    constexpr int MT = mt_of<MP>();
     const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    uint32_t sc[MT][2];
 #pragma unroll
-    for (int i = 0; i < 2; i++) {
-        const uint32_t sc0 = e4m3_to_h2_dup(st.sc[i][0]);
-        const uint32_t sc1 = e4m3_to_h2_dup(st.sc[i][1]);
-        uint32_t w0[8], w1[8];
-        e2m1x8_to_h2x4(st.c[i][0].x, w0);
-        e2m1x8_to_h2x4(st.c[i][0].y, w0 + 4);
-        e2m1x8_to_h2x4(st.c[i][1].x, w1);
-        e2m1x8_to_h2x4(st.c[i][1].y, w1 + 4);
+    for (int w = 0; w < 8; w++) {  // code word w = k-steps 2w, 2w+1
+        if ((w & 1) == 0) {        // a new scale block every two words
 #pragma unroll
-        for (int h = 0; h < 2; h++) {
-            uint4 xf[NT];
+            for (int i = 0; i < MT; i++)
 #pragma unroll
-            for (int nt = 0; nt < NT; nt++)
-                xf[nt] = xs[(h * MP + g + 8 * nt) * 4 + t];
+                for (int h = 0; h < 2; h++)
+                    sc[i][h] = e4m3_to_h2_dup((st.sc[i][h] >> (4 * w)) & 0xFFu);
+        }
+        uint4 xf[NT];
+#pragma unroll
+        for (int nt = 0; nt < NT; nt++) {
+            const int n = g + 8 * nt;
+            xf[nt] = xs[(n * 4 + t) * 8 + (w ^ ((n * 4 + t) & 7))];
+        }
+#pragma unroll
+        for (int i = 0; i < MT; i++) {
+            const uint4 &v0 = st.c[i][0][w >> 2];
+            const uint4 &v1 = st.c[i][1][w >> 2];
+            const uint32_t w0 = (w & 3) == 0 ? v0.x : (w & 3) == 1 ? v0.y : (w & 3) == 2 ? v0.z : v0.w;
+            const uint32_t w1 = (w & 3) == 0 ? v1.x : (w & 3) == 1 ? v1.y : (w & 3) == 2 ? v1.z : v1.w;
+            uint32_t r0[4], r1[4];
+            e2m1x8_to_h2x4(w0, r0);
+            e2m1x8_to_h2x4(w1, r1);
+            const uint32_t s0 = sc[i][0], s1 = sc[i][1];
 #pragma unroll
             for (int jj = 0; jj < 2; jj++) {
-                const int j = 2 * h + jj;
                 uint32_t a[4];
-                a[0] = hmul2_u32(w0[2 * j], sc0);
-                a[1] = hmul2_u32(w1[2 * j], sc1);
-                a[2] = hmul2_u32(w0[2 * j + 1], sc0);
-                a[3] = hmul2_u32(w1[2 * j + 1], sc1);
+                a[0] = hmul2_u32(r0[2 * jj], s0);
+                a[1] = hmul2_u32(r1[2 * jj], s1);
+                a[2] = hmul2_u32(r0[2 * jj + 1], s0);
+                a[3] = hmul2_u32(r1[2 * jj + 1], s1);
 #pragma unroll
                 for (int nt = 0; nt < NT; nt++)
                     mma_f16_16816(cacc[i][nt], a, jj ? xf[nt].z : xf[nt].x, jj ? xf[nt].w : xf[nt].y);
@@ -318,8 +354,8 @@ __device__ __forceinline__ void compute_stage(const Stage &st, const uint4 *xs, 
 }
 
 template <int MP>
-__device__ __forceinline__ void flush_chunk(const float *fac, int chunk, float (&acc)[2][MP / 8][4],
-                                            float (&cacc)[2][MP / 8][4])
+__device__ __forceinline__ void flush_chunk(const float *fac, int chunk, float (&acc)[mt_of<MP>()][MP / 8][4],
+                                            float (&cacc)[mt_of<MP>()][MP / 8][4])
 {
     constexpr int NT = MP / 8;
     const int t = threadIdx.x & 3;
@@ -327,7 +363,7 @@ __device__ __forceinline__ void flush_chunk(const float *fac, int chunk, float (
     for (int nt = 0; nt < NT; nt++) {
         const float2 f = *reinterpret_cast<const float2 *>(fac + chunk * MP + nt * 8 + 2 * t);
 #pragma unroll
-        for (int i = 0; i < 2; i++) {
+        for (int i = 0; i < mt_of<MP>(); i++) {
             acc[i][nt][0] = __fmaf_rn(cacc[i][nt][0], f.x, acc[i][nt][0]);
             acc[i][nt][1] = __fmaf_rn(cacc[i][nt][1], f.y, acc[i][nt][1]);
             acc[i][nt][2] = __fmaf_rn(cacc[i][nt][2], f.x, acc[i][nt][2]);
@@ -337,11 +373,10 @@ __device__ __forceinline__ void flush_chunk(const float *fac, int chunk, float (
     }
 }
 
-// The block's share of the unit range, cut into per-tile segments; warp
-// (rg, kl) takes rows rg*32.. of every tile and the kl-th contiguous part of
-// each segment's columns.
+// The block's range cut into per-tile segments; warp (rg, kl) takes rows
+// rg*32.. of every tile and the kl-th contiguous part of each segment.
 struct SegCursor {
-    int seg, s, end;  // current segment, step, end step of this warp's part
+    int seg, s, end;
 };
 
 __device__ __forceinline__ void seg_part(int u_begin, int u_end, int S, int seg, int kl, int KL, int &rt, int &a,
@@ -358,10 +393,11 @@ __device__ __forceinline__ void seg_part(int u_begin, int u_end, int S, int seg,
 }
 
 template <int MP>
-constexpr size_t main_smem_bytes()
+__host__ __device__ constexpr size_t main_smem_bytes()
 {
-    // X' staging + per-warp partial tiles (KL x ROWS = 256 for every RG) + T
-    return (size_t)kStageSteps * 2 * MP * 4 * 16 + (size_t)kMaxSeg * kThreads * MP * 4 + (size_t)MP * kMaxRSmem * 4;
+    // X' staging + per-warp partial tiles (KL x ROWS = 128 MT for every RG) + T
+    return (size_t)kStageUnits * MP * 512 + (size_t)kMaxSeg * 128 * mt_of<MP>() * MP * 4 +
+           (size_t)MP * kMaxRSmem * 4;
 }
 
 template <int MP, int RG>
@@ -369,13 +405,15 @@ __device__ __forceinline__ void decode_range(const MainParams &p, int u_begin, i
                                              bool &t_loaded)
 {
     constexpr int NT = MP / 8;
+    constexpr int MT = mt_of<MP>();
     constexpr int KL = kWarps / RG;
-    constexpr int ROWS = 32 * RG;
+    constexpr int ROWS = 16 * MT * RG;
+    constexpr int XU = MP * 32;  // uint4 of X' per stage
     extern __shared__ __align__(16) uint8_t smem_dyn[];
-    uint4 *s_x = reinterpret_cast<uint4 *>(smem_dyn);  // X' of this block's steps
-    float(*s_red)[KL][MP][ROWS] = reinterpret_cast<float(*)[KL][MP][ROWS]>(
-        smem_dyn + (size_t)kStageSteps * 2 * MP * 4 * 16);  // per-warp partial tiles
-    float *s_T = reinterpret_cast<float *>(smem_dyn + (size_t)kStageSteps * 2 * MP * 4 * 16 +
+    uint4 *s_x = reinterpret_cast<uint4 *>(smem_dyn);
+    float(*s_red)[KL][MP][ROWS] =
+        reinterpret_cast<float(*)[KL][MP][ROWS]>(smem_dyn + (size_t)kStageUnits * MP * 512);
+    float *s_T = reinterpret_cast<float *>(smem_dyn + (size_t)kStageUnits * MP * 512 +
                                            (size_t)kMaxSeg * KL * MP * ROWS * 4);
     __shared__ bool s_flag;
 
@@ -384,71 +422,57 @@ __device__ __forceinline__ void decode_range(const MainParams &p, int u_begin, i
     const int rg = warp % RG, kl = warp / RG;
     const int rt_first = u_begin / p.S, nseg = (u_end - 1) / p.S - rt_first + 1;
 
-    // cursors over this warp's steps: ld runs kDepth steps ahead of cm
-    SegCursor ld{0, 0, 0};
+    auto to_next = [&](SegCursor &c) {  // skip to the next non-empty part
+        while (c.s >= c.end && c.seg < nseg) {
+            c.seg++;
+            if (c.seg >= nseg)
+                break;
+            int rt, a, b;
+            seg_part(u_begin, u_end, p.S, c.seg, kl, KL, rt, a, b);
+            c.s = a;
+            c.end = b;
+        }
+    };
+    SegCursor ld;
     {
         int rt, a, b;
         seg_part(u_begin, u_end, p.S, 0, kl, KL, rt, a, b);
         ld = {0, a, b};
+        to_next(ld);
     }
-    auto advance = [&](SegCursor &c) {
-        c.s++;
-        while (c.s >= c.end && c.seg < nseg) {
-            c.seg++;
-            if (c.seg >= nseg)
-                break;
-            int rt, a, b;
-            seg_part(u_begin, u_end, p.S, c.seg, kl, KL, rt, a, b);
-            c.s = a;
-            c.end = b;
-        }
-    };
-    auto normalize = [&](SegCursor &c) {  // skip empty parts at the start
-        while (c.s >= c.end && c.seg < nseg) {
-            c.seg++;
-            if (c.seg >= nseg)
-                break;
-            int rt, a, b;
-            seg_part(u_begin, u_end, p.S, c.seg, kl, KL, rt, a, b);
-            c.s = a;
-            c.end = b;
-        }
-    };
-    normalize(ld);
     SegCursor cm = ld;
 
-    // start streaming the first weight units before waiting for the prologue
-    Stage st[kDepth];
+    // start streaming the first stages before waiting for the prologue
+    Stage<MT> st[kDepth];
 #pragma unroll
     for (int d = 0; d < kDepth; d++) {
         if (ld.seg < nseg) {
-            load_stage<RG>(p, st[d], rt_first + ld.seg, ld.s, rg);
-            advance(ld);
+            load_stage<MT, RG>(p, st[d], rt_first + ld.seg, ld.s, rg);
+            ld.s++;
+            to_next(ld);
         }
     }
     if (first_range)
         pdl_wait();
-    __syncthreads();  // shared buffers of the previous range are free
+    __syncthreads();  // shared buffers of a previous range are free
 
-    // X' of the block's steps (all of its segments) into shared memory
-    int nsteps = 0, off0 = 0, off1 = 0, off2 = 0;  // staged index of step s in segment j = off_j + s
+    // X' of the block's stages into shared memory
+    int nsteps = 0, off0 = 0, off1 = 0;  // staged index of stage s of segment j = off_j + s
     for (int j = 0; j < nseg && j < kMaxSeg; j++) {
         int rt, a, b;
         seg_part(u_begin, u_end, p.S, j, 0, 1, rt, a, b);
-        const int o = nsteps - a;
-        off0 = j == 0 ? o : off0;
-        off1 = j == 1 ? o : off1;
-        off2 = j == 2 ? o : off2;
+        off0 = j == 0 ? nsteps - a : off0;
+        off1 = j == 1 ? nsteps - a : off1;
         nsteps += b - a;
     }
-    const bool staged = nsteps <= kStageSteps;
+    const bool staged = nsteps <= kStageUnits;
     if (staged) {
         for (int j = 0, base = 0; j < nseg; j++) {
             int rt, a, b;
             seg_part(u_begin, u_end, p.S, j, 0, 1, rt, a, b);
-            const int n = (b - a) * 2 * MP * 4;
+            const int n = (b - a) * XU;
             for (int i = threadIdx.x; i < n; i += kThreads)
-                s_x[base * 2 * MP * 4 + i] = p.xh[(size_t)a * 2 * MP * 4 + i];
+                s_x[base * XU + i] = p.xh[(size_t)a * XU + i];
             base += b - a;
         }
     }
@@ -456,49 +480,46 @@ __device__ __forceinline__ void decode_range(const MainParams &p, int u_begin, i
         (&s_red[0][0][0][0])[i] = 0.0f;  // warps with an empty share leave zeros
     __syncthreads();
 
-    float acc[2][NT][4], cacc[2][NT][4];
+    float acc[MT][NT][4], cacc[MT][NT][4];
 #pragma unroll
-    for (int i = 0; i < 2; i++)
+    for (int i = 0; i < MT; i++)
 #pragma unroll
         for (int nt = 0; nt < NT; nt++)
 #pragma unroll
             for (int q = 0; q < 4; q++)
                 acc[i][nt][q] = cacc[i][nt][q] = 0.0f;
 
-    auto store_warp_partial = [&](int seg) {
-#pragma unroll
-        for (int i = 0; i < 2; i++)
-#pragma unroll
-            for (int nt = 0; nt < NT; nt++)
-#pragma unroll
-                for (int q = 0; q < 4; q++) {
-                    const int row = rg * 32 + 16 * i + g + 8 * (q >> 1);
-                    const int tok = nt * 8 + 2 * t + (q & 1);
-                    s_red[seg][kl][tok][row] = acc[i][nt][q];
-                    acc[i][nt][q] = 0.0f;
-                }
-    };
-
-    // main loop over this warp's steps, kDepth at a time (static register indices)
     while (cm.seg < nseg) {
 #pragma unroll
         for (int d = 0; d < kDepth; d++) {
             if (cm.seg < nseg) {
                 const int seg = cm.seg, s = cm.s;
-                const int soff = seg == 0 ? off0 : (seg == 1 ? off1 : off2);
-                const uint4 *xs = staged ? s_x + (size_t)(soff + s) * 2 * MP * 4
-                                         : p.xh + (size_t)s * 2 * MP * 4;
+                const uint4 *xs = staged ? s_x + (size_t)((seg == 0 ? off0 : off1) + s) * XU
+                                         : p.xh + (size_t)s * XU;
                 compute_stage<MP>(st[d], xs, cacc);
                 if (ld.seg < nseg) {
-                    load_stage<RG>(p, st[d], rt_first + ld.seg, ld.s, rg);
-                    advance(ld);
+                    load_stage<MT, RG>(p, st[d], rt_first + ld.seg, ld.s, rg);
+                    ld.s++;
+                    to_next(ld);
                 }
-                advance(cm);
+                cm.s++;
+                to_next(cm);
                 const bool seg_end = cm.seg != seg;
-                if ((s % kStepsPerChunk) == kStepsPerChunk - 1 || seg_end)
-                    flush_chunk<MP>(p.fac, s / kStepsPerChunk, acc, cacc);
-                if (seg_end && seg < kMaxSeg)
-                    store_warp_partial(seg);
+                if ((s % kStagesPerChunk) == kStagesPerChunk - 1 || seg_end)
+                    flush_chunk<MP>(p.fac, s / kStagesPerChunk, acc, cacc);
+                if (seg_end) {
+#pragma unroll
+                    for (int i = 0; i < MT; i++)
+#pragma unroll
+                        for (int nt = 0; nt < NT; nt++)
+#pragma unroll
+                            for (int q = 0; q < 4; q++) {
+                                const int row = rg * 16 * MT + 16 * i + g + 8 * (q >> 1);
+                                const int tok = nt * 8 + 2 * t + (q & 1);
+                                s_red[seg][kl][tok][row] = acc[i][nt][q];
+                                acc[i][nt][q] = 0.0f;
+                            }
+                }
             }
         }
     }
@@ -507,11 +528,10 @@ __device__ __forceinline__ void decode_range(const MainParams &p, int u_begin, i
     // per tile: sum the warps' partials (fixed order); finish or hand over
     const float s_t = *p.tensor_scale;
     const int r = p.r;
-    for (int j = 0; j < nseg && j < kMaxSeg; j++) {
+    for (int j = 0; j < nseg; j++) {
         const int rt = rt_first + j;
         const int first = owner_of(rt * p.S, p.U, P), last = owner_of(rt * p.S + p.S - 1, p.U, P);
         const int cover = last - first + 1;
-        // this block's partial tile (token-major) -> registers of threads (tok, row)
         if (cover > 1) {
             float *dst = p.part + ((size_t)(rt * p.maxseg + (bid - first)) * MP) * ROWS;
             for (int e = threadIdx.x; e < MP * ROWS; e += kThreads) {
@@ -531,14 +551,17 @@ __device__ __forceinline__ void decode_range(const MainParams &p, int u_begin, i
                 continue;
             __threadfence();
         }
-        // epilogue for tile rt: Y = s_t * acc + s * T B^T
+        // T = sum of its slices, fixed order (once per block)
         if (!t_loaded && r > 0 && r <= kMaxRSmem) {
-            for (int e = threadIdx.x; e < MP * r; e += kThreads)
-                s_T[e] = p.tfin[e];
+            for (int e = threadIdx.x; e < MP * r; e += kThreads) {
+                float sum = 0.0f;
+                for (int q = 0; q < p.NS; q++)
+                    sum += __ldcg(p.tpart + (size_t)q * MP * r + e);
+                s_T[e] = sum;
+            }
             __syncthreads();
             t_loaded = true;
         }
-        const float *T = r <= kMaxRSmem ? s_T : p.tfin;
         for (int e = threadIdx.x; e < p.M * ROWS; e += kThreads) {
             const int m = e / ROWS, row = e % ROWS;
             const int n = rt * ROWS + row;
@@ -556,22 +579,33 @@ __device__ __forceinline__ void decode_range(const MainParams &p, int u_begin, i
             }
             float lora = 0.0f;
             if (r > 0) {
-                const float *trow = T + m * r;
-                if ((r & 7) == 0) {
-                    const uint4 *brow = reinterpret_cast<const uint4 *>(p.lora_b + (size_t)n * r);
-                    for (int jj = 0; jj < r / 8; jj++) {
-                        const uint4 bv = brow[jj];
-                        const uint32_t bw[4] = {bv.x, bv.y, bv.z, bv.w};
+                if (r <= kMaxRSmem) {
+                    const float *trow = s_T + m * r;
+                    if ((r & 7) == 0) {
+                        const uint4 *brow = reinterpret_cast<const uint4 *>(p.lora_b + (size_t)n * r);
+                        for (int jj = 0; jj < r / 8; jj++) {
+                            const uint4 bv = brow[jj];
+                            const uint32_t bw[4] = {bv.x, bv.y, bv.z, bv.w};
 #pragma unroll
-                        for (int q = 0; q < 4; q++) {
-                            lora = __fmaf_rn(trow[8 * jj + 2 * q], bf16_bits_to_f32(bw[q] & 0xFFFFu), lora);
-                            lora = __fmaf_rn(trow[8 * jj + 2 * q + 1], bf16_bits_to_f32(bw[q] >> 16), lora);
+                            for (int q = 0; q < 4; q++) {
+                                lora = __fmaf_rn(trow[8 * jj + 2 * q], bf16_bits_to_f32(bw[q] & 0xFFFFu), lora);
+                                lora = __fmaf_rn(trow[8 * jj + 2 * q + 1], bf16_bits_to_f32(bw[q] >> 16), lora);
+                            }
                         }
+                    } else {
+                        const uint16_t *brow = p.lora_b + (size_t)n * r;
+                        for (int jj = 0; jj < r; jj++)
+                            lora = __fmaf_rn(trow[jj], bf16_bits_to_f32(brow[jj]), lora);
                     }
                 } else {
+                    // large rank: T elements summed on the fly
                     const uint16_t *brow = p.lora_b + (size_t)n * r;
-                    for (int jj = 0; jj < r; jj++)
-                        lora = __fmaf_rn(trow[jj], bf16_bits_to_f32(brow[jj]), lora);
+                    for (int jj = 0; jj < r; jj++) {
+                        float tv = 0.0f;
+                        for (int q = 0; q < p.NS; q++)
+                            tv += __ldcg(p.tpart + ((size_t)q * MP + m) * r + jj);
+                        lora = __fmaf_rn(tv, bf16_bits_to_f32(brow[jj]), lora);
+                    }
                 }
             }
             const float yv = __fmaf_rn(s_t, a1, p.lora_scale * lora);
@@ -604,26 +638,20 @@ __global__ void __launch_bounds__(kThreads, 2) decode_main_kernel(MainParams p)
 // ================================================================ host side
 struct DecodePlan {
     int MP, RG, P, S, NC, R, NS, NJG, maxseg, U, conv_blocks;
-    size_t off_xh, off_fac, off_tpart, off_tfin, off_jcnt, off_tcnt, off_part, total;
+    size_t off_xh, off_fac, off_tpart, off_tcnt, off_part, total;
 };
 
 static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 static int host_owner(int u, int U, int P) { return (int)(((long long)(u + 1) * P - 1) / U); }
 
-// Tiles a block touches at most, and the deepest split of a tile over blocks.
-static void split_stats(int R, int S, int P, int &max_tiles, int &max_cover)
+static int max_cover(int R, int S, int P)
 {
     const long long U = (long long)R * S;
-    max_tiles = 0;
-    max_cover = 0;
-    for (int b = 0; b < P; b++) {
-        const int ub = (int)(b * U / P), ue = (int)((b + 1) * U / P);
-        if (ue > ub)
-            max_tiles = std::max(max_tiles, (ue - 1) / S - ub / S + 1);
-    }
+    int mc = 0;
     for (int rt = 0; rt < R; rt++)
-        max_cover = std::max(max_cover, host_owner(rt * S + S - 1, (int)U, P) - host_owner(rt * S, (int)U, P) + 1);
+        mc = std::max(mc, host_owner(rt * S + S - 1, (int)U, P) - host_owner(rt * S, (int)U, P) + 1);
+    return mc;
 }
 
 static bool make_plan(int64_t M, int64_t N, int64_t K, int64_t r, const DeviceInfo &dev, DecodePlan &pl)
@@ -632,52 +660,41 @@ static bool make_plan(int64_t M, int64_t N, int64_t K, int64_t r, const DeviceIn
     const int bps = dev.decode_blocks_per_sm[pl.MP == 8 ? 0 : 1];
     if (bps < 1)
         return false;
-    pl.S = (int)((K + kStep - 1) / kStep);
+    pl.S = (int)((K + kStage - 1) / kStage);
     pl.NC = (int)((K + kChunk - 1) / kChunk);
     // tile height 32*RG: the tallest tile whose split over blocks stays <= 3
     // (less X' traffic per weight), else the shortest (cheapest reduction)
-    pl.RG = 0;
-    int fallback = 0;
+    const int wrows = pl.MP == 8 ? 32 : 16;  // rows per warp
+    pl.RG = 2;
     for (int rg : {8, 4, 2}) {
-        const int R = (int)((N + 32 * rg - 1) / (32 * rg));
+        const int R = (int)((N + wrows * rg - 1) / (wrows * rg));
         const long long U = (long long)R * pl.S;
         if (U > (1LL << 30))
             continue;
         const int P = (int)std::min<long long>((long long)dev.num_sms * bps, U);
-        int max_tiles, max_cover;
-        split_stats(R, pl.S, P, max_tiles, max_cover);
-        fallback = rg;
-        if (max_cover <= 3) {
+        if (max_cover(R, pl.S, P) <= 3) {
             pl.RG = rg;
             break;
         }
     }
-    if (!pl.RG)
-        pl.RG = fallback;
-    if (!pl.RG)
-        return false;
-    const int rows = 32 * pl.RG;
+    const int rows = wrows * pl.RG;
     pl.R = (int)((N + rows - 1) / rows);
-    pl.U = (int)((long long)pl.R * pl.S);
+    if ((long long)pl.R * pl.S > (1LL << 30) || pl.R > kCounterWords)
+        return false;
+    pl.U = pl.R * pl.S;
     pl.P = (int)std::min<long long>((long long)dev.num_sms * bps, pl.U);
-    int max_tiles;
-    split_stats(pl.R, pl.S, pl.P, max_tiles, pl.maxseg);
+    pl.maxseg = max_cover(pl.R, pl.S, pl.P);
     pl.NS = (int)((K + kLoraSlice - 1) / kLoraSlice);
     pl.NJG = (int)((r + 7) / 8);
     pl.conv_blocks = (pl.MP * pl.NC + kWarps - 1) / kWarps;
-    if (pl.NJG + pl.R > kCounterWords)
-        return false;
-    pl.off_jcnt = kCtlBytes;
-    pl.off_tcnt = kCtlBytes + 4 * (size_t)pl.NJG;
+    pl.off_tcnt = kCtlBytes;
     size_t off = kWsHeaderBytes;
     pl.off_xh = off;
-    off = align_up(off + (size_t)pl.NC * kStepsPerChunk * pl.MP * kStep * 2, 256);
+    off = align_up(off + (size_t)pl.NC * kStagesPerChunk * pl.MP * 512, 256);
     pl.off_fac = off;
     off = align_up(off + (size_t)pl.NC * pl.MP * 4, 256);
     pl.off_tpart = off;
     off = align_up(off + (size_t)pl.NS * pl.MP * std::max<int64_t>(r, 1) * 4, 256);
-    pl.off_tfin = off;
-    off = align_up(off + (size_t)pl.MP * std::max<int64_t>(r, 1) * 4, 256);
     pl.off_part = off;
     off = align_up(off + (size_t)pl.R * pl.maxseg * pl.MP * rows * 4, 256);
     pl.total = off;
@@ -742,8 +759,6 @@ cudaError_t launch_decode_gemm(const GemmArgs &a, cudaStream_t s, const DeviceIn
         pp.xh = reinterpret_cast<uint4 *>(a.ws + pl.off_xh);
         pp.fac = reinterpret_cast<float *>(a.ws + pl.off_fac);
         pp.tpart = reinterpret_cast<float *>(a.ws + pl.off_tpart);
-        pp.tfin = reinterpret_cast<float *>(a.ws + pl.off_tfin);
-        pp.jcnt = reinterpret_cast<uint32_t *>(a.ws + pl.off_jcnt);
         pp.NC = pl.NC;
         pp.NS = pl.NS;
         pp.NJG = pl.NJG;
@@ -769,7 +784,7 @@ cudaError_t launch_decode_gemm(const GemmArgs &a, cudaStream_t s, const DeviceIn
         p.lora_scale = a.lora_scale;
         p.xh = pp.xh;
         p.fac = pp.fac;
-        p.tfin = pp.tfin;
+        p.tpart = pp.tpart;
         p.part = reinterpret_cast<float *>(a.ws + pl.off_part);
         p.tcnt = reinterpret_cast<uint32_t *>(a.ws + pl.off_tcnt);
         p.y = a.y_fp32 ? (void *)((float *)a.y + m0 * a.N) : (void *)((uint16_t *)a.y + m0 * a.N);
@@ -778,6 +793,8 @@ cudaError_t launch_decode_gemm(const GemmArgs &a, cudaStream_t s, const DeviceIn
         p.R = pl.R;
         p.U = pl.U;
         p.maxseg = pl.maxseg;
+        p.NS = pl.NS;
+        p.fast = (a.K % 64) == 0 ? 1 : 0;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(pl.P);
         cfg.blockDim = dim3(kThreads);
