@@ -176,7 +176,11 @@ __device__ __forceinline__ uint32_t xprime_pair(const uint16_t *x, const float *
 template <int MP>
 __global__ void __launch_bounds__(kThreads) decode_prologue_kernel(PrologueParams p)
 {
+    // launched early behind the previous kernel of the stream: let the main
+    // kernel launch (it prefetches weights only), then wait for the previous
+    // kernel before reading any input, since it may have produced X
     pdl_launch_dependents();
+    pdl_wait();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if ((int)blockIdx.x < p.conv_blocks) {
         const int unit = blockIdx.x * kWarps + warp;
@@ -191,20 +195,42 @@ __global__ void __launch_bounds__(kThreads) decode_prologue_kernel(PrologueParam
     const int g = lane >> 2, t = lane & 3;
     const int j0 = jg * 8, jrow = j0 + g;
     const int ka = sl * kLoraSlice + warp * 64;
+    // every load first, from clamped addresses (no branch between loads);
+    // 16-column step q is inside K or entirely outside it (K % 16 == 0)
+    const int m0 = min(g, p.M - 1), m1 = min(g + 8, p.M - 1);
+    const int jc = min(jrow, max(p.r - 1, 0));
+    uint32_t x0[8], x1[8], aw[8];
+    float2 zz[8];
+#pragma unroll
+    for (int q = 0; q < 4; q++)
+#pragma unroll
+        for (int hh = 0; hh < 2; hh++) {
+            const int k = min(ka + 16 * q, p.K - 16) + 2 * t + 8 * hh;
+            x0[2 * q + hh] = *reinterpret_cast<const uint32_t *>(p.x + (size_t)m0 * p.K + k);
+            x1[2 * q + hh] = MP > 8 ? *reinterpret_cast<const uint32_t *>(p.x + (size_t)m1 * p.K + k) : 0u;
+            zz[2 * q + hh] = p.noise ? *reinterpret_cast<const float2 *>(p.noise + k) : make_float2(1.f, 1.f);
+            aw[2 * q + hh] = *reinterpret_cast<const uint32_t *>(p.lora_a + (size_t)jc * p.K + k);
+        }
+    auto xp = [&](uint32_t xb, float2 z, bool valid) -> uint32_t {
+        if (!valid)
+            return 0u;
+        if (!p.noise)
+            return xb;
+        __nv_bfloat162 o = __floats2bfloat162_rn(__fmul_rn(bf16_bits_to_f32(xb & 0xFFFFu), z.x),
+                                                 __fmul_rn(bf16_bits_to_f32(xb >> 16), z.y));
+        return *reinterpret_cast<uint32_t *>(&o);
+    };
     uint32_t a[4][4], b[4][2];
 #pragma unroll
     for (int q = 0; q < 4; q++) {
-        const int k0 = ka + 16 * q;
-        a[q][0] = xprime_pair(p.x, p.noise, p.M, p.K, g, k0 + 2 * t);
-        a[q][1] = MP > 8 ? xprime_pair(p.x, p.noise, p.M, p.K, g + 8, k0 + 2 * t) : 0u;
-        a[q][2] = xprime_pair(p.x, p.noise, p.M, p.K, g, k0 + 2 * t + 8);
-        a[q][3] = MP > 8 ? xprime_pair(p.x, p.noise, p.M, p.K, g + 8, k0 + 2 * t + 8) : 0u;
-        b[q][0] = b[q][1] = 0u;
-        if (jrow < p.r && k0 < p.K) {
-            const uint16_t *arow = p.lora_a + (size_t)jrow * p.K;
-            b[q][0] = *reinterpret_cast<const uint32_t *>(arow + k0 + 2 * t);
-            b[q][1] = *reinterpret_cast<const uint32_t *>(arow + k0 + 2 * t + 8);
-        }
+        const bool kin = ka + 16 * q < p.K;
+        const bool v0 = kin && g < p.M, v1 = kin && g + 8 < p.M && MP > 8, vb = kin && jrow < p.r;
+        a[q][0] = xp(x0[2 * q], zz[2 * q], v0);
+        a[q][1] = xp(x1[2 * q], zz[2 * q], v1);
+        a[q][2] = xp(x0[2 * q + 1], zz[2 * q + 1], v0);
+        a[q][3] = xp(x1[2 * q + 1], zz[2 * q + 1], v1);
+        b[q][0] = vb ? aw[2 * q] : 0u;
+        b[q][1] = vb ? aw[2 * q + 1] : 0u;
     }
     float c[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -471,8 +497,17 @@ __device__ __forceinline__ void decode_range(const MainParams &p, int u_begin, i
             int rt, a, b;
             seg_part(u_begin, u_end, p.S, j, 0, 1, rt, a, b);
             const int n = (b - a) * XU;
-            for (int i = threadIdx.x; i < n; i += kThreads)
-                s_x[base * XU + i] = p.xh[(size_t)a * XU + i];
+            for (int i0 = threadIdx.x; i0 < n; i0 += 4 * kThreads) {
+                uint4 v[4];
+#pragma unroll
+                for (int k = 0; k < 4; k++)
+                    if (i0 + k * kThreads < n)
+                        v[k] = __ldcg(p.xh + (size_t)a * XU + i0 + k * kThreads);
+#pragma unroll
+                for (int k = 0; k < 4; k++)
+                    if (i0 + k * kThreads < n)
+                        s_x[base * XU + i0 + k * kThreads] = v[k];
+            }
             base += b - a;
         }
     }
@@ -524,6 +559,7 @@ __device__ __forceinline__ void decode_range(const MainParams &p, int u_begin, i
         }
     }
     __syncthreads();
+    pdl_launch_dependents();  // the next call's prologue may start loading its inputs
 
     // per tile: sum the warps' partials (fixed order); finish or hand over
     const float s_t = *p.tensor_scale;
@@ -562,58 +598,97 @@ __device__ __forceinline__ void decode_range(const MainParams &p, int u_begin, i
             __syncthreads();
             t_loaded = true;
         }
-        for (int e = threadIdx.x; e < p.M * ROWS; e += kThreads) {
-            const int m = e / ROWS, row = e % ROWS;
+        // one thread per output row, all tokens; every load before the arithmetic
+        for (int row = threadIdx.x; row < ROWS; row += kThreads) {
             const int n = rt * ROWS + row;
             if (n >= p.N)
                 continue;
-            float a1 = 0.0f;
+            float a1[MP];
+#pragma unroll
+            for (int m = 0; m < MP; m++)
+                a1[m] = 0.0f;
             if (cover > 1) {
-                const float *src = p.part + ((size_t)(rt * p.maxseg) * MP + m) * ROWS + row;
-                for (int k = 0; k < cover; k++)
-                    a1 += __ldcg(src + (size_t)k * MP * ROWS);
+                const float *src = p.part + (size_t)(rt * p.maxseg) * MP * ROWS + row;
+                for (int k0 = 0; k0 < cover; k0 += 2) {
+                    float v[2][MP];
+#pragma unroll
+                    for (int kk = 0; kk < 2; kk++)
+#pragma unroll
+                        for (int m = 0; m < MP; m++)
+                            v[kk][m] = (k0 + kk < cover && m < p.M)
+                                           ? __ldcg(src + ((size_t)(k0 + kk) * MP + m) * ROWS)
+                                           : 0.0f;
+#pragma unroll
+                    for (int kk = 0; kk < 2; kk++)
+#pragma unroll
+                        for (int m = 0; m < MP; m++)
+                            a1[m] += v[kk][m];
+                }
             } else {
 #pragma unroll
                 for (int k = 0; k < KL; k++)
-                    a1 += s_red[j][k][m][row];
-            }
-            float lora = 0.0f;
-            if (r > 0) {
-                if (r <= kMaxRSmem) {
-                    const float *trow = s_T + m * r;
-                    if ((r & 7) == 0) {
-                        const uint4 *brow = reinterpret_cast<const uint4 *>(p.lora_b + (size_t)n * r);
-                        for (int jj = 0; jj < r / 8; jj++) {
-                            const uint4 bv = brow[jj];
-                            const uint32_t bw[4] = {bv.x, bv.y, bv.z, bv.w};
 #pragma unroll
-                            for (int q = 0; q < 4; q++) {
-                                lora = __fmaf_rn(trow[8 * jj + 2 * q], bf16_bits_to_f32(bw[q] & 0xFFFFu), lora);
-                                lora = __fmaf_rn(trow[8 * jj + 2 * q + 1], bf16_bits_to_f32(bw[q] >> 16), lora);
+                    for (int m = 0; m < MP; m++)
+                        a1[m] += s_red[j][k][m][row];
+            }
+            float lora[MP];
+#pragma unroll
+            for (int m = 0; m < MP; m++)
+                lora[m] = 0.0f;
+            if (r > 0 && r <= kMaxRSmem && (r & 7) == 0) {
+                const uint4 *brow = reinterpret_cast<const uint4 *>(p.lora_b + (size_t)n * r);
+#pragma unroll
+                for (int q0 = 0; q0 < kMaxRSmem / 8; q0 += 4) {  // 32 columns of B at a time
+                    if (8 * q0 < r) {
+                        uint4 bv[4];
+#pragma unroll
+                        for (int q = 0; q < 4; q++)
+                            bv[q] = 8 * (q0 + q) < r ? brow[q0 + q] : make_uint4(0, 0, 0, 0);
+#pragma unroll
+                        for (int q = 0; q < 4; q++) {
+                            if (8 * (q0 + q) < r) {
+                                const uint32_t bw[4] = {bv[q].x, bv[q].y, bv[q].z, bv[q].w};
+#pragma unroll
+                                for (int e = 0; e < 8; e++) {
+                                    const float bf = bf16_bits_to_f32((bw[e / 2] >> (16 * (e & 1))) & 0xFFFFu);
+#pragma unroll
+                                    for (int m = 0; m < MP; m++)
+                                        lora[m] = __fmaf_rn(s_T[m * r + 8 * (q0 + q) + e], bf, lora[m]);
+                                }
                             }
                         }
-                    } else {
-                        const uint16_t *brow = p.lora_b + (size_t)n * r;
-                        for (int jj = 0; jj < r; jj++)
-                            lora = __fmaf_rn(trow[jj], bf16_bits_to_f32(brow[jj]), lora);
                     }
-                } else {
-                    // large rank: T elements summed on the fly
-                    const uint16_t *brow = p.lora_b + (size_t)n * r;
-                    for (int jj = 0; jj < r; jj++) {
-                        float tv = 0.0f;
-                        for (int q = 0; q < p.NS; q++)
-                            tv += __ldcg(p.tpart + ((size_t)q * MP + m) * r + jj);
-                        lora = __fmaf_rn(tv, bf16_bits_to_f32(brow[jj]), lora);
+                }
+            } else if (r > 0) {
+                // ranks above 64 or not a multiple of 8: T summed on the fly
+                const uint16_t *brow = p.lora_b + (size_t)n * r;
+                for (int jj = 0; jj < r; jj++) {
+                    const float bf = bf16_bits_to_f32(brow[jj]);
+#pragma unroll
+                    for (int m = 0; m < MP; m++) {
+                        float tv;
+                        if (r <= kMaxRSmem) {
+                            tv = s_T[m * r + jj];
+                        } else {
+                            tv = 0.0f;
+                            for (int q = 0; q < p.NS; q++)
+                                tv += __ldcg(p.tpart + ((size_t)q * MP + m) * r + jj);
+                        }
+                        lora[m] = __fmaf_rn(tv, bf, lora[m]);
                     }
                 }
             }
-            const float yv = __fmaf_rn(s_t, a1, p.lora_scale * lora);
-            const size_t o = (size_t)m * p.N + n;
-            if (p.y_fp32)
-                reinterpret_cast<float *>(p.y)[o] = yv;
-            else
-                reinterpret_cast<__nv_bfloat16 *>(p.y)[o] = __float2bfloat16_rn(yv);
+#pragma unroll
+            for (int m = 0; m < MP; m++) {
+                if (m < p.M) {
+                    const float yv = __fmaf_rn(s_t, a1[m], p.lora_scale * lora[m]);
+                    const size_t o = (size_t)m * p.N + n;
+                    if (p.y_fp32)
+                        reinterpret_cast<float *>(p.y)[o] = yv;
+                    else
+                        reinterpret_cast<__nv_bfloat16 *>(p.y)[o] = __float2bfloat16_rn(yv);
+                }
+            }
         }
         if (cover > 1 && threadIdx.x == 0)
             p.tcnt[rt] = 0;
@@ -764,11 +839,19 @@ cudaError_t launch_decode_gemm(const GemmArgs &a, cudaStream_t s, const DeviceIn
         pp.NJG = pl.NJG;
         pp.conv_blocks = pl.conv_blocks;
         const int pro_blocks = pl.conv_blocks + (a.r > 0 ? pl.NJG * pl.NS : 0);
-        if (pl.MP == 8)
-            decode_prologue_kernel<8><<<pro_blocks, kThreads, 0, s>>>(pp);
-        else
-            decode_prologue_kernel<16><<<pro_blocks, kThreads, 0, s>>>(pp);
-        cudaError_t err = cudaGetLastError();
+        cudaLaunchAttribute pattr[1];
+        pattr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        pattr[0].val.programmaticStreamSerializationAllowed = 1;
+        cudaLaunchConfig_t pcfg = {};
+        pcfg.gridDim = dim3(pro_blocks);
+        pcfg.blockDim = dim3(kThreads);
+        pcfg.stream = s;
+        pcfg.attrs = pattr;
+        pcfg.numAttrs = 1;
+        void *pargs[] = {&pp};
+        cudaError_t err = cudaLaunchKernelExC(
+            &pcfg, pl.MP == 8 ? (const void *)decode_prologue_kernel<8> : (const void *)decode_prologue_kernel<16>,
+            pargs);
         if (err != cudaSuccess)
             return err;
 
