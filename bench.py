@@ -194,7 +194,26 @@ class Workload:
         self.new_scales = {n: t.empty_like(self.rep[0][n].scales) for n in ("up", "down")}
         self.qbuf = {n: (t.empty_like(self.rep[0][n].codes), t.empty_like(self.rep[0][n].scales),
                          t.zeros(1, dtype=t.float32, device=dev)) for n in ("up", "down")}
-        self.launches_per_step = 2 * 2 + len(MS) * 2 + 2
+        # fused quantiser: 1 kernel per matrix; GEMM: prologue + main kernel
+        self.launches_per_step = 2 * 1 + len(MS) * 2 * 2 + 2
+
+    def op_quantize(self):
+        for n in ("up", "down"):
+            codes, scales, ts = self.qbuf[n]
+            self.nv.nvfp4_quantize(self.w[n], codes, scales, ts, False, self.ws)
+
+    def op_gemm(self, M, i):
+        R = len(self.rep)
+        for j, n in enumerate(("up", "down")):
+            q = self.rep[(i * 2 + j) % R][n]
+            a, b = self.lora[n]
+            self.nv.nvfp4_w4a16_lora_gemm(self.x[(n, M)], q.codes, q.scales, q.tensor_scale, a, b,
+                                          LORA_SCALE, self.z[n], self.y[(n, M)], self.ws)
+
+    def op_round(self):
+        for n in ("up", "down"):
+            q = self.rep[0][n]
+            self.nv.nvfp4_round_scales(self.param[n], q.tensor_scale, self.new_scales[n], self.ws)
 
     def step(self, i, ev=None):
         """One pass of the path.  ev: optional dict of (start, end) event lists
@@ -231,12 +250,36 @@ class Workload:
                                                                 self.new_scales[n], self.ws))
 
 
-def kernel_breakdown(ev):
-    out = {}
-    for kind, pairs in ev.items():
-        ms = [s.elapsed_time(e) for s, e in pairs]
-        out[kind] = {"launches": len(ms), "mean_us": 1e3 * sum(ms) / len(ms), "total_ms": sum(ms)}
-    return out
+def capture(torch, fn):
+    """CUDA graph of fn() (None if capture is not possible here)."""
+    try:
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(side):
+            fn()  # warm path on the capture stream
+            torch.cuda.synchronize()
+            with torch.cuda.graph(g, stream=side):
+                fn()
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        return g
+    except Exception as exc:  # noqa: BLE001 - report and fall back to eager launches
+        print(f"graph capture unavailable: {exc}", file=sys.stderr)
+        return None
+
+
+def time_replays(torch, runs, reps):
+    """Mean device time (ms) of runs[i % len(runs)]() over reps calls."""
+    s = torch.cuda.Event(enable_timing=True)
+    e = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    s.record()
+    for i in range(reps):
+        runs[i % len(runs)]()
+    e.record()
+    torch.cuda.synchronize()
+    return s.elapsed_time(e) / reps
 
 
 def run_gpu(args):
@@ -254,15 +297,24 @@ def run_gpu(args):
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     dev = torch.device("cuda", local)
     nv.load()
-    wl = Workload(torch, nv, synth, dev, replicas=9)
+    R = 9
+    wl = Workload(torch, nv, synth, dev, replicas=R)
     torch.cuda.synchronize()
-
     for i in range(args.warmup):
         wl.step(i)
     torch.cuda.synchronize()
     st = nv.nvfp4_get_device_status(wl.ws)
     if st != nv.OK:
         raise RuntimeError(f"device status after warm-up: {nv.status_string(st)}")
+
+    # one graph per replica-rotation index: step i replays graph i % R
+    graphs = None if args.eager else [capture(torch, lambda i=i: wl.step(i)) for i in range(R)]
+    if graphs is not None and any(g is None for g in graphs):
+        graphs = None
+    runs = [g.replay for g in graphs] if graphs else [lambda i=i: wl.step(i) for i in range(R)]
+    for i in range(args.warmup):
+        runs[i % R]()
+    torch.cuda.synchronize()
 
     props = torch.cuda.get_device_properties(dev)
     uuid = "GPU-" + str(props.uuid) if not str(props.uuid).startswith("GPU-") else str(props.uuid)
@@ -278,7 +330,7 @@ def run_gpu(args):
     end = torch.cuda.Event(enable_timing=True)
     start.record()
     for i in range(args.steps):
-        wl.step(args.warmup + i)
+        runs[i % R]()
     end.record()
     torch.cuda.synchronize()
     total_ms = start.elapsed_time(end)
@@ -288,13 +340,20 @@ def run_gpu(args):
         total_ms = float(tt.item())
     clocks = sampler.stop()
 
-    # per-launch timing pass (separate, so that the event records do not
-    # perturb the timed region)
-    ev = {}
-    for i in range(args.steps):
-        wl.step(args.warmup + args.steps + i, ev)
-    torch.cuda.synchronize()
-    kb = kernel_breakdown(ev)
+    # per-operation device times, each operation kind in graphs of its own
+    def op_runs(fn_of_i):
+        if graphs:
+            gs = [capture(torch, lambda i=i: fn_of_i(i)) for i in range(R)]
+            if all(g is not None for g in gs):
+                return [g.replay for g in gs]
+        return [lambda i=i: fn_of_i(i) for i in range(R)]
+
+    reps = max(args.steps, 2 * R)
+    kb = {}
+    kb["quantize"] = time_replays(torch, op_runs(lambda i: wl.op_quantize()), reps) / 2
+    for M in MS:
+        kb[f"gemm_M{M}"] = time_replays(torch, op_runs(lambda i, M=M: wl.op_gemm(M, i)), reps) / 2
+    kb["round_scales"] = time_replays(torch, op_runs(lambda i: wl.op_round()), reps) / 2
     st = nv.nvfp4_get_device_status(wl.ws)
     if st != nv.OK:
         raise RuntimeError(f"device status after timing: {nv.status_string(st)}")
@@ -307,40 +366,36 @@ def run_gpu(args):
     value = world * bytes_step / (ms_step * 1e-3) / 1e9
     peak_hbm, peak_tf, peak_kind = load_peaks()
 
-    # roofline of the dominant kernel kind
-    gemm_kinds = [k for k in kb if k.startswith("gemm_")]
-    gemm_total = sum(kb[k]["total_ms"] for k in gemm_kinds)
-    quant_total = kb["quantize"]["total_ms"]
-    if gemm_total >= quant_total:
-        launches = sum(kb[k]["launches"] for k in gemm_kinds)
+    # roofline of the dominant operation kind (time per step)
+    gemm_ms = sum(kb[f"gemm_M{M}"] for M in MS) * 2
+    quant_ms = kb["quantize"] * 2
+    if gemm_ms >= quant_ms:
         alg = sum(gemm_bytes(M, *s, R_LORA) for M in MS for s in (UP, DOWN)) / (2 * len(MS))
-        dur = gemm_total / launches * 1e-3
-        kern = "decode_gemm"
+        dur = gemm_ms / (2 * len(MS)) * 1e-3
+        kern, tkey = "decode_gemm", "decode_main"
     else:
-        launches = kb["quantize"]["launches"]
         alg = sum(quant_bytes(*s) for s in (UP, DOWN)) / 2
-        dur = quant_total / launches * 1e-3
-        kern = "quantize"
+        dur = kb["quantize"] * 1e-3
+        kern, tkey = "quantize", "quantize_fused"
     achieved = alg / dur / 1e9
     roof = {"kernel": kern, "bound": "hbm", "achieved": round(achieved, 1), "peak": peak_hbm,
             "peak_source": peak_kind, "unit": "GB/s", "frac": round(achieved / peak_hbm, 4),
-            "traffic": traffic_record(kern), "alg_bytes_per_launch": alg}
+            "traffic": traffic_record(tkey), "alg_bytes_per_launch": alg,
+            "timing": "CUDA events around graph replays of the operation (all of its kernels)"}
 
     per_kernel = {}
     for M in MS:
-        k = f"gemm_M{M}"
-        if k in kb:
-            b = sum(gemm_bytes(M, *s, R_LORA) for s in (UP, DOWN)) / 2
-            f = sum(gemm_flops(M, *s, R_LORA) for s in (UP, DOWN)) / 2
-            us = kb[k]["mean_us"]
-            per_kernel[k] = {"mean_us": round(us, 2), "GB/s": round(b / us / 1e3, 1),
-                             "TFLOP/s": round(f / us / 1e6, 2),
-                             "frac_hbm": round(b / us / 1e3 / peak_hbm, 4)}
-    q_us = kb["quantize"]["mean_us"]
+        b = sum(gemm_bytes(M, *s, R_LORA) for s in (UP, DOWN)) / 2
+        f = sum(gemm_flops(M, *s, R_LORA) for s in (UP, DOWN)) / 2
+        us = kb[f"gemm_M{M}"] * 1e3
+        per_kernel[f"gemm_M{M}"] = {"mean_us": round(us, 2), "GB/s": round(b / us / 1e3, 1),
+                                    "TFLOP/s": round(f / us / 1e6, 2),
+                                    "frac_hbm": round(b / us / 1e3 / peak_hbm, 4)}
+    q_us = kb["quantize"] * 1e3
     qb = sum(quant_bytes(*s) for s in (UP, DOWN)) / 2
     per_kernel["quantize"] = {"mean_us": round(q_us, 2), "GB/s": round(qb / q_us / 1e3, 1),
                               "frac_hbm": round(qb / q_us / 1e3 / peak_hbm, 4)}
-    r_us = kb["round_scales"]["mean_us"]
+    r_us = kb["round_scales"] * 1e3
     rb = sum(round_bytes(*s) for s in (UP, DOWN)) / 2
     per_kernel["round_scales"] = {"mean_us": round(r_us, 2), "GB/s": round(rb / r_us / 1e3, 1)}
 
@@ -353,17 +408,41 @@ def run_gpu(args):
         "config": {"workload": WORKLOAD, "layers": {"up": list(UP), "down": list(DOWN)}, "M": list(MS),
                    "lora_rank": R_LORA, "noise_sigma": SIGMA, "bytes_per_step": bytes_step,
                    "l2": "inputs larger than L2 (272 MB bf16 weights; GEMMs read a 9-replica ring, 0.69 GB)",
+                   "launch": "CUDA graph replay of each step" if graphs else "eager launches",
                    "parallelism": f"replicas x{world}"},
         "roofline": roof, "kernels": per_kernel, "clocks": clocks, "e2e": e2e,
         "gpu_launches": wl.launches_per_step * args.steps,
     }
     if rank == 0:
+        if args.prefill:
+            line["prefill"] = run_prefill_case(torch, nv, synth, peak_tf)
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(seconds=args.cpu_seconds)
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()
+
+
+def run_prefill_case(torch, nv, synth, peak_tf):
+    """16384 tokens x 7B-shaped up projection (tensor-core path), bf16 output."""
+    M, (N, K) = 16384, UP
+    dev = lambda b: torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(torch.bfloat16).cuda()
+    w = dev(synth.normal_weight((N, K), 0.02, 0, outlier_frac=1e-3))
+    ws = nv.new_workspace(nv.nvfp4_workspace_bytes(M, N, K, R_LORA))
+    q = nv.quantize(w, workspace=ws)
+    a, b = synth.lora_pair(N, K, R_LORA, 0.01, 2)
+    a, b = dev(a), dev(b)
+    z = torch.from_numpy(synth.noise_vector(K, SIGMA, 3)).cuda()
+    x = dev(synth.activations(M, K, 10))
+    y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    op = lambda: nv.nvfp4_w4a16_lora_gemm(x, q.codes, q.scales, q.tensor_scale, a, b, LORA_SCALE, z, y, ws)
+    op()
+    ms = time_replays(torch, [op], 5)
+    f = gemm_flops(M, N, K, R_LORA)
+    return {"workload": "16384 x 18944 x 3584 + LoRA r=32, bf16 out", "ms": round(ms, 3),
+            "TFLOP/s": round(f / ms / 1e9, 1), "peak_bf16_tflops": peak_tf,
+            "frac": round(f / ms / 1e9 / peak_tf, 4)}
 
 
 def run_e2e(torch, nv, wl, dev, args):
@@ -541,19 +620,14 @@ def run_kernel_case(case, reps):
         nbytes, flops = gemm_bytes(M, *shape, R_LORA), gemm_flops(M, *shape, R_LORA)
     op()
     torch.cuda.synchronize()
-    s = torch.cuda.Event(enable_timing=True)
-    e = torch.cuda.Event(enable_timing=True)
-    s.record()
-    for _ in range(reps):
-        op()
-    e.record()
-    torch.cuda.synchronize()
-    us = s.elapsed_time(e) * 1e3 / reps
+    us_eager = time_replays(torch, [op], reps) * 1e3
+    g = capture(torch, op)
+    us = time_replays(torch, [g.replay], reps) * 1e3 if g is not None else us_eager
     st = nv.nvfp4_get_device_status(ws)
     if st != nv.OK:
         raise RuntimeError(nv.status_string(st))
-    print(f"kernel case {case}: {reps} reps, {us:.2f} us/call, {nbytes / us / 1e3:.1f} GB/s, "
-          f"{flops / us / 1e6:.1f} TFLOP/s")
+    print(f"kernel case {case}: {reps} reps, graph {us:.2f} us/call (eager {us_eager:.2f}), "
+          f"{nbytes / us / 1e3:.1f} GB/s, {flops / us / 1e6:.1f} TFLOP/s")
 
 
 def main():
@@ -566,6 +640,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--eager", action="store_true", help="time eager launches instead of CUDA graphs")
+    ap.add_argument("--prefill", action="store_true", help="also time the 16384-token tensor-core GEMM")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     args = ap.parse_args()
     if args.warmup < 3:

@@ -40,6 +40,7 @@
 //      order.
 #include <algorithm>
 #include <mutex>
+#include <unordered_map>
 
 #include "common.cuh"
 #include "internal.h"
@@ -808,11 +809,51 @@ void query_decode_occupancy(DeviceInfo &dev)
     dev.decode_blocks_per_sm[1] = lo16;
 }
 
+// Plans depend only on (device, token tile, N, K, r): computed once, then
+// looked up, so that a call costs the host a hash lookup and two launches.
+struct PlanKey {
+    int device, MP;
+    int64_t N, K, r;
+    bool operator==(const PlanKey &o) const
+    {
+        return device == o.device && MP == o.MP && N == o.N && K == o.K && r == o.r;
+    }
+};
+struct PlanKeyHash {
+    size_t operator()(const PlanKey &k) const
+    {
+        size_t h = std::hash<int64_t>()(k.N * 1000003 + k.K);
+        return h ^ (std::hash<int64_t>()(k.r * 131 + k.MP * 7 + k.device) << 1);
+    }
+};
+static std::mutex g_plan_mu;
+static std::unordered_map<PlanKey, DecodePlan, PlanKeyHash> g_plans;
+
+static bool cached_plan(int64_t M, int64_t N, int64_t K, int64_t r, const DeviceInfo &dev, DecodePlan &pl)
+{
+    const PlanKey key{dev.device, M <= 8 ? 8 : 16, N, K, r};
+    {
+        std::lock_guard<std::mutex> lk(g_plan_mu);
+        auto it = g_plans.find(key);
+        if (it != g_plans.end()) {
+            pl = it->second;
+            return true;
+        }
+    }
+    if (!make_plan(M, N, K, r, dev, pl))
+        return false;
+    std::lock_guard<std::mutex> lk(g_plan_mu);
+    if (g_plans.size() > 4096)
+        g_plans.clear();
+    g_plans[key] = pl;
+    return true;
+}
+
 size_t decode_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t r, const DeviceInfo &dev)
 {
     // token groups of 16 (M > 16) run one after another on the same workspace
     DecodePlan pl;
-    if (!make_plan(std::min<int64_t>(M, 16), N, K, r, dev, pl))
+    if (!cached_plan(std::min<int64_t>(M, 16), N, K, r, dev, pl))
         return 0;
     return pl.total;
 }
@@ -822,7 +863,7 @@ cudaError_t launch_decode_gemm(const GemmArgs &a, cudaStream_t s, const DeviceIn
     for (int64_t m0 = 0; m0 < a.M; m0 += 16) {
         const int64_t Mg = std::min<int64_t>(16, a.M - m0);
         DecodePlan pl;
-        if (!make_plan(Mg, a.N, a.K, a.r, dev, pl))
+        if (!cached_plan(Mg, a.N, a.K, a.r, dev, pl))
             return cudaErrorInvalidConfiguration;
         PrologueParams pp;
         pp.x = a.x + m0 * a.K;
