@@ -112,6 +112,13 @@ nvfp4_status nvfp4_w4a16_lora_gemm(const void *x_bf16, int64_t M, int64_t N, int
                                    void *y, nvfp4_dtype y_dtype,
                                    void *workspace, size_t ws_bytes, void *stream);
 
+/* Which kernel family nvfp4_w4a16_lora_gemm runs for these sizes on the
+ * current device (no counterpart on the pages): "prefill_tcgen05" (M >= 64,
+ * K % 64 == 0, r <= 64 and r % 8 == 0), "decode_stream" (bulk-copy streaming
+ * decode kernel: K % 256 == 0), "decode_registers" (any other K), or NULL
+ * for invalid sizes or an unsupported device.  A static string. */
+const char *nvfp4_gemm_kernel(int64_t M, int64_t N, int64_t K, int64_t r);
+
 /* Diagnostics (no counterpart on the pages): make one of the library's
  * bounded device-side waits run out on purpose -- which == 0: an mbarrier
  * wait that no arrival completes; which == 1: a grid barrier expecting one

@@ -25,7 +25,7 @@ OUT_BF16, OUT_FP32 = 0, 1
 EXPORTS = [
     "nvfp4_workspace_bytes", "nvfp4_quantize", "nvfp4_dequantize", "nvfp4_w4a16_lora_gemm",
     "nvfp4_round_scales", "nvfp4_get_device_status", "nvfp4_status_string", "nvfp4_encode_debug",
-    "nvfp4_quotient_check", "nvfp4_w4a16_lora_gemm_static", "nvfp4_wait_selftest",
+    "nvfp4_quotient_check", "nvfp4_w4a16_lora_gemm_static", "nvfp4_wait_selftest", "nvfp4_gemm_kernel",
 ]
 
 
@@ -67,6 +67,7 @@ def load(build_if_missing: bool = True):
             "nvfp4_w4a16_lora_gemm_static": (st, [P, i64, i64, i64, P, P, P, P, P, i64, ctypes.c_float,
                                                   P, P, ctypes.c_int, P]),
             "nvfp4_wait_selftest": (st, [P, ctypes.c_int, P]),
+            "nvfp4_gemm_kernel": (ctypes.c_char_p, [i64, i64, i64, i64]),
         }
         for name, (res, args) in sig.items():
             f = getattr(lib, name)
@@ -74,6 +75,12 @@ def load(build_if_missing: bool = True):
             f.argtypes = args
         _lib = lib
         return lib
+
+
+def gemm_kernel(M: int, N: int, K: int, r: int = 0):
+    """Kernel family nvfp4_w4a16_lora_gemm runs for these sizes (None if unsupported)."""
+    name = load().nvfp4_gemm_kernel(M, N, K, r)
+    return None if name is None else name.decode()
 
 
 def status_string(status: int) -> str:

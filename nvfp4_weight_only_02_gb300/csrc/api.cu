@@ -34,6 +34,7 @@ const DeviceInfo *device_info(nvfp4_status *st)
             return nullptr;
         }
         query_decode_occupancy(di);
+        query_stream_occupancy(di);
         query_quantize_occupancy(di);
         di.device = d;
     }
@@ -152,7 +153,24 @@ nvfp4_status nvfp4_w4a16_lora_gemm(const void *x_bf16, int64_t M, int64_t N, int
     a.ws_bytes = ws_bytes;
     if (prefill_supported(M, N, K, a.r))
         return from_cuda(launch_prefill_gemm(a, (cudaStream_t)stream, *dev));
+    if (stream_supported(N, K, a.r, *dev))
+        return from_cuda(launch_stream_gemm(a, (cudaStream_t)stream, *dev));
     return from_cuda(launch_decode_gemm(a, (cudaStream_t)stream, *dev));
+}
+
+const char *nvfp4_gemm_kernel(int64_t M, int64_t N, int64_t K, int64_t r)
+{
+    if (M < 1 || N < 1 || K < 16 || K % 16 != 0 || r < 0 || r > 256 || N > (1LL << 30) || K > (1LL << 30))
+        return nullptr;
+    nvfp4_status st;
+    const DeviceInfo *dev = device_info(&st);
+    if (!dev)
+        return nullptr;
+    if (prefill_supported(M, N, K, r))
+        return "prefill_tcgen05";
+    if (stream_supported(N, K, r, *dev))
+        return "decode_stream";
+    return "decode_registers";
 }
 
 nvfp4_status nvfp4_round_scales(const float *scale_param, const float *tensor_scale, int64_t N,

@@ -26,12 +26,18 @@ enum CtlWord : int {
     CTL_BAR_COUNT = 3,    // grid barrier: arrivals
     CTL_BAR_GEN = 4,      // grid barrier: generation
     CTL_RS_COUNT = 5,     // reserved
+    CTL_GEN = 6,          // streaming decode GEMM: calls completed on this workspace (mod 2^32)
+    CTL_DONE = 7,         // streaming decode GEMM: blocks of the current call that have finished
 };
 constexpr size_t kCtlBytes = 256;
 // After the control block: arrival counters at a fixed place, so that calls
 // of any shape find them at zero (every kernel that counts resets its
 // counters before it returns).  Per-call scratch starts after them.
+// Words [0, kTileCounters) count arrivals per output tile (decode GEMMs);
+// words [kTileCounters, kCounterWords) are the streaming decode GEMM's
+// per-chunk ready flags (they hold call generations, never need clearing).
 constexpr int kCounterWords = 8192;
+constexpr int kTileCounters = 4096;
 constexpr size_t kWsHeaderBytes = kCtlBytes + 4 * (size_t)kCounterWords;
 
 // Spin limit of every device-side wait: about a second of polling, after

@@ -755,7 +755,7 @@ static bool make_plan(int64_t M, int64_t N, int64_t K, int64_t r, const DeviceIn
     }
     const int rows = wrows * pl.RG;
     pl.R = (int)((N + rows - 1) / rows);
-    if ((long long)pl.R * pl.S > (1LL << 30) || pl.R > kCounterWords)
+    if ((long long)pl.R * pl.S > (1LL << 30) || pl.R > kTileCounters)
         return false;
     pl.U = pl.R * pl.S;
     pl.P = (int)std::min<long long>((long long)dev.num_sms * bps, pl.U);

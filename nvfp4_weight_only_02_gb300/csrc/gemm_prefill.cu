@@ -430,6 +430,24 @@ static cudaError_t get_encoder(PFN_cuTensorMapEncodeTiled_v12000 *fn)
     return cudaSuccess;
 }
 
+cudaError_t encode_tensor_map_2d(CUtensorMap *map, CUtensorMapDataType dt, const void *base, uint64_t inner,
+                                 uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
+                                 CUtensorMapSwizzle swizzle)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 encode;
+    cudaError_t e = get_encoder(&encode);
+    if (e != cudaSuccess)
+        return e;
+    const cuuint64_t gdim[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
+    const cuuint64_t gstride[1] = {(cuuint64_t)row_bytes};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t estride[2] = {1, 1};
+    CUresult cr = encode(map, dt, 2, const_cast<void *>(base), gdim, gstride, box, estride,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return cr == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 struct PrefillPlan {
     size_t off_xh, off_fac, off_T, total;
 };
@@ -474,20 +492,11 @@ cudaError_t launch_prefill_gemm(const GemmArgs &a, cudaStream_t s, const DeviceI
     if (r > 0)
         prefill_lora_down_kernel<<<(M + 63) / 64, 128, 0, s>>>(a.x, a.noise, a.lora_a, M, K, r, T);
 
-    PFN_cuTensorMapEncodeTiled_v12000 encode;
-    cudaError_t e = get_encoder(&encode);
+    CUtensorMap tmap;
+    cudaError_t e = encode_tensor_map_2d(&tmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, xh, (uint64_t)K, (uint64_t)M,
+                                         (uint64_t)K * 2, kPfBK, kPfBM, CU_TENSOR_MAP_SWIZZLE_128B);
     if (e != cudaSuccess)
         return e;
-    CUtensorMap tmap;
-    const cuuint64_t gdim[2] = {(cuuint64_t)K, (cuuint64_t)M};
-    const cuuint64_t gstride[1] = {(cuuint64_t)K * 2};
-    const cuuint32_t box[2] = {(cuuint32_t)kPfBK, (cuuint32_t)kPfBM};
-    const cuuint32_t estride[2] = {1, 1};
-    CUresult cr = encode(&tmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, xh, gdim, gstride, box, estride,
-                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (cr != CUDA_SUCCESS)
-        return cudaErrorInvalidValue;
 
     PrefillParams p;
     p.M = M;

@@ -1,0 +1,1030 @@
+// gemm_stream.cu -- the decode GEMM (M <= 16 tokens per launch, LoRA rank
+// r <= 64) for weights whose rows are 16-byte aligned in both arrays
+// (K % 256 == 0; every Qwen2.5 projection): one kernel per launch that
+// streams the weight bytes through a shared-memory ring with TMA.
+//
+//   X' = bf16(X * z),   Y = s_t * X' deq(W)^T + s * (X' A^T) B^T
+// ("RL with NVFP4 + LoRA" post, tggo.me/sberlogasci/42740, section "Метод";
+// rollouts are memory-bound on the weights, section "Эксперименты").
+//
+// Work is split into units (128-row tile, 512-column chunk), spread evenly
+// over one block per SM (stream-K).  A block has 16 consumer warps, one
+// producer warp and three idle warps (which keep the register split even
+// across the SM's four schedulers).
+//
+//  * Before the kernel may read anything an earlier kernel wrote, the
+//    producer asks L2 to prefetch the first weight boxes of its range (a
+//    prefetch moves nothing into the SM, so it cannot observe stale data);
+//    with programmatic dependent launch this overlaps the previous kernel.
+//  * Chunk c's activations are prepared once per launch by one block (chunk
+//    c belongs to block floor(c G / C)): its consumer warps form
+//    X' = bf16(X z), re-express it as f16 times a power of two per token
+//    (the chunk max lands in [2^14, 2^15); every bf16 value of the chunk
+//    within 2^28 of that max stays exact), store it in the order the MMA B
+//    fragments are read, and compute the chunk's LoRA down-projection
+//    T_c = X'_c A_c^T with bf16 mma.sync.  The block then publishes the chunk
+//    by writing the launch's generation number into the chunk's flag.
+//  * The producer streams each unit's codes (two 128 x 128-byte boxes, 128B
+//    swizzle) and block scales (128 x 32 bytes) with 2-D TMA into a 3- or
+//    4-deep ring of stages, and, once the chunk's flag is up, the chunk's X',
+//    power-of-two factors and T_c with bulk copies; all complete on the
+//    stage's mbarrier.
+//  * Consumer warp (row group mt, half h) owns 16 rows and 256 columns of a
+//    stage: lane t of a quad holds 64 consecutive columns (two 16-byte loads
+//    per row and one scale word), converts codes with cvt.e2m1x2 -> f16x2
+//    and one f16x2 multiply by the block scale (exact: v * dec(e) has at most
+//    6 significant bits) and issues mma.sync m16n8k16 (f16, FP32 accumulate)
+//    with the tokens as N; the MMA k index is permuted so these
+//    lane-contiguous columns meet the matching X' fragments.  Each unit's
+//    sums are scaled back by the chunk's power of two; half-1 warps also add
+//    up T over the block's chunks of the tile, in shared memory.
+//  * At the end of a tile segment the halves' sums are added in shared
+//    memory, and the block's share of the output, s_t * acc + s * T_R B^T
+//    (LoRA-up as bf16 MMAs against T_R split into hi + lo bf16 parts), is
+//    either stored (the block holds the whole tile) or left in the workspace
+//    for the last block to arrive, which adds the shares in block order
+//    (results do not depend on arrival order).
+//  * The last block to finish advances the workspace's generation number.
+#include <algorithm>
+#include <mutex>
+#include <unordered_map>
+
+#include "common.cuh"
+#include "internal.h"
+#include "sm100.cuh"
+
+namespace nvfp4 {
+namespace stream {
+
+using namespace sm100;
+
+constexpr int kRows = 128;               // weight rows per tile
+constexpr int kChunk = 512;              // columns per unit (= X' scaling chunk)
+constexpr int kBoxBytes = 128 * kRows;   // one code box: 128 rows x 128 bytes (256 columns)
+constexpr int kScaleBox = 32 * kRows;    // scale box: 128 rows x 32 bytes
+constexpr int kCWarps = 16;              // consumer warps: 8 row groups x 2 column halves
+constexpr int kProducer = kCWarps;       // warp index of the producer
+constexpr int kThreads = (kCWarps + 4) * 32;
+constexpr int kMaxR = 64;
+constexpr int kMaxKS = kMaxR / 16;       // LoRA k-steps of 16 columns of T
+constexpr int kPrefetchUnits = 6;        // units per block prefetched into L2 before the wait
+constexpr size_t kXhOff = 2 * kBoxBytes + kScaleBox;
+constexpr uint64_t kFlagWaitNs = 2000000000ull;
+
+// named barriers (0 is __syncthreads)
+constexpr int kBarGroup = 9;       // the 8 half-0 consumer warps
+constexpr int kBarConsumers = 10;  // all 16 consumer warps
+
+template <int MP>
+__host__ __device__ constexpr int n_stages()
+{
+    return MP == 8 ? 4 : 3;
+}
+template <int MP>
+__host__ __device__ constexpr size_t fac_off()
+{
+    return kXhOff + (size_t)MP * 1024;
+}
+template <int MP>
+__host__ __device__ constexpr size_t t_off()
+{
+    return fac_off<MP>() + 128;
+}
+template <int MP>
+__host__ __device__ constexpr size_t stage_bytes()  // a multiple of 1024 (swizzled boxes)
+{
+    return (t_off<MP>() + (size_t)kMaxKS * (MP / 8) * 512 + 1023) / 1024 * 1024;
+}
+template <int MP>
+__host__ __device__ constexpr size_t red_bytes()  // 2 buffers x 8 row groups x 32 lanes x MP/2 floats
+{
+    return (size_t)2 * 8 * 32 * (MP / 2) * 4;
+}
+template <int MP>
+__host__ __device__ constexpr size_t tacc_bytes()  // 2 buffers of T summed over a segment
+{
+    return (size_t)2 * kMaxKS * (MP / 8) * 32 * 16;
+}
+template <int MP>
+__host__ __device__ constexpr size_t xb_off()
+{
+    return n_stages<MP>() * stage_bytes<MP>() + red_bytes<MP>() + tacc_bytes<MP>();
+}
+template <int MP>
+__host__ __device__ constexpr size_t smem_bytes()  // + 1 KB to align the ring, + barriers
+{
+    return 1024 + xb_off<MP>() + (size_t)MP * 1024 + 128;
+}
+
+__device__ __forceinline__ void pdl_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void pdl_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_acquire(const uint32_t *p)
+{
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release(uint32_t *p, uint32_t v)
+{
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void prefetch_l2(const void *ptr)
+{
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
+}
+
+// Generic-proxy global writes/reads ordered against bulk-copy (async proxy) accesses.
+__device__ __forceinline__ void fence_proxy_async_global()
+{
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+__device__ __forceinline__ int owner_of(int u, int U, int G)
+{
+    return (int)(((long long)(u + 1) * G - 1) / U);
+}
+
+__device__ __forceinline__ int range_begin(int b, int U, int G)
+{
+    return (int)((long long)b * U / G);
+}
+
+// 16-byte unit `ux` (8 columns) of token `m` inside a chunk's 1 KB of X':
+// the unit index is XORed, inside its 8-unit group, by a key that differs
+// across the 8 lanes of each quarter warp that read it together.
+__host__ __device__ __forceinline__ int xh_unit(int m, int ux)
+{
+    return ux ^ (((m & 1) << 2) | ((ux >> 3) & 3));
+}
+
+__device__ __forceinline__ float bf16_round(float v) { return __bfloat162float(__float2bfloat16_rn(v)); }
+
+struct Params {
+    CUtensorMap tm_codes;   // codes, N x K/2 bytes: boxes of 128 x 128, 128B swizzle
+    CUtensorMap tm_scales;  // scales, N x K/16 bytes: boxes of 128 x 32
+    int M, N, K, r, C, U, KS;  // KS: LoRA k-steps (1, 2 or 4; 0 without LoRA)
+    const uint16_t *x;         // M x K bf16 (this token group)
+    const float *noise;        // K floats or null
+    const uint16_t *lora_a;    // r x K bf16
+    const uint16_t *lora_b;    // N x r bf16
+    float lora_scale;
+    const float *tensor_scale;
+    uint8_t *xh;               // [C][MP][1024]: X' as f16, swizzled
+    float *fac;                // [C][MP]: 2^p per token and chunk
+    float4 *tpart;             // [C][KS][MP/8][32]: T_c in B-fragment order
+    float *part;               // [G][2][8][32][MP/2]: tile shares left for the last block
+    uint32_t *tcnt;            // tile arrival counters
+    uint32_t *ready;           // chunk flags
+    uint32_t *ctl;
+    void *y;
+    int y_fp32;
+};
+
+// ---------------------------------------------------------------- chunk preparation
+// All 16 consumer warps of the block that owns chunk c.  Warp m < M forms
+// X' of token m (lane l: columns 16l..16l+15): bf16 into shared memory for
+// the LoRA down-projection, f16 times 2^p into the workspace for every
+// block.  Then T_c = X'_c A_c^T by bf16 mma.sync with the tokens as the M
+// dimension; the k index of each MMA is permuted exactly as in the main
+// loop (lane t of a quad holds 64 consecutive columns of a 256-column half),
+// so each lane reads A in 16-byte pieces and X' in conflict-free 16-byte
+// units.  Warps split (8-column n-tile of T, half, k-step pairs); one warp
+// per n-tile sums the parts in fixed order and stores them in the layout the
+// epilogue loads as B fragments.  Finally the chunk is published.
+template <int MP>
+__device__ void prepare_chunk(const Params &p, int c, uint32_t gen, uint8_t *xb, float4 *scratch)
+{
+    constexpr int NT = MP / 8;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    const int kbase = c * kChunk;
+    const int halves = kbase + kChunk <= p.K ? 2 : 1;
+    // the activations first: they are on the critical path
+    const int k0 = kbase + lane * 16;
+    const bool conv = warp < p.M, kin = conv && k0 < p.K;
+    uint4 xa = make_uint4(0u, 0u, 0u, 0u), xc = xa;
+    float4 z4[4];
+    if (kin) {
+        const uint4 *xs = reinterpret_cast<const uint4 *>(p.x + (size_t)warp * p.K + k0);
+        xa = __ldcg(xs);
+        xc = __ldcg(xs + 1);
+        if (p.noise) {
+            const float4 *zs = reinterpret_cast<const float4 *>(p.noise + k0);
+#pragma unroll
+            for (int q = 0; q < 4; q++)
+                z4[q] = __ldcg(zs + q);
+        }
+    }
+    // LoRA A operand: warp -> (n-tile jt, half hh, part sub of its 8 k-step pairs)
+    const int njt = 2 * p.KS;                  // 2, 4 or 8 n-tiles (0 without LoRA)
+    const int nunit = njt * halves;            // 2..16, divides 16
+    const int wpu = nunit > 0 ? kCWarps / nunit : 1;
+    const int unit = warp / wpu, sub = warp % wpu;
+    const int jt = unit / halves, hh = unit % halves;
+    const int npairs = 8 / wpu;                // k-step pairs per warp
+    const int jrow = jt * 8 + g;
+    // the first (up to) four pairs now, the rest (rank 64 only) after the conversion
+    const uint16_t *arow = p.lora_a + (size_t)min(jrow, max(p.r - 1, 0)) * p.K + kbase + 256 * hh + 64 * t;
+    uint4 af[4];
+    if (p.KS > 0) {
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+            const bool ok = q < npairs && jrow < p.r;
+            af[q] = ok ? __ldcg(reinterpret_cast<const uint4 *>(arow + 8 * (sub * npairs + q)))
+                       : make_uint4(0u, 0u, 0u, 0u);
+        }
+    }
+    if (conv) {
+        const uint32_t xw[8] = {xa.x, xa.y, xa.z, xa.w, xc.x, xc.y, xc.z, xc.w};
+        float v[16];
+        float mx = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 16; i++) {
+            float f = bf16_bits_to_f32((xw[i / 2] >> (16 * (i & 1))) & 0xFFFFu);
+            if (kin && p.noise) {
+                const float4 zq = z4[i / 4];
+                const float z = (i & 3) == 0 ? zq.x : (i & 3) == 1 ? zq.y : (i & 3) == 2 ? zq.z : zq.w;
+                f = bf16_round(__fmul_rn(f, z));
+            }
+            v[i] = f;
+            mx = fmaxf(mx, fabsf(f));
+        }
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1)
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+        int pexp = 0;
+        if (mx > 0.0f) {
+            const uint32_t b = __float_as_uint(mx);
+            const int e = (b >> 23) ? (int)(b >> 23) - 127 : (31 - __clz(b)) - 149;
+            pexp = e - 14;
+        }
+        uint8_t *dst = p.xh + ((size_t)c * MP + warp) * 1024;
+#pragma unroll
+        for (int u2 = 0; u2 < 2; u2++) {
+            uint32_t hw[4], bw[4];
+#pragma unroll
+            for (int i = 0; i < 4; i++) {
+                const float lo = v[8 * u2 + 2 * i], hi = v[8 * u2 + 2 * i + 1];
+                __half2 h2 = __halves2half2(__float2half_rn(scale_pow2(lo, -pexp)),
+                                            __float2half_rn(scale_pow2(hi, -pexp)));
+                hw[i] = *reinterpret_cast<uint32_t *>(&h2);
+                __nv_bfloat162 b2 = __floats2bfloat162_rn(lo, hi);  // exact: lo, hi are bf16 values
+                bw[i] = *reinterpret_cast<uint32_t *>(&b2);
+            }
+            const int off = 16 * xh_unit(warp, 2 * lane + u2);
+            *reinterpret_cast<uint4 *>(dst + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            *reinterpret_cast<uint4 *>(xb + warp * 1024 + off) = make_uint4(bw[0], bw[1], bw[2], bw[3]);
+        }
+        if (lane == 0)
+            p.fac[c * MP + warp] = exp2i(pexp);
+    }
+    named_sync(kBarConsumers, kCWarps * 32);  // bf16 X' complete in shared memory
+    if (p.KS > 0) {
+        float cc[4] = {0.f, 0.f, 0.f, 0.f};
+        const uint8_t *x0r = xb + g * 1024, *x1r = xb + (g + 8) * 1024;
+#pragma unroll
+        for (int q = 0; q < 8; q++) {
+            if (q == 4 && npairs > 4) {
+#pragma unroll
+                for (int q2 = 0; q2 < 4; q2++)
+                    af[q2] = jrow < p.r ? __ldcg(reinterpret_cast<const uint4 *>(arow + 8 * (sub * npairs + 4 + q2)))
+                                        : make_uint4(0u, 0u, 0u, 0u);
+            }
+            if (q < npairs) {
+                const int ux = 32 * hh + 8 * t + sub * npairs + q;  // 8 columns: two k-steps
+                const uint4 x0 = g < p.M ? *reinterpret_cast<const uint4 *>(x0r + 16 * xh_unit(g, ux))
+                                         : make_uint4(0u, 0u, 0u, 0u);
+                const uint4 x1 = g + 8 < p.M ? *reinterpret_cast<const uint4 *>(x1r + 16 * xh_unit(g + 8, ux))
+                                             : make_uint4(0u, 0u, 0u, 0u);
+                uint32_t a[4] = {x0.x, x1.x, x0.y, x1.y};
+                mma_bf16_16816(cc, a, af[q & 3].x, af[q & 3].y);
+                a[0] = x0.z;
+                a[1] = x1.z;
+                a[2] = x0.w;
+                a[3] = x1.w;
+                mma_bf16_16816(cc, a, af[q & 3].z, af[q & 3].w);
+            }
+        }
+        scratch[warp * 32 + lane] = make_float4(cc[0], cc[1], cc[2], cc[3]);
+        named_sync(kBarConsumers, kCWarps * 32);
+        if (hh == 0 && sub == 0) {  // sum n-tile jt over halves and parts, fixed order
+            float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int w = 0; w < halves * wpu; w++) {
+                const float4 o = scratch[(warp + w) * 32 + lane];
+                s.x += o.x;
+                s.y += o.y;
+                s.z += o.z;
+                s.w += o.w;
+            }
+            // lane (g, t) holds T[g][8jt + 2t, +1] (x, y) and T[g+8][...] (z, w)
+            const int ks = jt / 2, jh = jt % 2;
+            float2 *d0 = reinterpret_cast<float2 *>(p.tpart + (((size_t)c * p.KS + ks) * NT + 0) * 32 + lane) + jh;
+            *d0 = make_float2(s.x, s.y);
+            if (NT == 2) {
+                float2 *d1 = reinterpret_cast<float2 *>(p.tpart + (((size_t)c * p.KS + ks) * NT + 1) * 32 + lane) + jh;
+                *d1 = make_float2(s.z, s.w);
+            }
+        }
+    }
+    __threadfence();
+    named_sync(kBarConsumers, kCWarps * 32);  // every store of the chunk done and fenced
+    if (threadIdx.x == 0)
+        st_release(&p.ready[c], gen + 1u);
+}
+
+// ---------------------------------------------------------------- consumers
+// Four E4M3 scale bytes -> four f16x2, each holding one scale twice (exact).
+__device__ __forceinline__ void e4m3x4_to_h2dup(uint32_t w, uint32_t (&o)[4])
+{
+    uint32_t lo, hi;
+    const uint16_t w0 = (uint16_t)(w & 0xFFFFu), w1 = (uint16_t)(w >> 16);
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(lo) : "h"(w0));
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(hi) : "h"(w1));
+    o[0] = __byte_perm(lo, 0, 0x1010);
+    o[1] = __byte_perm(lo, 0, 0x3232);
+    o[2] = __byte_perm(hi, 0, 0x1010);
+    o[3] = __byte_perm(hi, 0, 0x3232);
+}
+
+__device__ __forceinline__ uint32_t word_of(const uint4 &v, int i)
+{
+    return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
+
+// One consumer warp's share of a stage: rows 16*mt + g, +8; columns
+// 256*h + 64*t .. +63.  k-step 2j+e uses columns 64t + 8j + 4e .. +3: code
+// bytes 2e, 2e+1 of word j, scale byte j/2, X' unit j (words 2e, 2e+1).
+// Code box h holds 128-byte rows whose 16-byte chunk c sits at c ^ (row % 8).
+template <int MP>
+__device__ __forceinline__ void compute_unit(const uint8_t *st, int mt, int h, int g, int t, int M,
+                                             float (&acc)[MP / 8][4])
+{
+    constexpr int NT = MP / 8;
+    const uint8_t *cb = st + h * kBoxBytes;
+    const uint8_t *sb = st + 2 * kBoxBytes;
+    const uint8_t *xb = st + kXhOff;
+    const float *fb = reinterpret_cast<const float *>(st + fac_off<MP>());
+    const int row0 = 16 * mt + g;  // row0 % 8 == g, and (row0 + 8) % 8 == g
+    const uint8_t *r0p = cb + row0 * 128, *r1p = cb + (row0 + 8) * 128;
+    const int ca = 16 * ((2 * t) ^ g), cbb = 16 * ((2 * t + 1) ^ g);
+    const uint4 c00 = *reinterpret_cast<const uint4 *>(r0p + ca);
+    const uint4 c01 = *reinterpret_cast<const uint4 *>(r0p + cbb);
+    const uint4 c10 = *reinterpret_cast<const uint4 *>(r1p + ca);
+    const uint4 c11 = *reinterpret_cast<const uint4 *>(r1p + cbb);
+    const uint32_t sw0 = *reinterpret_cast<const uint32_t *>(sb + row0 * 32 + h * 16 + 4 * t);
+    const uint32_t sw1 = *reinterpret_cast<const uint32_t *>(sb + (row0 + 8) * 32 + h * 16 + 4 * t);
+    uint32_t s0[4], s1[4];
+    e4m3x4_to_h2dup(sw0, s0);
+    e4m3x4_to_h2dup(sw1, s1);
+    const int key = ((g & 1) << 2) | t;
+    const uint8_t *xrow = xb + h * 512 + t * 128;
+    // CS independent accumulator sets (by k-step) keep four MMA chains in flight
+    constexpr int CS = 4 / NT;
+    float cur[CS][NT][4];
+#pragma unroll
+    for (int c = 0; c < CS; c++)
+#pragma unroll
+        for (int nt = 0; nt < NT; nt++)
+#pragma unroll
+            for (int q = 0; q < 4; q++)
+                cur[c][nt][q] = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 8; j++) {
+        uint4 xf[NT];
+#pragma unroll
+        for (int nt = 0; nt < NT; nt++) {
+            const int tok = g + 8 * nt;
+            xf[nt] = tok < M ? *reinterpret_cast<const uint4 *>(xrow + tok * 1024 + 16 * (j ^ key))
+                             : make_uint4(0u, 0u, 0u, 0u);
+        }
+        const uint32_t w0 = word_of(j < 4 ? c00 : c01, j & 3);
+        const uint32_t w1 = word_of(j < 4 ? c10 : c11, j & 3);
+        uint32_t r0[4], r1[4];
+        e2m1x8_to_h2x4(w0, r0);
+        e2m1x8_to_h2x4(w1, r1);
+        const uint32_t sa = s0[j >> 1], sc = s1[j >> 1];
+        uint32_t a[4];
+        a[0] = hmul2_u32(r0[0], sa);
+        a[1] = hmul2_u32(r1[0], sc);
+        a[2] = hmul2_u32(r0[1], sa);
+        a[3] = hmul2_u32(r1[1], sc);
+#pragma unroll
+        for (int nt = 0; nt < NT; nt++)
+            mma_f16_16816(cur[(2 * j) % CS][nt], a, xf[nt].x, xf[nt].y);
+        a[0] = hmul2_u32(r0[2], sa);
+        a[1] = hmul2_u32(r1[2], sc);
+        a[2] = hmul2_u32(r0[3], sa);
+        a[3] = hmul2_u32(r1[3], sc);
+#pragma unroll
+        for (int nt = 0; nt < NT; nt++)
+            mma_f16_16816(cur[(2 * j + 1) % CS][nt], a, xf[nt].z, xf[nt].w);
+    }
+#pragma unroll
+    for (int nt = 0; nt < NT; nt++) {
+        const float2 f = *reinterpret_cast<const float2 *>(fb + 8 * nt + 2 * t);
+        float v[4];
+#pragma unroll
+        for (int q = 0; q < 4; q++)
+            v[q] = CS == 4 ? (cur[0][nt][q] + cur[1][nt][q]) + (cur[2 % CS][nt][q] + cur[3 % CS][nt][q])
+                           : cur[0][nt][q] + cur[1 % CS][nt][q];
+        acc[nt][0] = __fmaf_rn(v[0], f.x, acc[nt][0]);
+        acc[nt][1] = __fmaf_rn(v[1], f.y, acc[nt][1]);
+        acc[nt][2] = __fmaf_rn(v[2], f.x, acc[nt][2]);
+        acc[nt][3] = __fmaf_rn(v[3], f.y, acc[nt][3]);
+    }
+}
+
+// Two LoRA B entries (row R, columns j, j+1) as a bf16 pair; zero outside.
+__device__ __forceinline__ uint32_t lora_pair(const Params &p, int R, int j)
+{
+    if (R >= p.N || j >= p.r)
+        return 0u;
+    const uint16_t *row = p.lora_b + (size_t)R * p.r;
+    if ((p.r & 1) == 0)
+        return __ldcg(reinterpret_cast<const uint32_t *>(row + j));
+    const uint32_t lo = __ldcg(row + j);
+    const uint32_t hi = j + 1 < p.r ? (uint32_t)__ldcg(row + j + 1) : 0u;
+    return lo | (hi << 16);
+}
+
+__device__ __forceinline__ uint32_t bf16x2_bits(float a, float b)
+{
+    __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// The block's share of tile n for half-0 warp mt: s_t * acc + s * T_R B^T.
+template <int MP>
+__device__ __forceinline__ void tile_share(const Params &p, int n, int mt, int lane, float s_t,
+                                           const float (&acc)[MP / 8][4], const float4 *tr, float (&out)[MP / 8][4])
+{
+    constexpr int NT = MP / 8;
+    const int g = lane >> 2, t = lane & 3;
+    const int R0 = n * kRows + 16 * mt + g, R1 = R0 + 8;
+    float cl[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; nt++)
+#pragma unroll
+        for (int q = 0; q < 4; q++)
+            cl[nt][q] = 0.0f;
+#pragma unroll
+    for (int ks = 0; ks < kMaxKS; ks++) {
+        if (ks < p.KS) {
+            uint32_t a[4];
+            a[0] = lora_pair(p, R0, 16 * ks + 2 * t);
+            a[1] = lora_pair(p, R1, 16 * ks + 2 * t);
+            a[2] = lora_pair(p, R0, 16 * ks + 8 + 2 * t);
+            a[3] = lora_pair(p, R1, 16 * ks + 8 + 2 * t);
+#pragma unroll
+            for (int nt = 0; nt < NT; nt++) {
+                const float4 v = tr[(ks * NT + nt) * 32 + lane];
+                const uint32_t h0 = bf16x2_bits(v.x, v.y), h1 = bf16x2_bits(v.z, v.w);
+                const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&h0));
+                const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&h1));
+                const uint32_t l0 = bf16x2_bits(v.x - f0.x, v.y - f0.y), l1 = bf16x2_bits(v.z - f1.x, v.w - f1.y);
+                mma_bf16_16816(cl[nt], a, h0, h1);
+                mma_bf16_16816(cl[nt], a, l0, l1);
+            }
+        }
+    }
+#pragma unroll
+    for (int nt = 0; nt < NT; nt++)
+#pragma unroll
+        for (int q = 0; q < 4; q++)
+            out[nt][q] = __fmaf_rn(s_t, acc[nt][q], p.lora_scale * cl[nt][q]);
+}
+
+template <int MP>
+__device__ __forceinline__ void store_tile(const Params &p, int n, int mt, int lane, const float (&y)[MP / 8][4])
+{
+    constexpr int NT = MP / 8;
+    const int g = lane >> 2, t = lane & 3;
+    const int R0 = n * kRows + 16 * mt + g;
+#pragma unroll
+    for (int nt = 0; nt < NT; nt++)
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+            const int R = R0 + 8 * (q >> 1);
+            const int tok = 8 * nt + 2 * t + (q & 1);
+            if (tok < p.M && R < p.N) {
+                const size_t o = (size_t)tok * p.N + R;
+                if (p.y_fp32)
+                    reinterpret_cast<float *>(p.y)[o] = y[nt][q];
+                else
+                    reinterpret_cast<__nv_bfloat16 *>(p.y)[o] = __float2bfloat16_rn(y[nt][q]);
+            }
+        }
+}
+
+// End of the block's segment of tile n (consumer warp mt, half h).
+template <int MP>
+__device__ __forceinline__ void finish_segment(const Params &p, int n, int u0, int mt, int h, int lane,
+                                               float (&acc)[MP / 8][4], const float4 *tr, float *red, int buf,
+                                               volatile uint32_t *s_flag, float s_t)
+{
+    constexpr int NT = MP / 8;
+    const int G = gridDim.x, b = blockIdx.x;
+    float4 *rb = reinterpret_cast<float4 *>(red) + ((size_t)(buf * 8 + mt) * 32 + lane) * NT;
+    if (h == 1) {
+#pragma unroll
+        for (int nt = 0; nt < NT; nt++)
+            rb[nt] = make_float4(acc[nt][0], acc[nt][1], acc[nt][2], acc[nt][3]);
+    }
+    named_sync(kBarConsumers, kCWarps * 32);  // half-1 sums and the segment's T in shared memory
+    if (h == 0) {
+#pragma unroll
+        for (int nt = 0; nt < NT; nt++) {
+            const float4 v = rb[nt];
+            acc[nt][0] += v.x;
+            acc[nt][1] += v.y;
+            acc[nt][2] += v.z;
+            acc[nt][3] += v.w;
+        }
+        float y[NT][4];
+        tile_share<MP>(p, n, mt, lane, s_t, acc, tr, y);
+        const int first = owner_of(n * p.C, p.U, G), last = owner_of(n * p.C + p.C - 1, p.U, G);
+        bool finish = true;
+        if (last > first) {
+            const int slot = (u0 / p.C == n) ? 0 : 1;
+            float4 *dst = reinterpret_cast<float4 *>(p.part) + ((((size_t)b * 2 + slot) * 8 + mt) * 32 + lane) * NT;
+#pragma unroll
+            for (int nt = 0; nt < NT; nt++)
+                __stcg(dst + nt, make_float4(y[nt][0], y[nt][1], y[nt][2], y[nt][3]));
+            named_sync(kBarGroup, 256);
+            if (mt == 0 && lane == 0) {
+                __threadfence();
+                *s_flag = atomicAdd(&p.tcnt[n], 1u) == (uint32_t)(last - first);
+            }
+            named_sync(kBarGroup, 256);
+            finish = *s_flag != 0;
+            if (finish) {
+                __threadfence();
+                // every other block's share in batched loads, added in block order
+                constexpr int KB = 4;
+                float tot[NT][4];
+#pragma unroll
+                for (int nt = 0; nt < NT; nt++)
+#pragma unroll
+                    for (int q = 0; q < 4; q++)
+                        tot[nt][q] = 0.0f;
+                for (int bb0 = first; bb0 <= last; bb0 += KB) {
+                    float4 v[KB][NT];
+#pragma unroll
+                    for (int k = 0; k < KB; k++) {
+                        const int bb = bb0 + k;
+                        const int sl = (range_begin(bb, p.U, G) / p.C == n) ? 0 : 1;
+                        const float4 *src = reinterpret_cast<const float4 *>(p.part) +
+                                            ((((size_t)bb * 2 + sl) * 8 + mt) * 32 + lane) * NT;
+#pragma unroll
+                        for (int nt = 0; nt < NT; nt++)
+                            v[k][nt] = (bb <= last && bb != b) ? __ldcg(src + nt)
+                                                               : make_float4(y[nt][0], y[nt][1], y[nt][2], y[nt][3]);
+                    }
+#pragma unroll
+                    for (int k = 0; k < KB; k++)
+                        if (bb0 + k <= last)
+#pragma unroll
+                            for (int nt = 0; nt < NT; nt++) {
+                                tot[nt][0] += v[k][nt].x;
+                                tot[nt][1] += v[k][nt].y;
+                                tot[nt][2] += v[k][nt].z;
+                                tot[nt][3] += v[k][nt].w;
+                            }
+                }
+#pragma unroll
+                for (int nt = 0; nt < NT; nt++)
+#pragma unroll
+                    for (int q = 0; q < 4; q++)
+                        y[nt][q] = tot[nt][q];
+                if (mt == 0 && lane == 0)
+                    p.tcnt[n] = 0;
+            }
+        }
+        if (finish)
+            store_tile<MP>(p, n, mt, lane, y);
+    }
+#pragma unroll
+    for (int nt = 0; nt < NT; nt++)
+#pragma unroll
+        for (int q = 0; q < 4; q++)
+            acc[nt][q] = 0.0f;
+}
+
+template <int MP>
+__global__ void __launch_bounds__(kThreads, 1) stream_gemm_kernel(const __grid_constant__ Params p)
+{
+    constexpr int NT = MP / 8;
+    constexpr int S = n_stages<MP>();
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    float *red = reinterpret_cast<float *>(smem + S * stage_bytes<MP>());
+    float4 *tacc = reinterpret_cast<float4 *>(smem + S * stage_bytes<MP>() + red_bytes<MP>());
+    uint8_t *xb = smem + xb_off<MP>();
+    uint64_t *full = reinterpret_cast<uint64_t *>(xb + MP * 1024);
+    uint64_t *empty = full + S;
+    volatile uint32_t *s_flag = reinterpret_cast<volatile uint32_t *>(empty + S);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int G = gridDim.x, b = blockIdx.x;
+    const int u0 = range_begin(b, p.U, G), u1 = range_begin(b + 1, p.U, G);
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; s++) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kCWarps);
+        }
+        mbar_fence_init();
+    }
+    __syncthreads();
+
+    if (warp == kProducer) {
+        // ---------------- producer warp (lane 0 issues every copy)
+        if (lane == 0) {
+            // the weights of the first units into L2 while the previous kernels finish
+            for (int u = u0; u < min(u1, u0 + kPrefetchUnits); u++) {
+                const int n = u / p.C, c = u - n * p.C;
+                tma_prefetch_2d(&p.tm_codes, c * (kChunk / 2), n * kRows);
+                if ((c + 1) * kChunk <= p.K)
+                    tma_prefetch_2d(&p.tm_codes, c * (kChunk / 2) + 128, n * kRows);
+                tma_prefetch_2d(&p.tm_scales, c * (kChunk / 16), n * kRows);
+            }
+        }
+        pdl_wait();
+        const uint32_t gen = *reinterpret_cast<volatile const uint32_t *>(&p.ctl[CTL_GEN]);
+        const uint32_t xbytes = (uint32_t)p.M * 1024u, fbytes = (uint32_t)MP * 4u;
+        const uint32_t tbytes = (uint32_t)p.KS * NT * 512u;
+        const int nunits = u1 - u0;
+        bool ok = true;
+        auto issue_weights = [&](int i) {
+            const int u = u0 + i, s = i % S;
+            const int n = u / p.C, c = u - n * p.C;
+            const bool two = (c + 1) * kChunk <= p.K;  // else a last 256-column chunk
+            uint8_t *st = smem + (size_t)s * stage_bytes<MP>();
+            mbar_arrive_expect_tx(&full[s], (two ? 2 : 1) * kBoxBytes + kScaleBox + xbytes + fbytes + tbytes);
+            tma_load_2d(st, &p.tm_codes, &full[s], c * (kChunk / 2), n * kRows);
+            if (two)
+                tma_load_2d(st + kBoxBytes, &p.tm_codes, &full[s], c * (kChunk / 2) + 128, n * kRows);
+            tma_load_2d(st + 2 * kBoxBytes, &p.tm_scales, &full[s], c * (kChunk / 16), n * kRows);
+        };
+        if (lane == 0)
+            for (int i = 0; i < min(S, nunits); i++)
+                issue_weights(i);
+        // every chunk of the range published (one acquire per chunk, all lanes at once)
+        {
+            const int nchk = min(nunits, p.C);
+            const uint64_t t0 = globaltimer();
+            for (;;) {
+                bool ready = true;
+                for (int k = lane; k < nchk; k += 32)
+                    ready = ready && ld_acquire(&p.ready[(u0 + k) % p.C]) == gen + 1u;
+                if (__all_sync(0xffffffffu, ready))
+                    break;
+                if (globaltimer() - t0 > kFlagWaitNs) {
+                    if (lane == 0)
+                        record_status(p.ctl, NVFP4_ERR_TIMEOUT);
+                    break;
+                }
+                __nanosleep(32);
+            }
+            __syncwarp();
+        }
+        if (lane == 0) {
+            fence_proxy_async_global();
+            for (int i = 0; i < nunits; i++) {
+                const int u = u0 + i, s = i % S;
+                if (i >= S) {
+                    if (ok && !mbar_wait(&empty[s], ((i / S) + 1) & 1)) {
+                        record_status(p.ctl, NVFP4_ERR_TIMEOUT);
+                        ok = false;
+                    }
+                    if (!ok)
+                        continue;  // stop copying; consumers time out and wind down
+                    issue_weights(i);
+                }
+                const int c = u % p.C;
+                uint8_t *st = smem + (size_t)s * stage_bytes<MP>();
+                bulk_g2s(st + kXhOff, p.xh + (size_t)c * MP * 1024, xbytes, &full[s]);
+                bulk_g2s(st + fac_off<MP>(), p.fac + (size_t)c * MP, fbytes, &full[s]);
+                if (tbytes)
+                    bulk_g2s(st + t_off<MP>(), p.tpart + (size_t)c * p.KS * NT * 32, tbytes, &full[s]);
+            }
+        }
+        __syncwarp();
+        pdl_launch_dependents();
+    } else if (warp < kCWarps) {
+        // ---------------- consumer warps
+        // chunks this block prepares: those with floor(c G / C) == b
+        const int c_lo = (int)(((long long)b * p.C + G - 1) / G);
+        const int c_hi = (int)(((long long)(b + 1) * p.C + G - 1) / G);
+        // before the wait: L2 prefetches of the chunk's activations, noise and
+        // LoRA A rows (no data reaches the SM; address translation and L2
+        // fills overlap the previous kernel)
+        for (int c = c_lo; c < c_hi; c++) {
+            const int kb = c * kChunk + lane * 16;
+            if (kb < p.K) {
+                if (warp < p.M)
+                    prefetch_l2(p.x + (size_t)warp * p.K + kb);
+                if (warp == kCWarps - 1 && p.noise)
+                    prefetch_l2(p.noise + kb);
+                if (p.KS > 0)
+                    for (int j = warp; j < p.r; j += kCWarps)
+                        prefetch_l2(p.lora_a + (size_t)j * p.K + kb);
+            }
+        }
+        pdl_wait();
+        const uint32_t gen = *reinterpret_cast<volatile const uint32_t *>(&p.ctl[CTL_GEN]);
+        for (int c = c_lo; c < c_hi; c++)
+            prepare_chunk<MP>(p, c, gen, xb, reinterpret_cast<float4 *>(red));
+        if (c_hi > c_lo)
+            named_sync(kBarConsumers, kCWarps * 32);  // scratch free before segment ends use it
+
+        const int mt = warp & 7, h = warp >> 3, g = lane >> 2, t = lane & 3;
+        const float s_t = __ldcg(p.tensor_scale);
+        float acc[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; nt++)
+#pragma unroll
+            for (int q = 0; q < 4; q++)
+                acc[nt][q] = 0.0f;
+        const int tn = p.KS * NT * 32;  // float4 of T per chunk
+        bool ok = true;
+        bool seg_start = true;
+        int buf = 0;
+        for (int u = u0, i = 0; u < u1; u++, i++) {
+            const int s = i % S;
+            if (ok && !mbar_wait(&full[s], (i / S) & 1)) {
+                ok = false;
+                if (lane == 0)
+                    record_status(p.ctl, NVFP4_ERR_TIMEOUT);
+            }
+            const int n = u / p.C, c = u - n * p.C;
+            const uint8_t *st = smem + (size_t)s * stage_bytes<MP>();
+            if (h == 0 || (c + 1) * kChunk <= p.K)
+                compute_unit<MP>(st, mt, h, g, t, p.M, acc);
+            if (h == 1) {  // T of this chunk into the segment's sum (element mt*32 + lane, ...)
+                const float4 *ts = reinterpret_cast<const float4 *>(st + t_off<MP>());
+                float4 *ta = tacc + buf * (kMaxKS * NT * 32);
+                for (int e = mt * 32 + lane; e < tn; e += 256) {
+                    const float4 v = ts[e];
+                    if (seg_start) {
+                        ta[e] = v;
+                    } else {
+                        float4 o = ta[e];
+                        o.x += v.x;
+                        o.y += v.y;
+                        o.z += v.z;
+                        o.w += v.w;
+                        ta[e] = o;
+                    }
+                }
+            }
+            seg_start = false;
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&empty[s]);
+            if (u + 1 == u1)
+                pdl_launch_dependents();
+            if (u + 1 == u1 || c + 1 == p.C) {
+                finish_segment<MP>(p, n, u0, mt, h, lane, acc, tacc + buf * (kMaxKS * NT * 32), red, buf, s_flag,
+                                   s_t);
+                buf ^= 1;
+                seg_start = true;
+            }
+        }
+    } else {
+        pdl_launch_dependents();  // idle warps
+    }
+
+    // the last block to finish advances the workspace generation
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const uint32_t gen = *reinterpret_cast<volatile const uint32_t *>(&p.ctl[CTL_GEN]);
+        __threadfence();
+        if (atomicAdd(&p.ctl[CTL_DONE], 1u) == (uint32_t)G - 1) {
+            p.ctl[CTL_DONE] = 0;
+            p.ctl[CTL_GEN] = gen + 1u;
+            __threadfence();
+        }
+    }
+}
+
+// ================================================================ host side
+struct Plan {
+    int MP, C, tiles, U, G, KS;
+    size_t off_xh, off_fac, off_tpart, off_part, total;
+};
+
+static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+static bool make_plan(int64_t M, int64_t N, int64_t K, int64_t r, const DeviceInfo &dev, Plan &pl)
+{
+    if (!dev.stream_ok || K % 256 != 0 || M < 1 || M > 16 || r < 0 || r > kMaxR)
+        return false;
+    pl.MP = M <= 8 ? 8 : 16;
+    pl.C = (int)((K + kChunk - 1) / kChunk);
+    pl.tiles = (int)((N + kRows - 1) / kRows);
+    if (pl.tiles > kTileCounters || pl.C > kCounterWords - kTileCounters ||
+        (long long)pl.tiles * pl.C > (1LL << 30))
+        return false;
+    pl.U = pl.tiles * pl.C;
+    pl.G = std::min(dev.num_sms, pl.U);
+    pl.KS = r == 0 ? 0 : r <= 16 ? 1 : r <= 32 ? 2 : 4;
+    size_t off = kWsHeaderBytes;
+    pl.off_xh = off;
+    off = align_up(off + (size_t)pl.C * pl.MP * 1024, 256);
+    pl.off_fac = off;
+    off = align_up(off + (size_t)pl.C * pl.MP * 4, 256);
+    pl.off_tpart = off;
+    off = align_up(off + (size_t)pl.C * std::max(pl.KS, 1) * (pl.MP / 8) * 512, 256);
+    pl.off_part = off;
+    off = align_up(off + (size_t)pl.G * 2 * kRows * pl.MP * 4, 256);
+    pl.total = off;
+    return true;
+}
+
+struct PlanKey {
+    int device, MP;
+    int64_t N, K, r;
+    bool operator==(const PlanKey &o) const
+    {
+        return device == o.device && MP == o.MP && N == o.N && K == o.K && r == o.r;
+    }
+};
+struct PlanKeyHash {
+    size_t operator()(const PlanKey &k) const
+    {
+        size_t h = std::hash<int64_t>()(k.N * 1000003 + k.K);
+        return h ^ (std::hash<int64_t>()(k.r * 131 + k.MP * 7 + k.device) << 1);
+    }
+};
+static std::mutex g_plan_mu;
+static std::unordered_map<PlanKey, Plan, PlanKeyHash> g_plans;
+
+static bool cached_plan(int64_t M, int64_t N, int64_t K, int64_t r, const DeviceInfo &dev, Plan &pl)
+{
+    const PlanKey key{dev.device, M <= 8 ? 8 : 16, N, K, r};
+    {
+        std::lock_guard<std::mutex> lk(g_plan_mu);
+        auto it = g_plans.find(key);
+        if (it != g_plans.end()) {
+            pl = it->second;
+            return true;
+        }
+    }
+    if (!make_plan(M, N, K, r, dev, pl))
+        return false;
+    std::lock_guard<std::mutex> lk(g_plan_mu);
+    if (g_plans.size() > 4096)
+        g_plans.clear();
+    g_plans[key] = pl;
+    return true;
+}
+
+// Tensor maps of one weight (codes, scales), cached by address and shape.
+struct MapKey {
+    const void *codes, *scales;
+    int64_t N, K;
+    bool operator==(const MapKey &o) const
+    {
+        return codes == o.codes && scales == o.scales && N == o.N && K == o.K;
+    }
+};
+struct MapKeyHash {
+    size_t operator()(const MapKey &k) const
+    {
+        return std::hash<const void *>()(k.codes) ^ (std::hash<const void *>()(k.scales) << 1) ^
+               std::hash<int64_t>()(k.N * 1000003 + k.K);
+    }
+};
+struct MapPair {
+    CUtensorMap codes, scales;
+};
+static std::mutex g_map_mu;
+static std::unordered_map<MapKey, MapPair, MapKeyHash> g_maps;
+
+static cudaError_t weight_maps(const GemmArgs &a, MapPair &mp)
+{
+    const MapKey key{a.codes, a.scales, a.N, a.K};
+    {
+        std::lock_guard<std::mutex> lk(g_map_mu);
+        auto it = g_maps.find(key);
+        if (it != g_maps.end()) {
+            mp = it->second;
+            return cudaSuccess;
+        }
+    }
+    cudaError_t e = encode_tensor_map_2d(&mp.codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.codes, (uint64_t)a.K / 2,
+                                         (uint64_t)a.N, (uint64_t)a.K / 2, 128, kRows, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (e != cudaSuccess)
+        return e;
+    e = encode_tensor_map_2d(&mp.scales, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.scales, (uint64_t)a.K / 16,
+                             (uint64_t)a.N, (uint64_t)a.K / 16, 32, kRows, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (e != cudaSuccess)
+        return e;
+    std::lock_guard<std::mutex> lk(g_map_mu);
+    if (g_maps.size() > 4096)
+        g_maps.clear();
+    g_maps[key] = mp;
+    return cudaSuccess;
+}
+
+}  // namespace stream
+
+void query_stream_occupancy(DeviceInfo &dev)
+{
+    using namespace stream;
+    int b8 = 0, b16 = 0;
+    if (cudaFuncSetAttribute(stream_gemm_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem_bytes<8>()) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b8, stream_gemm_kernel<8>, kThreads, smem_bytes<8>()) !=
+            cudaSuccess)
+        b8 = 0;
+    if (cudaFuncSetAttribute(stream_gemm_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem_bytes<16>()) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b16, stream_gemm_kernel<16>, kThreads, smem_bytes<16>()) !=
+            cudaSuccess)
+        b16 = 0;
+    cudaGetLastError();
+    dev.stream_ok = b8 >= 1 && b16 >= 1;
+}
+
+bool stream_supported(int64_t N, int64_t K, int64_t r, const DeviceInfo &dev)
+{
+    stream::Plan pl;
+    return stream::cached_plan(1, N, K, r, dev, pl) && stream::cached_plan(16, N, K, r, dev, pl);
+}
+
+size_t stream_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t r, const DeviceInfo &dev)
+{
+    // token groups of 16 (M > 16) run one after another on the same workspace
+    stream::Plan pl;
+    if (!stream::cached_plan(std::min<int64_t>(M, 16), N, K, r, dev, pl))
+        return 0;
+    return pl.total;
+}
+
+cudaError_t launch_stream_gemm(const GemmArgs &a, cudaStream_t s, const DeviceInfo &dev)
+{
+    using namespace stream;
+    MapPair maps;
+    cudaError_t err = weight_maps(a, maps);
+    if (err != cudaSuccess)
+        return err;
+    for (int64_t m0 = 0; m0 < a.M; m0 += 16) {
+        const int64_t Mg = std::min<int64_t>(16, a.M - m0);
+        Plan pl;
+        if (!cached_plan(Mg, a.N, a.K, a.r, dev, pl))
+            return cudaErrorInvalidConfiguration;
+        Params p;
+        p.tm_codes = maps.codes;
+        p.tm_scales = maps.scales;
+        p.M = (int)Mg;
+        p.N = (int)a.N;
+        p.K = (int)a.K;
+        p.r = (int)a.r;
+        p.C = pl.C;
+        p.U = pl.U;
+        p.KS = pl.KS;
+        p.x = a.x + m0 * a.K;
+        p.noise = a.noise;
+        p.lora_a = a.lora_a;
+        p.lora_b = a.lora_b;
+        p.lora_scale = a.lora_scale;
+        p.tensor_scale = a.tensor_scale;
+        p.xh = a.ws + pl.off_xh;
+        p.fac = reinterpret_cast<float *>(a.ws + pl.off_fac);
+        p.tpart = reinterpret_cast<float4 *>(a.ws + pl.off_tpart);
+        p.part = reinterpret_cast<float *>(a.ws + pl.off_part);
+        p.tcnt = reinterpret_cast<uint32_t *>(a.ws + kCtlBytes);
+        p.ready = p.tcnt + kTileCounters;
+        p.ctl = reinterpret_cast<uint32_t *>(a.ws);
+        p.y = a.y_fp32 ? (void *)((float *)a.y + m0 * a.N) : (void *)((uint16_t *)a.y + m0 * a.N);
+        p.y_fp32 = a.y_fp32 ? 1 : 0;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(pl.G);
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = pl.MP == 8 ? smem_bytes<8>() : smem_bytes<16>();
+        cfg.stream = s;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        void *args[] = {&p};
+        err = cudaLaunchKernelExC(
+            &cfg, pl.MP == 8 ? (const void *)stream_gemm_kernel<8> : (const void *)stream_gemm_kernel<16>, args);
+        if (err != cudaSuccess)
+            return err;
+    }
+    return cudaSuccess;
+}
+
+}  // namespace nvfp4

@@ -1,6 +1,7 @@
 // internal.h -- host-side declarations shared by the library's translation units.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -14,6 +15,7 @@ struct DeviceInfo {
     int cc_major = 0, cc_minor = 0;
     int decode_blocks_per_sm[2] = {0, 0};  // residency of the decode main kernel (MP 8, 16)
     int fused_quant_blocks = 0;            // grid of the fused dynamic quantiser (0: unavailable)
+    bool stream_ok = false;                // the streaming decode kernel fits on this device
 };
 
 // Cached per-device facts; nullptr (and *st set) when the device is unusable.
@@ -55,17 +57,34 @@ void query_decode_occupancy(DeviceInfo &dev);
 size_t decode_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t r, const DeviceInfo &dev);
 cudaError_t launch_decode_gemm(const GemmArgs &a, cudaStream_t s, const DeviceInfo &dev);
 
+// Streaming decode kernel (bulk copies through a shared-memory ring) for
+// K % 256 == 0; other K use the register-streaming decode kernel above.
+void query_stream_occupancy(DeviceInfo &dev);
+bool stream_supported(int64_t N, int64_t K, int64_t r, const DeviceInfo &dev);
+size_t stream_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t r, const DeviceInfo &dev);
+cudaError_t launch_stream_gemm(const GemmArgs &a, cudaStream_t s, const DeviceInfo &dev);
+
 // Tensor-core (tcgen05) path for many tokens; smaller M uses the decode kernel.
 constexpr int64_t kPrefillMinM = 64;
 bool prefill_supported(int64_t M, int64_t N, int64_t K, int64_t r);
 size_t prefill_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t r);
 cudaError_t launch_prefill_gemm(const GemmArgs &a, cudaStream_t s, const DeviceInfo &dev);
 
+// 2-D tiled tensor map (row-major, `row_bytes` between rows, box of
+// box_inner x box_outer elements, zero fill outside) through the driver's
+// encoder, looked up once.
+cudaError_t encode_tensor_map_2d(CUtensorMap *map, CUtensorMapDataType dt, const void *base, uint64_t inner,
+                                 uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
+                                 CUtensorMapSwizzle swizzle);
+
 // Workspace of nvfp4_w4a16_lora_gemm for these sizes (0: unsupported).
 inline size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t r, const DeviceInfo &dev)
 {
-    return prefill_supported(M, N, K, r) ? prefill_workspace_bytes(M, N, K, r)
-                                         : decode_workspace_bytes(M, N, K, r, dev);
+    if (prefill_supported(M, N, K, r))
+        return prefill_workspace_bytes(M, N, K, r);
+    if (stream_supported(N, K, r, dev))
+        return stream_workspace_bytes(M, N, K, r, dev);
+    return decode_workspace_bytes(M, N, K, r, dev);
 }
 
 }  // namespace nvfp4

@@ -1,6 +1,7 @@
 // sm100.cuh -- inline-PTX wrappers for the Blackwell data-centre features used
-// by the tensor-core prefill kernel: mbarriers, TMA tensor loads, and the
-// tcgen05 family (TMEM allocation, MMA with TMEM accumulators, commit, loads).
+// by the streaming decode and tensor-core prefill kernels: mbarriers, bulk
+// and TMA tensor copies, and the tcgen05 family (TMEM allocation, MMA with
+// TMEM accumulators, commit, loads).
 // Every wait is bounded: after about two seconds it gives up and reports it.
 #pragma once
 
@@ -81,6 +82,37 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, u
             smem_addr(dst)),
         "l"((uint64_t)map), "r"(smem_addr(bar)), "r"(x), "r"(y)
         : "memory");
+}
+
+// Hint: bring one box of a 2-D tensor map into L2 (nothing reaches the SM).
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *map, int x, int y)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"((uint64_t)map), "r"(x),
+                 "r"(y)
+                 : "memory");
+}
+
+// Plain (untiled) bulk copy of `bytes` contiguous bytes global -> shared,
+// completing on *bar.  Both addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_addr(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_addr(bar))
+                 : "memory");
+}
+
+// Hint: bring `bytes` contiguous bytes (16-byte aligned, multiple of 16) into
+// L2.  No data reaches the SM, so it is safe before the grid may read them.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+// Barrier `id` (1..15) among `nthreads` threads (a multiple of 32).
+__device__ __forceinline__ void named_sync(int id, int nthreads)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
 __device__ __forceinline__ void fence_proxy_async_smem()

@@ -66,6 +66,7 @@ def test_host_checks_reject_before_launch(lib):
     assert lib.nvfp4_dequantize(good, good, good, 4, 32, bad_align, 1, null) == binding.ERR_ALIGNMENT
     assert lib.nvfp4_round_scales(good, good, 4, 31, good, good, 256, null) == binding.ERR_SHAPE
     assert lib.nvfp4_workspace_bytes(1, 16, 30, 0) == 0
+    assert lib.nvfp4_gemm_kernel(1, 16, 30, 0) is None
     assert lib.nvfp4_encode_debug(good, 8, 5, good, null) == binding.ERR_INVALID_ARG
     assert lib.nvfp4_quotient_check(0, (1 << 23) + 1, good, null) == binding.ERR_INVALID_ARG
 

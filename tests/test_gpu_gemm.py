@@ -70,6 +70,11 @@ CASES = [
     (9, 1000, 3584, 32, True, True),
     (2, 70, 8192, 24, True, True),
     (16, 2048, 640, 64, True, True),
+    # K % 256 == 0 with a last 256-column chunk (half-chunk units)
+    (7, 200, 1280, 16, True, True),
+    (16, 129, 768, 8, True, True),
+    (12, 640, 4096, 64, True, True),
+    (1, 3, 256, 0, False, False),
 ]
 
 
@@ -83,6 +88,18 @@ def test_small_and_ragged(nv, orc, M, N, K, r, lora, noise):
     # bf16 output is the RNE rounding of the same FP32 result
     yb = _run_gpu(nv, c, q, torch.bfloat16)
     assert torch.equal(yb.cpu(), torch.from_numpy(y).to(torch.bfloat16))
+
+
+def test_kernel_selection(nv):
+    """K % 256 == 0 (every Qwen2.5 projection) takes the bulk-copy streaming
+    kernel, other K the register-streaming one, M >= 64 the tensor cores."""
+    assert nv.gemm_kernel(8, 18944, 3584, 32) == "decode_stream"
+    assert nv.gemm_kernel(16, 3584, 18944, 32) == "decode_stream"
+    assert nv.gemm_kernel(1, 27648, 5120, 64) == "decode_stream"
+    assert nv.gemm_kernel(8, 300, 1040, 16) == "decode_registers"
+    assert nv.gemm_kernel(16, 2048, 640, 64) == "decode_registers"
+    assert nv.gemm_kernel(16384, 18944, 3584, 32) == "prefill_tcgen05"
+    assert nv.gemm_kernel(8, 300, 1000, 16) is None
 
 
 def test_single_layer_case(nv, orc):
