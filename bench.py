@@ -372,7 +372,7 @@ def run_gpu(args):
     if gemm_ms >= quant_ms:
         alg = sum(gemm_bytes(M, *s, R_LORA) for M in MS for s in (UP, DOWN)) / (2 * len(MS))
         dur = gemm_ms / (2 * len(MS)) * 1e-3
-        kern, tkey = "decode_gemm", "decode_main"
+        kern, tkey = "decode_gemm", "decode_stream"
     else:
         alg = sum(quant_bytes(*s) for s in (UP, DOWN)) / 2
         dur = kb["quantize"] * 1e-3
