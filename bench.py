@@ -150,6 +150,21 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+# ----------------------------------------------------------------- ranks
+def max_over_ranks(torch, dist, ms, device, world):
+    """The slowest rank's time: every rank gets the maximum (one all-reduce)."""
+    if world <= 1:
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(world, bytes_per_step, ms_per_step):
+    """Whole-job throughput in GB/s: every rank moves bytes_per_step per step."""
+    return world * bytes_per_step / (ms_per_step * 1e-3) / 1e9
+
+
 # ----------------------------------------------------------------- GPU arm
 class Workload:
     def __init__(self, torch, nv, synth, device, replicas):
@@ -334,10 +349,7 @@ def run_gpu(args):
     end.record()
     torch.cuda.synchronize()
     total_ms = start.elapsed_time(end)
-    if world > 1:
-        tt = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    total_ms = max_over_ranks(torch, dist, total_ms, dev, world)
     clocks = sampler.stop()
 
     # per-operation device times, each operation kind in graphs of its own
@@ -363,7 +375,7 @@ def run_gpu(args):
 
     bytes_step = step_bytes()
     ms_step = total_ms / args.steps
-    value = world * bytes_step / (ms_step * 1e-3) / 1e9
+    value = job_value(world, bytes_step, ms_step)
     peak_hbm, peak_tf, peak_kind = load_peaks()
 
     # roofline of the dominant operation kind (time per step)

@@ -8,7 +8,8 @@
 // rollouts are memory-bound on the weights, section "Эксперименты").
 //
 // Work is split into units (128-row tile, 512-column chunk), spread evenly
-// over one block per SM (stream-K).  A block has 16 consumer warps, one
+// over one block per SM (stream-K; one whole tile per block when there are
+// about as many tiles as SMs).  A block has 16 consumer warps, one
 // producer warp and three idle warps (which keep the register split even
 // across the SM's four schedulers).
 //
@@ -25,8 +26,8 @@
 //    T_c = X'_c A_c^T with bf16 mma.sync.  The block then publishes the chunk
 //    by writing the launch's generation number into the chunk's flag.
 //  * The producer streams each unit's codes (two 128 x 128-byte boxes, 128B
-//    swizzle) and block scales (128 x 32 bytes) with 2-D TMA into a 3- or
-//    4-deep ring of stages, and, once the chunk's flag is up, the chunk's X',
+//    swizzle) and block scales (128 x 32 bytes) with 2-D TMA into a 2-deep
+//    ring of stages, and, once the chunk's flag is up, the chunk's X',
 //    power-of-two factors and T_c with bulk copies; all complete on the
 //    stage's mbarrier.
 //  * Consumer warp (row group mt, half h) owns 16 rows and 256 columns of a
@@ -74,11 +75,15 @@ constexpr uint64_t kFlagWaitNs = 2000000000ull;
 // named barriers (0 is __syncthreads)
 constexpr int kBarGroup = 9;       // the 8 half-0 consumer warps
 constexpr int kBarConsumers = 10;  // all 16 consumer warps
+constexpr int kBarGen = 11;        // consumers, producer and counting warp: generation read
+constexpr int kGenThreads = (kCWarps + 2) * 32;
 
+// Two stages: with the first units already prefetched into L2, a deeper ring
+// only lengthens the memory queue that every other load of the kernel waits in.
 template <int MP>
 __host__ __device__ constexpr int n_stages()
 {
-    return MP == 8 ? 4 : 3;
+    return 2;
 }
 template <int MP>
 __host__ __device__ constexpr size_t fac_off()
@@ -632,6 +637,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_gemm_kernel(const __grid_c
     uint64_t *full = reinterpret_cast<uint64_t *>(xb + MP * 1024);
     uint64_t *empty = full + S;
     volatile uint32_t *s_flag = reinterpret_cast<volatile uint32_t *>(empty + S);
+    volatile uint32_t *s_gen = s_flag + 1;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = gridDim.x, b = blockIdx.x;
@@ -658,7 +664,10 @@ __global__ void __launch_bounds__(kThreads, 1) stream_gemm_kernel(const __grid_c
             }
         }
         pdl_wait();
-        const uint32_t gen = *reinterpret_cast<volatile const uint32_t *>(&p.ctl[CTL_GEN]);
+        if (lane == 0)
+            *s_gen = *reinterpret_cast<volatile const uint32_t *>(&p.ctl[CTL_GEN]);
+        named_sync(kBarGen, kGenThreads);  // the block's generation is in shared memory
+        const uint32_t gen = *s_gen;
         const uint32_t xbytes = (uint32_t)p.M * 1024u, fbytes = (uint32_t)MP * 4u;
         const uint32_t tbytes = (uint32_t)p.KS * NT * 512u;
         const int nunits = u1 - u0;
@@ -740,7 +749,8 @@ __global__ void __launch_bounds__(kThreads, 1) stream_gemm_kernel(const __grid_c
             }
         }
         pdl_wait();
-        const uint32_t gen = *reinterpret_cast<volatile const uint32_t *>(&p.ctl[CTL_GEN]);
+        named_sync(kBarGen, kGenThreads);
+        const uint32_t gen = *s_gen;
         for (int c = c_lo; c < c_hi; c++)
             prepare_chunk<MP>(p, c, gen, xb, reinterpret_cast<float4 *>(red));
         if (c_hi > c_lo)
@@ -799,20 +809,22 @@ __global__ void __launch_bounds__(kThreads, 1) stream_gemm_kernel(const __grid_c
                 seg_start = true;
             }
         }
+    } else if (warp == kCWarps + 1) {
+        // once every block has read this launch's generation (below, after the
+        // wait, by the producer and consumer warps), the last block to count
+        // itself advances it for the next launch on this workspace
+        pdl_wait();
+        named_sync(kBarGen, kGenThreads);
+        if (lane == 0) {
+            __threadfence();
+            if (atomicAdd(&p.ctl[CTL_DONE], 1u) == (uint32_t)G - 1) {
+                p.ctl[CTL_DONE] = 0;
+                p.ctl[CTL_GEN] = *s_gen + 1u;
+            }
+        }
+        pdl_launch_dependents();
     } else {
         pdl_launch_dependents();  // idle warps
-    }
-
-    // the last block to finish advances the workspace generation
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        const uint32_t gen = *reinterpret_cast<volatile const uint32_t *>(&p.ctl[CTL_GEN]);
-        __threadfence();
-        if (atomicAdd(&p.ctl[CTL_DONE], 1u) == (uint32_t)G - 1) {
-            p.ctl[CTL_DONE] = 0;
-            p.ctl[CTL_GEN] = gen + 1u;
-            __threadfence();
-        }
     }
 }
 
@@ -836,6 +848,10 @@ static bool make_plan(int64_t M, int64_t N, int64_t K, int64_t r, const DeviceIn
         return false;
     pl.U = pl.tiles * pl.C;
     pl.G = std::min(dev.num_sms, pl.U);
+    // as many tiles as SMs, give or take 10 %: one whole tile per block, so
+    // no tile needs a cross-block hand-over at the end
+    if (pl.tiles <= dev.num_sms && pl.tiles * 10 >= dev.num_sms * 9)
+        pl.G = pl.tiles;
     pl.KS = r == 0 ? 0 : r <= 16 ? 1 : r <= 32 ? 2 : 4;
     size_t off = kWsHeaderBytes;
     pl.off_xh = off;
