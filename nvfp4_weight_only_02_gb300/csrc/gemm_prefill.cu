@@ -6,26 +6,24 @@
 // 16-bit).  With thousands of tokens the product is a dense contraction, so
 // it runs on tcgen05 MMAs with the accumulator in tensor memory.
 //
-// Operands are f16 (tcgen05 kind::f16, fp32 accumulate):
-//   * B = deq(W) / s_t = v(q) * dec(e): exact in f16 (at most 6 significant
-//     bits, 2^-10 <= |value| <= 2688), produced tile by tile in shared memory
-//     by four dequantiser warps (cvt.e2m1x2 -> f16x2, one f16x2 multiply by
-//     the block scale) in the 128-byte-swizzled K-major layout the tensor
-//     core reads;
-//   * A = X' * 2^-p_m, f16, one power of two per token chosen so that the
-//     token's largest |X'| lies in [2^14, 2^15) (exact for every value within
-//     2^28 of it), written once by a prologue kernel and fed by TMA;
-//   * Y = (s_t * 2^p_m) * acc + s * T B^T in the epilogue, with T = X' A^T
-//     computed in fp32 by a second prologue kernel (bf16 mma.sync).
-//
-// Roles in a block of 10 warps (persistent over 128 x 256 output tiles):
-//   warps 0-3  epilogue: tcgen05.ld of the accumulator, scaling, LoRA-up,
-//              stores (one TMEM lane = one output row per thread);
-//   warps 4-7  dequantiser: codes + block scales -> f16 B stage;
-//   warp 8     TMA producer of the A stage;
-//   warp 9     TMEM allocation and the single-thread MMA issue.
-// Four pipeline stages of K = 64; two accumulators of 128 x 256 fp32 in
-// TMEM (512 columns) so the epilogue of one tile overlaps the next tile.
+// Four kernels per call:
+//   * dequantise W once into f16, v(q) * dec(e) (exact in f16: at most 6
+//     significant bits, 2^-10 <= |value| <= 2688; s_t is applied in the
+//     epilogue), and lay out the LoRA B operand for the tensor core;
+//   * X' = bf16(X z) re-expressed per token as f16 * 2^p_m (the token's
+//     largest |X'| in [2^14, 2^15); exact for every value within 2^28 of it);
+//   * T = X' A^T (fp32, bf16 mma.sync), stored pre-scaled by s / c_m with
+//     c_m = s_t 2^p_m as a hi + lo pair of bf16 (2^-16 relative);
+//   * the GEMM: TMA brings 128 x 64 tiles of X' and 256 x 64 tiles of W into
+//     a 4-deep ring (128-byte swizzle); one thread issues tcgen05.mma
+//     kind::f16 (f16 operands) over K, then one or two extra K-steps of bf16
+//     MMAs of [T hi | T lo] against [B | B] into the same TMEM accumulator, so
+//     acc = X' 2^-p W^T + s T B^T / c_m and the epilogue only computes
+//     c_m * acc, converts and stores.  Two 128 x 256 fp32 accumulators in TMEM
+//     (512 columns) let the epilogue of one tile overlap the next tile.
+// Roles in a block of 6 warps (persistent over 128 x 256 output tiles):
+//   warps 0-3  epilogue (one TMEM lane = one output row per thread);
+//   warp 4     TMA producer;  warp 5  TMEM allocation and MMA issue.
 #include <cudaTypedefs.h>
 
 #include <algorithm>
@@ -43,7 +41,7 @@ constexpr int kPfBM = 128;         // tokens per tile
 constexpr int kPfBN = 256;         // weight rows per tile
 constexpr int kPfBK = 64;          // K per stage (128 bytes of f16)
 constexpr int kPfStages = 4;
-constexpr int kPfThreads = 320;
+constexpr int kPfThreads = 192;
 constexpr int kPfGroupN = 8;       // tile raster: n-tiles per group
 constexpr int kPfMaxR = 64;
 constexpr uint32_t kPfABytes = kPfBM * kPfBK * 2;  // 16 KB
@@ -51,18 +49,22 @@ constexpr uint32_t kPfBBytes = kPfBN * kPfBK * 2;  // 32 KB
 constexpr size_t kPfSmem = 1024 + kPfStages * (kPfABytes + kPfBBytes) + 256;
 
 struct PrefillParams {
-    int M, N, K, r;
-    const uint8_t *codes, *scales;
+    int M, N, K, ES;          // ES: extra K-steps of 64 for the LoRA term (0, 1 or 2)
     const float *tensor_scale;
-    const uint16_t *lora_b;  // N x r bf16
-    float lora_scale;
-    const float *fac;   // M: 2^p_m
-    const float *T;     // M x r fp32
+    const float *fac;         // M: 2^p_m
     void *y;
     int y_fp32;
     uint32_t *ctl;
     int mtiles, ntiles;
 };
+
+// c_m = s_t 2^p_m, the factor between the accumulator and Y (1 where it is
+// zero: then either the row of X' or every weight is zero)
+__device__ __forceinline__ float row_factor(float s_t, float fac_m)
+{
+    const float c = __fmul_rn(s_t != 0.0f ? s_t : 1.0f, fac_m);
+    return c != 0.0f ? c : 1.0f;
+}
 
 // ---------------------------------------------------------------- prologue
 // One warp per token: X' = bf16(X z), its max, and X' 2^-p as f16.
@@ -138,49 +140,116 @@ __device__ __forceinline__ uint32_t xprime_pair_g(const uint16_t *x, const float
     return *reinterpret_cast<uint32_t *>(&o);
 }
 
-// T = X' A^T (fp32), one warp per 16 tokens and up to 64 LoRA columns.
-__global__ void __launch_bounds__(128) prefill_lora_down_kernel(const uint16_t *__restrict__ x,
-                                                                const float *__restrict__ z,
-                                                                const uint16_t *__restrict__ a, int M, int K,
-                                                                int r, float *__restrict__ T)
+// Column of the LoRA extension operand that holds T'[.][j] (part 0 = hi,
+// 1 = lo): r <= 32 uses one 64-column step [hi | lo], r <= 64 two steps.
+__device__ __forceinline__ int ext_col(int j, int part, int ES)
+{
+    return ES == 1 ? 32 * part + j : 64 * part + j;
+}
+
+// T = X' A^T (fp32, one warp per 16 tokens, up to 64 LoRA columns), written
+// as T' = s T / c_m in bf16 hi + lo at the extension columns.  ta (M x 64 ES
+// bf16) must be zero elsewhere.
+__global__ void __launch_bounds__(128) prefill_lora_ext_kernel(const uint16_t *__restrict__ x,
+                                                               const float *__restrict__ z,
+                                                               const uint16_t *__restrict__ a, int M, int K,
+                                                               int r, int ES, float lora_scale,
+                                                               const float *__restrict__ tensor_scale,
+                                                               const float *__restrict__ fac,
+                                                               uint16_t *__restrict__ ta)
 {
     const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
     const int m0 = warp * 16;
     if (m0 >= M)
         return;
-    for (int jbase = 0; jbase < r; jbase += 64) {
-        float c[8][4];
+    float c[8][4];
 #pragma unroll
-        for (int jg = 0; jg < 8; jg++)
-            c[jg][0] = c[jg][1] = c[jg][2] = c[jg][3] = 0.0f;
-        for (int k0 = 0; k0 < K; k0 += 16) {
-            uint32_t af[4];
-            af[0] = xprime_pair_g(x, z, M, K, m0 + g, k0 + 2 * t);
-            af[1] = xprime_pair_g(x, z, M, K, m0 + g + 8, k0 + 2 * t);
-            af[2] = xprime_pair_g(x, z, M, K, m0 + g, k0 + 2 * t + 8);
-            af[3] = xprime_pair_g(x, z, M, K, m0 + g + 8, k0 + 2 * t + 8);
-#pragma unroll
-            for (int jg = 0; jg < 8; jg++) {
-                const int j = jbase + jg * 8 + g;
-                uint32_t b0 = 0, b1 = 0;
-                if (j < r) {
-                    b0 = *reinterpret_cast<const uint32_t *>(a + (size_t)j * K + k0 + 2 * t);
-                    b1 = *reinterpret_cast<const uint32_t *>(a + (size_t)j * K + k0 + 2 * t + 8);
-                }
-                mma_bf16_16816(c[jg], af, b0, b1);
-            }
-        }
+    for (int jg = 0; jg < 8; jg++)
+        c[jg][0] = c[jg][1] = c[jg][2] = c[jg][3] = 0.0f;
+    for (int k0 = 0; k0 < K; k0 += 16) {
+        uint32_t af[4];
+        af[0] = xprime_pair_g(x, z, M, K, m0 + g, k0 + 2 * t);
+        af[1] = xprime_pair_g(x, z, M, K, m0 + g + 8, k0 + 2 * t);
+        af[2] = xprime_pair_g(x, z, M, K, m0 + g, k0 + 2 * t + 8);
+        af[3] = xprime_pair_g(x, z, M, K, m0 + g + 8, k0 + 2 * t + 8);
 #pragma unroll
         for (int jg = 0; jg < 8; jg++) {
-            const int j = jbase + jg * 8 + 2 * t;
+            const int j = jg * 8 + g;
+            uint32_t b0 = 0, b1 = 0;
+            if (j < r) {
+                b0 = *reinterpret_cast<const uint32_t *>(a + (size_t)j * K + k0 + 2 * t);
+                b1 = *reinterpret_cast<const uint32_t *>(a + (size_t)j * K + k0 + 2 * t + 8);
+            }
+            mma_bf16_16816(c[jg], af, b0, b1);
+        }
+    }
+    const float s_t = *tensor_scale;
+    const int W = 64 * ES;
 #pragma unroll
-            for (int q = 0; q < 4; q++) {
-                const int m = m0 + g + 8 * (q >> 1), jj = j + (q & 1);
-                if (m < M && jj < r)
-                    T[(size_t)m * r + jj] = c[jg][q];
+    for (int q = 0; q < 4; q++) {
+        const int m = m0 + g + 8 * (q >> 1);
+        if (m >= M)
+            continue;
+        const float cm = row_factor(s_t, fac[m]);
+#pragma unroll
+        for (int jg = 0; jg < 8; jg++) {
+            const int j = jg * 8 + 2 * t + (q & 1);
+            if (j < r) {
+                const float tv = __fdiv_rn(__fmul_rn(lora_scale, c[jg][q]), cm);
+                const __nv_bfloat16 hi = __float2bfloat16_rn(tv);
+                const __nv_bfloat16 lo = __float2bfloat16_rn(tv - __bfloat162float(hi));
+                ta[(size_t)m * W + ext_col(j, 0, ES)] = *reinterpret_cast<const uint16_t *>(&hi);
+                ta[(size_t)m * W + ext_col(j, 1, ES)] = *reinterpret_cast<const uint16_t *>(&lo);
             }
         }
+    }
+}
+
+// 16 codes (8 bytes) times their block scale -> 16 f16 (two 16-byte chunks).
+__device__ __forceinline__ void dequant16(uint2 c, uint32_t sc2, uint32_t (&o)[8])
+{
+    e2m1x8_to_h2x4(c.x, o);
+    e2m1x8_to_h2x4(c.y, o + 4);
+#pragma unroll
+    for (int i = 0; i < 8; i++)
+        o[i] = hmul2_u32(o[i], sc2);
+}
+
+// deq(W)/s_t = v(q) dec(e) as f16 (N x K), and the LoRA B operand of the
+// extension steps (N x 64 ES bf16: B at the hi and at the lo columns).
+__global__ void __launch_bounds__(256) prefill_weight_kernel(const uint2 *__restrict__ codes,
+                                                             const uint8_t *__restrict__ scales, int64_t nblocks,
+                                                             uint4 *__restrict__ wh, const uint16_t *__restrict__ b,
+                                                             int N, int r, int ES, uint4 *__restrict__ tb)
+{
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nblocks; i += stride) {
+        uint32_t o[8];
+        dequant16(codes[i], e4m3_to_h2_dup(scales[i]), o);
+        wh[2 * i] = make_uint4(o[0], o[1], o[2], o[3]);
+        wh[2 * i + 1] = make_uint4(o[4], o[5], o[6], o[7]);
+    }
+    if (ES == 0)
+        return;
+    const int64_t nq = (int64_t)N * 8 * ES;  // 16-byte groups of 8 columns
+    for (int64_t q = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; q < nq; q += stride) {
+        const int64_t n = q / (8 * ES);
+        const int c0 = (int)(q % (8 * ES)) * 8;
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; e++) {
+            uint32_t v = 0;
+#pragma unroll
+            for (int h = 0; h < 2; h++) {
+                const int c = c0 + 2 * e + h;
+                const int j = ES == 1 ? c % 32 : c % 64;
+                const uint32_t bv = j < r ? (uint32_t)b[n * r + j] : 0u;
+                v |= bv << (16 * h);
+            }
+            w[e] = v;
+        }
+        tb[q] = make_uint4(w[0], w[1], w[2], w[3]);
     }
 }
 
@@ -194,18 +263,10 @@ __device__ __forceinline__ void tile_coords(int t, int mtiles, int ntiles, int &
     nt = gi * kPfGroupN + idx % gn;
 }
 
-// 16 codes (8 bytes) times their block scale -> 16 f16 (two 16-byte chunks).
-__device__ __forceinline__ void dequant16(uint2 c, uint32_t sc2, uint32_t (&o)[8])
-{
-    e2m1x8_to_h2x4(c.x, o);
-    e2m1x8_to_h2x4(c.y, o + 4);
-#pragma unroll
-    for (int i = 0; i < 8; i++)
-        o[i] = hmul2_u32(o[i], sc2);
-}
-
 __global__ void __launch_bounds__(kPfThreads, 1)
-    prefill_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, PrefillParams p)
+    prefill_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_w,
+                        const __grid_constant__ CUtensorMap tmap_ta, const __grid_constant__ CUtensorMap tmap_tb,
+                        PrefillParams p)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -221,8 +282,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int s = 0; s < kPfStages; s++) {
-            mbar_init(&full[s], 1 + 4);  // TMA producer (with tx bytes) + 4 dequantiser warps
-            mbar_init(&empty[s], 1);     // tcgen05.commit
+            mbar_init(&full[s], 1);   // TMA producer (with tx bytes)
+            mbar_init(&empty[s], 1);  // tcgen05.commit
         }
         for (int b = 0; b < 2; b++) {
             mbar_init(&acc_full[b], 1);
@@ -231,7 +292,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         *s_abort = 0;
         mbar_fence_init();
     }
-    if (warp == 9) {
+    if (warp == 5) {
         tmem_alloc(s_tmem, 512);
         tmem_relinquish();
     }
@@ -241,15 +302,15 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const uint32_t tmem = *s_tmem;
 
     const int ntile_total = p.mtiles * p.ntiles;
-    const int KS = p.K / kPfBK;
+    const int KB = p.K / kPfBK, KS = KB + p.ES;
 
     auto fail = [&]() {
         record_status(p.ctl, NVFP4_ERR_TIMEOUT);
         *s_abort = 1;
     };
 
-    if (warp == 8) {
-        // ---------------- TMA producer of A (X' f16 tiles)
+    if (warp == 4) {
+        // ---------------- TMA producer: X' and W tiles, then the LoRA extension
         if (lane == 0) {
             uint32_t it = 0;
             for (int tile = blockIdx.x; tile < ntile_total && !*s_abort; tile += gridDim.x) {
@@ -259,15 +320,22 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                     const int st = it % kPfStages;
                     const uint32_t ph = (it / kPfStages) & 1;
                     if (!mbar_wait(&empty[st], ph ^ 1)) { fail(); break; }
-                    mbar_arrive_expect_tx(&full[st], kPfABytes);
-                    tma_load_2d(sA + st * kPfABytes, &tmap_x, &full[st], ks * kPfBK, mt * kPfBM);
+                    mbar_arrive_expect_tx(&full[st], kPfABytes + kPfBBytes);
+                    if (ks < KB) {
+                        tma_load_2d(sA + st * kPfABytes, &tmap_x, &full[st], ks * kPfBK, mt * kPfBM);
+                        tma_load_2d(sB + st * kPfBBytes, &tmap_w, &full[st], ks * kPfBK, nt * kPfBN);
+                    } else {
+                        tma_load_2d(sA + st * kPfABytes, &tmap_ta, &full[st], (ks - KB) * kPfBK, mt * kPfBM);
+                        tma_load_2d(sB + st * kPfBBytes, &tmap_tb, &full[st], (ks - KB) * kPfBK, nt * kPfBN);
+                    }
                 }
             }
         }
-    } else if (warp == 9) {
+    } else if (warp == 5) {
         // ---------------- MMA issue
         if (lane == 0) {
-            constexpr uint32_t idesc = idesc_f16(kPfBM, kPfBN, 0);
+            constexpr uint32_t idesc_h = idesc_f16(kPfBM, kPfBN, 0);  // f16 x f16
+            constexpr uint32_t idesc_b = idesc_f16(kPfBM, kPfBN, 1);  // bf16 x bf16 (LoRA steps)
             uint32_t it = 0, lt = 0;
             for (int tile = blockIdx.x; tile < ntile_total && !*s_abort; tile += gridDim.x, lt++) {
                 const int buf = lt & 1;
@@ -283,6 +351,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                     tc_fence_after();
                     const uint64_t ad = smem_desc_sw128(smem_addr(sA + st * kPfABytes));
                     const uint64_t bd = smem_desc_sw128(smem_addr(sB + st * kPfBBytes));
+                    const uint32_t idesc = ks < KB ? idesc_h : idesc_b;
 #pragma unroll
                     for (int j = 0; j < kPfBK / 16; j++)
                         mma_f16_ss(d, ad + 2 * j, bd + 2 * j, idesc, (ks | j) != 0);
@@ -291,56 +360,6 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                 if (!ok) { fail(); break; }
                 mma_commit(&acc_full[buf]);
             }
-        }
-    } else if (warp >= 4) {
-        // ---------------- dequantiser: two rows of the 256-row B tile per thread
-        const int dt = threadIdx.x - 128;
-        uint32_t it = 0;
-        for (int tile = blockIdx.x; tile < ntile_total && !*s_abort; tile += gridDim.x) {
-            int mt, nt;
-            tile_coords(tile, p.mtiles, p.ntiles, mt, nt);
-            bool ok = true;
-            for (int ks = 0; ks < KS; ks++, it++) {
-                const int st = it % kPfStages;
-                const uint32_t ph = (it / kPfStages) & 1;
-                uint4 cw[2][2];
-                uint32_t sw[2];
-#pragma unroll
-                for (int h = 0; h < 2; h++) {
-                    const int n = nt * kPfBN + dt + 128 * h;
-                    if (n < p.N) {
-                        const uint4 *src = reinterpret_cast<const uint4 *>(p.codes + (size_t)n * (p.K / 2) + ks * 32);
-                        cw[h][0] = src[0];
-                        cw[h][1] = src[1];
-                        sw[h] = *reinterpret_cast<const uint32_t *>(p.scales + (size_t)n * (p.K / 16) + ks * 4);
-                    } else {
-                        cw[h][0] = cw[h][1] = make_uint4(0, 0, 0, 0);
-                        sw[h] = 0;
-                    }
-                }
-                if (!mbar_wait(&empty[st], ph ^ 1)) { ok = false; break; }
-                uint8_t *tileB = sB + st * kPfBBytes;
-#pragma unroll
-                for (int h = 0; h < 2; h++) {
-                    const int rrow = dt + 128 * h;
-                    uint8_t *rowp = tileB + (rrow >> 3) * 1024 + (rrow & 7) * 128;
-                    const uint2 blocks[4] = {make_uint2(cw[h][0].x, cw[h][0].y), make_uint2(cw[h][0].z, cw[h][0].w),
-                                             make_uint2(cw[h][1].x, cw[h][1].y), make_uint2(cw[h][1].z, cw[h][1].w)};
-#pragma unroll
-                    for (int b = 0; b < 4; b++) {
-                        uint32_t o[8];
-                        dequant16(blocks[b], e4m3_to_h2_dup((sw[h] >> (8 * b)) & 0xFFu), o);
-                        const int c0 = 2 * b, c1 = 2 * b + 1;
-                        *reinterpret_cast<uint4 *>(rowp + ((c0 ^ (rrow & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
-                        *reinterpret_cast<uint4 *>(rowp + ((c1 ^ (rrow & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
-                    }
-                }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(&full[st]);
-            }
-            if (!ok) { fail(); break; }
         }
     } else {
         // ---------------- epilogue: warps 0-3, one accumulator row per thread
@@ -356,41 +375,48 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             tc_fence_after();
             const int m = mt * kPfBM + row;
             const bool mrow = m < p.M;
-            const float fm = mrow ? __fmul_rn(s_t, p.fac[m]) : 0.0f;
-            float trow[kPfMaxR];
-#pragma unroll
-            for (int j = 0; j < kPfMaxR; j++)
-                trow[j] = (mrow && j < p.r) ? p.T[(size_t)m * p.r + j] : 0.0f;
+            const float cm = mrow ? row_factor(s_t, p.fac[m]) : 0.0f;
             for (int cc = 0; cc < kPfBN / 32; cc++) {
                 uint32_t v[32];
                 tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + buf * kPfBN + cc * 32, v);
+                const int n0 = nt * kPfBN + cc * 32;
+                if (!mrow || n0 >= p.N)
+                    continue;
+                float yv[32];
 #pragma unroll
-                for (int i = 0; i < 32; i++) {
-                    const int n = nt * kPfBN + cc * 32 + i;
-                    if (n >= p.N)
-                        continue;
-                    float lora = 0.0f;
-                    if (p.r > 0) {
-                        const uint4 *brow = reinterpret_cast<const uint4 *>(p.lora_b + (size_t)n * p.r);
+                for (int i = 0; i < 32; i++)
+                    yv[i] = __fmul_rn(cm, __uint_as_float(v[i]));
+                if (p.y_fp32) {
+                    float *dst = reinterpret_cast<float *>(p.y) + (size_t)m * p.N + n0;
+                    if (n0 + 32 <= p.N && (p.N & 3) == 0) {
 #pragma unroll
-                        for (int q = 0; q < kPfMaxR / 8; q++) {
-                            if (8 * q < p.r) {
-                                const uint4 bv = brow[q];
-                                const uint32_t bw[4] = {bv.x, bv.y, bv.z, bv.w};
+                        for (int q = 0; q < 8; q++)
+                            reinterpret_cast<float4 *>(dst)[q] =
+                                make_float4(yv[4 * q], yv[4 * q + 1], yv[4 * q + 2], yv[4 * q + 3]);
+                    } else {
 #pragma unroll
-                                for (int e = 0; e < 4; e++) {
-                                    lora = __fmaf_rn(trow[8 * q + 2 * e], bf16_bits_to_f32(bw[e] & 0xFFFFu), lora);
-                                    lora = __fmaf_rn(trow[8 * q + 2 * e + 1], bf16_bits_to_f32(bw[e] >> 16), lora);
-                                }
-                            }
-                        }
+                        for (int i = 0; i < 32; i++)
+                            if (n0 + i < p.N)
+                                dst[i] = yv[i];
                     }
-                    const float yv = __fmaf_rn(fm, __uint_as_float(v[i]), p.lora_scale * lora);
-                    if (mrow) {
-                        if (p.y_fp32)
-                            reinterpret_cast<float *>(p.y)[(size_t)m * p.N + n] = yv;
-                        else
-                            reinterpret_cast<__nv_bfloat16 *>(p.y)[(size_t)m * p.N + n] = __float2bfloat16_rn(yv);
+                } else {
+                    __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(p.y) + (size_t)m * p.N + n0;
+                    if (n0 + 32 <= p.N && (p.N & 7) == 0) {
+#pragma unroll
+                        for (int q = 0; q < 4; q++) {
+                            uint32_t w[4];
+#pragma unroll
+                            for (int e = 0; e < 4; e++) {
+                                __nv_bfloat162 b2 = __floats2bfloat162_rn(yv[8 * q + 2 * e], yv[8 * q + 2 * e + 1]);
+                                w[e] = *reinterpret_cast<uint32_t *>(&b2);
+                            }
+                            reinterpret_cast<uint4 *>(dst)[q] = make_uint4(w[0], w[1], w[2], w[3]);
+                        }
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; i++)
+                            if (n0 + i < p.N)
+                                dst[i] = __float2bfloat16_rn(yv[i]);
                     }
                 }
             }
@@ -403,7 +429,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 9) {
+    if (warp == 5) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
@@ -449,52 +475,82 @@ cudaError_t encode_tensor_map_2d(CUtensorMap *map, CUtensorMapDataType dt, const
 }
 
 struct PrefillPlan {
-    size_t off_xh, off_fac, off_T, total;
+    int ES;
+    size_t off_xh, off_fac, off_wh, off_ta, off_tb, total;
 };
 
 static size_t pf_align(size_t v) { return (v + 255) / 256 * 256; }
 
-static PrefillPlan prefill_plan(int64_t M, int64_t K, int64_t r)
+static PrefillPlan prefill_plan(int64_t M, int64_t N, int64_t K, int64_t r)
 {
     PrefillPlan pl;
+    pl.ES = r == 0 ? 0 : r <= 32 ? 1 : 2;
     size_t off = kWsHeaderBytes;
     pl.off_xh = off;
     off = pf_align(off + (size_t)M * K * 2);
     pl.off_fac = off;
     off = pf_align(off + (size_t)M * 4);
-    pl.off_T = off;
-    off = pf_align(off + (size_t)M * std::max<int64_t>(r, 1) * 4);
+    pl.off_wh = off;
+    off = pf_align(off + (size_t)N * K * 2);
+    pl.off_ta = off;
+    off = pf_align(off + (size_t)M * 64 * pl.ES * 2);
+    pl.off_tb = off;
+    off = pf_align(off + (size_t)N * 64 * pl.ES * 2);
     pl.total = off;
     return pl;
 }
 
 bool prefill_supported(int64_t M, int64_t N, int64_t K, int64_t r)
 {
-    return M >= kPrefillMinM && K % kPfBK == 0 && r <= kPfMaxR && r % 8 == 0 &&
-           M <= (1LL << 31) / std::max<int64_t>(K, 1) && N <= (1LL << 30);
+    return M >= kPrefillMinM && K % kPfBK == 0 && r <= kPfMaxR && M <= (1LL << 31) / std::max<int64_t>(K, 1) &&
+           N <= (1LL << 30) && N * K <= (1LL << 40);
 }
 
 size_t prefill_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t r)
 {
-    (void)N;
-    return prefill_plan(M, K, r).total;
+    return prefill_plan(M, N, K, r).total;
 }
 
 cudaError_t launch_prefill_gemm(const GemmArgs &a, cudaStream_t s, const DeviceInfo &dev)
 {
-    const PrefillPlan pl = prefill_plan(a.M, a.K, a.r);
+    const PrefillPlan pl = prefill_plan(a.M, a.N, a.K, a.r);
+    const int M = (int)a.M, N = (int)a.N, K = (int)a.K, r = (int)a.r;
     __half *xh = reinterpret_cast<__half *>(a.ws + pl.off_xh);
     float *fac = reinterpret_cast<float *>(a.ws + pl.off_fac);
-    float *T = reinterpret_cast<float *>(a.ws + pl.off_T);
-    const int M = (int)a.M, N = (int)a.N, K = (int)a.K, r = (int)a.r;
+    uint4 *wh = reinterpret_cast<uint4 *>(a.ws + pl.off_wh);
+    uint16_t *ta = reinterpret_cast<uint16_t *>(a.ws + pl.off_ta);
+    uint4 *tb = reinterpret_cast<uint4 *>(a.ws + pl.off_tb);
 
+    const int64_t nblocks = (int64_t)N * K / 16;
+    const int wgrid = (int)std::min<int64_t>((nblocks + 255) / 256, (int64_t)dev.num_sms * 16);
+    prefill_weight_kernel<<<wgrid, 256, 0, s>>>(reinterpret_cast<const uint2 *>(a.codes), a.scales, nblocks, wh,
+                                                a.lora_b, N, r, pl.ES, tb);
     prefill_xprime_kernel<<<(M + 7) / 8, 256, 0, s>>>(a.x, a.noise, M, K, xh, fac);
-    if (r > 0)
-        prefill_lora_down_kernel<<<(M + 63) / 64, 128, 0, s>>>(a.x, a.noise, a.lora_a, M, K, r, T);
+    if (pl.ES > 0) {
+        cudaError_t e = cudaMemsetAsync(ta, 0, (size_t)M * 64 * pl.ES * 2, s);
+        if (e != cudaSuccess)
+            return e;
+        prefill_lora_ext_kernel<<<(M + 63) / 64, 128, 0, s>>>(a.x, a.noise, a.lora_a, M, K, r, pl.ES, a.lora_scale,
+                                                              a.tensor_scale, fac, ta);
+    }
 
-    CUtensorMap tmap;
-    cudaError_t e = encode_tensor_map_2d(&tmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, xh, (uint64_t)K, (uint64_t)M,
+    CUtensorMap tmx, tmw, tma_, tmb;
+    cudaError_t e = encode_tensor_map_2d(&tmx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, xh, (uint64_t)K, (uint64_t)M,
                                          (uint64_t)K * 2, kPfBK, kPfBM, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (e == cudaSuccess)
+        e = encode_tensor_map_2d(&tmw, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, wh, (uint64_t)K, (uint64_t)N,
+                                 (uint64_t)K * 2, kPfBK, kPfBN, CU_TENSOR_MAP_SWIZZLE_128B);
+    // without LoRA the extension maps are never used: point them at X' and W
+    if (e == cudaSuccess)
+        e = pl.ES > 0 ? encode_tensor_map_2d(&tma_, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, ta, (uint64_t)64 * pl.ES,
+                                             (uint64_t)M, (uint64_t)128 * pl.ES, kPfBK, kPfBM,
+                                             CU_TENSOR_MAP_SWIZZLE_128B)
+                      : (tma_ = tmx, cudaSuccess);
+    if (e == cudaSuccess)
+        e = pl.ES > 0 ? encode_tensor_map_2d(&tmb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, tb, (uint64_t)64 * pl.ES,
+                                             (uint64_t)N, (uint64_t)128 * pl.ES, kPfBK, kPfBN,
+                                             CU_TENSOR_MAP_SWIZZLE_128B)
+                      : (tmb = tmw, cudaSuccess);
     if (e != cudaSuccess)
         return e;
 
@@ -502,14 +558,9 @@ cudaError_t launch_prefill_gemm(const GemmArgs &a, cudaStream_t s, const DeviceI
     p.M = M;
     p.N = N;
     p.K = K;
-    p.r = r;
-    p.codes = a.codes;
-    p.scales = a.scales;
+    p.ES = pl.ES;
     p.tensor_scale = a.tensor_scale;
-    p.lora_b = a.lora_b;
-    p.lora_scale = a.lora_scale;
     p.fac = fac;
-    p.T = T;
     p.y = a.y;
     p.y_fp32 = a.y_fp32 ? 1 : 0;
     p.ctl = reinterpret_cast<uint32_t *>(a.ws);
@@ -520,7 +571,7 @@ cudaError_t launch_prefill_gemm(const GemmArgs &a, cudaStream_t s, const DeviceI
         return e;
     const int tiles = p.mtiles * p.ntiles;
     const int grid = std::min(tiles, dev.num_sms);
-    prefill_gemm_kernel<<<grid, kPfThreads, kPfSmem, s>>>(tmap, p);
+    prefill_gemm_kernel<<<grid, kPfThreads, kPfSmem, s>>>(tmx, tmw, tma_, tmb, p);
     return cudaGetLastError();
 }
 
