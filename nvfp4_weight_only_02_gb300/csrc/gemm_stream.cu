@@ -7,29 +7,27 @@
 // ("RL with NVFP4 + LoRA" post, tggo.me/sberlogasci/42740, section "Метод";
 // rollouts are memory-bound on the weights, section "Эксперименты").
 //
-// Work is split into units (128-row tile, 512-column chunk), spread evenly
-// over one block per SM (stream-K; one whole tile per block when there are
-// about as many tiles as SMs).  A block has 16 consumer warps, one
-// producer warp and three idle warps (which keep the register split even
-// across the SM's four schedulers).
+// Two kernels per group of up to 16 tokens, chained by programmatic
+// dependent launch (PDL):
 //
-//  * Before the kernel may read anything an earlier kernel wrote, the
+//  * xprep (one block per 512-column chunk c): X' = bf16(X z), re-expressed
+//    as f16 times a power of two per token (the chunk max lands in
+//    [2^14, 2^15); every bf16 value of the chunk within 2^28 of that max
+//    stays exact), stored in the order the MMA B fragments are read, and
+//    the chunk's LoRA down-projection T_c = X'_c A_c^T (bf16 mma.sync).
+//    Both go into one contiguous record per chunk: [2^p per token | T_c |
+//    X' rows], so the GEMM fetches a unit's activations with one bulk copy
+//    (each TMA or bulk copy costs a producer thread about 50 ns to issue,
+//    whatever its size).
+//  * the streaming GEMM: work is split into units (128-row tile, 512-column
+//    chunk), spread evenly over one block per SM (stream-K; one whole tile
+//    per block when there are about as many tiles as SMs).  A block has 16
+//    consumer warps and one producer warp.  Before the wait for xprep the
 //    producer asks L2 to prefetch the first weight boxes of its range (a
-//    prefetch moves nothing into the SM, so it cannot observe stale data);
-//    with programmatic dependent launch this overlaps the previous kernel.
-//  * Chunk c's activations are prepared once per launch by one block (chunk
-//    c belongs to block floor(c G / C)): its consumer warps form
-//    X' = bf16(X z), re-express it as f16 times a power of two per token
-//    (the chunk max lands in [2^14, 2^15); every bf16 value of the chunk
-//    within 2^28 of that max stays exact), store it in the order the MMA B
-//    fragments are read, and compute the chunk's LoRA down-projection
-//    T_c = X'_c A_c^T with bf16 mma.sync.  The block then publishes the chunk
-//    by writing the launch's generation number into the chunk's flag.
-//  * The producer streams each unit's codes (two 128 x 128-byte boxes, 128B
-//    swizzle) and block scales (128 x 32 bytes) with 2-D TMA into a 2-deep
-//    ring of stages, and, once the chunk's flag is up, the chunk's X',
-//    power-of-two factors and T_c with bulk copies; all complete on the
-//    stage's mbarrier.
+//    prefetch moves nothing into the SM, so it cannot observe stale data).
+//    It then streams each unit's codes (two 128 x 128-byte boxes, 128B
+//    swizzle), block scales (128 x 32 bytes) and the chunk's record into a
+//    ring of stages, all completing on the stage's mbarrier.
 //  * Consumer warp (row group mt, half h) owns 16 rows and 256 columns of a
 //    stage: lane t of a quad holds 64 consecutive columns (two 16-byte loads
 //    per row and one scale word), converts codes with cvt.e2m1x2 -> f16x2
@@ -45,7 +43,6 @@
 //    either stored (the block holds the whole tile) or left in the workspace
 //    for the last block to arrive, which adds the shares in block order
 //    (results do not depend on arrival order).
-//  * The last block to finish advances the workspace's generation number.
 #include <algorithm>
 #include <mutex>
 #include <unordered_map>
@@ -65,40 +62,33 @@ constexpr int kBoxBytes = 128 * kRows;   // one code box: 128 rows x 128 bytes (
 constexpr int kScaleBox = 32 * kRows;    // scale box: 128 rows x 32 bytes
 constexpr int kCWarps = 16;              // consumer warps: 8 row groups x 2 column halves
 constexpr int kProducer = kCWarps;       // warp index of the producer
+// three idle warps keep the register split even across the SM's four schedulers
 constexpr int kThreads = (kCWarps + 4) * 32;
+constexpr int kPrepThreads = kCWarps * 32;  // xprep: one warp per token, then T_c
 constexpr int kMaxR = 64;
 constexpr int kMaxKS = kMaxR / 16;       // LoRA k-steps of 16 columns of T
 constexpr int kPrefetchUnits = 6;        // units per block prefetched into L2 before the wait
-constexpr size_t kXhOff = 2 * kBoxBytes + kScaleBox;
-constexpr uint64_t kFlagWaitNs = 2000000000ull;
+constexpr size_t kXhOff = 2 * kBoxBytes + kScaleBox;  // the record in a stage
 
 // named barriers (0 is __syncthreads)
 constexpr int kBarGroup = 9;       // the 8 half-0 consumer warps
 constexpr int kBarConsumers = 10;  // all 16 consumer warps
-constexpr int kBarGen = 11;        // consumers, producer and counting warp: generation read
-constexpr int kGenThreads = (kCWarps + 2) * 32;
 
-// Two stages: with the first units already prefetched into L2, a deeper ring
-// only lengthens the memory queue that every other load of the kernel waits in.
+// As many stages as fit next to the rest of shared memory (227 KB).
 template <int MP>
 __host__ __device__ constexpr int n_stages()
 {
-    return 2;
+    return MP == 8 ? 4 : 3;
 }
-template <int MP>
-__host__ __device__ constexpr size_t fac_off()
-{
-    return kXhOff + (size_t)MP * 1024;
-}
-template <int MP>
-__host__ __device__ constexpr size_t t_off()
-{
-    return fac_off<MP>() + 128;
-}
+// A chunk's record (workspace and stage alike): 2^p per token (128 bytes),
+// T_c (KS * MP/8 * 512 bytes) and X' (1 KB per token).
+constexpr size_t kFacBytes = 128;
+__host__ __device__ constexpr size_t t_bytes(int KS, int MP) { return (size_t)KS * (MP / 8) * 512; }
+__host__ __device__ constexpr size_t rec_bytes(int KS, int MP) { return kFacBytes + t_bytes(KS, MP) + (size_t)MP * 1024; }
 template <int MP>
 __host__ __device__ constexpr size_t stage_bytes()  // a multiple of 1024 (swizzled boxes)
 {
-    return (t_off<MP>() + (size_t)kMaxKS * (MP / 8) * 512 + 1023) / 1024 * 1024;
+    return (kXhOff + rec_bytes(kMaxKS, MP) + 1023) / 1024 * 1024;
 }
 template <int MP>
 __host__ __device__ constexpr size_t red_bytes()  // 2 buffers x 8 row groups x 32 lanes x MP/2 floats
@@ -111,15 +101,11 @@ __host__ __device__ constexpr size_t tacc_bytes()  // 2 buffers of T summed over
     return (size_t)2 * kMaxKS * (MP / 8) * 32 * 16;
 }
 template <int MP>
-__host__ __device__ constexpr size_t xb_off()
-{
-    return n_stages<MP>() * stage_bytes<MP>() + red_bytes<MP>() + tacc_bytes<MP>();
-}
-template <int MP>
 __host__ __device__ constexpr size_t smem_bytes()  // + 1 KB to align the ring, + barriers
 {
-    return 1024 + xb_off<MP>() + (size_t)MP * 1024 + 128;
+    return 1024 + n_stages<MP>() * stage_bytes<MP>() + red_bytes<MP>() + tacc_bytes<MP>() + 128;
 }
+static_assert(smem_bytes<8>() <= 232448 && smem_bytes<16>() <= 232448, "shared memory");
 
 __device__ __forceinline__ void pdl_launch_dependents()
 {
@@ -129,29 +115,6 @@ __device__ __forceinline__ void pdl_launch_dependents()
 __device__ __forceinline__ void pdl_wait()
 {
     asm volatile("griddepcontrol.wait;" ::: "memory");
-}
-
-__device__ __forceinline__ uint32_t ld_acquire(const uint32_t *p)
-{
-    uint32_t v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-
-__device__ __forceinline__ void st_release(uint32_t *p, uint32_t v)
-{
-    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
-__device__ __forceinline__ void prefetch_l2(const void *ptr)
-{
-    asm volatile("prefetch.global.L2 [%0];" ::"l"(ptr));
-}
-
-// Generic-proxy global writes/reads ordered against bulk-copy (async proxy) accesses.
-__device__ __forceinline__ void fence_proxy_async_global()
-{
-    asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
 __device__ __forceinline__ int owner_of(int u, int U, int G)
@@ -174,6 +137,13 @@ __host__ __device__ __forceinline__ int xh_unit(int m, int ux)
 
 __device__ __forceinline__ float bf16_round(float v) { return __bfloat162float(__float2bfloat16_rn(v)); }
 
+__device__ __forceinline__ uint32_t bf16x2_bits(float a, float b)
+{
+    __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+
 struct Params {
     CUtensorMap tm_codes;   // codes, N x K/2 bytes: boxes of 128 x 128, 128B swizzle
     CUtensorMap tm_scales;  // scales, N x K/16 bytes: boxes of 128 x 32
@@ -184,36 +154,59 @@ struct Params {
     const uint16_t *lora_b;    // N x r bf16
     float lora_scale;
     const float *tensor_scale;
-    uint8_t *xh;               // [C][MP][1024]: X' as f16, swizzled
-    float *fac;                // [C][MP]: 2^p per token and chunk
-    float4 *tpart;             // [C][KS][MP/8][32]: T_c in B-fragment order
+    const uint8_t *rec;        // [C] chunk records: 2^p per token | T_c | X' rows
+    int rec_bytes;
     float *part;               // [G][2][8][32][MP/2]: tile shares left for the last block
     uint32_t *tcnt;            // tile arrival counters
-    uint32_t *ready;           // chunk flags
     uint32_t *ctl;
     void *y;
     int y_fp32;
 };
 
-// ---------------------------------------------------------------- chunk preparation
-// All 16 consumer warps of the block that owns chunk c.  Warp m < M forms
-// X' of token m (lane l: columns 16l..16l+15): bf16 into shared memory for
-// the LoRA down-projection, f16 times 2^p into the workspace for every
-// block.  Then T_c = X'_c A_c^T by bf16 mma.sync with the tokens as the M
-// dimension; the k index of each MMA is permuted exactly as in the main
-// loop (lane t of a quad holds 64 consecutive columns of a 256-column half),
-// so each lane reads A in 16-byte pieces and X' in conflict-free 16-byte
-// units.  Warps split (8-column n-tile of T, half, k-step pairs); one warp
-// per n-tile sums the parts in fixed order and stores them in the layout the
-// epilogue loads as B fragments.  Finally the chunk is published.
+// ---------------------------------------------------------------- xprep kernel
+struct PrepParams {
+    int M, K, r, KS;
+    const uint16_t *x;       // M x K bf16
+    const float *noise;      // K floats or null
+    const uint16_t *lora_a;  // r x K bf16
+    uint8_t *rec;            // [C] records of rec_bytes(KS, MP)
+};
+
+// Block c: warp m < M forms X' of token m (lane l: columns 16l .. 16l+15 of
+// the chunk): bf16 into shared memory for the LoRA down-projection, f16
+// times 2^-p into the record.  Then T_c = X'_c A_c^T by bf16 mma.sync with
+// the tokens as the M dimension; the k index of each MMA is permuted exactly
+// as in the GEMM's main loop (lane t of a quad holds 64 consecutive columns
+// of a 256-column half), so each lane reads A in 16-byte pieces and X' in
+// conflict-free 16-byte units.  Warps split (8-column n-tile of T, half,
+// k-step pairs); one warp per n-tile sums the parts in fixed order and
+// stores them in the layout the epilogue loads as B fragments.
 template <int MP>
-__device__ void prepare_chunk(const Params &p, int c, uint32_t gen, uint8_t *xb, float4 *scratch)
+__global__ void __launch_bounds__(kPrepThreads, 1) xprep_kernel(const __grid_constant__ PrepParams p)
 {
     constexpr int NT = MP / 8;
+    __shared__ __align__(16) uint8_t xb[MP * 1024];
+    __shared__ float4 scratch[kCWarps * 32];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    const int c = blockIdx.x;
     const int kbase = c * kChunk;
     const int halves = kbase + kChunk <= p.K ? 2 : 1;
-    // the activations first: they are on the critical path
+    const uint32_t cbytes = (uint32_t)min(kChunk, p.K - kbase) * 2u;
+    // the chunk's activations, noise and A rows into L2 while the previous kernel finishes
+    if (warp < p.M && lane == 0)
+        bulk_prefetch_l2(p.x + (size_t)warp * p.K + kbase, cbytes);
+    if (warp == kCWarps - 1 && lane == 0 && p.noise)
+        bulk_prefetch_l2(p.noise + kbase, 2 * cbytes);
+    if (p.KS > 0 && lane == 0)
+        for (int j = warp; j < p.r; j += kCWarps)
+            bulk_prefetch_l2(p.lora_a + (size_t)j * p.K + kbase, cbytes);
+    pdl_launch_dependents();  // the GEMM's blocks may start prefetching weights
+    pdl_wait();
+
+    uint8_t *rec = p.rec + (size_t)c * rec_bytes(p.KS, MP);
+    float *fac = reinterpret_cast<float *>(rec);
+    float4 *trec = reinterpret_cast<float4 *>(rec + kFacBytes);
+    uint8_t *xrec = rec + kFacBytes + t_bytes(p.KS, MP);
     const int k0 = kbase + lane * 16;
     const bool conv = warp < p.M, kin = conv && k0 < p.K;
     uint4 xa = make_uint4(0u, 0u, 0u, 0u), xc = xa;
@@ -237,12 +230,11 @@ __device__ void prepare_chunk(const Params &p, int c, uint32_t gen, uint8_t *xb,
     const int jt = unit / halves, hh = unit % halves;
     const int npairs = 8 / wpu;                // k-step pairs per warp
     const int jrow = jt * 8 + g;
-    // the first (up to) four pairs now, the rest (rank 64 only) after the conversion
     const uint16_t *arow = p.lora_a + (size_t)min(jrow, max(p.r - 1, 0)) * p.K + kbase + 256 * hh + 64 * t;
-    uint4 af[4];
+    uint4 af[8];
     if (p.KS > 0) {
 #pragma unroll
-        for (int q = 0; q < 4; q++) {
+        for (int q = 0; q < 8; q++) {
             const bool ok = q < npairs && jrow < p.r;
             af[q] = ok ? __ldcg(reinterpret_cast<const uint4 *>(arow + 8 * (sub * npairs + q)))
                        : make_uint4(0u, 0u, 0u, 0u);
@@ -272,7 +264,6 @@ __device__ void prepare_chunk(const Params &p, int c, uint32_t gen, uint8_t *xb,
             const int e = (b >> 23) ? (int)(b >> 23) - 127 : (31 - __clz(b)) - 149;
             pexp = e - 14;
         }
-        uint8_t *dst = p.xh + ((size_t)c * MP + warp) * 1024;
 #pragma unroll
         for (int u2 = 0; u2 < 2; u2++) {
             uint32_t hw[4], bw[4];
@@ -282,68 +273,56 @@ __device__ void prepare_chunk(const Params &p, int c, uint32_t gen, uint8_t *xb,
                 __half2 h2 = __halves2half2(__float2half_rn(scale_pow2(lo, -pexp)),
                                             __float2half_rn(scale_pow2(hi, -pexp)));
                 hw[i] = *reinterpret_cast<uint32_t *>(&h2);
-                __nv_bfloat162 b2 = __floats2bfloat162_rn(lo, hi);  // exact: lo, hi are bf16 values
-                bw[i] = *reinterpret_cast<uint32_t *>(&b2);
+                bw[i] = bf16x2_bits(lo, hi);  // exact: lo, hi are bf16 values
             }
             const int off = 16 * xh_unit(warp, 2 * lane + u2);
-            *reinterpret_cast<uint4 *>(dst + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            *reinterpret_cast<uint4 *>(xrec + warp * 1024 + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
             *reinterpret_cast<uint4 *>(xb + warp * 1024 + off) = make_uint4(bw[0], bw[1], bw[2], bw[3]);
         }
         if (lane == 0)
-            p.fac[c * MP + warp] = exp2i(pexp);
+            fac[warp] = exp2i(pexp);
+    } else if (warp < MP && lane == 0) {
+        fac[warp] = 0.0f;  // tokens past M: their MMA columns are zero
     }
-    named_sync(kBarConsumers, kCWarps * 32);  // bf16 X' complete in shared memory
-    if (p.KS > 0) {
-        float cc[4] = {0.f, 0.f, 0.f, 0.f};
-        const uint8_t *x0r = xb + g * 1024, *x1r = xb + (g + 8) * 1024;
+    if (p.KS == 0)
+        return;
+    __syncthreads();  // bf16 X' complete in shared memory
+    float cc[4] = {0.f, 0.f, 0.f, 0.f};
+    const uint8_t *x0r = xb + g * 1024, *x1r = xb + (g + 8) * 1024;
 #pragma unroll
-        for (int q = 0; q < 8; q++) {
-            if (q == 4 && npairs > 4) {
-#pragma unroll
-                for (int q2 = 0; q2 < 4; q2++)
-                    af[q2] = jrow < p.r ? __ldcg(reinterpret_cast<const uint4 *>(arow + 8 * (sub * npairs + 4 + q2)))
-                                        : make_uint4(0u, 0u, 0u, 0u);
-            }
-            if (q < npairs) {
-                const int ux = 32 * hh + 8 * t + sub * npairs + q;  // 8 columns: two k-steps
-                const uint4 x0 = g < p.M ? *reinterpret_cast<const uint4 *>(x0r + 16 * xh_unit(g, ux))
+    for (int q = 0; q < 8; q++) {
+        if (q < npairs) {
+            const int ux = 32 * hh + 8 * t + sub * npairs + q;  // 8 columns: two k-steps
+            const uint4 x0 = g < p.M ? *reinterpret_cast<const uint4 *>(x0r + 16 * xh_unit(g, ux))
+                                     : make_uint4(0u, 0u, 0u, 0u);
+            const uint4 x1 = g + 8 < p.M ? *reinterpret_cast<const uint4 *>(x1r + 16 * xh_unit(g + 8, ux))
                                          : make_uint4(0u, 0u, 0u, 0u);
-                const uint4 x1 = g + 8 < p.M ? *reinterpret_cast<const uint4 *>(x1r + 16 * xh_unit(g + 8, ux))
-                                             : make_uint4(0u, 0u, 0u, 0u);
-                uint32_t a[4] = {x0.x, x1.x, x0.y, x1.y};
-                mma_bf16_16816(cc, a, af[q & 3].x, af[q & 3].y);
-                a[0] = x0.z;
-                a[1] = x1.z;
-                a[2] = x0.w;
-                a[3] = x1.w;
-                mma_bf16_16816(cc, a, af[q & 3].z, af[q & 3].w);
-            }
-        }
-        scratch[warp * 32 + lane] = make_float4(cc[0], cc[1], cc[2], cc[3]);
-        named_sync(kBarConsumers, kCWarps * 32);
-        if (hh == 0 && sub == 0) {  // sum n-tile jt over halves and parts, fixed order
-            float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int w = 0; w < halves * wpu; w++) {
-                const float4 o = scratch[(warp + w) * 32 + lane];
-                s.x += o.x;
-                s.y += o.y;
-                s.z += o.z;
-                s.w += o.w;
-            }
-            // lane (g, t) holds T[g][8jt + 2t, +1] (x, y) and T[g+8][...] (z, w)
-            const int ks = jt / 2, jh = jt % 2;
-            float2 *d0 = reinterpret_cast<float2 *>(p.tpart + (((size_t)c * p.KS + ks) * NT + 0) * 32 + lane) + jh;
-            *d0 = make_float2(s.x, s.y);
-            if (NT == 2) {
-                float2 *d1 = reinterpret_cast<float2 *>(p.tpart + (((size_t)c * p.KS + ks) * NT + 1) * 32 + lane) + jh;
-                *d1 = make_float2(s.z, s.w);
-            }
+            uint32_t a[4] = {x0.x, x1.x, x0.y, x1.y};
+            mma_bf16_16816(cc, a, af[q].x, af[q].y);
+            a[0] = x0.z;
+            a[1] = x1.z;
+            a[2] = x0.w;
+            a[3] = x1.w;
+            mma_bf16_16816(cc, a, af[q].z, af[q].w);
         }
     }
-    __threadfence();
-    named_sync(kBarConsumers, kCWarps * 32);  // every store of the chunk done and fenced
-    if (threadIdx.x == 0)
-        st_release(&p.ready[c], gen + 1u);
+    scratch[warp * 32 + lane] = make_float4(cc[0], cc[1], cc[2], cc[3]);
+    __syncthreads();
+    if (hh == 0 && sub == 0) {  // sum n-tile jt over halves and parts, fixed order
+        float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int w = 0; w < halves * wpu; w++) {
+            const float4 o = scratch[(warp + w) * 32 + lane];
+            s.x += o.x;
+            s.y += o.y;
+            s.z += o.z;
+            s.w += o.w;
+        }
+        // lane (g, t) holds T[g][8jt + 2t, +1] (x, y) and T[g+8][...] (z, w)
+        const int ks = jt / 2, jh = jt % 2;
+        reinterpret_cast<float2 *>(trec + ((size_t)ks * NT + 0) * 32 + lane)[jh] = make_float2(s.x, s.y);
+        if (NT == 2)
+            reinterpret_cast<float2 *>(trec + ((size_t)ks * NT + 1) * 32 + lane)[jh] = make_float2(s.z, s.w);
+    }
 }
 
 // ---------------------------------------------------------------- consumers
@@ -370,14 +349,14 @@ __device__ __forceinline__ uint32_t word_of(const uint4 &v, int i)
 // bytes 2e, 2e+1 of word j, scale byte j/2, X' unit j (words 2e, 2e+1).
 // Code box h holds 128-byte rows whose 16-byte chunk c sits at c ^ (row % 8).
 template <int MP>
-__device__ __forceinline__ void compute_unit(const uint8_t *st, int mt, int h, int g, int t, int M,
+__device__ __forceinline__ void compute_unit(const uint8_t *st, int xoff, int mt, int h, int g, int t, int M,
                                              float (&acc)[MP / 8][4])
 {
     constexpr int NT = MP / 8;
     const uint8_t *cb = st + h * kBoxBytes;
     const uint8_t *sb = st + 2 * kBoxBytes;
-    const uint8_t *xb = st + kXhOff;
-    const float *fb = reinterpret_cast<const float *>(st + fac_off<MP>());
+    const uint8_t *xb = st + xoff;  // the record's X' rows
+    const float *fb = reinterpret_cast<const float *>(st + kXhOff);
     const int row0 = 16 * mt + g;  // row0 % 8 == g, and (row0 + 8) % 8 == g
     const uint8_t *r0p = cb + row0 * 128, *r1p = cb + (row0 + 8) * 128;
     const int ca = 16 * ((2 * t) ^ g), cbb = 16 * ((2 * t + 1) ^ g);
@@ -459,12 +438,6 @@ __device__ __forceinline__ uint32_t lora_pair(const Params &p, int R, int j)
     const uint32_t lo = __ldcg(row + j);
     const uint32_t hi = j + 1 < p.r ? (uint32_t)__ldcg(row + j + 1) : 0u;
     return lo | (hi << 16);
-}
-
-__device__ __forceinline__ uint32_t bf16x2_bits(float a, float b)
-{
-    __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
-    return *reinterpret_cast<uint32_t *>(&v);
 }
 
 // The block's share of tile n for half-0 warp mt: s_t * acc + s * T_R B^T.
@@ -633,11 +606,9 @@ __global__ void __launch_bounds__(kThreads, 1) stream_gemm_kernel(const __grid_c
     uint8_t *smem = reinterpret_cast<uint8_t *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     float *red = reinterpret_cast<float *>(smem + S * stage_bytes<MP>());
     float4 *tacc = reinterpret_cast<float4 *>(smem + S * stage_bytes<MP>() + red_bytes<MP>());
-    uint8_t *xb = smem + xb_off<MP>();
-    uint64_t *full = reinterpret_cast<uint64_t *>(xb + MP * 1024);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + S * stage_bytes<MP>() + red_bytes<MP>() + tacc_bytes<MP>());
     uint64_t *empty = full + S;
     volatile uint32_t *s_flag = reinterpret_cast<volatile uint32_t *>(empty + S);
-    volatile uint32_t *s_gen = s_flag + 1;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = gridDim.x, b = blockIdx.x;
@@ -654,7 +625,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_gemm_kernel(const __grid_c
     if (warp == kProducer) {
         // ---------------- producer warp (lane 0 issues every copy)
         if (lane == 0) {
-            // the weights of the first units into L2 while the previous kernels finish
+            // the weights of the first units into L2 while xprep runs
             for (int u = u0; u < min(u1, u0 + kPrefetchUnits); u++) {
                 const int n = u / p.C, c = u - n * p.C;
                 tma_prefetch_2d(&p.tm_codes, c * (kChunk / 2), n * kRows);
@@ -664,100 +635,34 @@ __global__ void __launch_bounds__(kThreads, 1) stream_gemm_kernel(const __grid_c
             }
         }
         pdl_wait();
-        if (lane == 0)
-            *s_gen = *reinterpret_cast<volatile const uint32_t *>(&p.ctl[CTL_GEN]);
-        named_sync(kBarGen, kGenThreads);  // the block's generation is in shared memory
-        const uint32_t gen = *s_gen;
-        const uint32_t xbytes = (uint32_t)p.M * 1024u, fbytes = (uint32_t)MP * 4u;
-        const uint32_t tbytes = (uint32_t)p.KS * NT * 512u;
-        const int nunits = u1 - u0;
-        bool ok = true;
-        auto issue_weights = [&](int i) {
-            const int u = u0 + i, s = i % S;
-            const int n = u / p.C, c = u - n * p.C;
-            const bool two = (c + 1) * kChunk <= p.K;  // else a last 256-column chunk
-            uint8_t *st = smem + (size_t)s * stage_bytes<MP>();
-            mbar_arrive_expect_tx(&full[s], (two ? 2 : 1) * kBoxBytes + kScaleBox + xbytes + fbytes + tbytes);
-            tma_load_2d(st, &p.tm_codes, &full[s], c * (kChunk / 2), n * kRows);
-            if (two)
-                tma_load_2d(st + kBoxBytes, &p.tm_codes, &full[s], c * (kChunk / 2) + 128, n * kRows);
-            tma_load_2d(st + 2 * kBoxBytes, &p.tm_scales, &full[s], c * (kChunk / 16), n * kRows);
-        };
-        if (lane == 0)
-            for (int i = 0; i < min(S, nunits); i++)
-                issue_weights(i);
-        // every chunk of the range published (one acquire per chunk, all lanes at once)
-        {
-            const int nchk = min(nunits, p.C);
-            const uint64_t t0 = globaltimer();
-            for (;;) {
-                bool ready = true;
-                for (int k = lane; k < nchk; k += 32)
-                    ready = ready && ld_acquire(&p.ready[(u0 + k) % p.C]) == gen + 1u;
-                if (__all_sync(0xffffffffu, ready))
-                    break;
-                if (globaltimer() - t0 > kFlagWaitNs) {
-                    if (lane == 0)
-                        record_status(p.ctl, NVFP4_ERR_TIMEOUT);
-                    break;
-                }
-                __nanosleep(32);
-            }
-            __syncwarp();
-        }
         if (lane == 0) {
-            fence_proxy_async_global();
-            for (int i = 0; i < nunits; i++) {
+            // a unit's record: 2^p, T_c and the first M rows of X'
+            const uint32_t rbytes = (uint32_t)(kFacBytes + t_bytes(p.KS, MP)) + (uint32_t)p.M * 1024u;
+            for (int i = 0; i < u1 - u0; i++) {
                 const int u = u0 + i, s = i % S;
-                if (i >= S) {
-                    if (ok && !mbar_wait(&empty[s], ((i / S) + 1) & 1)) {
-                        record_status(p.ctl, NVFP4_ERR_TIMEOUT);
-                        ok = false;
-                    }
-                    if (!ok)
-                        continue;  // stop copying; consumers time out and wind down
-                    issue_weights(i);
+                if (i >= S && !mbar_wait(&empty[s], ((i / S) + 1) & 1)) {
+                    record_status(p.ctl, NVFP4_ERR_TIMEOUT);
+                    break;  // stop copying; consumers time out and wind down
                 }
-                const int c = u % p.C;
+                const int n = u / p.C, c = u - n * p.C;
+                const bool two = (c + 1) * kChunk <= p.K;  // else a last 256-column chunk
                 uint8_t *st = smem + (size_t)s * stage_bytes<MP>();
-                bulk_g2s(st + kXhOff, p.xh + (size_t)c * MP * 1024, xbytes, &full[s]);
-                bulk_g2s(st + fac_off<MP>(), p.fac + (size_t)c * MP, fbytes, &full[s]);
-                if (tbytes)
-                    bulk_g2s(st + t_off<MP>(), p.tpart + (size_t)c * p.KS * NT * 32, tbytes, &full[s]);
+                mbar_arrive_expect_tx(&full[s], (two ? 2 : 1) * kBoxBytes + kScaleBox + rbytes);
+                tma_load_2d(st, &p.tm_codes, &full[s], c * (kChunk / 2), n * kRows);
+                if (two)
+                    tma_load_2d(st + kBoxBytes, &p.tm_codes, &full[s], c * (kChunk / 2) + 128, n * kRows);
+                tma_load_2d(st + 2 * kBoxBytes, &p.tm_scales, &full[s], c * (kChunk / 16), n * kRows);
+                bulk_g2s(st + kXhOff, p.rec + (size_t)c * p.rec_bytes, rbytes, &full[s]);
             }
         }
         __syncwarp();
         pdl_launch_dependents();
     } else if (warp < kCWarps) {
         // ---------------- consumer warps
-        // chunks this block prepares: those with floor(c G / C) == b
-        const int c_lo = (int)(((long long)b * p.C + G - 1) / G);
-        const int c_hi = (int)(((long long)(b + 1) * p.C + G - 1) / G);
-        // before the wait: L2 prefetches of the chunk's activations, noise and
-        // LoRA A rows (no data reaches the SM; address translation and L2
-        // fills overlap the previous kernel)
-        for (int c = c_lo; c < c_hi; c++) {
-            const int kb = c * kChunk + lane * 16;
-            if (kb < p.K) {
-                if (warp < p.M)
-                    prefetch_l2(p.x + (size_t)warp * p.K + kb);
-                if (warp == kCWarps - 1 && p.noise)
-                    prefetch_l2(p.noise + kb);
-                if (p.KS > 0)
-                    for (int j = warp; j < p.r; j += kCWarps)
-                        prefetch_l2(p.lora_a + (size_t)j * p.K + kb);
-            }
-        }
         pdl_wait();
-        named_sync(kBarGen, kGenThreads);
-        const uint32_t gen = *s_gen;
-        for (int c = c_lo; c < c_hi; c++)
-            prepare_chunk<MP>(p, c, gen, xb, reinterpret_cast<float4 *>(red));
-        if (c_hi > c_lo)
-            named_sync(kBarConsumers, kCWarps * 32);  // scratch free before segment ends use it
-
         const int mt = warp & 7, h = warp >> 3, g = lane >> 2, t = lane & 3;
         const float s_t = __ldcg(p.tensor_scale);
+        const int xoff = (int)(kXhOff + kFacBytes + t_bytes(p.KS, MP));
         float acc[NT][4];
 #pragma unroll
         for (int nt = 0; nt < NT; nt++)
@@ -778,9 +683,9 @@ __global__ void __launch_bounds__(kThreads, 1) stream_gemm_kernel(const __grid_c
             const int n = u / p.C, c = u - n * p.C;
             const uint8_t *st = smem + (size_t)s * stage_bytes<MP>();
             if (h == 0 || (c + 1) * kChunk <= p.K)
-                compute_unit<MP>(st, mt, h, g, t, p.M, acc);
+                compute_unit<MP>(st, xoff, mt, h, g, t, p.M, acc);
             if (h == 1) {  // T of this chunk into the segment's sum (element mt*32 + lane, ...)
-                const float4 *ts = reinterpret_cast<const float4 *>(st + t_off<MP>());
+                const float4 *ts = reinterpret_cast<const float4 *>(st + kXhOff + kFacBytes);
                 float4 *ta = tacc + buf * (kMaxKS * NT * 32);
                 for (int e = mt * 32 + lane; e < tn; e += 256) {
                     const float4 v = ts[e];
@@ -809,20 +714,6 @@ __global__ void __launch_bounds__(kThreads, 1) stream_gemm_kernel(const __grid_c
                 seg_start = true;
             }
         }
-    } else if (warp == kCWarps + 1) {
-        // once every block has read this launch's generation (below, after the
-        // wait, by the producer and consumer warps), the last block to count
-        // itself advances it for the next launch on this workspace
-        pdl_wait();
-        named_sync(kBarGen, kGenThreads);
-        if (lane == 0) {
-            __threadfence();
-            if (atomicAdd(&p.ctl[CTL_DONE], 1u) == (uint32_t)G - 1) {
-                p.ctl[CTL_DONE] = 0;
-                p.ctl[CTL_GEN] = *s_gen + 1u;
-            }
-        }
-        pdl_launch_dependents();
     } else {
         pdl_launch_dependents();  // idle warps
     }
@@ -831,7 +722,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_gemm_kernel(const __grid_c
 // ================================================================ host side
 struct Plan {
     int MP, C, tiles, U, G, KS;
-    size_t off_xh, off_fac, off_tpart, off_part, total;
+    size_t rec, off_rec, off_part, total;
 };
 
 static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -843,8 +734,7 @@ static bool make_plan(int64_t M, int64_t N, int64_t K, int64_t r, const DeviceIn
     pl.MP = M <= 8 ? 8 : 16;
     pl.C = (int)((K + kChunk - 1) / kChunk);
     pl.tiles = (int)((N + kRows - 1) / kRows);
-    if (pl.tiles > kTileCounters || pl.C > kCounterWords - kTileCounters ||
-        (long long)pl.tiles * pl.C > (1LL << 30))
+    if (pl.tiles > kTileCounters || pl.C > (1 << 20) || (long long)pl.tiles * pl.C > (1LL << 30))
         return false;
     pl.U = pl.tiles * pl.C;
     pl.G = std::min(dev.num_sms, pl.U);
@@ -854,12 +744,9 @@ static bool make_plan(int64_t M, int64_t N, int64_t K, int64_t r, const DeviceIn
         pl.G = pl.tiles;
     pl.KS = r == 0 ? 0 : r <= 16 ? 1 : r <= 32 ? 2 : 4;
     size_t off = kWsHeaderBytes;
-    pl.off_xh = off;
-    off = align_up(off + (size_t)pl.C * pl.MP * 1024, 256);
-    pl.off_fac = off;
-    off = align_up(off + (size_t)pl.C * pl.MP * 4, 256);
-    pl.off_tpart = off;
-    off = align_up(off + (size_t)pl.C * std::max(pl.KS, 1) * (pl.MP / 8) * 512, 256);
+    pl.rec = rec_bytes(pl.KS, pl.MP);
+    pl.off_rec = off;
+    off = align_up(off + (size_t)pl.C * pl.rec, 256);
     pl.off_part = off;
     off = align_up(off + (size_t)pl.G * 2 * kRows * pl.MP * 4, 256);
     pl.total = off;
@@ -994,11 +881,37 @@ cudaError_t launch_stream_gemm(const GemmArgs &a, cudaStream_t s, const DeviceIn
     cudaError_t err = weight_maps(a, maps);
     if (err != cudaSuccess)
         return err;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
     for (int64_t m0 = 0; m0 < a.M; m0 += 16) {
         const int64_t Mg = std::min<int64_t>(16, a.M - m0);
         Plan pl;
         if (!cached_plan(Mg, a.N, a.K, a.r, dev, pl))
             return cudaErrorInvalidConfiguration;
+        uint8_t *rec = a.ws + pl.off_rec;
+        PrepParams pp;
+        pp.M = (int)Mg;
+        pp.K = (int)a.K;
+        pp.r = (int)a.r;
+        pp.KS = pl.KS;
+        pp.x = a.x + m0 * a.K;
+        pp.noise = a.noise;
+        pp.lora_a = a.lora_a;
+        pp.rec = rec;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(pl.C);
+        cfg.blockDim = dim3(kPrepThreads);
+        cfg.dynamicSmemBytes = 0;
+        cfg.stream = s;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        void *pargs[] = {&pp};
+        err = cudaLaunchKernelExC(&cfg, pl.MP == 8 ? (const void *)xprep_kernel<8> : (const void *)xprep_kernel<16>,
+                                  pargs);
+        if (err != cudaSuccess)
+            return err;
+
         Params p;
         p.tm_codes = maps.codes;
         p.tm_scales = maps.scales;
@@ -1015,25 +928,16 @@ cudaError_t launch_stream_gemm(const GemmArgs &a, cudaStream_t s, const DeviceIn
         p.lora_b = a.lora_b;
         p.lora_scale = a.lora_scale;
         p.tensor_scale = a.tensor_scale;
-        p.xh = a.ws + pl.off_xh;
-        p.fac = reinterpret_cast<float *>(a.ws + pl.off_fac);
-        p.tpart = reinterpret_cast<float4 *>(a.ws + pl.off_tpart);
+        p.rec = rec;
+        p.rec_bytes = (int)pl.rec;
         p.part = reinterpret_cast<float *>(a.ws + pl.off_part);
         p.tcnt = reinterpret_cast<uint32_t *>(a.ws + kCtlBytes);
-        p.ready = p.tcnt + kTileCounters;
         p.ctl = reinterpret_cast<uint32_t *>(a.ws);
         p.y = a.y_fp32 ? (void *)((float *)a.y + m0 * a.N) : (void *)((uint16_t *)a.y + m0 * a.N);
         p.y_fp32 = a.y_fp32 ? 1 : 0;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-        cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(pl.G);
         cfg.blockDim = dim3(kThreads);
         cfg.dynamicSmemBytes = pl.MP == 8 ? smem_bytes<8>() : smem_bytes<16>();
-        cfg.stream = s;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
         void *args[] = {&p};
         err = cudaLaunchKernelExC(
             &cfg, pl.MP == 8 ? (const void *)stream_gemm_kernel<8> : (const void *)stream_gemm_kernel<16>, args);

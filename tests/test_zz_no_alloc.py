@@ -66,8 +66,9 @@ def test_static_scratch_matches_workspace_entry_point(nv, case):
 
 def test_static_scratch_rejects_oversized_problems(nv):
     # a workspace beyond the 8 MiB scratch is refused before anything runs
-    # (16 tokens x 2048 chunks of 512 columns of X' alone fill 32 MiB)
-    N, K = 256, 1 << 20
+    # (K % 256 != 0 takes the register-streaming kernel, whose f16 X' of
+    # 16 tokens x 2^20 columns alone fills 32 MiB)
+    N, K = 256, (1 << 20) + 16
     assert nv.nvfp4_workspace_bytes(16, N, K, 0) > (8 << 20)
     x = torch.zeros((16, K), dtype=torch.bfloat16, device="cuda")
     q = nv.QuantizedWeight(torch.zeros((N, K // 2), dtype=torch.uint8, device="cuda"),
