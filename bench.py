@@ -209,9 +209,9 @@ class Workload:
         self.new_scales = {n: t.empty_like(self.rep[0][n].scales) for n in ("up", "down")}
         self.qbuf = {n: (t.empty_like(self.rep[0][n].codes), t.empty_like(self.rep[0][n].scales),
                          t.zeros(1, dtype=t.float32, device=dev)) for n in ("up", "down")}
-        # kernels per call: the streaming decode GEMM is one launch per 16 tokens,
-        # the register-streaming one two; quantiser and scale update one each
-        per_gemm = {"decode_stream": 1, "decode_registers": 2}
+        # kernels per call and 16-token group: two for either decode GEMM path
+        # (activation preparation, then the GEMM); quantiser and scale update one each
+        per_gemm = {"decode_stream": 2, "decode_registers": 2}
         self.launches_per_step = 2 + 2 + sum(
             per_gemm[nv.gemm_kernel(M, *shape, R_LORA)] * ((M + 15) // 16) for M in MS for shape in (UP, DOWN))
 

@@ -101,8 +101,9 @@ nvfp4_status nvfp4_dequantize(const uint8_t *codes, const uint8_t *scales_e4m3,
  *   x_bf16: M x K; noise_fp32: K floats or NULL (then X' = X);
  *   lora_a_bf16: r x K, lora_b_bf16: N x r (both NULL or r == 0: no LoRA);
  *   y: M x N, FP32 or bf16 (RNE of the FP32 result).
- * Accumulation is FP32.  M < 64 takes a weight-streaming decode kernel (16
- * tokens per launch); M >= 64 takes the tensor-core (tcgen05) prefill
+ * Accumulation is FP32.  M < 64 takes a weight-streaming decode path (per
+ * 16 tokens: an activation-preparation kernel, then the GEMM kernel, chained
+ * by programmatic dependent launch); M >= 64 takes the tensor-core (tcgen05) prefill
  * kernel, whose workspace holds an f16 copy of v(q) dec(e) (2 N K bytes);
  * nvfp4_gemm_kernel() says which.
  * workspace: nvfp4_workspace_bytes(M, N, K, r) bytes. */
@@ -116,7 +117,7 @@ nvfp4_status nvfp4_w4a16_lora_gemm(const void *x_bf16, int64_t M, int64_t N, int
 
 /* Which kernel family nvfp4_w4a16_lora_gemm runs for these sizes on the
  * current device (no counterpart on the pages): "prefill_tcgen05" (M >= 64,
- * K % 64 == 0, r <= 64), "decode_stream" (TMA-streaming decode kernel:
+ * K % 64 == 0, r <= 64), "decode_stream" (TMA-streaming decode GEMM:
  * K % 256 == 0, r <= 64), "decode_registers" (any other shape), or NULL for
  * invalid sizes or an unsupported device.  A static string. */
 const char *nvfp4_gemm_kernel(int64_t M, int64_t N, int64_t K, int64_t r);

@@ -75,6 +75,9 @@ CASES = [
     (16, 129, 768, 8, True, True),
     (12, 640, 4096, 64, True, True),
     (1, 3, 256, 0, False, False),
+    # more units than SMs: block ranges of one or two units that cross tile ends
+    (6, 2000, 5632, 32, True, True),
+    (8, 2000, 5376, 40, True, True),
 ]
 
 
