@@ -100,10 +100,17 @@ __host__ __device__ constexpr size_t tacc_bytes()  // 2 buffers of T summed over
 {
     return (size_t)2 * kMaxKS * (MP / 8) * 32 * 16;
 }
+constexpr int kBsmMaxR = 32;                       // LoRA B rows staged in shared memory up to this rank
+constexpr size_t kBBytes = (size_t)kRows * kBsmMaxR * 2;  // one tile's B rows (bf16)
+template <int MP>
+__host__ __device__ constexpr size_t bbuf_off()  // 2 buffers of a tile's B rows
+{
+    return n_stages<MP>() * stage_bytes<MP>() + red_bytes<MP>() + tacc_bytes<MP>();
+}
 template <int MP>
 __host__ __device__ constexpr size_t smem_bytes()  // + 1 KB to align the ring, + barriers
 {
-    return 1024 + n_stages<MP>() * stage_bytes<MP>() + red_bytes<MP>() + tacc_bytes<MP>() + 128;
+    return 1024 + bbuf_off<MP>() + 2 * kBBytes + 128;
 }
 static_assert(smem_bytes<8>() <= 232448 && smem_bytes<16>() <= 232448, "shared memory");
 
@@ -156,6 +163,7 @@ struct Params {
     const float *tensor_scale;
     const uint8_t *rec;        // [C] chunk records: 2^p per token | T_c | X' rows
     int rec_bytes;
+    int bsm;                   // 1: the producer stages each tile's B rows in shared memory
     float *part;               // [G][2][8][32][MP/2]: tile shares left for the last block
     uint32_t *tcnt;            // tile arrival counters
     uint32_t *ctl;
@@ -440,10 +448,20 @@ __device__ __forceinline__ uint32_t lora_pair(const Params &p, int R, int j)
     return lo | (hi << 16);
 }
 
-// The block's share of tile n for half-0 warp mt: s_t * acc + s * T_R B^T.
+// The same from a tile's B rows staged in shared memory (bs: row R - 128 n).
+__device__ __forceinline__ uint32_t lora_pair_s(const Params &p, const uint16_t *bs, int n, int R, int j)
+{
+    if (R >= p.N || j >= p.r)
+        return 0u;
+    return *reinterpret_cast<const uint32_t *>(bs + (size_t)(R - n * kRows) * p.r + j);
+}
+
+// The block's share of tile n for half-0 warp mt: s_t * acc + s * T_R B^T
+// (B rows from bs in shared memory, or from global memory when bs is null).
 template <int MP>
 __device__ __forceinline__ void tile_share(const Params &p, int n, int mt, int lane, float s_t,
-                                           const float (&acc)[MP / 8][4], const float4 *tr, float (&out)[MP / 8][4])
+                                           const float (&acc)[MP / 8][4], const float4 *tr, const uint16_t *bs,
+                                           float (&out)[MP / 8][4])
 {
     constexpr int NT = MP / 8;
     const int g = lane >> 2, t = lane & 3;
@@ -458,10 +476,17 @@ __device__ __forceinline__ void tile_share(const Params &p, int n, int mt, int l
     for (int ks = 0; ks < kMaxKS; ks++) {
         if (ks < p.KS) {
             uint32_t a[4];
-            a[0] = lora_pair(p, R0, 16 * ks + 2 * t);
-            a[1] = lora_pair(p, R1, 16 * ks + 2 * t);
-            a[2] = lora_pair(p, R0, 16 * ks + 8 + 2 * t);
-            a[3] = lora_pair(p, R1, 16 * ks + 8 + 2 * t);
+            if (bs) {
+                a[0] = lora_pair_s(p, bs, n, R0, 16 * ks + 2 * t);
+                a[1] = lora_pair_s(p, bs, n, R1, 16 * ks + 2 * t);
+                a[2] = lora_pair_s(p, bs, n, R0, 16 * ks + 8 + 2 * t);
+                a[3] = lora_pair_s(p, bs, n, R1, 16 * ks + 8 + 2 * t);
+            } else {
+                a[0] = lora_pair(p, R0, 16 * ks + 2 * t);
+                a[1] = lora_pair(p, R1, 16 * ks + 2 * t);
+                a[2] = lora_pair(p, R0, 16 * ks + 8 + 2 * t);
+                a[3] = lora_pair(p, R1, 16 * ks + 8 + 2 * t);
+            }
 #pragma unroll
             for (int nt = 0; nt < NT; nt++) {
                 const float4 v = tr[(ks * NT + nt) * 32 + lane];
@@ -506,8 +531,8 @@ __device__ __forceinline__ void store_tile(const Params &p, int n, int mt, int l
 // End of the block's segment of tile n (consumer warp mt, half h).
 template <int MP>
 __device__ __forceinline__ void finish_segment(const Params &p, int n, int u0, int mt, int h, int lane,
-                                               float (&acc)[MP / 8][4], const float4 *tr, float *red, int buf,
-                                               volatile uint32_t *s_flag, float s_t)
+                                               float (&acc)[MP / 8][4], const float4 *tr, const uint16_t *bs,
+                                               float *red, int buf, volatile uint32_t *s_flag, float s_t)
 {
     constexpr int NT = MP / 8;
     const int G = gridDim.x, b = blockIdx.x;
@@ -528,7 +553,7 @@ __device__ __forceinline__ void finish_segment(const Params &p, int n, int u0, i
             acc[nt][3] += v.w;
         }
         float y[NT][4];
-        tile_share<MP>(p, n, mt, lane, s_t, acc, tr, y);
+        tile_share<MP>(p, n, mt, lane, s_t, acc, tr, bs, y);
         const int first = owner_of(n * p.C, p.U, G), last = owner_of(n * p.C + p.C - 1, p.U, G);
         bool finish = true;
         if (last > first) {
@@ -606,9 +631,12 @@ __global__ void __launch_bounds__(kThreads, 1) stream_gemm_kernel(const __grid_c
     uint8_t *smem = reinterpret_cast<uint8_t *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     float *red = reinterpret_cast<float *>(smem + S * stage_bytes<MP>());
     float4 *tacc = reinterpret_cast<float4 *>(smem + S * stage_bytes<MP>() + red_bytes<MP>());
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + S * stage_bytes<MP>() + red_bytes<MP>() + tacc_bytes<MP>());
+    uint16_t *bbuf = reinterpret_cast<uint16_t *>(smem + bbuf_off<MP>());
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + bbuf_off<MP>() + 2 * kBBytes);
     uint64_t *empty = full + S;
-    volatile uint32_t *s_flag = reinterpret_cast<volatile uint32_t *>(empty + S);
+    uint64_t *bfull = empty + S;   // a segment's B rows in shared memory (2 buffers)
+    uint64_t *bempty = bfull + 2;  // B buffer free again
+    volatile uint32_t *s_flag = reinterpret_cast<volatile uint32_t *>(bempty + 2);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = gridDim.x, b = blockIdx.x;
@@ -617,6 +645,10 @@ __global__ void __launch_bounds__(kThreads, 1) stream_gemm_kernel(const __grid_c
         for (int s = 0; s < S; s++) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], kCWarps);
+        }
+        for (int k = 0; k < 2; k++) {
+            mbar_init(&bfull[k], 1);
+            mbar_init(&bempty[k], kCWarps);
         }
         mbar_fence_init();
     }
@@ -638,6 +670,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_gemm_kernel(const __grid_c
         if (lane == 0) {
             // a unit's record: 2^p, T_c and the first M rows of X'
             const uint32_t rbytes = (uint32_t)(kFacBytes + t_bytes(p.KS, MP)) + (uint32_t)p.M * 1024u;
+            int q = 0;  // segment
             for (int i = 0; i < u1 - u0; i++) {
                 const int u = u0 + i, s = i % S;
                 if (i >= S && !mbar_wait(&empty[s], ((i / S) + 1) & 1)) {
@@ -653,6 +686,17 @@ __global__ void __launch_bounds__(kThreads, 1) stream_gemm_kernel(const __grid_c
                     tma_load_2d(st + kBoxBytes, &p.tm_codes, &full[s], c * (kChunk / 2) + 128, n * kRows);
                 tma_load_2d(st + 2 * kBoxBytes, &p.tm_scales, &full[s], c * (kChunk / 16), n * kRows);
                 bulk_g2s(st + kXhOff, p.rec + (size_t)c * p.rec_bytes, rbytes, &full[s]);
+                if (p.bsm && (u + 1 == u1 || c + 1 == p.C)) {
+                    // the tile's B rows, for the epilogue of the segment this unit ends
+                    if (q >= 2 && !mbar_wait(&bempty[q & 1], ((q >> 1) + 1) & 1)) {
+                        record_status(p.ctl, NVFP4_ERR_TIMEOUT);
+                        break;
+                    }
+                    const uint32_t bbytes = (uint32_t)min(kRows, p.N - n * kRows) * (uint32_t)p.r * 2u;
+                    mbar_arrive_expect_tx(&bfull[q & 1], bbytes);
+                    bulk_g2s(bbuf + (q & 1) * (kBBytes / 2), p.lora_b + (size_t)n * kRows * p.r, bbytes, &bfull[q & 1]);
+                    q++;
+                }
             }
         }
         __syncwarp();
@@ -672,7 +716,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_gemm_kernel(const __grid_c
         const int tn = p.KS * NT * 32;  // float4 of T per chunk
         bool ok = true;
         bool seg_start = true;
-        int buf = 0;
+        int buf = 0, q = 0;  // T / B buffer, segment
         for (int u = u0, i = 0; u < u1; u++, i++) {
             const int s = i % S;
             if (ok && !mbar_wait(&full[s], (i / S) & 1)) {
@@ -708,9 +752,18 @@ __global__ void __launch_bounds__(kThreads, 1) stream_gemm_kernel(const __grid_c
             if (u + 1 == u1)
                 pdl_launch_dependents();
             if (u + 1 == u1 || c + 1 == p.C) {
-                finish_segment<MP>(p, n, u0, mt, h, lane, acc, tacc + buf * (kMaxKS * NT * 32), red, buf, s_flag,
-                                   s_t);
+                if (p.bsm && ok && !mbar_wait(&bfull[buf], (q >> 1) & 1)) {
+                    ok = false;
+                    if (lane == 0)
+                        record_status(p.ctl, NVFP4_ERR_TIMEOUT);
+                }
+                finish_segment<MP>(p, n, u0, mt, h, lane, acc, tacc + buf * (kMaxKS * NT * 32),
+                                   p.bsm ? bbuf + buf * (kBBytes / 2) : nullptr, red, buf, s_flag, s_t);
+                __syncwarp();
+                if (p.bsm && lane == 0)
+                    mbar_arrive(&bempty[buf]);
                 buf ^= 1;
+                q++;
                 seg_start = true;
             }
         }
@@ -930,6 +983,7 @@ cudaError_t launch_stream_gemm(const GemmArgs &a, cudaStream_t s, const DeviceIn
         p.tensor_scale = a.tensor_scale;
         p.rec = rec;
         p.rec_bytes = (int)pl.rec;
+        p.bsm = pl.KS > 0 && a.r <= kBsmMaxR && a.r % 8 == 0 ? 1 : 0;
         p.part = reinterpret_cast<float *>(a.ws + pl.off_part);
         p.tcnt = reinterpret_cast<uint32_t *>(a.ws + kCtlBytes);
         p.ctl = reinterpret_cast<uint32_t *>(a.ws);
