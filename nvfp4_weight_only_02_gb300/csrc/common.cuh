@@ -26,19 +26,15 @@ enum CtlWord : int {
     CTL_BAR_COUNT = 3,    // grid barrier: arrivals
     CTL_BAR_GEN = 4,      // grid barrier: generation
     CTL_RS_COUNT = 5,     // reserved
-    CTL_GEN = 6,          // streaming decode GEMM: calls completed on this workspace (mod 2^32)
-    CTL_DONE = 7,         // streaming decode GEMM: blocks of the current call that have finished
 };
 constexpr size_t kCtlBytes = 256;
 // After the control block: arrival counters at a fixed place, so that calls
 // of any shape find them at zero (every kernel that counts resets its
 // counters before it returns).  Per-call scratch starts after them.
-// Words [0, kTileCounters) count arrivals per output tile (decode GEMMs);
-// words [kTileCounters, kCounterWords) are the streaming decode GEMM's
-// per-chunk ready flags (they hold call generations, never need clearing).
-constexpr int kCounterWords = 8192;
+// The words count arrivals per output tile (decode GEMMs: the last block to
+// arrive at a tile adds up the shares of the others).
 constexpr int kTileCounters = 4096;
-constexpr size_t kWsHeaderBytes = kCtlBytes + 4 * (size_t)kCounterWords;
+constexpr size_t kWsHeaderBytes = kCtlBytes + 4 * (size_t)kTileCounters;
 
 // Spin limit of every device-side wait: about a second of polling, after
 // which the kernel records NVFP4_ERR_TIMEOUT and gives up instead of hanging.
