@@ -429,7 +429,7 @@ def run_gpu(args):
         "gpu_launches": wl.launches_per_step * args.steps,
     }
     if rank == 0:
-        if args.prefill:
+        if not args.no_prefill:
             line["prefill"] = run_prefill_case(torch, nv, synth, peak_tf)
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(seconds=args.cpu_seconds)
@@ -656,7 +656,7 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--eager", action="store_true", help="time eager launches instead of CUDA graphs")
-    ap.add_argument("--prefill", action="store_true", help="also time the 16384-token tensor-core GEMM")
+    ap.add_argument("--no-prefill", action="store_true", help="skip the 16384-token tensor-core GEMM line")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     args = ap.parse_args()
     if args.warmup < 3:

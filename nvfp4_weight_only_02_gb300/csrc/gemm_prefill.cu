@@ -127,19 +127,6 @@ __global__ void __launch_bounds__(256) prefill_xprime_kernel(const uint16_t *__r
         fac[warp] = exp2i(pexp);
 }
 
-__device__ __forceinline__ uint32_t xprime_pair_g(const uint16_t *x, const float *z, int M, int K, int m, int k)
-{
-    if (m >= M)
-        return 0u;
-    const uint32_t xb = *reinterpret_cast<const uint32_t *>(x + (size_t)m * K + k);
-    if (!z)
-        return xb;
-    const float2 zz = *reinterpret_cast<const float2 *>(z + k);
-    __nv_bfloat162 o = __floats2bfloat162_rn(__fmul_rn(bf16_bits_to_f32(xb & 0xFFFFu), zz.x),
-                                             __fmul_rn(bf16_bits_to_f32(xb >> 16), zz.y));
-    return *reinterpret_cast<uint32_t *>(&o);
-}
-
 // Column of the LoRA extension operand that holds T'[.][j] (part 0 = hi,
 // 1 = lo): r <= 32 uses one 64-column step [hi | lo], r <= 64 two steps.
 __device__ __forceinline__ int ext_col(int j, int part, int ES)
@@ -147,56 +134,93 @@ __device__ __forceinline__ int ext_col(int j, int part, int ES)
     return ES == 1 ? 32 * part + j : 64 * part + j;
 }
 
-// T = X' A^T (fp32, one warp per 16 tokens, up to 64 LoRA columns), written
-// as T' = s T / c_m in bf16 hi + lo at the extension columns.  ta (M x 64 ES
-// bf16) must be zero elsewhere.
-__global__ void __launch_bounds__(128) prefill_lora_ext_kernel(const uint16_t *__restrict__ x,
-                                                               const float *__restrict__ z,
+// f16x2 -> bf16x2, exact for the values X' 2^-p (at most 8 significant bits).
+__device__ __forceinline__ uint32_t h2_to_bf2(uint32_t h)
+{
+    const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&h));
+    __nv_bfloat162 o = __floats2bfloat162_rn(f.x, f.y);
+    return *reinterpret_cast<uint32_t *>(&o);
+}
+
+// The LoRA term in the accumulator's units: T' = s T / c_m = (s / s_t)
+// X'' A^T with X'' = X' 2^-p, the f16 rows the GEMM reads (exact in bf16),
+// written as bf16 hi + lo at the extension columns.  A block takes 64 tokens
+// (one warp per 16, up to 64 LoRA columns) and walks K in steps of 64,
+// staging those columns of X'' and of A in shared memory (the next step's
+// loads are in flight while the current one is multiplied); bf16 mma.sync,
+// FP32 accumulate.  ta (M x 64 ES bf16) must be zero elsewhere.
+constexpr int kLtRows = 64, kLtK = 64, kLtLd = kLtK + 8;  // padded rows: conflict-free fragments
+__global__ void __launch_bounds__(128) prefill_lora_ext_kernel(const __half *__restrict__ xh,
                                                                const uint16_t *__restrict__ a, int M, int K,
                                                                int r, int ES, float lora_scale,
                                                                const float *__restrict__ tensor_scale,
-                                                               const float *__restrict__ fac,
                                                                uint16_t *__restrict__ ta)
 {
-    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
-    const int g = lane >> 2, t = lane & 3;
-    const int m0 = warp * 16;
-    if (m0 >= M)
-        return;
+    __shared__ __align__(16) uint16_t xs[kLtRows * kLtLd];
+    __shared__ __align__(16) uint16_t as[kPfMaxR * kLtLd];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
+    const int m0 = blockIdx.x * kLtRows;
+    const int njt = (r + 7) / 8;
+    const uint16_t *x16 = reinterpret_cast<const uint16_t *>(xh);
+    // thread tid stages 16-byte pieces i = tid + 128 q: row i / 8, columns 8 (i % 8) ..
+    uint4 xv[4], av[4];
+    auto load = [&](int k0) {
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+            const int i = tid + 128 * q, row = i >> 3, col = (i & 7) * 8;
+            xv[q] = m0 + row < M ? *reinterpret_cast<const uint4 *>(x16 + (size_t)(m0 + row) * K + k0 + col)
+                                 : make_uint4(0u, 0u, 0u, 0u);
+            av[q] = row < r ? *reinterpret_cast<const uint4 *>(a + (size_t)row * K + k0 + col)
+                            : make_uint4(0u, 0u, 0u, 0u);
+        }
+    };
     float c[8][4];
 #pragma unroll
-    for (int jg = 0; jg < 8; jg++)
-        c[jg][0] = c[jg][1] = c[jg][2] = c[jg][3] = 0.0f;
-    for (int k0 = 0; k0 < K; k0 += 16) {
-        uint32_t af[4];
-        af[0] = xprime_pair_g(x, z, M, K, m0 + g, k0 + 2 * t);
-        af[1] = xprime_pair_g(x, z, M, K, m0 + g + 8, k0 + 2 * t);
-        af[2] = xprime_pair_g(x, z, M, K, m0 + g, k0 + 2 * t + 8);
-        af[3] = xprime_pair_g(x, z, M, K, m0 + g + 8, k0 + 2 * t + 8);
+    for (int jt = 0; jt < 8; jt++)
+        c[jt][0] = c[jt][1] = c[jt][2] = c[jt][3] = 0.0f;
+    load(0);
+    for (int k0 = 0; k0 < K; k0 += kLtK) {
 #pragma unroll
-        for (int jg = 0; jg < 8; jg++) {
-            const int j = jg * 8 + g;
-            uint32_t b0 = 0, b1 = 0;
-            if (j < r) {
-                b0 = *reinterpret_cast<const uint32_t *>(a + (size_t)j * K + k0 + 2 * t);
-                b1 = *reinterpret_cast<const uint32_t *>(a + (size_t)j * K + k0 + 2 * t + 8);
-            }
-            mma_bf16_16816(c[jg], af, b0, b1);
+        for (int q = 0; q < 4; q++) {
+            const int i = tid + 128 * q, row = i >> 3, col = (i & 7) * 8;
+            *reinterpret_cast<uint4 *>(xs + row * kLtLd + col) = xv[q];
+            *reinterpret_cast<uint4 *>(as + row * kLtLd + col) = av[q];
         }
+        __syncthreads();
+        if (k0 + kLtK < K)
+            load(k0 + kLtK);
+        const uint16_t *xr0 = xs + (16 * warp + g) * kLtLd, *xr1 = xr0 + 8 * kLtLd;
+#pragma unroll
+        for (int kk = 0; kk < kLtK; kk += 16) {
+            uint32_t af[4];
+            af[0] = h2_to_bf2(*reinterpret_cast<const uint32_t *>(xr0 + kk + 2 * t));
+            af[1] = h2_to_bf2(*reinterpret_cast<const uint32_t *>(xr1 + kk + 2 * t));
+            af[2] = h2_to_bf2(*reinterpret_cast<const uint32_t *>(xr0 + kk + 2 * t + 8));
+            af[3] = h2_to_bf2(*reinterpret_cast<const uint32_t *>(xr1 + kk + 2 * t + 8));
+#pragma unroll
+            for (int jt = 0; jt < 8; jt++) {
+                if (jt < njt) {
+                    const uint16_t *br = as + (8 * jt + g) * kLtLd + kk + 2 * t;
+                    mma_bf16_16816(c[jt], af, *reinterpret_cast<const uint32_t *>(br),
+                                   *reinterpret_cast<const uint32_t *>(br + 8));
+                }
+            }
+        }
+        __syncthreads();
     }
     const float s_t = *tensor_scale;
+    const float ratio = __fdiv_rn(lora_scale, s_t != 0.0f ? s_t : 1.0f);
     const int W = 64 * ES;
 #pragma unroll
     for (int q = 0; q < 4; q++) {
-        const int m = m0 + g + 8 * (q >> 1);
+        const int m = m0 + 16 * warp + g + 8 * (q >> 1);
         if (m >= M)
             continue;
-        const float cm = row_factor(s_t, fac[m]);
 #pragma unroll
-        for (int jg = 0; jg < 8; jg++) {
-            const int j = jg * 8 + 2 * t + (q & 1);
+        for (int jt = 0; jt < 8; jt++) {
+            const int j = jt * 8 + 2 * t + (q & 1);
             if (j < r) {
-                const float tv = __fdiv_rn(__fmul_rn(lora_scale, c[jg][q]), cm);
+                const float tv = __fmul_rn(ratio, c[jt][q]);
                 const __nv_bfloat16 hi = __float2bfloat16_rn(tv);
                 const __nv_bfloat16 lo = __float2bfloat16_rn(tv - __bfloat162float(hi));
                 ta[(size_t)m * W + ext_col(j, 0, ES)] = *reinterpret_cast<const uint16_t *>(&hi);
@@ -530,8 +554,8 @@ cudaError_t launch_prefill_gemm(const GemmArgs &a, cudaStream_t s, const DeviceI
         cudaError_t e = cudaMemsetAsync(ta, 0, (size_t)M * 64 * pl.ES * 2, s);
         if (e != cudaSuccess)
             return e;
-        prefill_lora_ext_kernel<<<(M + 63) / 64, 128, 0, s>>>(a.x, a.noise, a.lora_a, M, K, r, pl.ES, a.lora_scale,
-                                                              a.tensor_scale, fac, ta);
+        prefill_lora_ext_kernel<<<(M + kLtRows - 1) / kLtRows, 128, 0, s>>>(xh, a.lora_a, M, K, r, pl.ES,
+                                                                            a.lora_scale, a.tensor_scale, ta);
     }
 
     CUtensorMap tmx, tmw, tma_, tmb;
