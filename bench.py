@@ -77,10 +77,18 @@ def load_peaks():
     return 6800.0, 1900.0, "fallback"
 
 
-def source_hash():
+# The sources each profiled kernel is built from: a committed DRAM-traffic
+# figure counts only while none of them has changed since it was taken.
+KERNEL_SOURCES = {
+    "decode_stream": ("gemm_stream.cu", "common.cuh", "sm100.cuh", "internal.h"),
+    "quantize_fused": ("quantize.cu", "common.cuh", "internal.h"),
+}
+
+
+def source_hash(kernel):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "nvfp4_weight_only_02_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in KERNEL_SOURCES[kernel]:
         h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
@@ -93,7 +101,7 @@ def traffic_record(kernel):
         return None
     d = json.load(open(p))
     rec = d.get(kernel)
-    if not rec or rec.get("source_hash") != source_hash():
+    if not rec or kernel not in KERNEL_SOURCES or rec.get("source_hash") != source_hash(kernel):
         return None
     return rec.get("dram_bytes_per_launch")
 
