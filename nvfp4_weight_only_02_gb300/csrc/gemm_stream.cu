@@ -67,7 +67,8 @@ constexpr int kThreads = (kCWarps + 4) * 32;
 constexpr int kPrepThreads = kCWarps * 32;  // xprep: one warp per token, then T_c
 constexpr int kMaxR = 64;
 constexpr int kMaxKS = kMaxR / 16;       // LoRA k-steps of 16 columns of T
-constexpr int kPrefetchUnits = 6;        // units per block prefetched into L2 before the wait
+constexpr int kPrefetchUnits = 2;        // units per block prefetched into L2 before the wait
+                                         // (deeper prefetch slows the preparation kernel's loads)
 constexpr size_t kXhOff = 2 * kBoxBytes + kScaleBox;  // the record in a stage
 
 // named barriers (0 is __syncthreads)
@@ -673,6 +674,12 @@ __global__ void __launch_bounds__(kThreads, 1) stream_gemm_kernel(const __grid_c
             int q = 0;  // segment
             for (int i = 0; i < u1 - u0; i++) {
                 const int u = u0 + i, s = i % S;
+                // the first unit alone: its stage lands before the other stages
+                // of every block queue up in front of it
+                if (i == 1 && !mbar_wait(&full[0], 0)) {
+                    record_status(p.ctl, NVFP4_ERR_TIMEOUT);
+                    break;
+                }
                 if (i >= S && !mbar_wait(&empty[s], ((i / S) + 1) & 1)) {
                     record_status(p.ctl, NVFP4_ERR_TIMEOUT);
                     break;  // stop copying; consumers time out and wind down
