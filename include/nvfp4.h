@@ -115,6 +115,25 @@ nvfp4_status nvfp4_w4a16_lora_gemm(const void *x_bf16, int64_t M, int64_t N, int
                                    void *y, nvfp4_dtype y_dtype,
                                    void *workspace, size_t ws_bytes, void *stream);
 
+/* Scale-QLoRA forward (Scale-QLoRA post, method): the block scales are
+ * trainable FP32 parameters (decoded block scales in weight units, N x K/16,
+ * as for nvfp4_round_scales) and the codes stay frozen.  Each call rounds the
+ * parameters to E4M3 against *tensor_scale into scales_e4m3 (exactly
+ * nvfp4_round_scales: parameters <= 0 give 0, non-finite ones record
+ * NVFP4_ERR_NONFINITE) and then runs nvfp4_w4a16_lora_gemm with codes,
+ * scales_e4m3 and the same remaining arguments, on the same stream.  On
+ * return scales_e4m3 holds the merged model's scales: merging is this
+ * rounding, with the codes copied verbatim.  scales_e4m3: N x K/16 bytes,
+ * caller-owned, 16-byte aligned.  Every host check of both steps runs before
+ * anything is launched.  workspace: nvfp4_workspace_bytes(M, N, K, r). */
+nvfp4_status nvfp4_scale_qlora_gemm(const void *x_bf16, int64_t M, int64_t N, int64_t K,
+                                    const uint8_t *codes, const float *scale_param,
+                                    const float *tensor_scale, uint8_t *scales_e4m3,
+                                    const void *lora_a_bf16, const void *lora_b_bf16,
+                                    int64_t r, float lora_scale, const float *noise_fp32,
+                                    void *y, nvfp4_dtype y_dtype,
+                                    void *workspace, size_t ws_bytes, void *stream);
+
 /* Which kernel family nvfp4_w4a16_lora_gemm runs for these sizes on the
  * current device (no counterpart on the pages): "prefill_tcgen05" (M >= 64,
  * K % 64 == 0, r <= 64), "decode_stream" (TMA-streaming decode GEMM:

@@ -26,6 +26,7 @@ EXPORTS = [
     "nvfp4_workspace_bytes", "nvfp4_quantize", "nvfp4_dequantize", "nvfp4_w4a16_lora_gemm",
     "nvfp4_round_scales", "nvfp4_get_device_status", "nvfp4_status_string", "nvfp4_encode_debug",
     "nvfp4_quotient_check", "nvfp4_w4a16_lora_gemm_static", "nvfp4_wait_selftest", "nvfp4_gemm_kernel",
+    "nvfp4_scale_qlora_gemm",
 ]
 
 
@@ -68,6 +69,8 @@ def load(build_if_missing: bool = True):
                                                   P, P, ctypes.c_int, P]),
             "nvfp4_wait_selftest": (st, [P, ctypes.c_int, P]),
             "nvfp4_gemm_kernel": (ctypes.c_char_p, [i64, i64, i64, i64]),
+            "nvfp4_scale_qlora_gemm": (st, [P, i64, i64, i64, P, P, P, P, P, P, i64, ctypes.c_float, P, P,
+                                            ctypes.c_int, P, ctypes.c_size_t, P]),
         }
         for name, (res, args) in sig.items():
             f = getattr(lib, name)
@@ -191,6 +194,34 @@ def nvfp4_round_scales(scale_param: torch.Tensor, tensor_scale: torch.Tensor,
     st = load().nvfp4_round_scales(_ptr(scale_param), _ptr(tensor_scale), N, KB * 16,
                                    _ptr(scales), _ptr(workspace), workspace.numel(), _stream())
     _check(st, "nvfp4_round_scales")
+
+
+def nvfp4_scale_qlora_gemm(x: torch.Tensor, codes: torch.Tensor, scale_param: torch.Tensor,
+                           tensor_scale: torch.Tensor, scales: torch.Tensor, lora_a, lora_b,
+                           lora_scale: float, noise, y: torch.Tensor, workspace: torch.Tensor):
+    M, K = x.shape
+    N = codes.shape[0]
+    _need(x, torch.bfloat16, (M, K), "x")
+    _need(codes, torch.uint8, (N, K // 2), "codes")
+    _need(scale_param, torch.float32, (N, K // 16), "scale_param")
+    _need(scales, torch.uint8, (N, K // 16), "scales")
+    _need(tensor_scale, torch.float32, (1,), "tensor_scale")
+    r = 0
+    if lora_a is not None:
+        r = lora_a.shape[0]
+        _need(lora_a, torch.bfloat16, (r, K), "lora_a")
+        _need(lora_b, torch.bfloat16, (N, r), "lora_b")
+    if noise is not None:
+        _need(noise, torch.float32, (K,), "noise")
+    if y.dtype not in (torch.float32, torch.bfloat16):
+        raise ValueError("y must be float32 or bfloat16")
+    _need(y, y.dtype, (M, N), "y")
+    st = load().nvfp4_scale_qlora_gemm(
+        _ptr(x), M, N, K, _ptr(codes), _ptr(scale_param), _ptr(tensor_scale), _ptr(scales),
+        _ptr(lora_a), _ptr(lora_b), r, float(lora_scale), _ptr(noise), _ptr(y),
+        OUT_FP32 if y.dtype == torch.float32 else OUT_BF16, _ptr(workspace), workspace.numel(),
+        _stream())
+    _check(st, "nvfp4_scale_qlora_gemm")
 
 
 def nvfp4_encode_debug(x: torch.Tensor, which: int) -> torch.Tensor:

@@ -191,6 +191,32 @@ nvfp4_status nvfp4_round_scales(const float *scale_param, const float *tensor_sc
                                          (uint32_t *)workspace, (cudaStream_t)stream, *dev));
 }
 
+nvfp4_status nvfp4_scale_qlora_gemm(const void *x_bf16, int64_t M, int64_t N, int64_t K, const uint8_t *codes,
+                                    const float *scale_param, const float *tensor_scale, uint8_t *scales_e4m3,
+                                    const void *lora_a_bf16, const void *lora_b_bf16, int64_t r,
+                                    float lora_scale, const float *noise_fp32, void *y, nvfp4_dtype y_dtype,
+                                    void *workspace, size_t ws_bytes, void *stream)
+{
+    // every host check of both steps before anything is launched
+    if (!x_bf16 || !codes || !scale_param || !tensor_scale || !scales_e4m3 || !y || !workspace)
+        return NVFP4_ERR_INVALID_ARG;
+    if (M < 1 || N < 1 || K < 16 || K % 16 != 0 || r < 0 || r > 256 || N > (1LL << 30) || K > (1LL << 30))
+        return NVFP4_ERR_SHAPE;
+    if (!aligned16(scale_param) || !aligned16(scales_e4m3))
+        return NVFP4_ERR_ALIGNMENT;
+    const size_t need = nvfp4_workspace_bytes(M, N, K, (lora_a_bf16 && lora_b_bf16) ? r : 0);
+    if (need == 0)
+        return NVFP4_ERR_UNSUPPORTED_DEVICE;
+    if (ws_bytes < need)
+        return NVFP4_ERR_WORKSPACE;
+    nvfp4_status st = nvfp4_round_scales(scale_param, tensor_scale, N, K, scales_e4m3, workspace, ws_bytes,
+                                         stream);
+    if (st != NVFP4_OK)
+        return st;
+    return nvfp4_w4a16_lora_gemm(x_bf16, M, N, K, codes, scales_e4m3, tensor_scale, lora_a_bf16, lora_b_bf16, r,
+                                 lora_scale, noise_fp32, y, y_dtype, workspace, ws_bytes, stream);
+}
+
 nvfp4_status nvfp4_get_device_status(void *workspace, void *stream)
 {
     if (!workspace)

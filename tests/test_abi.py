@@ -65,6 +65,13 @@ def test_host_checks_reject_before_launch(lib):
                                      0, good, 1 << 20, null) == binding.ERR_SHAPE
     assert lib.nvfp4_dequantize(good, good, good, 4, 32, bad_align, 1, null) == binding.ERR_ALIGNMENT
     assert lib.nvfp4_round_scales(good, good, 4, 31, good, good, 256, null) == binding.ERR_SHAPE
+    # Scale-QLoRA forward: both steps' host checks before any launch
+    assert lib.nvfp4_scale_qlora_gemm(good, 1, 16, 32, good, null, good, good, null, null, 0, 0.0, null,
+                                      good, 1, good, 1 << 20, null) == binding.ERR_INVALID_ARG
+    assert lib.nvfp4_scale_qlora_gemm(good, 1, 16, 24, good, good, good, good, null, null, 0, 0.0, null,
+                                      good, 1, good, 1 << 20, null) == binding.ERR_SHAPE
+    assert lib.nvfp4_scale_qlora_gemm(good, 1, 16, 32, good, bad_align, good, good, null, null, 0, 0.0, null,
+                                      good, 1, good, 1 << 20, null) == binding.ERR_ALIGNMENT
     assert lib.nvfp4_workspace_bytes(1, 16, 30, 0) == 0
     assert lib.nvfp4_gemm_kernel(1, 16, 30, 0) is None
     assert lib.nvfp4_encode_debug(good, 8, 5, good, null) == binding.ERR_INVALID_ARG

@@ -189,3 +189,32 @@ def test_full_size_decode(nv, orc, model, which, M):
     ref = orc.gemm(c.x, codes, scales, st, c.a, c.b, c.lora_scale, c.z)
     max_rel, mean_rel = _check(y, ref)
     print(f"{model} {which} M={M}: max_rel {max_rel:.3e} mean_rel {mean_rel:.3e}")
+
+
+def test_scale_qlora_forward(nv, orc):
+    """Scale-QLoRA forward on 32B-shaped weights (W 27648 x 5120, 8 tokens,
+    LoRA r = 64, noise): trainable FP32 block scales rounded on the way in,
+    codes frozen.  The rounded scales are the CPU definition bit for bit, the
+    output matches the FP64 oracle on the merged weights, and equals the plain
+    GEMM on the merged weights exactly (the same kernels run)."""
+    c = synth.qwen32b_case("up", 8, seed=41)
+    q, codes, scales, st = _quantize_both(nv, orc, c.w)
+    g = torch.Generator(device="cpu").manual_seed(42)
+    dec = q.scales.view(torch.float8_e4m3fn).float()
+    jitter = (torch.rand(dec.shape, generator=g) * 0.2 - 0.1).cuda()
+    param = (dec * q.tensor_scale * (1 + jitter)).contiguous()
+    x, a, b, z = _dev(c.x), _dev(c.a), _dev(c.b), torch.from_numpy(c.z).cuda()
+    M, K = c.x.shape
+    N = q.shape[0]
+    rounded = torch.empty_like(q.scales)
+    y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    ws = nv.new_workspace(nv.nvfp4_workspace_bytes(M, N, K, 64))
+    nv.nvfp4_scale_qlora_gemm(x, q.codes, param, q.tensor_scale, rounded, a, b, c.lora_scale, z, y, ws)
+    assert nv.nvfp4_get_device_status(ws) == nv.OK
+    rc, ref_scales = orc.round_scales(param.cpu().numpy(), np.float32(q.tensor_scale.item()))
+    assert rc == orc.OK and np.array_equal(rounded.cpu().numpy(), ref_scales)
+    ref = orc.gemm(c.x, codes, ref_scales, st, c.a, c.b, c.lora_scale, c.z)
+    _check(y.cpu().numpy(), ref)
+    merged = nv.QuantizedWeight(q.codes, rounded, q.tensor_scale)
+    y2 = nv.gemm(x, merged, a, b, c.lora_scale, z)
+    assert torch.equal(y, y2)
