@@ -1,0 +1,55 @@
+"""Whole-stack quantise + decode: the 28 layers of a Qwen2.5-7B-shaped model
+(q/o 3584x3584, k/v 512x3584, gate/up 18944x3584, down 3584x18944), BF16
+weights ~N(0, 0.02^2) drawn on the device from seeded generators, every one of
+the 196 matrices quantised with its own dynamic tensor scale and multiplied by
+the same 8 tokens.
+
+Each matrix is checked against the oracle on sampled rows: the row holding the
+matrix's largest |w| plus three random rows, quantised by the oracle in
+dynamic mode (so its tensor scale comes from the same amax), must give the
+GPU's tensor scale, codes and block scales bit for bit, and the GPU's GEMM
+outputs for those rows must match the oracle's FP64 GEMM within tolerance.
+"""
+import numpy as np
+import pytest
+import torch
+
+from nvfp4_weight_only_02_gb300 import synth
+from tests.test_gpu_gemm import _check
+
+pytestmark = pytest.mark.gpu
+
+LAYERS = 28
+SHAPES = [("q", 3584, 3584), ("k", 512, 3584), ("v", 512, 3584), ("o", 3584, 3584),
+          ("gate", 18944, 3584), ("up", 18944, 3584), ("down", 3584, 18944)]
+
+
+def test_whole_stack_quantise_and_decode(nv, orc):
+    M = 8
+    xb = {K: synth.activations(M, K, 70 + K) for K in (3584, 18944)}
+    xd = {K: torch.from_numpy(b.view(np.int16)).view(torch.bfloat16).cuda() for K, b in xb.items()}
+    ws = nv.new_workspace(max(nv.nvfp4_workspace_bytes(M, N, K, 0) for _, N, K in SHAPES))
+    gen = torch.Generator(device="cuda")
+    pick = np.random.default_rng(2048)
+    checked = 0
+    for layer in range(LAYERS):
+        for j, (name, N, K) in enumerate(SHAPES):
+            gen.manual_seed(1000 * layer + j)
+            w = (torch.randn((N, K), generator=gen, device="cuda") * 0.02).to(torch.bfloat16)
+            q = nv.quantize(w, workspace=ws)
+            y = nv.gemm(xd[K], q, workspace=ws)
+            top = int(torch.argmax(w.abs().float()).item()) // K
+            rows = [top] + [int(r) for r in pick.choice(np.delete(np.arange(N), top), size=3, replace=False)]
+            wb = w[rows].view(torch.int16).cpu().numpy().view(np.uint16)
+            rc, codes, scales, st = orc.quantize(wb)
+            assert rc == orc.OK
+            where = f"layer {layer} {name}"
+            assert np.float32(q.tensor_scale.item()) == st, where
+            assert np.array_equal(q.codes[rows].cpu().numpy(), codes), where
+            assert np.array_equal(q.scales[rows].cpu().numpy(), scales), where
+            ref = orc.gemm(xb[K], codes, scales, st)
+            _check(y[:, rows].cpu().numpy(), ref)
+            checked += 1
+            del w, q, y
+    assert checked == LAYERS * len(SHAPES)
+    assert nv.nvfp4_get_device_status(ws) == nv.OK
