@@ -1,7 +1,8 @@
 // gemm_stream.cu -- the decode GEMM (M <= 16 tokens per launch, LoRA rank
 // r <= 64) for weights whose rows are 16-byte aligned in both arrays
-// (K % 256 == 0; every Qwen2.5 projection): one kernel per launch that
-// streams the weight bytes through a shared-memory ring with TMA.
+// (K % 256 == 0; every Qwen2.5 projection): a small activation-preparation
+// kernel, then a kernel that streams the weight bytes through a
+// shared-memory ring with TMA.
 //
 //   X' = bf16(X * z),   Y = s_t * X' deq(W)^T + s * (X' A^T) B^T
 // ("RL with NVFP4 + LoRA" post, tggo.me/sberlogasci/42740, section "Метод";
