@@ -1,0 +1,89 @@
+"""Out-of-bounds writes (compute-sanitizer is closed on this machine): every
+output buffer and the workspace sit between guard bytes holding a fixed
+pattern, which must be untouched after each call, on ragged and tiled shapes
+of every kernel family (quantiser both modes, dequantiser, scale update, and
+the GEMM's streaming, register-streaming and tcgen05 paths)."""
+import numpy as np
+import pytest
+import torch
+
+from nvfp4_weight_only_02_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+GUARD = 4096  # bytes on each side (keeps the payload 16-byte aligned)
+PATTERN = 0xA5
+
+
+class Guarded:
+    """nbytes of payload inside a buffer whose head and tail hold PATTERN."""
+
+    def __init__(self, nbytes, fill=PATTERN):
+        self.n = int(nbytes)
+        self.buf = torch.full((self.n + 2 * GUARD,), PATTERN, dtype=torch.uint8, device="cuda")
+        self.buf[GUARD:GUARD + self.n].fill_(fill)
+
+    def view(self, dtype, shape):
+        return self.buf[GUARD:GUARD + self.n].view(dtype).view(shape)
+
+    def intact(self):
+        torch.cuda.synchronize()
+        return bool((self.buf[:GUARD] == PATTERN).all()) and bool((self.buf[GUARD + self.n:] == PATTERN).all())
+
+
+def _dev(bits):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()
+
+
+@pytest.mark.parametrize("N,K", [(1, 16), (17, 48), (129, 256), (300, 1040), (513, 2064), (1000, 3584)])
+def test_quantize_dequantize_and_scale_update_stay_in_bounds(nv, N, K):
+    w = _dev(synth.normal_weight((N, K), 0.02, N + K, outlier_frac=1e-3))
+    for given in (False, True):
+        codes, scales, ts = Guarded(N * K // 2), Guarded(N * K // 16), Guarded(4, fill=0)
+        ws = Guarded(256, fill=0)
+        t = ts.view(torch.float32, (1,))
+        if given:
+            t.fill_(0.01)
+        nv.nvfp4_quantize(w, codes.view(torch.uint8, (N, K // 2)), scales.view(torch.uint8, (N, K // 16)), t,
+                          given, ws.view(torch.uint8, (256,)))
+        assert nv.nvfp4_get_device_status(ws.view(torch.uint8, (256,))) == nv.OK
+        assert codes.intact() and scales.intact() and ts.intact() and ws.intact()
+    q = nv.QuantizedWeight(codes.view(torch.uint8, (N, K // 2)), scales.view(torch.uint8, (N, K // 16)), t)
+    for dt, es in ((torch.float32, 4), (torch.bfloat16, 2)):
+        out = Guarded(N * K * es)
+        nv.nvfp4_dequantize(q.codes, q.scales, q.tensor_scale, out.view(dt, (N, K)))
+        assert out.intact()
+    param = (q.scales.view(torch.float8_e4m3fn).float() * t * 1.03).contiguous()
+    new = Guarded(N * K // 16)
+    ws = Guarded(256, fill=0)
+    nv.nvfp4_round_scales(param, t, new.view(torch.uint8, (N, K // 16)), ws.view(torch.uint8, (256,)))
+    assert new.intact() and ws.intact()
+
+
+# M, N, K, r: streaming decode (K % 256 == 0), register-streaming (other K),
+# tcgen05 prefill (M >= 64), with ragged tiles, half chunks and LoRA ranks
+GEMM_CASES = [
+    (1, 3, 256, 0), (7, 200, 1280, 16), (16, 129, 768, 8), (12, 640, 4096, 64), (6, 2000, 5632, 32),
+    (3, 17, 48, 4), (8, 300, 1040, 16), (16, 513, 2064, 8),
+    (64, 256, 64, 0), (200, 300, 1024, 32), (1000, 129, 640, 64),
+]
+
+
+@pytest.mark.parametrize("M,N,K,r", GEMM_CASES)
+def test_gemm_stays_in_bounds(nv, M, N, K, r):
+    c = synth.small_case(M, N, K, max(r, 1), seed=M + N + K, with_lora=r > 0, with_noise=True)
+    q = nv.quantize(_dev(c.w))
+    a = _dev(c.a) if r > 0 else None
+    b = _dev(c.b) if r > 0 else None
+    z = torch.from_numpy(c.z).cuda()
+    x = _dev(c.x)
+    need = nv.nvfp4_workspace_bytes(M, N, K, r)
+    for dt, es in ((torch.float32, 4), (torch.bfloat16, 2)):
+        y = Guarded(M * N * es)
+        ws = Guarded((need + 255) // 256 * 256, fill=0)
+        for _ in range(2):  # a second call on the same workspace
+            nv.nvfp4_w4a16_lora_gemm(x, q.codes, q.scales, q.tensor_scale, a, b, c.lora_scale if r else 0.0, z,
+                                     y.view(dt, (M, N)), ws.view(torch.uint8, (ws.n,)))
+        assert nv.nvfp4_get_device_status(ws.view(torch.uint8, (ws.n,))) == nv.OK
+        assert y.intact(), "output guard overwritten"
+        assert ws.intact(), "workspace guard overwritten"
