@@ -41,6 +41,10 @@ MUTATIONS = [
     ("scale update divides wrong way", "p / s_t;", "p * s_t;"),
     ("reciprocal instead of division", "float x = orc_bf16_to_f32(row[b * 16 + i]) / S_b;",
      "float x = orc_bf16_to_f32(row[b * 16 + i]) * (1.0f / S_b);"),
+    ("zero block scale not special-cased", "if (S_b != 0.0f) {", "if (1) {"),
+    ("tensor amax without abs", "float v = fabsf(orc_bf16_to_f32(w[i]));", "float v = orc_bf16_to_f32(w[i]);"),
+    ("LoRA branch without noise", "t += (double)orc_bf16_to_f32(xp[m * K + k])",
+     "t += (double)orc_bf16_to_f32(x[m * K + k])"),
 ]
 
 PINS = [
@@ -59,6 +63,7 @@ PINS = [
     quant.test_exact_ties_resolve_to_even_code_at_every_scale,
     quant.test_scale_only_update_merge_is_bit_identical,
     quant.test_round_scales_edge_values,
+    quant.test_sign_symmetry,
     lambda o: gemm.test_gemm_vs_exact_rationals(o, 3, 5, 32, 2),
     lambda o: gemm.test_gemm_vs_exact_rationals(o, 2, 8, 48, 4),
     gemm.test_gemm_dyadic_is_exact,

@@ -144,6 +144,26 @@ def test_error_bound(orc, kind):
     assert np.all(err[normal] <= bound[normal])
 
 
+def test_sign_symmetry(orc):
+    """Negating W keeps the tensor scale (an amax of magnitudes) and every
+    block scale, and flips exactly the sign bit of every code (the E2M1 code
+    carries the sign of w, zeros included).  The largest magnitudes are made
+    negative so a signed max would give a different tensor scale."""
+    g = np.random.default_rng(7)
+    w = g.standard_normal((24, 96)).astype(np.float32) * 0.02
+    w[3, 5] = -0.5   # tensor amax, negative
+    w[7, 40] = -0.3
+    bits = synth.to_bf16_bits(w)
+    rc, codes, scales, st = orc.quantize(bits)
+    assert rc == orc.OK
+    rcn, codes_n, scales_n, st_n = orc.quantize(bits ^ np.uint16(0x8000))
+    assert rcn == orc.OK
+    assert st_n == st
+    assert np.array_equal(scales_n, scales)
+    assert np.all(scales != 0)
+    assert np.array_equal(codes_n, codes ^ np.uint8(0x88))
+
+
 def test_code_share_is_eight_ninths(orc):
     # "codes are about 90% of the file": 16-element blocks with 1-byte scales
     for N, K in [(512, 2048), (18944, 3584), (27648, 5120)]:
