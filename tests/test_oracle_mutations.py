@@ -45,6 +45,14 @@ MUTATIONS = [
     ("tensor amax without abs", "float v = fabsf(orc_bf16_to_f32(w[i]));", "float v = orc_bf16_to_f32(w[i]);"),
     ("LoRA branch without noise", "t += (double)orc_bf16_to_f32(xp[m * K + k])",
      "t += (double)orc_bf16_to_f32(x[m * K + k])"),
+    ("frozen scale ignored", "    if (given) {\n        s_t = *st_io;", "    if (0) {\n        s_t = *st_io;"),
+    ("dequant scales by s_t before the block scale",
+     "float vd = (float)(orc_e2m1_value(code_at(codes, K, n, k)) *\n                               orc_e4m3_value(scales[n * (K / 16) + k / 16]));\n            float v = vd * s_t;",
+     "float vd = (float)orc_e2m1_value(code_at(codes, K, n, k)) * s_t;\n            float v = vd * (float)orc_e4m3_value(scales[n * (K / 16) + k / 16]);"),
+    ("LoRA term subtracted", "acc + c->s * lora", "acc - c->s * lora"),
+    ("GEMM accumulates in float", "        double acc = 0.0;\n        for (int64_t k = 0; k < c->K; k++) {",
+     "        float acc = 0.0f;\n        for (int64_t k = 0; k < c->K; k++) {"),
+    ("LoRA down-projection in float", "            double t = 0.0;", "            float t = 0.0f;"),
 ]
 
 PINS = [
@@ -64,6 +72,7 @@ PINS = [
     quant.test_scale_only_update_merge_is_bit_identical,
     quant.test_round_scales_edge_values,
     quant.test_sign_symmetry,
+    quant.test_frozen_scale_used_verbatim,
     lambda o: gemm.test_gemm_vs_exact_rationals(o, 3, 5, 32, 2),
     lambda o: gemm.test_gemm_vs_exact_rationals(o, 2, 8, 48, 4),
     gemm.test_gemm_dyadic_is_exact,

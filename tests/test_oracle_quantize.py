@@ -200,6 +200,17 @@ def test_frozen_scale_used_verbatim(orc):
     # a larger frozen scale pushes every block scale down
     rc2, c2, s2, _ = orc.quantize(wb, tensor_scale=st0 * 4)
     assert np.all(s2 <= s0)
+    # twice the tensor scale: every block target e_f halves, and halving is
+    # exact on the E4M3 grid while the result stays normal, so each such block
+    # scale byte drops by one exponent step (8) and S_b = dec(e) s_t, hence
+    # every code, is unchanged
+    rc3, c3, s3, st3 = orc.quantize(wb, tensor_scale=st0 * 2)
+    assert rc3 == orc.OK and st3 == np.float32(st0 * 2)
+    normal = s0 >= 16
+    assert normal.mean() > 0.9
+    assert np.array_equal(s3[normal], s0[normal] - 8)
+    rows = np.repeat(normal, 8, axis=1)  # 8 code bytes per 16-element block
+    assert np.array_equal(c3[rows], c0[rows])
 
 
 def test_subnormal_scale_blocks_saturate(orc):
