@@ -53,6 +53,9 @@ MUTATIONS = [
     ("GEMM accumulates in float", "        double acc = 0.0;\n        for (int64_t k = 0; k < c->K; k++) {",
      "        float acc = 0.0f;\n        for (int64_t k = 0; k < c->K; k++) {"),
     ("LoRA down-projection in float", "            double t = 0.0;", "            float t = 0.0f;"),
+    ("negative scale parameter not zeroed", "(s_t == 0.0f || p <= 0.0f) ? 0.0f : p / s_t",
+     "(s_t == 0.0f) ? 0.0f : fabsf(p) / s_t"),
+    ("LoRA A read transposed", "(double)orc_bf16_to_f32(A[j * K + k])", "(double)orc_bf16_to_f32(A[k * r + j])"),
 ]
 
 PINS = [
