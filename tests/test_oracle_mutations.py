@@ -56,6 +56,11 @@ MUTATIONS = [
     ("negative scale parameter not zeroed", "(s_t == 0.0f || p <= 0.0f) ? 0.0f : p / s_t",
      "(s_t == 0.0f) ? 0.0f : fabsf(p) / s_t"),
     ("LoRA A read transposed", "(double)orc_bf16_to_f32(A[j * K + k])", "(double)orc_bf16_to_f32(A[k * r + j])"),
+    ("block amax over half the block", "        float a_b = 0.0f;\n        for (int i = 0; i < 16; i++) {",
+     "        float a_b = 0.0f;\n        for (int i = 0; i < 8; i++) {"),
+    ("LoRA scale on the base term", "c->y[m * c->N + n] = acc + c->s * lora;", "c->y[m * c->N + n] = c->s * acc + lora;"),
+    ("output rows and columns swapped", "c->y[m * c->N + n] = acc + c->s * lora;",
+     "c->y[n * c->M + m] = acc + c->s * lora;"),
 ]
 
 PINS = [
