@@ -128,3 +128,42 @@ def test_bf16_conversion_vs_torch(orc):
     bits = bits[(bits & 0x7F80) != 0x7F80]
     back = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).float().numpy()
     assert np.array_equal(orc.bf16_to_f32(bits).view(np.uint32), back.view(np.uint32))
+
+
+def _threshold_e2m1_vec(x):
+    """Vectorised form of the threshold encoder above (same midpoints and tie
+    rule), written independently of the oracle's nearest-grid search."""
+    x = np.asarray(x, np.float32)
+    a = np.abs(x.astype(np.float64))
+    m = np.select([a <= 0.25, a < 0.75, a <= 1.25, a < 1.75, a <= 2.5, a < 3.5, a <= 5.0],
+                  [0, 1, 2, 3, 4, 5, 6], default=7)
+    return (m | np.where(np.signbit(x), 8, 0)).astype(np.uint8)
+
+
+@pytest.mark.parametrize("nthreads", [1, 5])
+def test_encode_array_matches_independent_encoders(orc, nthreads):
+    """The array encoder (the checker behind the device encoder sweeps) splits
+    its input into 65,536-element pieces over threads; on lengths that are not
+    a multiple of that piece, every byte must equal an independent encoder:
+    the E2M1 thresholds for which == 0, PyTorch's float8_e4m3fn conversion
+    (saturated at 448 first) for which == 1."""
+    rng = np.random.default_rng(11)
+    n = 3 * (1 << 16) + 12345
+    x = np.concatenate([
+        rng.uniform(-7, 7, n // 2).astype(np.float32),
+        (rng.standard_normal(n - n // 2 - 6) * 0.3).astype(np.float32),
+        np.array([0.25, -0.75, 5.0, -0.0, 6.5, 0.0], np.float32)])
+    assert x.size == n and n % (1 << 16) != 0
+    got = orc.encode_array(x, 0, nthreads=nthreads)
+    ref = _threshold_e2m1_vec(x)
+    bad = np.nonzero(got != ref)[0]
+    assert bad.size == 0, [(x[i], got[i], ref[i]) for i in bad[:5]]
+
+    y = np.concatenate([np.exp(rng.uniform(np.log(1e-4), np.log(600.0), n - 5)).astype(np.float32),
+                        np.array([0.0, 448.0, 464.0, 470.0, 1e6], np.float32)])
+    got = orc.encode_array(y, 1, nthreads=nthreads)
+    ref = torch.from_numpy(np.minimum(y, np.float32(448.0))).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    bad = np.nonzero(got != ref)[0]
+    assert bad.size == 0, [(y[i], got[i], ref[i]) for i in bad[:5]]
+    # the tail piece (shorter than 65,536) is encoded too
+    assert got[-1] == 0x7E and got[-5] == 0

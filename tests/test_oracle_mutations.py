@@ -61,6 +61,14 @@ MUTATIONS = [
     ("LoRA scale on the base term", "c->y[m * c->N + n] = acc + c->s * lora;", "c->y[m * c->N + n] = c->s * acc + lora;"),
     ("output rows and columns swapped", "c->y[m * c->N + n] = acc + c->s * lora;",
      "c->y[n * c->M + m] = acc + c->s * lora;"),
+    ("array encoder drops the short last piece", "for_rows((n + c.per - 1) / c.per, nthreads, enc_row, &c);",
+     "for_rows(n / c.per, nthreads, enc_row, &c);"),
+    ("array encoder swaps the two encoders",
+     "c->out[i] = (uint8_t)(c->which == 0 ? orc_e2m1_encode(c->x[i]) : orc_e4m3_encode_nonneg(c->x[i]));",
+     "c->out[i] = (uint8_t)(c->which == 1 ? orc_e2m1_encode(c->x[i]) : orc_e4m3_encode_nonneg(c->x[i]));"),
+    ("array encoder skips the last element of each piece",
+     "int64_t lo = r * c->per, hi = lo + c->per < c->n ? lo + c->per : c->n;",
+     "int64_t lo = r * c->per, hi = lo + c->per - 1 < c->n ? lo + c->per - 1 : c->n;"),
 ]
 
 PINS = [
@@ -70,6 +78,7 @@ PINS = [
     codecs.test_e4m3_decode_all_bytes_vs_torch,
     codecs.test_e4m3_encoder_vs_torch_in_range,
     codecs.test_e4m3_encoder_saturates,
+    lambda o: codecs.test_encode_array_matches_independent_encoders(o, 5),
     quant.test_worked_example,
     lambda o: quant.test_grid_round_trip(o, False),
     lambda o: quant.test_grid_round_trip(o, True),
