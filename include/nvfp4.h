@@ -31,7 +31,11 @@
  *     the workspace, read with nvfp4_get_device_status().  Outputs of a call
  *     that recorded such a status are unspecified.
  *   - A workspace must be zero-filled once before its first use (e.g. with
- *     cudaMemsetAsync); every call leaves its counters at zero again.  One
+ *     cudaMemsetAsync); every call that completes normally leaves its
+ *     counters at zero again.  After a call whose device wait gave up
+ *     (NVFP4_ERR_TIMEOUT), its counters and flags may be left mid-way: call
+ *     nvfp4_get_device_status() on that workspace, which returns the timeout
+ *     and sets them back to zero, before the workspace is used again.  One
  *     workspace serves one call at a time: calls that share a workspace must
  *     be ordered on one stream.
  *
@@ -91,8 +95,13 @@ nvfp4_status nvfp4_quantize(const void *w_bf16, int64_t N, int64_t K,
                             int use_given_tensor_scale, void *workspace, size_t ws_bytes,
                             void *stream);
 
-/* Dequantise: out[n][k] = fl32(fl32(v(q) * dec(e_b)) * s_t) (the inner
- * product is exact), written as FP32 or rounded to bf16 (RNE). */
+/* Dequantise ("Scale-QLoRA", rit.work, format paragraph: a weight is its
+ * E2M1 code times the shared scale of its block; here times the FP32 tensor
+ * scale as well): out[n][k] = fl32(fl32(v(q) * dec(e_b)) * s_t) (the inner
+ * product is exact), written as FP32 or rounded to bf16 (RNE).
+ * Inputs: codes (N x K/2 bytes), scales_e4m3 (N x K/16 bytes), tensor_scale
+ * (1 float, device).  out: N x K floats or bf16 values.  No workspace; nothing
+ * is recorded on the device. */
 nvfp4_status nvfp4_dequantize(const uint8_t *codes, const uint8_t *scales_e4m3,
                               const float *tensor_scale, int64_t N, int64_t K,
                               void *out, nvfp4_dtype out_dtype, void *stream);
@@ -102,9 +111,12 @@ nvfp4_status nvfp4_dequantize(const uint8_t *codes, const uint8_t *scales_e4m3,
  *   lora_a_bf16: r x K, lora_b_bf16: N x r (both NULL or r == 0: no LoRA);
  *   y: M x N, FP32 or bf16 (RNE of the FP32 result).
  * Accumulation is FP32.  M < 64 takes a weight-streaming decode path (per
- * 16 tokens: an activation-preparation kernel, then the GEMM kernel, chained
- * by programmatic dependent launch); M >= 64 takes the tensor-core (tcgen05) prefill
- * kernel, whose workspace holds an f16 copy of v(q) dec(e) (2 N K bytes);
+ * 16 tokens: an activation-preparation kernel, then the GEMM kernel, both
+ * launched with programmatic dependent launch; the preparation kernel asks
+ * L2 for the GEMM's first weights while the previous work on the stream is
+ * still running, and the GEMM streams its weights while the preparation
+ * finishes); M >= 64 takes the tensor-core (tcgen05) prefill kernel, whose
+ * workspace holds an f16 copy of v(q) dec(e) (2 N K bytes);
  * nvfp4_gemm_kernel() says which.
  * workspace: nvfp4_workspace_bytes(M, N, K, r) bytes. */
 nvfp4_status nvfp4_w4a16_lora_gemm(const void *x_bf16, int64_t M, int64_t N, int64_t K,
@@ -144,10 +156,13 @@ const char *nvfp4_gemm_kernel(int64_t M, int64_t N, int64_t K, int64_t r);
 /* Diagnostics (no counterpart on the pages): make one of the library's
  * bounded device-side waits run out on purpose -- which == 0: an mbarrier
  * wait that no arrival completes; which == 1: a grid barrier expecting one
- * block more than are launched.  The wait gives up after about two seconds
- * and records NVFP4_ERR_TIMEOUT in the workspace status word (read it with
- * nvfp4_get_device_status); the context stays usable.  workspace: >= 256
- * bytes, zero-filled. */
+ * block more than are launched; which == 2: an mbarrier wait in a kernel
+ * that has already counted arrivals at four output tiles, as a decode GEMM
+ * block does, so its tile counters are left non-zero.  The wait gives up
+ * after about two seconds and records NVFP4_ERR_TIMEOUT in the workspace
+ * status word; nvfp4_get_device_status reports it and sets the counters back
+ * to zero.  The context stays usable.  workspace: zero-filled, >= 256 bytes
+ * for which 0 and 1, >= nvfp4_workspace_bytes(1, 128, 256, 0) for which 2. */
 nvfp4_status nvfp4_wait_selftest(void *workspace, int which, void *stream);
 
 /* nvfp4_w4a16_lora_gemm without a workspace argument, for callers that
@@ -163,12 +178,14 @@ nvfp4_status nvfp4_wait_selftest(void *workspace, int which, void *stream);
  *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
  *     The caller still passes inputs and outputs as for the workspace variant.
  *   - The first call on a device looks up the array's device address (once per
- *     device, with that device current) and caches it; make that first call
- *     before any stream capture.
- *   - All calls share the one array.  Each call clears its control words
- *     (an asynchronous memset on `stream`) before launching; two calls whose
- *     executions overlap on the GPU (different streams, no ordering) race on
- *     the array and give wrong results.
+ *     device and driver context, with that device current) and caches it;
+ *     make that first call before any stream capture.  After a device reset
+ *     the next call looks the address up again.
+ *   - Every host check of nvfp4_w4a16_lora_gemm (and the size limit) runs
+ *     before anything is queued.  Then the call clears the array's control
+ *     words (an asynchronous memset on `stream`) and launches; all calls share
+ *     the one array, so two calls whose executions overlap on the GPU
+ *     (different streams, no ordering) race on it and give wrong results.
  *   - The device status word lives in the shared array and is cleared by the
  *     next call; this variant does not report device-side statuses. */
 nvfp4_status nvfp4_w4a16_lora_gemm_static(const void *x_bf16, int64_t M, int64_t N, int64_t K,

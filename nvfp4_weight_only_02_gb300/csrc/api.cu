@@ -42,7 +42,68 @@ const DeviceInfo *device_info(nvfp4_status *st)
     return &di;
 }
 
-static bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+// Every host-side check of a GEMM call, in one place so that the entry points
+// built on the GEMM (the Scale-QLoRA forward, the fixed-scratch variant) run
+// all of them before they launch anything.  Fills *a and *dev on success.
+nvfp4_status gemm_host_checks(const void *x_bf16, int64_t M, int64_t N, int64_t K, const uint8_t *codes,
+                              const uint8_t *scales_e4m3, const float *tensor_scale, const void *lora_a_bf16,
+                              const void *lora_b_bf16, int64_t r, float lora_scale, const float *noise_fp32,
+                              void *y, nvfp4_dtype y_dtype, void *workspace, size_t ws_bytes, GemmArgs *a,
+                              const DeviceInfo **devp)
+{
+    if (!x_bf16 || !codes || !scales_e4m3 || !tensor_scale || !y || !workspace)
+        return NVFP4_ERR_INVALID_ARG;
+    if (y_dtype != NVFP4_OUT_BF16 && y_dtype != NVFP4_OUT_FP32)
+        return NVFP4_ERR_INVALID_ARG;
+    if (M < 1 || N < 1 || K < 16 || K % 16 != 0 || r < 0 || r > 256 || N > (1LL << 30) ||
+        K > (1LL << 30) || M > (1LL << 31))
+        return NVFP4_ERR_SHAPE;
+    const bool lora = r > 0 && lora_a_bf16 && lora_b_bf16;
+    if (r > 0 && (!lora_a_bf16) != (!lora_b_bf16))
+        return NVFP4_ERR_INVALID_ARG;
+    if (!aligned16(x_bf16) || !aligned16(codes) || !aligned16(scales_e4m3) || !aligned16(tensor_scale) ||
+        !aligned16(y) || !aligned16(workspace) || (noise_fp32 && !aligned16(noise_fp32)) ||
+        (lora && (!aligned16(lora_a_bf16) || !aligned16(lora_b_bf16))))
+        return NVFP4_ERR_ALIGNMENT;
+    nvfp4_status st;
+    const DeviceInfo *dev = device_info(&st);
+    if (!dev)
+        return st;
+    const size_t need = gemm_workspace_bytes(M, N, K, lora ? r : 0, *dev);
+    if (need == 0)
+        return NVFP4_ERR_UNSUPPORTED_DEVICE;
+    if (ws_bytes < need)
+        return NVFP4_ERR_WORKSPACE;
+    a->x = (const uint16_t *)x_bf16;
+    a->M = M;
+    a->N = N;
+    a->K = K;
+    a->r = lora ? r : 0;
+    a->codes = codes;
+    a->scales = scales_e4m3;
+    a->tensor_scale = tensor_scale;
+    a->lora_a = lora ? (const uint16_t *)lora_a_bf16 : nullptr;
+    a->lora_b = lora ? (const uint16_t *)lora_b_bf16 : nullptr;
+    a->lora_scale = lora ? lora_scale : 0.0f;
+    a->noise = noise_fp32;
+    a->y = y;
+    a->y_fp32 = y_dtype == NVFP4_OUT_FP32;
+    a->ws = (uint8_t *)workspace;
+    a->ws_bytes = ws_bytes;
+    *devp = dev;
+    return NVFP4_OK;
+}
+
+cudaError_t launch_gemm(const GemmArgs &a, cudaStream_t s, const DeviceInfo &dev)
+{
+    if (prefill_supported(a.M, a.N, a.K, a.r))
+        return launch_prefill_gemm(a, s, dev);
+    if (stream_supported(a.N, a.K, a.r, dev))
+        return launch_stream_gemm(a, s, dev);
+    return launch_decode_gemm(a, s, dev);
+}
 
 }  // namespace nvfp4
 
@@ -114,48 +175,14 @@ nvfp4_status nvfp4_w4a16_lora_gemm(const void *x_bf16, int64_t M, int64_t N, int
                                    const float *noise_fp32, void *y, nvfp4_dtype y_dtype,
                                    void *workspace, size_t ws_bytes, void *stream)
 {
-    if (!x_bf16 || !codes || !scales_e4m3 || !tensor_scale || !y || !workspace)
-        return NVFP4_ERR_INVALID_ARG;
-    if (y_dtype != NVFP4_OUT_BF16 && y_dtype != NVFP4_OUT_FP32)
-        return NVFP4_ERR_INVALID_ARG;
-    if (M < 1 || N < 1 || K < 16 || K % 16 != 0 || r < 0 || r > 256 || N > (1LL << 30) ||
-        K > (1LL << 30) || M > (1LL << 31) / 1)
-        return NVFP4_ERR_SHAPE;
-    const bool lora = r > 0 && lora_a_bf16 && lora_b_bf16;
-    if (r > 0 && (!lora_a_bf16) != (!lora_b_bf16))
-        return NVFP4_ERR_INVALID_ARG;
-    if (!aligned16(x_bf16) || !aligned16(codes) || !aligned16(scales_e4m3) || !aligned16(tensor_scale) ||
-        !aligned16(y) || !aligned16(workspace) || (noise_fp32 && !aligned16(noise_fp32)) ||
-        (lora && (!aligned16(lora_a_bf16) || !aligned16(lora_b_bf16))))
-        return NVFP4_ERR_ALIGNMENT;
-    NVFP4_TRY_DEVICE(dev);
-    const size_t need = gemm_workspace_bytes(M, N, K, lora ? r : 0, *dev);
-    if (need == 0)
-        return NVFP4_ERR_UNSUPPORTED_DEVICE;
-    if (ws_bytes < need)
-        return NVFP4_ERR_WORKSPACE;
     GemmArgs a;
-    a.x = (const uint16_t *)x_bf16;
-    a.M = M;
-    a.N = N;
-    a.K = K;
-    a.r = lora ? r : 0;
-    a.codes = codes;
-    a.scales = scales_e4m3;
-    a.tensor_scale = tensor_scale;
-    a.lora_a = lora ? (const uint16_t *)lora_a_bf16 : nullptr;
-    a.lora_b = lora ? (const uint16_t *)lora_b_bf16 : nullptr;
-    a.lora_scale = lora ? lora_scale : 0.0f;
-    a.noise = noise_fp32;
-    a.y = y;
-    a.y_fp32 = y_dtype == NVFP4_OUT_FP32;
-    a.ws = (uint8_t *)workspace;
-    a.ws_bytes = ws_bytes;
-    if (prefill_supported(M, N, K, a.r))
-        return from_cuda(launch_prefill_gemm(a, (cudaStream_t)stream, *dev));
-    if (stream_supported(N, K, a.r, *dev))
-        return from_cuda(launch_stream_gemm(a, (cudaStream_t)stream, *dev));
-    return from_cuda(launch_decode_gemm(a, (cudaStream_t)stream, *dev));
+    const DeviceInfo *dev = nullptr;
+    const nvfp4_status st = gemm_host_checks(x_bf16, M, N, K, codes, scales_e4m3, tensor_scale, lora_a_bf16,
+                                             lora_b_bf16, r, lora_scale, noise_fp32, y, y_dtype, workspace,
+                                             ws_bytes, &a, &dev);
+    if (st != NVFP4_OK)
+        return st;
+    return from_cuda(launch_gemm(a, (cudaStream_t)stream, *dev));
 }
 
 const char *nvfp4_gemm_kernel(int64_t M, int64_t N, int64_t K, int64_t r)
@@ -198,23 +225,22 @@ nvfp4_status nvfp4_scale_qlora_gemm(const void *x_bf16, int64_t M, int64_t N, in
                                     void *workspace, size_t ws_bytes, void *stream)
 {
     // every host check of both steps before anything is launched
-    if (!x_bf16 || !codes || !scale_param || !tensor_scale || !scales_e4m3 || !y || !workspace)
+    if (!scale_param)
         return NVFP4_ERR_INVALID_ARG;
-    if (M < 1 || N < 1 || K < 16 || K % 16 != 0 || r < 0 || r > 256 || N > (1LL << 30) || K > (1LL << 30))
-        return NVFP4_ERR_SHAPE;
-    if (!aligned16(scale_param) || !aligned16(scales_e4m3))
+    if (!aligned16(scale_param))
         return NVFP4_ERR_ALIGNMENT;
-    const size_t need = nvfp4_workspace_bytes(M, N, K, (lora_a_bf16 && lora_b_bf16) ? r : 0);
-    if (need == 0)
-        return NVFP4_ERR_UNSUPPORTED_DEVICE;
-    if (ws_bytes < need)
-        return NVFP4_ERR_WORKSPACE;
-    nvfp4_status st = nvfp4_round_scales(scale_param, tensor_scale, N, K, scales_e4m3, workspace, ws_bytes,
-                                         stream);
+    GemmArgs a;
+    const DeviceInfo *dev = nullptr;
+    nvfp4_status st = gemm_host_checks(x_bf16, M, N, K, codes, scales_e4m3, tensor_scale, lora_a_bf16, lora_b_bf16,
+                                       r, lora_scale, noise_fp32, y, y_dtype, workspace, ws_bytes, &a, &dev);
     if (st != NVFP4_OK)
         return st;
-    return nvfp4_w4a16_lora_gemm(x_bf16, M, N, K, codes, scales_e4m3, tensor_scale, lora_a_bf16, lora_b_bf16, r,
-                                 lora_scale, noise_fp32, y, y_dtype, workspace, ws_bytes, stream);
+    cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e = launch_round_scales(scale_param, tensor_scale, N * (K / 16), scales_e4m3,
+                                        (uint32_t *)workspace, s, *dev);
+    if (e != cudaSuccess)
+        return NVFP4_ERR_CUDA;
+    return from_cuda(launch_gemm(a, s, *dev));
 }
 
 nvfp4_status nvfp4_get_device_status(void *workspace, void *stream)
@@ -222,11 +248,22 @@ nvfp4_status nvfp4_get_device_status(void *workspace, void *stream)
     if (!workspace)
         return NVFP4_ERR_INVALID_ARG;
     cudaStream_t s = (cudaStream_t)stream;
-    uint32_t word = 0;
-    if (cudaMemcpyAsync(&word, workspace, 4, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
-        cudaMemsetAsync(workspace, 0, 4, s) != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess)
+    uint32_t w[CTL_WORDS_USED] = {};
+    if (cudaMemcpyAsync(w, workspace, sizeof(w), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
         return NVFP4_ERR_CUDA;
-    return (nvfp4_status)word;
+    uint8_t *ws = (uint8_t *)workspace;
+    if (w[CTL_STATUS] == NVFP4_ERR_TIMEOUT) {
+        // a wait gave up: counters, barriers and flags may be mid-way; start them over
+        if (cudaMemsetAsync(ws + 4, 0, (CTL_WORDS_USED - 1) * 4, s) != cudaSuccess)
+            return NVFP4_ERR_CUDA;
+        if (w[CTL_DIRTY] == kTilesDirty &&
+            cudaMemsetAsync(ws + kCtlBytes, 0, 4 * (size_t)kTileCounters, s) != cudaSuccess)
+            return NVFP4_ERR_CUDA;
+    }
+    if (cudaMemsetAsync(ws, 0, 4, s) != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess)
+        return NVFP4_ERR_CUDA;
+    return (nvfp4_status)w[CTL_STATUS];
 }
 
 const char *nvfp4_status_string(nvfp4_status s)

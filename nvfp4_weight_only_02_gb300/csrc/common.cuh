@@ -25,9 +25,17 @@ enum CtlWord : int {
     CTL_AMAX_COUNT = 2,   // blocks of the amax kernel that have finished
     CTL_BAR_COUNT = 3,    // grid barrier: arrivals
     CTL_BAR_GEN = 4,      // grid barrier: generation
-    CTL_RS_COUNT = 5,     // reserved
+    CTL_DIRTY = 5,        // kTilesDirty: a wait gave up while tile counters were in use
+    CTL_XFLAG = 6,        // decode: activation records of the current call are ready
+    CTL_XCNT = 7,         // decode: preparation blocks that have written their record
+    CTL_TFLAG = 8,        // decode: the LoRA down-projection of the current call is ready
+    CTL_TCNT = 9,         // decode: preparation blocks that have written their LoRA partial
+    CTL_WFLAG = 10,       // decode: the preparation kernel has passed its dependency wait
+    CTL_TREAD = 11,       // decode: GEMM blocks that have fetched the LoRA down-projection
+    CTL_WORDS_USED = 12,
 };
 constexpr size_t kCtlBytes = 256;
+constexpr uint32_t kTilesDirty = 0x7D17u;
 // After the control block: arrival counters at a fixed place, so that calls
 // of any shape find them at zero (every kernel that counts resets its
 // counters before it returns).  Per-call scratch starts after them.
@@ -43,6 +51,15 @@ constexpr uint32_t kSpinLimit = 1u << 24;
 __device__ __forceinline__ void record_status(uint32_t *ctl, nvfp4_status s)
 {
     atomicCAS(&ctl[CTL_STATUS], 0u, (uint32_t)s);
+}
+
+// A bounded wait gave up in a kernel that counts arrivals per output tile:
+// the counters may be left non-zero, so besides the status the workspace is
+// marked, and nvfp4_get_device_status clears them when it reports the timeout.
+__device__ __forceinline__ void record_timeout_tiles(uint32_t *ctl)
+{
+    record_status(ctl, NVFP4_ERR_TIMEOUT);
+    atomicExch(&ctl[CTL_DIRTY], kTilesDirty);
 }
 
 // ---------------------------------------------------------------- scalars

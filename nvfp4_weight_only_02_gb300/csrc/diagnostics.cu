@@ -21,6 +21,24 @@ __global__ void wait_mbarrier_kernel(uint32_t *ctl)
         record_status(ctl, NVFP4_ERR_TIMEOUT);
 }
 
+// A kernel that has counted arrivals at a few output tiles (as a decode GEMM
+// block does before its last-arriver test) and then gives up on a wait: it
+// leaves the counters non-zero and marks the workspace.
+__global__ void wait_tiles_kernel(uint32_t *ctl)
+{
+    __shared__ uint64_t bar;
+    uint32_t *tcnt = ctl + kCtlBytes / 4;
+    if (threadIdx.x < 4)
+        atomicAdd(&tcnt[threadIdx.x * 7], 1u);
+    if (threadIdx.x == 0) {
+        sm100::mbar_init(&bar, 1);
+        sm100::mbar_fence_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && !sm100::mbar_wait(&bar, 0))
+        record_timeout_tiles(ctl);
+}
+
 // A grid barrier told to expect one block more than were launched.
 __global__ void wait_grid_kernel(uint32_t *ctl, uint32_t expected)
 {
@@ -31,6 +49,10 @@ cudaError_t launch_wait_selftest(uint32_t *ctl, int which, cudaStream_t s)
 {
     if (which == 0) {
         wait_mbarrier_kernel<<<1, 32, 0, s>>>(ctl);
+        return cudaGetLastError();
+    }
+    if (which == 2) {
+        wait_tiles_kernel<<<1, 32, 0, s>>>(ctl);
         return cudaGetLastError();
     }
     uint32_t *c = ctl;
@@ -47,7 +69,7 @@ cudaError_t launch_wait_selftest(uint32_t *ctl, int which, cudaStream_t s)
 
 extern "C" nvfp4_status nvfp4_wait_selftest(void *workspace, int which, void *stream)
 {
-    if (!workspace || (which != 0 && which != 1))
+    if (!workspace || which < 0 || which > 2)
         return NVFP4_ERR_INVALID_ARG;
     nvfp4_status st;
     if (!nvfp4::device_info(&st))

@@ -39,6 +39,7 @@
 //      over its slices in fixed order).  Results do not depend on arrival
 //      order.
 #include <algorithm>
+#include <cudaTypedefs.h>
 #include <mutex>
 #include <unordered_map>
 
@@ -950,12 +951,39 @@ namespace nvfp4 {
 constexpr size_t kStaticWsBytes = size_t(8) << 20;
 static __device__ __align__(256) uint8_t g_static_ws[kStaticWsBytes];
 
+struct StaticSlot {
+    unsigned long long ctx_id = 0;  // driver context the address belongs to (0: none yet)
+    void *ptr = nullptr;
+};
 static std::mutex g_static_mu;
-static void *g_static_ptr[64];
+static StaticSlot g_static_slot[64];
+static PFN_cuCtxGetCurrent_v4000 g_ctx_current = nullptr;
+static PFN_cuCtxGetId_v12000 g_ctx_id = nullptr;
+
+// Unique id of the current device's driver context (a reset device gets a
+// new context, and the array a new address).
+static cudaError_t current_context_id(unsigned long long *id)
+{
+    if (!g_ctx_current || !g_ctx_id) {
+        void *f1 = nullptr, *f2 = nullptr;
+        cudaDriverEntryPointQueryResult q1, q2;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f1, 4000, cudaEnableDefault, &q1) != cudaSuccess ||
+            cudaGetDriverEntryPointByVersion("cuCtxGetId", &f2, 12000, cudaEnableDefault, &q2) != cudaSuccess ||
+            q1 != cudaDriverEntryPointSuccess || q2 != cudaDriverEntryPointSuccess || !f1 || !f2)
+            return cudaErrorNotSupported;
+        g_ctx_current = (PFN_cuCtxGetCurrent_v4000)f1;
+        g_ctx_id = (PFN_cuCtxGetId_v12000)f2;
+    }
+    CUcontext c = nullptr;
+    if (g_ctx_current(&c) != CUDA_SUCCESS || !c || g_ctx_id(c, id) != CUDA_SUCCESS)
+        return cudaErrorDeviceUninitialized;
+    return cudaSuccess;
+}
 
 // Device address of g_static_ws on the current device.  In host code the
 // array's name is only a host-side stand-in, so its device address is looked
-// up once per device (with that device current) and cached.
+// up with that device current, once per device and driver context, and
+// cached; a device reset (new context) makes the next call look it up again.
 static cudaError_t static_workspace(void **out)
 {
     int d = -1;
@@ -965,14 +993,20 @@ static cudaError_t static_workspace(void **out)
     if (d < 0 || d >= 64)
         return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lk(g_static_mu);
-    if (!g_static_ptr[d]) {
+    unsigned long long id = 0;
+    e = current_context_id(&id);
+    if (e != cudaSuccess)
+        return e;
+    StaticSlot &slot = g_static_slot[d];
+    if (slot.ctx_id != id || !slot.ptr) {
         void *p = nullptr;
         e = cudaGetSymbolAddress(&p, g_static_ws);
         if (e != cudaSuccess)
             return e;
-        g_static_ptr[d] = p;
+        slot.ptr = p;
+        slot.ctx_id = id;
     }
-    *out = g_static_ptr[d];
+    *out = slot.ptr;
     return cudaSuccess;
 }
 
@@ -987,13 +1021,17 @@ extern "C" nvfp4_status nvfp4_w4a16_lora_gemm_static(
     void *ws = nullptr;
     if (nvfp4::static_workspace(&ws) != cudaSuccess)
         return NVFP4_ERR_CUDA;
-    const size_t need = nvfp4_workspace_bytes(M, N, K, (lora_a_bf16 && lora_b_bf16) ? r : 0);
-    if (need > nvfp4::kStaticWsBytes)
-        return NVFP4_ERR_WORKSPACE;  // beyond the fixed scratch size
+    // every host check (including the fixed size) before anything is queued
+    nvfp4::GemmArgs a;
+    const nvfp4::DeviceInfo *dev = nullptr;
+    const nvfp4_status st = nvfp4::gemm_host_checks(x_bf16, M, N, K, codes, scales_e4m3, tensor_scale, lora_a_bf16,
+                                                    lora_b_bf16, r, lora_scale, noise_fp32, y, y_dtype, ws,
+                                                    nvfp4::kStaticWsBytes, &a, &dev);
+    if (st != NVFP4_OK)
+        return st;
     // every call shares the array: its control words and counters must start at zero
-    if (cudaMemsetAsync(ws, 0, nvfp4::kWsHeaderBytes, (cudaStream_t)stream) != cudaSuccess)
+    cudaStream_t s = (cudaStream_t)stream;
+    if (cudaMemsetAsync(ws, 0, nvfp4::kWsHeaderBytes, s) != cudaSuccess)
         return NVFP4_ERR_CUDA;
-    return nvfp4_w4a16_lora_gemm(x_bf16, M, N, K, codes, scales_e4m3, tensor_scale, lora_a_bf16,
-                                 lora_b_bf16, r, lora_scale, noise_fp32, y, y_dtype, ws,
-                                 nvfp4::kStaticWsBytes, stream);
+    return nvfp4::launch_gemm(a, s, *dev) == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
 }

@@ -77,6 +77,20 @@ cudaError_t encode_tensor_map_2d(CUtensorMap *map, CUtensorMapDataType dt, const
                                  uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
                                  CUtensorMapSwizzle swizzle);
 
+bool aligned16(const void *p);
+
+// All host-side checks of nvfp4_w4a16_lora_gemm's arguments (pointers, enum
+// values, shapes, alignment, device, workspace size); on NVFP4_OK *a and
+// *dev describe the call.  Launches nothing.
+nvfp4_status gemm_host_checks(const void *x_bf16, int64_t M, int64_t N, int64_t K, const uint8_t *codes,
+                              const uint8_t *scales_e4m3, const float *tensor_scale, const void *lora_a_bf16,
+                              const void *lora_b_bf16, int64_t r, float lora_scale, const float *noise_fp32,
+                              void *y, nvfp4_dtype y_dtype, void *workspace, size_t ws_bytes, GemmArgs *a,
+                              const DeviceInfo **dev);
+
+// The kernels of one checked GEMM call (prefill, streaming or register-streaming decode).
+cudaError_t launch_gemm(const GemmArgs &a, cudaStream_t s, const DeviceInfo &dev);
+
 // Workspace of nvfp4_w4a16_lora_gemm for these sizes (0: unsupported).
 inline size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t r, const DeviceInfo &dev)
 {

@@ -72,6 +72,22 @@ def test_host_checks_reject_before_launch(lib):
                                       good, 1, good, 1 << 20, null) == binding.ERR_SHAPE
     assert lib.nvfp4_scale_qlora_gemm(good, 1, 16, 32, good, bad_align, good, good, null, null, 0, 0.0, null,
                                       good, 1, good, 1 << 20, null) == binding.ERR_ALIGNMENT
+    # ... and every host check of the GEMM step too (these run before the
+    # device query, so they fail here on a machine without a GPU)
+    sq = lambda x, y, ydt, a, b, r, z=null: lib.nvfp4_scale_qlora_gemm(
+        x, 1, 16, 32, good, good, good, good, a, b, r, 1.0, z, y, ydt, good, 1 << 20, null)
+    assert sq(bad_align, good, 1, null, null, 0) == binding.ERR_ALIGNMENT        # x misaligned
+    assert sq(good, bad_align, 1, null, null, 0) == binding.ERR_ALIGNMENT        # y misaligned
+    assert sq(good, good, 7, null, null, 0) == binding.ERR_INVALID_ARG           # bad output dtype
+    assert sq(good, good, 1, good, null, 4) == binding.ERR_INVALID_ARG           # half a LoRA pair
+    assert sq(good, good, 1, null, null, 0, bad_align) == binding.ERR_ALIGNMENT  # noise misaligned
+    assert sq(good, good, 1, good, bad_align, 4) == binding.ERR_ALIGNMENT        # LoRA B misaligned
+    assert lib.nvfp4_scale_qlora_gemm(good, 1, 16, 32, bad_align, good, good, good, null, null, 0, 0.0, null,
+                                      good, 1, good, 1 << 20, null) == binding.ERR_ALIGNMENT  # codes
+    # the fixed-scratch variant checks its arguments before it queues anything
+    st = lib.nvfp4_w4a16_lora_gemm_static(good, 1, 16, 32, good, good, good, good, null, 4, 1.0, null, good, 1,
+                                          null)
+    assert st in (binding.ERR_INVALID_ARG, binding.ERR_CUDA)  # ERR_CUDA: no device to look the array up on
     assert lib.nvfp4_workspace_bytes(1, 16, 30, 0) == 0
     assert lib.nvfp4_gemm_kernel(1, 16, 30, 0) is None
     assert lib.nvfp4_encode_debug(good, 8, 5, good, null) == binding.ERR_INVALID_ARG

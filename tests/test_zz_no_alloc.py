@@ -7,7 +7,8 @@ library offers nvfp4_w4a16_lora_gemm_static, which uses an 8 MiB scratch array
 built into the library instead of a caller workspace.  This test calls it
 through the C ABI twice in a row (the array keeps the previous call's
 contents) and compares each result with the workspace entry point, within the
-tolerance the other GEMM tests use.  The file is named so that pytest
+tolerance the other GEMM tests use; the device's free memory must not change
+across those two calls.  The file is named so that pytest
 collects it last.
 """
 import ctypes
@@ -45,10 +46,14 @@ def _close(y, ref):
     assert err.sum().item() <= MEAN_REL * ref.abs().sum().item()
 
 
-@pytest.mark.parametrize("case", ["small", "7b_up_M8", "7b_down_M16"])
+@pytest.mark.parametrize("case", ["small", "registers_K1040", "7b_up_M8", "7b_down_M16"])
 def test_static_scratch_matches_workspace_entry_point(nv, case):
     if case == "small":
         c = synth.small_case(5, 300, 1024, 8, seed=3)
+    elif case == "registers_K1040":
+        # K % 256 != 0: the register-streaming decode kernel on the fixed scratch
+        c = synth.small_case(8, 300, 1040, 16, seed=4)
+        assert nv.gemm_kernel(8, 300, 1040, 16) == "decode_registers"
     elif case == "7b_up_M8":
         c = synth.qwen7b_case("up", 8, seed=5)
     else:
@@ -57,11 +62,30 @@ def test_static_scratch_matches_workspace_entry_point(nv, case):
     x, a, b = _dev(c.x), _dev(c.a), _dev(c.b)
     z = torch.from_numpy(c.z).cuda()
     ref = nv.gemm(x, q, a, b, c.lora_scale, z)
-    for _ in range(2):
-        y = torch.full(ref.shape, float("nan"), dtype=torch.float32, device="cuda")
+    ys = [torch.full(ref.shape, float("nan"), dtype=torch.float32, device="cuda") for _ in range(3)]
+    # a first call loads the library's device code and looks up the array
+    assert _static_gemm(nv, x, q, a, b, c.lora_scale, z, ys.pop()) == nv.OK
+    torch.cuda.synchronize()
+    free_before, _ = torch.cuda.mem_get_info()
+    for y in ys:
         assert _static_gemm(nv, x, q, a, b, c.lora_scale, z, y) == nv.OK
-        torch.cuda.synchronize()
+    torch.cuda.synchronize()
+    free_after, _ = torch.cuda.mem_get_info()
+    for y in ys:
         _close(y, ref)
+    # the calls took no device memory (the device's free bytes are unchanged)
+    assert free_after == free_before
+
+
+def test_static_scratch_covers_qwen_projections(nv):
+    """Every Qwen2.5-7B and -32B projection at up to 16 tokens, LoRA rank 32 or
+    64, fits the fixed 8 MiB scratch."""
+    shapes = list(synth.QWEN7B_LAYER.values()) + [synth.QWEN32B_UP, synth.QWEN32B_DOWN, (5120, 5120),
+                                                  (1024, 5120)]
+    for N, K in shapes:
+        for M in (1, 8, 16):
+            for r in (32, 64):
+                assert 0 < nv.nvfp4_workspace_bytes(M, N, K, r) <= (8 << 20), (N, K, M, r)
 
 
 def test_static_scratch_rejects_oversized_problems(nv):
