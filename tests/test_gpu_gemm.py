@@ -78,6 +78,12 @@ CASES = [
     # more units than SMs: block ranges of one or two units that cross tile ends
     (6, 2000, 5632, 32, True, True),
     (8, 2000, 5376, 40, True, True),
+    # LoRA ranks that are not multiples of 8 on the streaming kernel (K % 256 == 0)
+    (8, 700, 2048, 1, True, True),
+    (4, 300, 1536, 5, True, True),
+    (16, 256, 2560, 12, True, True),
+    (3, 1100, 1024, 20, True, True),
+    (8, 513, 3072, 33, True, True),
 ]
 
 
@@ -91,6 +97,13 @@ def test_small_and_ragged(nv, orc, M, N, K, r, lora, noise):
     # bf16 output is the RNE rounding of the same FP32 result
     yb = _run_gpu(nv, c, q, torch.bfloat16)
     assert torch.equal(yb.cpu(), torch.from_numpy(y).to(torch.bfloat16))
+
+
+def test_streaming_kernel_takes_ragged_lora_ranks(nv):
+    """The odd-rank cases above really run the streaming kernel."""
+    for M, N, K, r in ((8, 700, 2048, 1), (4, 300, 1536, 5), (16, 256, 2560, 12), (3, 1100, 1024, 20),
+                       (8, 513, 3072, 33)):
+        assert nv.gemm_kernel(M, N, K, r) == "decode_stream"
 
 
 def test_kernel_selection(nv):
@@ -181,7 +194,8 @@ def _full_case(which, model, M):
 
 
 @pytest.mark.parametrize("model,which,M", [("7b", "up", 1), ("7b", "up", 16), ("7b", "down", 4),
-                                           ("7b", "down", 8), ("32b", "up", 8), ("32b", "down", 1)])
+                                           ("7b", "down", 8), ("32b", "up", 1), ("32b", "up", 8),
+                                           ("32b", "down", 1), ("32b", "down", 8)])
 def test_full_size_decode(nv, orc, model, which, M):
     c = _full_case(which, model, M)
     q, codes, scales, st = _quantize_both(nv, orc, c.w)

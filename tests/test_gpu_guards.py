@@ -66,6 +66,8 @@ GEMM_CASES = [
     (1, 3, 256, 0), (7, 200, 1280, 16), (16, 129, 768, 8), (12, 640, 4096, 64), (6, 2000, 5632, 32),
     (3, 17, 48, 4), (8, 300, 1040, 16), (16, 513, 2064, 8),
     (64, 256, 64, 0), (200, 300, 1024, 32), (1000, 129, 640, 64),
+    # LoRA ranks that are not multiples of 8 on the streaming kernel
+    (8, 700, 2048, 1), (4, 300, 1536, 5), (16, 256, 2560, 12), (3, 1100, 1024, 20), (8, 513, 3072, 33),
 ]
 
 

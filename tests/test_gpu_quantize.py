@@ -163,11 +163,12 @@ def test_dequantize_bit_exact(nv, orc, N, K):
     assert np.array_equal(b16, rb)
 
 
-def test_round_scales_and_scale_only_merge(nv, orc):
-    """Scale-QLoRA on 32B-shaped weights: codes untouched by the update,
-    rounded scales bit-identical to the CPU definition, merged weights equal
-    to the training-time fake-quantised weights."""
-    bits = synth.student_t_weight(synth.QWEN32B_UP, 0.02, 4.0, seed=31)
+@pytest.mark.parametrize("shape", [synth.QWEN32B_UP, synth.QWEN32B_DOWN])
+def test_round_scales_and_scale_only_merge(nv, orc, shape):
+    """Scale-QLoRA on 32B-shaped weights (both projections): codes untouched
+    by the update, rounded scales bit-identical to the CPU definition, merged
+    weights equal to the training-time fake-quantised weights."""
+    bits = synth.student_t_weight(shape, 0.02, 4.0, seed=31 if shape == synth.QWEN32B_UP else 33)
     q = _quant_gpu(nv, bits)
     codes_before = q.codes.clone()
     st = q.tensor_scale
