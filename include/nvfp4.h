@@ -111,13 +111,10 @@ nvfp4_status nvfp4_dequantize(const uint8_t *codes, const uint8_t *scales_e4m3,
  *   lora_a_bf16: r x K, lora_b_bf16: N x r (both NULL or r == 0: no LoRA);
  *   y: M x N, FP32 or bf16 (RNE of the FP32 result).
  * Accumulation is FP32.  M < 64 takes a weight-streaming decode path (per
- * 16 tokens: an activation-preparation kernel, then the GEMM kernel, both
- * launched with programmatic dependent launch; the preparation kernel asks
- * L2 for the GEMM's first weights while the previous work on the stream is
- * still running, and the GEMM streams its weights while the preparation
- * finishes); M >= 64 takes the tensor-core (tcgen05) prefill kernel, whose
- * workspace holds an f16 copy of v(q) dec(e) (2 N K bytes);
- * nvfp4_gemm_kernel() says which.
+ * 16 tokens: an activation-preparation kernel, then the GEMM kernel, chained
+ * by programmatic dependent launch); M >= 64 takes the tensor-core (tcgen05)
+ * prefill kernel, whose workspace holds an f16 copy of v(q) dec(e) (2 N K
+ * bytes); nvfp4_gemm_kernel() says which.
  * workspace: nvfp4_workspace_bytes(M, N, K, r) bytes. */
 nvfp4_status nvfp4_w4a16_lora_gemm(const void *x_bf16, int64_t M, int64_t N, int64_t K,
                                    const uint8_t *codes, const uint8_t *scales_e4m3,

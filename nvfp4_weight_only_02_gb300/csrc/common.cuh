@@ -26,13 +26,7 @@ enum CtlWord : int {
     CTL_BAR_COUNT = 3,    // grid barrier: arrivals
     CTL_BAR_GEN = 4,      // grid barrier: generation
     CTL_DIRTY = 5,        // kTilesDirty: a wait gave up while tile counters were in use
-    CTL_XFLAG = 6,        // decode: activation records of the current call are ready
-    CTL_XCNT = 7,         // decode: preparation blocks that have written their record
-    CTL_TFLAG = 8,        // decode: the LoRA down-projection of the current call is ready
-    CTL_TCNT = 9,         // decode: preparation blocks that have written their LoRA partial
-    CTL_WFLAG = 10,       // decode: the preparation kernel has passed its dependency wait
-    CTL_TREAD = 11,       // decode: GEMM blocks that have fetched the LoRA down-projection
-    CTL_WORDS_USED = 12,
+    CTL_WORDS_USED = 6,
 };
 constexpr size_t kCtlBytes = 256;
 constexpr uint32_t kTilesDirty = 0x7D17u;

@@ -1,8 +1,8 @@
 // gemm_stream.cu -- the decode GEMM (M <= 16 tokens per launch, LoRA rank
 // r <= 64) for weights whose rows are 16-byte aligned in both arrays
-// (K % 256 == 0; every Qwen2.5 projection): a small preparation kernel and
-// a kernel that streams the weight bytes through a shared-memory ring with
-// TMA, overlapped with each other and with the previous call.
+// (K % 256 == 0; every Qwen2.5 projection): a small activation-preparation
+// kernel, then a kernel that streams the weight bytes through a
+// shared-memory ring with TMA.
 //
 //   X' = bf16(X * z),   Y = s_t * X' deq(W)^T + s * (X' A^T) B^T
 // ("RL with NVFP4 + LoRA" post, tggo.me/sberlogasci/42740, section "Метод";
@@ -11,32 +11,24 @@
 // Two kernels per group of up to 16 tokens, chained by programmatic
 // dependent launch (PDL):
 //
-//  * prep (one 4-warp block per SM; blocks c < C also own 512-column chunk
-//    c).  Before its dependency wait -- i.e. while the previous call still
-//    runs -- every block asks L2 to prefetch the first units of the weight
-//    range that the GEMM block of the same index will stream, and the chunk
-//    blocks the chunk's activations, noise and LoRA A rows (a prefetch moves
-//    nothing into the SM, so it cannot observe stale data).  After the wait
-//    block 0 clears the hand-over flags, and every block lets the GEMM
-//    launch.  Chunk block c then forms X' = bf16(X z), re-expressed as f16
-//    times a power of two per token (the chunk max lands in [2^14, 2^15);
-//    every bf16 value of the chunk within 2^28 of that max stays exact),
-//    stored in the order the MMA B fragments are read ("record" of the
-//    chunk), and raises the records flag once all chunks are written.  It
-//    then computes T_c = X'_c A_c^T (bf16 mma.sync); the last chunk block to
-//    finish adds the T_c in chunk order into T and raises the T flag.
-//  * the streaming GEMM starts as soon as the preparation kernel has passed
-//    its wait (everything before it has completed), and lets the next call's
-//    preparation kernel launch at once.  Work is split into units (128-row
-//    tile, 512-column chunk), spread evenly over one block per SM (stream-K;
-//    one whole tile per block when there are about as many tiles as SMs).
-//    A block has 16 consumer warps and one producer warp.  The producer
-//    streams each unit's codes (two 128 x 128-byte boxes, 128B swizzle),
-//    block scales (128 x 32 bytes) and -- once the records flag is up -- the
-//    chunk's record into a ring of stages, all completing on the stage's
-//    mbarrier; it fetches T into shared memory when the T flag is up.  The
-//    weights need no hand-over: they are inputs of the call, written before
-//    the preparation kernel's wait.
+//  * xprep (one block per 512-column chunk c): X' = bf16(X z), re-expressed
+//    as f16 times a power of two per token (the chunk max lands in
+//    [2^14, 2^15); every bf16 value of the chunk within 2^28 of that max
+//    stays exact), stored in the order the MMA B fragments are read, and
+//    the chunk's LoRA down-projection T_c = X'_c A_c^T (bf16 mma.sync).
+//    Both go into one contiguous record per chunk: [2^p per token | T_c |
+//    X' rows], so the GEMM fetches a unit's activations with one bulk copy
+//    (each TMA or bulk copy costs a producer thread about 50 ns to issue,
+//    whatever its size).
+//  * the streaming GEMM: work is split into units (128-row tile, 512-column
+//    chunk), spread evenly over one block per SM (stream-K; one whole tile
+//    per block when there are about as many tiles as SMs).  A block has 16
+//    consumer warps and one producer warp.  Before the wait for xprep the
+//    producer asks L2 to prefetch the first weight boxes of its range (a
+//    prefetch moves nothing into the SM, so it cannot observe stale data).
+//    It then streams each unit's codes (two 128 x 128-byte boxes, 128B
+//    swizzle), block scales (128 x 32 bytes) and the chunk's record into a
+//    ring of stages, all completing on the stage's mbarrier.
 //  * Consumer warp (row group mt, half h) owns 16 rows and 256 columns of a
 //    stage: lane t of a quad holds 64 consecutive columns (two 16-byte loads
 //    per row and one scale word), converts codes with cvt.e2m1x2 -> f16x2
@@ -44,15 +36,14 @@
 //    6 significant bits) and issues mma.sync m16n8k16 (f16, FP32 accumulate)
 //    with the tokens as N; the MMA k index is permuted so these
 //    lane-contiguous columns meet the matching X' fragments.  Each unit's
-//    sums are scaled back by the chunk's power of two.
+//    sums are scaled back by the chunk's power of two; half-1 warps also add
+//    up T over the block's chunks of the tile, in shared memory.
 //  * At the end of a tile segment the halves' sums are added in shared
-//    memory.  A block that holds the whole tile stores s_t * acc + s * T B^T
-//    (LoRA-up as bf16 MMAs against T split into hi + lo bf16 parts); a block
-//    that holds part of it leaves s_t * acc in the workspace, and the last
-//    block to arrive adds the shares in block order (results do not depend
-//    on arrival order) and applies the LoRA term.
-// Every wait is bounded (about two seconds), after which the kernel records
-// NVFP4_ERR_TIMEOUT and winds down.
+//    memory, and the block's share of the output, s_t * acc + s * T_R B^T
+//    (LoRA-up as bf16 MMAs against T_R split into hi + lo bf16 parts), is
+//    either stored (the block holds the whole tile) or left in the workspace
+//    for the last block to arrive, which adds the shares in block order
+//    (results do not depend on arrival order).
 #include <algorithm>
 #include <mutex>
 #include <unordered_map>
@@ -72,69 +63,58 @@ constexpr int kBoxBytes = 128 * kRows;   // one code box: 128 rows x 128 bytes (
 constexpr int kScaleBox = 32 * kRows;    // scale box: 128 rows x 32 bytes
 constexpr int kCWarps = 16;              // consumer warps: 8 row groups x 2 column halves
 constexpr int kProducer = kCWarps;       // warp index of the producer
-constexpr int kTail = kCWarps + 1;       // warp that fetches T and waits for the preparation grid
-constexpr int kThreads = (kCWarps + 2) * 32;
-constexpr int kPrepWarps = 4;
-constexpr int kPrepThreads = kPrepWarps * 32;
+// three idle warps keep the register split even across the SM's four schedulers
+constexpr int kThreads = (kCWarps + 4) * 32;
+constexpr int kPrepThreads = kCWarps * 32;  // xprep: one warp per token, then T_c
 constexpr int kMaxR = 64;
 constexpr int kMaxKS = kMaxR / 16;       // LoRA k-steps of 16 columns of T
+constexpr int kPrefetchUnits = 2;        // units per block prefetched into L2 before the wait
+                                         // (deeper prefetch slows the preparation kernel's loads)
 constexpr size_t kXhOff = 2 * kBoxBytes + kScaleBox;  // the record in a stage
-// Weight bytes per GEMM block that the preparation kernel asks L2 to hold
-// ahead of the GEMM (two calls' worth must fit in L2 together).
-constexpr size_t kPrefetchBytesPerBlock = (size_t)320 << 10;
 
 // named barriers (0 is __syncthreads)
 constexpr int kBarGroup = 9;       // the 8 half-0 consumer warps
 constexpr int kBarConsumers = 10;  // all 16 consumer warps
 
+// As many stages as fit next to the rest of shared memory (227 KB).
 template <int MP>
 __host__ __device__ constexpr int n_stages()
 {
     return MP == 8 ? 4 : 3;
 }
-// A chunk's record (workspace and stage alike): 2^p per token (128 bytes)
-// and X' (1 KB per token).
+// A chunk's record (workspace and stage alike): 2^p per token (128 bytes),
+// T_c (KS * MP/8 * 512 bytes) and X' (1 KB per token).
 constexpr size_t kFacBytes = 128;
-__host__ __device__ constexpr size_t rec_bytes(int MP) { return kFacBytes + (size_t)MP * 1024; }
-// T (or a chunk's part of it) in B-fragment order: KS x MP/8 x 32 lanes x float4
 __host__ __device__ constexpr size_t t_bytes(int KS, int MP) { return (size_t)KS * (MP / 8) * 512; }
+__host__ __device__ constexpr size_t rec_bytes(int KS, int MP) { return kFacBytes + t_bytes(KS, MP) + (size_t)MP * 1024; }
 template <int MP>
 __host__ __device__ constexpr size_t stage_bytes()  // a multiple of 1024 (swizzled boxes)
 {
-    return (kXhOff + rec_bytes(MP) + 1023) / 1024 * 1024;
+    return (kXhOff + rec_bytes(kMaxKS, MP) + 1023) / 1024 * 1024;
 }
 template <int MP>
 __host__ __device__ constexpr size_t red_bytes()  // 2 buffers x 8 row groups x 32 lanes x MP/2 floats
 {
     return (size_t)2 * 8 * 32 * (MP / 2) * 4;
 }
+template <int MP>
+__host__ __device__ constexpr size_t tacc_bytes()  // 2 buffers of T summed over a segment
+{
+    return (size_t)2 * kMaxKS * (MP / 8) * 32 * 16;
+}
 constexpr int kBsmMaxR = 32;                       // LoRA B rows staged in shared memory up to this rank
 constexpr size_t kBBytes = (size_t)kRows * kBsmMaxR * 2;  // one tile's B rows (bf16)
 template <int MP>
 __host__ __device__ constexpr size_t bbuf_off()  // 2 buffers of a tile's B rows
 {
-    return n_stages<MP>() * stage_bytes<MP>() + red_bytes<MP>();
-}
-template <int MP>
-__host__ __device__ constexpr size_t tsm_off()  // T
-{
-    return bbuf_off<MP>() + 2 * kBBytes;
+    return n_stages<MP>() * stage_bytes<MP>() + red_bytes<MP>() + tacc_bytes<MP>();
 }
 template <int MP>
 __host__ __device__ constexpr size_t smem_bytes()  // + 1 KB to align the ring, + barriers
 {
-    return 1024 + tsm_off<MP>() + t_bytes(kMaxKS, MP) + 128;
+    return 1024 + bbuf_off<MP>() + 2 * kBBytes + 128;
 }
-// static shared memory of the preparation kernel
-template <int MP>
-__host__ __device__ constexpr size_t prep_smem_bytes()
-{
-    return (size_t)MP * 1024 + 1024;
-}
-// The preparation kernel of the next call must fit next to a GEMM block
-// (228 KB of shared memory per SM, 1 KB reserved per block).
-static_assert(smem_bytes<8>() + prep_smem_bytes<8>() + 2048 <= 233472, "shared memory (8 tokens)");
-static_assert(smem_bytes<16>() + prep_smem_bytes<16>() + 2048 <= 233472, "shared memory (16 tokens)");
+static_assert(smem_bytes<8>() <= 232448 && smem_bytes<16>() <= 232448, "shared memory");
 
 __device__ __forceinline__ void pdl_launch_dependents()
 {
@@ -144,25 +124,6 @@ __device__ __forceinline__ void pdl_launch_dependents()
 __device__ __forceinline__ void pdl_wait()
 {
     asm volatile("griddepcontrol.wait;" ::: "memory");
-}
-
-__device__ __forceinline__ uint32_t ld_acquire(const uint32_t *p)
-{
-    uint32_t v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-
-__device__ __forceinline__ void st_release(uint32_t *p, uint32_t v)
-{
-    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
-// Orders this thread's preceding generic-proxy accesses (a flag read) before
-// its following async-proxy (bulk copy) reads of global memory.
-__device__ __forceinline__ void fence_proxy_async_global()
-{
-    asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
 __device__ __forceinline__ int owner_of(int u, int U, int G)
@@ -191,16 +152,19 @@ __device__ __forceinline__ uint32_t bf16x2_bits(float a, float b)
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
+
 struct Params {
     CUtensorMap tm_codes;   // codes, N x K/2 bytes: boxes of 128 x 128, 128B swizzle
     CUtensorMap tm_scales;  // scales, N x K/16 bytes: boxes of 128 x 32
     int M, N, K, r, C, U, KS;  // KS: LoRA k-steps (1, 2 or 4; 0 without LoRA)
+    const uint16_t *x;         // M x K bf16 (this token group)
+    const float *noise;        // K floats or null
+    const uint16_t *lora_a;    // r x K bf16
     const uint16_t *lora_b;    // N x r bf16
     float lora_scale;
     const float *tensor_scale;
-    const uint8_t *rec;        // [C] chunk records: 2^p per token | X' rows
+    const uint8_t *rec;        // [C] chunk records: 2^p per token | T_c | X' rows
     int rec_bytes;
-    const float4 *tfull;       // T in B-fragment order
     int bsm;                   // 1: the producer stages each tile's B rows in shared memory
     float *part;               // [G][2][8][32][MP/2]: tile shares left for the last block
     uint32_t *tcnt;            // tile arrival counters
@@ -209,258 +173,165 @@ struct Params {
     int y_fp32;
 };
 
-// ---------------------------------------------------------------- preparation
+// ---------------------------------------------------------------- xprep kernel
 struct PrepParams {
-    CUtensorMap tm_codes, tm_scales;  // the GEMM's weight maps (L2 prefetch only)
-    int M, N, K, r, KS, C, U, G;      // G: the GEMM's grid
-    int pf_units;                     // units per GEMM block to prefetch
-    const uint16_t *x;                // M x K bf16
-    const float *noise;               // K floats or null
-    const uint16_t *lora_a;           // r x K bf16
-    const uint16_t *lora_b;           // N x r bf16 (L2 prefetch only)
-    uint8_t *rec;                     // [C] records of rec_bytes(MP)
-    float4 *tpart;                    // [C] T_c in B-fragment order
-    float4 *tfull;                    // T
-    uint32_t *ctl;
+    int M, K, r, KS;
+    const uint16_t *x;       // M x K bf16
+    const float *noise;      // K floats or null
+    const uint16_t *lora_a;  // r x K bf16
+    uint8_t *rec;            // [C] records of rec_bytes(KS, MP)
 };
 
-// Block b lets the GEMM launch at once: block 0 first clears the two flags
-// the GEMM polls first (every GEMM block of the previous call has seen them
-// before this grid could launch).  Warp 0 then asks L2 to prefetch the first
-// units of the weight range that GEMM block b will stream and this chunk's
-// inputs -- before the dependency wait, so while the previous call still
-// runs; a prefetch moves nothing into the SM, so it cannot observe stale
-// data, and a prefetch instruction may stall its warp for as long as the TMA
-// unit is busy, so no other work waits for it.  Warps 1..3 pass the
-// dependency wait (every earlier kernel of the stream has completed), block 0
-// raises the wait flag, and chunk block c forms chunk c's record: warp w
-// converts tokens w-1, w+2, ... (lane l: columns 16l .. 16l+15 of the chunk),
-// bf16 into shared memory for the LoRA down-projection, f16 times 2^-p into
-// the record.  T_c = X'_c A_c^T by bf16 mma.sync with the tokens as the M
-// dimension; the k index of each MMA is permuted exactly as in the GEMM's
-// main loop (lane t of a quad holds 64 consecutive columns of a 256-column
-// half), so each lane reads A in 16-byte pieces and X' in conflict-free
-// 16-byte units.  Warp w owns the 8-column n-tiles jt = w-1, w+2, ... of T and
-// walks both halves of the chunk in a fixed order.
+// Block c: warp m < M forms X' of token m (lane l: columns 16l .. 16l+15 of
+// the chunk): bf16 into shared memory for the LoRA down-projection, f16
+// times 2^-p into the record.  Then T_c = X'_c A_c^T by bf16 mma.sync with
+// the tokens as the M dimension; the k index of each MMA is permuted exactly
+// as in the GEMM's main loop (lane t of a quad holds 64 consecutive columns
+// of a 256-column half), so each lane reads A in 16-byte pieces and X' in
+// conflict-free 16-byte units.  Warps split (8-column n-tile of T, half,
+// k-step pairs); one warp per n-tile sums the parts in fixed order and
+// stores them in the layout the epilogue loads as B fragments.
 template <int MP>
-__global__ void __launch_bounds__(kPrepThreads, 8) prep_kernel(const __grid_constant__ PrepParams p)
+__global__ void __launch_bounds__(kPrepThreads, 1) xprep_kernel(const __grid_constant__ PrepParams p)
 {
     constexpr int NT = MP / 8;
-    constexpr int W = kPrepWarps - 1;  // working warps (warp 0 prefetches)
     __shared__ __align__(16) uint8_t xb[MP * 1024];
-    __shared__ int s_last;
+    __shared__ float4 scratch[kCWarps * 32];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-    const int b = blockIdx.x;
-
-    if (b == 0 && threadIdx.x == 0) {
-        p.ctl[CTL_WFLAG] = 0u;
-        p.ctl[CTL_XFLAG] = 0u;
-        __threadfence();
-    }
-    __syncthreads();
-    pdl_launch_dependents();  // the GEMM may start; it reads nothing before the wait flag
-
-    if (warp == 0) {
-        // ---- L2 prefetch only (no data reaches the SM)
-        if (lane == 0 && b < p.G) {
-            const int u0 = range_begin(b, p.U, p.G), u1 = range_begin(b + 1, p.U, p.G);
-            for (int u = u0; u < min(u1, u0 + p.pf_units); u++) {
-                const int n = u / p.C, c = u - n * p.C;
-                tma_prefetch_2d(&p.tm_codes, c * (kChunk / 2), n * kRows);
-                if ((c + 1) * kChunk <= p.K)
-                    tma_prefetch_2d(&p.tm_codes, c * (kChunk / 2) + 128, n * kRows);
-                tma_prefetch_2d(&p.tm_scales, c * (kChunk / 16), n * kRows);
-            }
-        }
-        if (lane == 1 && p.KS > 0) {  // this block's share of LoRA B
-            const size_t total = ((size_t)p.N * p.r * 2) & ~(size_t)15;
-            const size_t piece = (total / gridDim.x + 15) & ~(size_t)15;
-            const size_t off = (size_t)b * piece;
-            if (piece > 0 && off < total)
-                bulk_prefetch_l2(reinterpret_cast<const uint8_t *>(p.lora_b) + off,
-                                 (uint32_t)min(piece, total - off));
-        }
-        if (b < p.C) {
-            const int kbase = b * kChunk;
-            const uint32_t cbytes = (uint32_t)min(kChunk, p.K - kbase) * 2u;
-            if (lane >= 2 && lane - 2 < p.M)
-                bulk_prefetch_l2(p.x + (size_t)(lane - 2) * p.K + kbase, cbytes);
-            if (lane == 31 && p.noise)
-                bulk_prefetch_l2(p.noise + kbase, 2 * cbytes);
-            if (p.KS > 0)
-                for (int j = lane; j < p.r; j += 32)
-                    bulk_prefetch_l2(p.lora_a + (size_t)j * p.K + kbase, cbytes);
-        }
-        return;
-    }
-    pdl_wait();  // every earlier kernel of the stream has completed
-    if (b == 0 && threadIdx.x == 32)
-        st_release(&p.ctl[CTL_WFLAG], 1u);  // the GEMM may read its inputs
-    if (b >= p.C)
-        return;
-
-    const int w = warp - 1;
-    const int c = b;
+    const int c = blockIdx.x;
     const int kbase = c * kChunk;
     const int halves = kbase + kChunk <= p.K ? 2 : 1;
-    uint8_t *rec = p.rec + (size_t)c * rec_bytes(MP);
+    const uint32_t cbytes = (uint32_t)min(kChunk, p.K - kbase) * 2u;
+    // the chunk's activations, noise and A rows into L2 while the previous kernel finishes
+    if (warp < p.M && lane == 0)
+        bulk_prefetch_l2(p.x + (size_t)warp * p.K + kbase, cbytes);
+    if (warp == kCWarps - 1 && lane == 0 && p.noise)
+        bulk_prefetch_l2(p.noise + kbase, 2 * cbytes);
+    if (p.KS > 0 && lane == 0)
+        for (int j = warp; j < p.r; j += kCWarps)
+            bulk_prefetch_l2(p.lora_a + (size_t)j * p.K + kbase, cbytes);
+    pdl_launch_dependents();  // the GEMM's blocks may start prefetching weights
+    pdl_wait();
+
+    uint8_t *rec = p.rec + (size_t)c * rec_bytes(p.KS, MP);
     float *fac = reinterpret_cast<float *>(rec);
-    uint8_t *xrec = rec + kFacBytes;
+    float4 *trec = reinterpret_cast<float4 *>(rec + kFacBytes);
+    uint8_t *xrec = rec + kFacBytes + t_bytes(p.KS, MP);
     const int k0 = kbase + lane * 16;
-    const bool kin = k0 < p.K;
+    const bool conv = warp < p.M, kin = conv && k0 < p.K;
+    uint4 xa = make_uint4(0u, 0u, 0u, 0u), xc = xa;
     float4 z4[4];
-    if (kin && p.noise) {
-        const float4 *zs = reinterpret_cast<const float4 *>(p.noise + k0);
+    if (kin) {
+        const uint4 *xs = reinterpret_cast<const uint4 *>(p.x + (size_t)warp * p.K + k0);
+        xa = __ldcg(xs);
+        xc = __ldcg(xs + 1);
+        if (p.noise) {
+            const float4 *zs = reinterpret_cast<const float4 *>(p.noise + k0);
 #pragma unroll
-        for (int q = 0; q < 4; q++)
-            z4[q] = __ldcg(zs + q);
-    }
-    // this warp's tokens: w, w + 3, ... (< MP); loads of up to three tokens in flight
-    constexpr int TPW = (MP + W - 1) / W;
-    constexpr int TB = 3;
-#pragma unroll 1
-    for (int i0 = 0; i0 < TPW; i0 += TB) {
-        uint4 xv[TB][2];
-#pragma unroll
-        for (int i = 0; i < TB; i++) {
-            const int tok = w + W * (i0 + i);
-            xv[i][0] = xv[i][1] = make_uint4(0u, 0u, 0u, 0u);
-            if (i0 + i < TPW && tok < p.M && kin) {
-                const uint4 *xs = reinterpret_cast<const uint4 *>(p.x + (size_t)tok * p.K + k0);
-                xv[i][0] = __ldcg(xs);
-                xv[i][1] = __ldcg(xs + 1);
-            }
-        }
-#pragma unroll
-        for (int i = 0; i < TB; i++) {
-            const int tok = w + W * (i0 + i);
-            if (i0 + i >= TPW || tok >= MP)
-                break;
-            if (tok >= p.M) {
-                if (lane == 0)
-                    fac[tok] = 0.0f;  // tokens past M: their MMA columns are zero
-                continue;
-            }
-            const uint32_t xw[8] = {xv[i][0].x, xv[i][0].y, xv[i][0].z, xv[i][0].w,
-                                    xv[i][1].x, xv[i][1].y, xv[i][1].z, xv[i][1].w};
-            float v[16];
-            float mx = 0.0f;
-#pragma unroll
-            for (int e = 0; e < 16; e++) {
-                float f = bf16_bits_to_f32((xw[e / 2] >> (16 * (e & 1))) & 0xFFFFu);
-                if (kin && p.noise) {
-                    const float4 zq = z4[e / 4];
-                    const float z = (e & 3) == 0 ? zq.x : (e & 3) == 1 ? zq.y : (e & 3) == 2 ? zq.z : zq.w;
-                    f = bf16_round(__fmul_rn(f, z));
-                }
-                v[e] = f;
-                mx = fmaxf(mx, fabsf(f));
-            }
-#pragma unroll
-            for (int off = 16; off >= 1; off >>= 1)
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-            int pexp = 0;
-            if (mx > 0.0f) {
-                const uint32_t bb = __float_as_uint(mx);
-                const int e = (bb >> 23) ? (int)(bb >> 23) - 127 : (31 - __clz(bb)) - 149;
-                pexp = e - 14;
-            }
-#pragma unroll
-            for (int u2 = 0; u2 < 2; u2++) {
-                uint32_t hw[4], bw[4];
-#pragma unroll
-                for (int e = 0; e < 4; e++) {
-                    const float lo = v[8 * u2 + 2 * e], hi = v[8 * u2 + 2 * e + 1];
-                    __half2 h2 = __halves2half2(__float2half_rn(scale_pow2(lo, -pexp)),
-                                                __float2half_rn(scale_pow2(hi, -pexp)));
-                    hw[e] = *reinterpret_cast<uint32_t *>(&h2);
-                    bw[e] = bf16x2_bits(lo, hi);  // exact: lo, hi are bf16 values
-                }
-                const int off = 16 * xh_unit(tok, 2 * lane + u2);
-                *reinterpret_cast<uint4 *>(xrec + tok * 1024 + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                *reinterpret_cast<uint4 *>(xb + tok * 1024 + off) = make_uint4(bw[0], bw[1], bw[2], bw[3]);
-            }
-            if (lane == 0)
-                fac[tok] = exp2i(pexp);
+            for (int q = 0; q < 4; q++)
+                z4[q] = __ldcg(zs + q);
         }
     }
-    named_sync(1, W * 32);  // this chunk's record written (and its bf16 X' in shared memory)
-    if (threadIdx.x == 32) {
-        __threadfence();
-        if (atomicAdd(&p.ctl[CTL_XCNT], 1u) == (uint32_t)p.C - 1) {
-            p.ctl[CTL_XCNT] = 0u;
-            __threadfence();
-            st_release(&p.ctl[CTL_XFLAG], 1u);  // every chunk's record is in place
+    // LoRA A operand: warp -> (n-tile jt, half hh, part sub of its 8 k-step pairs)
+    const int njt = 2 * p.KS;                  // 2, 4 or 8 n-tiles (0 without LoRA)
+    const int nunit = njt * halves;            // 2..16, divides 16
+    const int wpu = nunit > 0 ? kCWarps / nunit : 1;
+    const int unit = warp / wpu, sub = warp % wpu;
+    const int jt = unit / halves, hh = unit % halves;
+    const int npairs = 8 / wpu;                // k-step pairs per warp
+    const int jrow = jt * 8 + g;
+    const uint16_t *arow = p.lora_a + (size_t)min(jrow, max(p.r - 1, 0)) * p.K + kbase + 256 * hh + 64 * t;
+    uint4 af[8];
+    if (p.KS > 0) {
+#pragma unroll
+        for (int q = 0; q < 8; q++) {
+            const bool ok = q < npairs && jrow < p.r;
+            af[q] = ok ? __ldcg(reinterpret_cast<const uint4 *>(arow + 8 * (sub * npairs + q)))
+                       : make_uint4(0u, 0u, 0u, 0u);
         }
+    }
+    if (conv) {
+        const uint32_t xw[8] = {xa.x, xa.y, xa.z, xa.w, xc.x, xc.y, xc.z, xc.w};
+        float v[16];
+        float mx = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 16; i++) {
+            float f = bf16_bits_to_f32((xw[i / 2] >> (16 * (i & 1))) & 0xFFFFu);
+            if (kin && p.noise) {
+                const float4 zq = z4[i / 4];
+                const float z = (i & 3) == 0 ? zq.x : (i & 3) == 1 ? zq.y : (i & 3) == 2 ? zq.z : zq.w;
+                f = bf16_round(__fmul_rn(f, z));
+            }
+            v[i] = f;
+            mx = fmaxf(mx, fabsf(f));
+        }
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1)
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+        int pexp = 0;
+        if (mx > 0.0f) {
+            const uint32_t b = __float_as_uint(mx);
+            const int e = (b >> 23) ? (int)(b >> 23) - 127 : (31 - __clz(b)) - 149;
+            pexp = e - 14;
+        }
+#pragma unroll
+        for (int u2 = 0; u2 < 2; u2++) {
+            uint32_t hw[4], bw[4];
+#pragma unroll
+            for (int i = 0; i < 4; i++) {
+                const float lo = v[8 * u2 + 2 * i], hi = v[8 * u2 + 2 * i + 1];
+                __half2 h2 = __halves2half2(__float2half_rn(scale_pow2(lo, -pexp)),
+                                            __float2half_rn(scale_pow2(hi, -pexp)));
+                hw[i] = *reinterpret_cast<uint32_t *>(&h2);
+                bw[i] = bf16x2_bits(lo, hi);  // exact: lo, hi are bf16 values
+            }
+            const int off = 16 * xh_unit(warp, 2 * lane + u2);
+            *reinterpret_cast<uint4 *>(xrec + warp * 1024 + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            *reinterpret_cast<uint4 *>(xb + warp * 1024 + off) = make_uint4(bw[0], bw[1], bw[2], bw[3]);
+        }
+        if (lane == 0)
+            fac[warp] = exp2i(pexp);
+    } else if (warp < MP && lane == 0) {
+        fac[warp] = 0.0f;  // tokens past M: their MMA columns are zero
     }
     if (p.KS == 0)
         return;
-
-    // ---- T_c = X'_c A_c^T; warp w: n-tiles jt = w, w + 3, ... (8 columns of T each)
-    float4 *tp = p.tpart + (size_t)c * (t_bytes(p.KS, MP) / 16);
+    __syncthreads();  // bf16 X' complete in shared memory
+    float cc[4] = {0.f, 0.f, 0.f, 0.f};
     const uint8_t *x0r = xb + g * 1024, *x1r = xb + (g + 8) * 1024;
-    for (int jt = w; jt < 2 * p.KS; jt += W) {
-        const int jrow = jt * 8 + g;
-        const uint16_t *arow = p.lora_a + (size_t)min(jrow, p.r - 1) * p.K + kbase + 64 * t;
-        float cc[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int hh = 0; hh < halves; hh++) {
 #pragma unroll
-            for (int q0 = 0; q0 < 8; q0 += 4) {
-                uint4 af[4];
-#pragma unroll
-                for (int q = 0; q < 4; q++)
-                    af[q] = jrow < p.r ? __ldcg(reinterpret_cast<const uint4 *>(arow + 256 * hh + 8 * (q0 + q)))
-                                       : make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-                for (int q = 0; q < 4; q++) {
-                    const int ux = 32 * hh + 8 * t + q0 + q;  // 8 columns: two k-steps
-                    const uint4 x0 = g < p.M ? *reinterpret_cast<const uint4 *>(x0r + 16 * xh_unit(g, ux))
-                                             : make_uint4(0u, 0u, 0u, 0u);
-                    const uint4 x1 = g + 8 < p.M ? *reinterpret_cast<const uint4 *>(x1r + 16 * xh_unit(g + 8, ux))
-                                                 : make_uint4(0u, 0u, 0u, 0u);
-                    uint32_t a[4] = {x0.x, x1.x, x0.y, x1.y};
-                    mma_bf16_16816(cc, a, af[q].x, af[q].y);
-                    a[0] = x0.z;
-                    a[1] = x1.z;
-                    a[2] = x0.w;
-                    a[3] = x1.w;
-                    mma_bf16_16816(cc, a, af[q].z, af[q].w);
-                }
-            }
+    for (int q = 0; q < 8; q++) {
+        if (q < npairs) {
+            const int ux = 32 * hh + 8 * t + sub * npairs + q;  // 8 columns: two k-steps
+            const uint4 x0 = g < p.M ? *reinterpret_cast<const uint4 *>(x0r + 16 * xh_unit(g, ux))
+                                     : make_uint4(0u, 0u, 0u, 0u);
+            const uint4 x1 = g + 8 < p.M ? *reinterpret_cast<const uint4 *>(x1r + 16 * xh_unit(g + 8, ux))
+                                         : make_uint4(0u, 0u, 0u, 0u);
+            uint32_t a[4] = {x0.x, x1.x, x0.y, x1.y};
+            mma_bf16_16816(cc, a, af[q].x, af[q].y);
+            a[0] = x0.z;
+            a[1] = x1.z;
+            a[2] = x0.w;
+            a[3] = x1.w;
+            mma_bf16_16816(cc, a, af[q].z, af[q].w);
         }
-        // lane (g, t) holds T[g][8jt + 2t, +1] and T[g + 8][8jt + 2t, +1]
+    }
+    scratch[warp * 32 + lane] = make_float4(cc[0], cc[1], cc[2], cc[3]);
+    __syncthreads();
+    if (hh == 0 && sub == 0) {  // sum n-tile jt over halves and parts, fixed order
+        float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int w = 0; w < halves * wpu; w++) {
+            const float4 o = scratch[(warp + w) * 32 + lane];
+            s.x += o.x;
+            s.y += o.y;
+            s.z += o.z;
+            s.w += o.w;
+        }
+        // lane (g, t) holds T[g][8jt + 2t, +1] (x, y) and T[g+8][...] (z, w)
         const int ks = jt / 2, jh = jt % 2;
-        reinterpret_cast<float2 *>(tp + ((size_t)ks * NT + 0) * 32 + lane)[jh] = make_float2(cc[0], cc[1]);
+        reinterpret_cast<float2 *>(trec + ((size_t)ks * NT + 0) * 32 + lane)[jh] = make_float2(s.x, s.y);
         if (NT == 2)
-            reinterpret_cast<float2 *>(tp + ((size_t)ks * NT + 1) * 32 + lane)[jh] = make_float2(cc[2], cc[3]);
-    }
-    named_sync(1, W * 32);
-    if (threadIdx.x == 32) {
-        __threadfence();
-        s_last = atomicAdd(&p.ctl[CTL_TCNT], 1u) == (uint32_t)p.C - 1;
-    }
-    named_sync(1, W * 32);
-    if (!s_last)
-        return;
-    // the last chunk block: T = sum of T_c in chunk order
-    __threadfence();
-    const int nf = (int)(t_bytes(p.KS, MP) / 16);
-    for (int e = threadIdx.x - 32; e < nf; e += W * 32) {
-        float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int cc2 = 0; cc2 < p.C; cc2++) {
-            const float4 v = __ldcg(p.tpart + (size_t)cc2 * nf + e);
-            sum.x += v.x;
-            sum.y += v.y;
-            sum.z += v.z;
-            sum.w += v.w;
-        }
-        p.tfull[e] = sum;
-    }
-    named_sync(1, W * 32);
-    if (threadIdx.x == 32) {
-        p.ctl[CTL_TCNT] = 0u;
-        __threadfence();
-        st_release(&p.ctl[CTL_TFLAG], 1u);
+            reinterpret_cast<float2 *>(trec + ((size_t)ks * NT + 1) * 32 + lane)[jh] = make_float2(s.z, s.w);
     }
 }
 
@@ -587,11 +458,12 @@ __device__ __forceinline__ uint32_t lora_pair_s(const Params &p, const uint16_t 
     return *reinterpret_cast<const uint32_t *>(bs + (size_t)(R - n * kRows) * p.r + j);
 }
 
-// The block's share of tile n for half-0 warp mt: s * T B^T (B rows from bs
-// in shared memory, or from global memory when bs is null), added to base.
+// The block's share of tile n for half-0 warp mt: s_t * acc + s * T_R B^T
+// (B rows from bs in shared memory, or from global memory when bs is null).
 template <int MP>
-__device__ __forceinline__ void add_lora(const Params &p, int n, int mt, int lane, const float4 *tr,
-                                         const uint16_t *bs, float (&y)[MP / 8][4])
+__device__ __forceinline__ void tile_share(const Params &p, int n, int mt, int lane, float s_t,
+                                           const float (&acc)[MP / 8][4], const float4 *tr, const uint16_t *bs,
+                                           float (&out)[MP / 8][4])
 {
     constexpr int NT = MP / 8;
     const int g = lane >> 2, t = lane & 3;
@@ -633,7 +505,7 @@ __device__ __forceinline__ void add_lora(const Params &p, int n, int mt, int lan
     for (int nt = 0; nt < NT; nt++)
 #pragma unroll
         for (int q = 0; q < 4; q++)
-            y[nt][q] = __fmaf_rn(p.lora_scale, cl[nt][q], y[nt][q]);
+            out[nt][q] = __fmaf_rn(s_t, acc[nt][q], p.lora_scale * cl[nt][q]);
 }
 
 template <int MP>
@@ -658,14 +530,11 @@ __device__ __forceinline__ void store_tile(const Params &p, int n, int mt, int l
         }
 }
 
-// End of the block's segment of tile n (consumer warp mt, half h).  tsm: T in
-// shared memory, ready once *tbar completes (waited for only by a block that
-// finishes the tile).
+// End of the block's segment of tile n (consumer warp mt, half h).
 template <int MP>
 __device__ __forceinline__ void finish_segment(const Params &p, int n, int u0, int mt, int h, int lane,
-                                               float (&acc)[MP / 8][4], const float4 *tsm, uint64_t *tbar,
-                                               const uint16_t *bs, float *red, int buf,
-                                               volatile uint32_t *s_flag, float s_t, bool &ok)
+                                               float (&acc)[MP / 8][4], const float4 *tr, const uint16_t *bs,
+                                               float *red, int buf, volatile uint32_t *s_flag, float s_t)
 {
     constexpr int NT = MP / 8;
     const int G = gridDim.x, b = blockIdx.x;
@@ -675,17 +544,18 @@ __device__ __forceinline__ void finish_segment(const Params &p, int n, int u0, i
         for (int nt = 0; nt < NT; nt++)
             rb[nt] = make_float4(acc[nt][0], acc[nt][1], acc[nt][2], acc[nt][3]);
     }
-    named_sync(kBarConsumers, kCWarps * 32);  // half-1 sums in shared memory
+    named_sync(kBarConsumers, kCWarps * 32);  // half-1 sums and the segment's T in shared memory
     if (h == 0) {
-        float y[NT][4];
 #pragma unroll
         for (int nt = 0; nt < NT; nt++) {
             const float4 v = rb[nt];
-            y[nt][0] = s_t * (acc[nt][0] + v.x);
-            y[nt][1] = s_t * (acc[nt][1] + v.y);
-            y[nt][2] = s_t * (acc[nt][2] + v.z);
-            y[nt][3] = s_t * (acc[nt][3] + v.w);
+            acc[nt][0] += v.x;
+            acc[nt][1] += v.y;
+            acc[nt][2] += v.z;
+            acc[nt][3] += v.w;
         }
+        float y[NT][4];
+        tile_share<MP>(p, n, mt, lane, s_t, acc, tr, bs, y);
         const int first = owner_of(n * p.C, p.U, G), last = owner_of(n * p.C + p.C - 1, p.U, G);
         bool finish = true;
         if (last > first) {
@@ -744,18 +614,8 @@ __device__ __forceinline__ void finish_segment(const Params &p, int n, int u0, i
                     p.tcnt[n] = 0;
             }
         }
-        if (finish) {
-            if (p.KS > 0) {
-                if (ok && !mbar_wait(tbar, 0)) {
-                    ok = false;
-                    if (lane == 0)
-                        record_timeout_tiles(p.ctl);
-                }
-                if (ok)
-                    add_lora<MP>(p, n, mt, lane, tsm, bs, y);
-            }
+        if (finish)
             store_tile<MP>(p, n, mt, lane, y);
-        }
     }
 #pragma unroll
     for (int nt = 0; nt < NT; nt++)
@@ -764,51 +624,34 @@ __device__ __forceinline__ void finish_segment(const Params &p, int n, int u0, i
             acc[nt][q] = 0.0f;
 }
 
-// Bounded wait for a flag word to become non-zero (acquire).
-__device__ __forceinline__ bool flag_wait(const uint32_t *f)
-{
-    if (ld_acquire(f) != 0u)
-        return true;
-    const uint64_t t0 = globaltimer();
-    for (uint32_t i = 0;; i++) {
-        __nanosleep(32);
-        if (ld_acquire(f) != 0u)
-            return true;
-        if ((i & 255) == 255 && globaltimer() - t0 > 2000000000ull)
-            return false;
-    }
-}
-
 template <int MP>
-__global__ void __maxnreg__(88) stream_gemm_kernel(const __grid_constant__ Params p)
+__global__ void __launch_bounds__(kThreads, 1) stream_gemm_kernel(const __grid_constant__ Params p)
 {
     constexpr int NT = MP / 8;
     constexpr int S = n_stages<MP>();
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     float *red = reinterpret_cast<float *>(smem + S * stage_bytes<MP>());
+    float4 *tacc = reinterpret_cast<float4 *>(smem + S * stage_bytes<MP>() + red_bytes<MP>());
     uint16_t *bbuf = reinterpret_cast<uint16_t *>(smem + bbuf_off<MP>());
-    float4 *tsm = reinterpret_cast<float4 *>(smem + tsm_off<MP>());
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + tsm_off<MP>() + t_bytes(kMaxKS, MP));
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + bbuf_off<MP>() + 2 * kBBytes);
     uint64_t *empty = full + S;
     uint64_t *bfull = empty + S;   // a segment's B rows in shared memory (2 buffers)
     uint64_t *bempty = bfull + 2;  // B buffer free again
-    uint64_t *tbar = bempty + 2;   // T in shared memory
-    volatile uint32_t *s_flag = reinterpret_cast<volatile uint32_t *>(tbar + 1);
+    volatile uint32_t *s_flag = reinterpret_cast<volatile uint32_t *>(bempty + 2);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = gridDim.x, b = blockIdx.x;
     const int u0 = range_begin(b, p.U, G), u1 = range_begin(b + 1, p.U, G);
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; s++) {
-            mbar_init(&full[s], 2);  // the weight copies (with their bytes) + the record
+            mbar_init(&full[s], 1);
             mbar_init(&empty[s], kCWarps);
         }
         for (int k = 0; k < 2; k++) {
             mbar_init(&bfull[k], 1);
             mbar_init(&bempty[k], kCWarps);
         }
-        mbar_init(tbar, 1);
         mbar_fence_init();
     }
     __syncthreads();
@@ -816,103 +659,72 @@ __global__ void __maxnreg__(88) stream_gemm_kernel(const __grid_constant__ Param
     if (warp == kProducer) {
         // ---------------- producer warp (lane 0 issues every copy)
         if (lane == 0) {
-            const uint32_t rbytes = (uint32_t)kFacBytes + (uint32_t)p.M * 1024u;
-            const int nu = u1 - u0;
-            // nothing is read before the preparation kernel has passed its
-            // dependency wait (every kernel before it has completed)
-            bool ok = flag_wait(&p.ctl[CTL_WFLAG]);
-            // the weights of the first stages at once: they need no hand-over
-            for (int i = 0; ok && i < min(nu, S); i++) {
-                const int u = u0 + i, n = u / p.C, c = u - n * p.C;
-                const bool two = (c + 1) * kChunk <= p.K;  // else a last 256-column chunk
-                uint8_t *st = smem + (size_t)i * stage_bytes<MP>();
-                mbar_arrive_expect_tx(&full[i], (two ? 2 : 1) * kBoxBytes + kScaleBox + rbytes);
-                tma_load_2d(st, &p.tm_codes, &full[i], c * (kChunk / 2), n * kRows);
-                if (two)
-                    tma_load_2d(st + kBoxBytes, &p.tm_codes, &full[i], c * (kChunk / 2) + 128, n * kRows);
-                tma_load_2d(st + 2 * kBoxBytes, &p.tm_scales, &full[i], c * (kChunk / 16), n * kRows);
-            }
-            // the records only once the preparation kernel has written all of them
-            if (ok && !flag_wait(&p.ctl[CTL_XFLAG]))
-                ok = false;
-            fence_proxy_async_global();
-            // Both flags seen: the next call's preparation kernel may launch (it
-            // clears them first) and prefetch the next weights meanwhile.
-            pdl_launch_dependents();
-            int q = 0;  // segment
-            for (int i = 0; i < nu && ok; i++) {
-                const int u = u0 + i, s = i % S;
+            // the weights of the first units into L2 while xprep runs
+            for (int u = u0; u < min(u1, u0 + kPrefetchUnits); u++) {
                 const int n = u / p.C, c = u - n * p.C;
-                uint8_t *st = smem + (size_t)s * stage_bytes<MP>();
-                if (i >= S) {
-                    if (!mbar_wait(&empty[s], ((i / S) + 1) & 1)) {
-                        ok = false;
-                        break;
-                    }
-                    const bool two = (c + 1) * kChunk <= p.K;
-                    mbar_arrive_expect_tx(&full[s], (two ? 2 : 1) * kBoxBytes + kScaleBox + rbytes);
-                    tma_load_2d(st, &p.tm_codes, &full[s], c * (kChunk / 2), n * kRows);
-                    if (two)
-                        tma_load_2d(st + kBoxBytes, &p.tm_codes, &full[s], c * (kChunk / 2) + 128, n * kRows);
-                    tma_load_2d(st + 2 * kBoxBytes, &p.tm_scales, &full[s], c * (kChunk / 16), n * kRows);
+                tma_prefetch_2d(&p.tm_codes, c * (kChunk / 2), n * kRows);
+                if ((c + 1) * kChunk <= p.K)
+                    tma_prefetch_2d(&p.tm_codes, c * (kChunk / 2) + 128, n * kRows);
+                tma_prefetch_2d(&p.tm_scales, c * (kChunk / 16), n * kRows);
+            }
+        }
+        pdl_wait();
+        if (lane == 0) {
+            // a unit's record: 2^p, T_c and the first M rows of X'
+            const uint32_t rbytes = (uint32_t)(kFacBytes + t_bytes(p.KS, MP)) + (uint32_t)p.M * 1024u;
+            int q = 0;  // segment
+            for (int i = 0; i < u1 - u0; i++) {
+                const int u = u0 + i, s = i % S;
+                // the first unit alone: its stage lands before the other stages
+                // of every block queue up in front of it
+                if (i == 1 && !mbar_wait(&full[0], 0)) {
+                    record_timeout_tiles(p.ctl);
+                    break;
                 }
+                if (i >= S && !mbar_wait(&empty[s], ((i / S) + 1) & 1)) {
+                    record_timeout_tiles(p.ctl);
+                    break;  // stop copying; consumers time out and wind down
+                }
+                const int n = u / p.C, c = u - n * p.C;
+                const bool two = (c + 1) * kChunk <= p.K;  // else a last 256-column chunk
+                uint8_t *st = smem + (size_t)s * stage_bytes<MP>();
+                mbar_arrive_expect_tx(&full[s], (two ? 2 : 1) * kBoxBytes + kScaleBox + rbytes);
+                tma_load_2d(st, &p.tm_codes, &full[s], c * (kChunk / 2), n * kRows);
+                if (two)
+                    tma_load_2d(st + kBoxBytes, &p.tm_codes, &full[s], c * (kChunk / 2) + 128, n * kRows);
+                tma_load_2d(st + 2 * kBoxBytes, &p.tm_scales, &full[s], c * (kChunk / 16), n * kRows);
                 bulk_g2s(st + kXhOff, p.rec + (size_t)c * p.rec_bytes, rbytes, &full[s]);
-                mbar_arrive(&full[s]);
                 if (p.bsm && (u + 1 == u1 || c + 1 == p.C)) {
                     // the tile's B rows, for the epilogue of the segment this unit ends
                     if (q >= 2 && !mbar_wait(&bempty[q & 1], ((q >> 1) + 1) & 1)) {
-                        ok = false;
+                        record_timeout_tiles(p.ctl);
                         break;
                     }
                     const uint32_t bbytes = (uint32_t)min(kRows, p.N - n * kRows) * (uint32_t)p.r * 2u;
                     mbar_arrive_expect_tx(&bfull[q & 1], bbytes);
-                    bulk_g2s(bbuf + (q & 1) * (kBBytes / 2), p.lora_b + (size_t)n * kRows * p.r, bbytes,
-                             &bfull[q & 1]);
+                    bulk_g2s(bbuf + (q & 1) * (kBBytes / 2), p.lora_b + (size_t)n * kRows * p.r, bbytes, &bfull[q & 1]);
                     q++;
                 }
             }
-            if (!ok)
-                record_timeout_tiles(p.ctl);  // consumers time out and wind down
-        }
-    } else if (warp == kTail) {
-        // ---------------- tail warp: T into shared memory once it is ready
-        if (lane == 0 && p.KS > 0) {
-            // the T flag belongs to this call only once the preparation kernel
-            // has passed its wait: until then the previous call's may be up
-            if (flag_wait(&p.ctl[CTL_WFLAG]) && flag_wait(&p.ctl[CTL_TFLAG])) {
-                fence_proxy_async_global();
-                const uint32_t tbytes = (uint32_t)t_bytes(p.KS, MP);
-                mbar_arrive_expect_tx(tbar, tbytes);
-                bulk_g2s(tsm, p.tfull, tbytes, tbar);
-                // the last block to take T lowers the flag for the next call
-                if (atomicAdd(&p.ctl[CTL_TREAD], 1u) == (uint32_t)G - 1) {
-                    p.ctl[CTL_TREAD] = 0u;
-                    p.ctl[CTL_TFLAG] = 0u;
-                    __threadfence();
-                }
-                // no copy may still be landing in shared memory when the block exits
-                if (!mbar_wait(tbar, 0))
-                    record_timeout_tiles(p.ctl);
-            } else {
-                record_timeout_tiles(p.ctl);
-            }
         }
         __syncwarp();
-        // this grid completes only after the preparation grid has
-        pdl_wait();
-    } else {
+        pdl_launch_dependents();
+    } else if (warp < kCWarps) {
         // ---------------- consumer warps
+        pdl_wait();
         const int mt = warp & 7, h = warp >> 3, g = lane >> 2, t = lane & 3;
         const float s_t = __ldcg(p.tensor_scale);
-        const int xoff = (int)(kXhOff + kFacBytes);
+        const int xoff = (int)(kXhOff + kFacBytes + t_bytes(p.KS, MP));
         float acc[NT][4];
 #pragma unroll
         for (int nt = 0; nt < NT; nt++)
 #pragma unroll
             for (int q = 0; q < 4; q++)
                 acc[nt][q] = 0.0f;
+        const int tn = p.KS * NT * 32;  // float4 of T per chunk
         bool ok = true;
-        int buf = 0, q = 0;  // B buffer, segment
+        bool seg_start = true;
+        int buf = 0, q = 0;  // T / B buffer, segment
         for (int u = u0, i = 0; u < u1; u++, i++) {
             const int s = i % S;
             if (ok && !mbar_wait(&full[s], (i / S) & 1)) {
@@ -922,33 +734,56 @@ __global__ void __maxnreg__(88) stream_gemm_kernel(const __grid_constant__ Param
             }
             const int n = u / p.C, c = u - n * p.C;
             const uint8_t *st = smem + (size_t)s * stage_bytes<MP>();
-            if (ok && (h == 0 || (c + 1) * kChunk <= p.K))
+            if (h == 0 || (c + 1) * kChunk <= p.K)
                 compute_unit<MP>(st, xoff, mt, h, g, t, p.M, acc);
+            if (h == 1) {  // T of this chunk into the segment's sum (element mt*32 + lane, ...)
+                const float4 *ts = reinterpret_cast<const float4 *>(st + kXhOff + kFacBytes);
+                float4 *ta = tacc + buf * (kMaxKS * NT * 32);
+                for (int e = mt * 32 + lane; e < tn; e += 256) {
+                    const float4 v = ts[e];
+                    if (seg_start) {
+                        ta[e] = v;
+                    } else {
+                        float4 o = ta[e];
+                        o.x += v.x;
+                        o.y += v.y;
+                        o.z += v.z;
+                        o.w += v.w;
+                        ta[e] = o;
+                    }
+                }
+            }
+            seg_start = false;
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(&empty[s]);
+            if (u + 1 == u1)
+                pdl_launch_dependents();
             if (u + 1 == u1 || c + 1 == p.C) {
                 if (p.bsm && ok && !mbar_wait(&bfull[buf], (q >> 1) & 1)) {
                     ok = false;
                     if (lane == 0)
                         record_timeout_tiles(p.ctl);
                 }
-                finish_segment<MP>(p, n, u0, mt, h, lane, acc, tsm, tbar,
-                                   p.bsm ? bbuf + buf * (kBBytes / 2) : nullptr, red, buf, s_flag, s_t, ok);
+                finish_segment<MP>(p, n, u0, mt, h, lane, acc, tacc + buf * (kMaxKS * NT * 32),
+                                   p.bsm ? bbuf + buf * (kBBytes / 2) : nullptr, red, buf, s_flag, s_t);
                 __syncwarp();
                 if (p.bsm && lane == 0)
                     mbar_arrive(&bempty[buf]);
                 buf ^= 1;
                 q++;
+                seg_start = true;
             }
         }
+    } else {
+        pdl_launch_dependents();  // idle warps
     }
 }
 
 // ================================================================ host side
 struct Plan {
-    int MP, C, tiles, U, G, KS, pf_units;
-    size_t rec, off_rec, off_tpart, off_tfull, off_part, total;
+    int MP, C, tiles, U, G, KS;
+    size_t rec, off_rec, off_part, total;
 };
 
 static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -969,17 +804,10 @@ static bool make_plan(int64_t M, int64_t N, int64_t K, int64_t r, const DeviceIn
     if (pl.tiles <= dev.num_sms && pl.tiles * 10 >= dev.num_sms * 9)
         pl.G = pl.tiles;
     pl.KS = r == 0 ? 0 : r <= 16 ? 1 : r <= 32 ? 2 : 4;
-    const size_t unit_bytes = (size_t)kRows * kChunk * 9 / 16;  // codes + scales of a full unit
-    const int per_block = (pl.U + pl.G - 1) / pl.G;
-    pl.pf_units = (int)std::min<size_t>((size_t)per_block, std::max<size_t>(1, kPrefetchBytesPerBlock / unit_bytes));
     size_t off = kWsHeaderBytes;
-    pl.rec = rec_bytes(pl.MP);
+    pl.rec = rec_bytes(pl.KS, pl.MP);
     pl.off_rec = off;
     off = align_up(off + (size_t)pl.C * pl.rec, 256);
-    pl.off_tpart = off;
-    off = align_up(off + (size_t)pl.C * t_bytes(pl.KS, pl.MP), 256);
-    pl.off_tfull = off;
-    off = align_up(off + t_bytes(kMaxKS, pl.MP), 256);
     pl.off_part = off;
     off = align_up(off + (size_t)pl.G * 2 * kRows * pl.MP * 4, 256);
     pl.total = off;
@@ -1077,7 +905,7 @@ static cudaError_t weight_maps(const GemmArgs &a, MapPair &mp)
 void query_stream_occupancy(DeviceInfo &dev)
 {
     using namespace stream;
-    int b8 = 0, b16 = 0, p8 = 0, p16 = 0;
+    int b8 = 0, b16 = 0;
     if (cudaFuncSetAttribute(stream_gemm_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem_bytes<8>()) != cudaSuccess ||
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b8, stream_gemm_kernel<8>, kThreads, smem_bytes<8>()) !=
@@ -1088,18 +916,8 @@ void query_stream_occupancy(DeviceInfo &dev)
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b16, stream_gemm_kernel<16>, kThreads, smem_bytes<16>()) !=
             cudaSuccess)
         b16 = 0;
-    // both kernels ask for the largest shared-memory carve-out, so that a
-    // preparation block can run next to a GEMM block
-    cudaFuncSetAttribute(stream_gemm_kernel<8>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-    cudaFuncSetAttribute(stream_gemm_kernel<16>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-    cudaFuncSetAttribute(prep_kernel<8>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-    cudaFuncSetAttribute(prep_kernel<16>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&p8, prep_kernel<8>, kPrepThreads, 0) != cudaSuccess)
-        p8 = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&p16, prep_kernel<16>, kPrepThreads, 0) != cudaSuccess)
-        p16 = 0;
     cudaGetLastError();
-    dev.stream_ok = b8 >= 1 && b16 >= 1 && p8 >= 1 && p16 >= 1;
+    dev.stream_ok = b8 >= 1 && b16 >= 1;
 }
 
 bool stream_supported(int64_t N, int64_t K, int64_t r, const DeviceInfo &dev)
@@ -1133,36 +951,24 @@ cudaError_t launch_stream_gemm(const GemmArgs &a, cudaStream_t s, const DeviceIn
         if (!cached_plan(Mg, a.N, a.K, a.r, dev, pl))
             return cudaErrorInvalidConfiguration;
         uint8_t *rec = a.ws + pl.off_rec;
-        float4 *tfull = reinterpret_cast<float4 *>(a.ws + pl.off_tfull);
         PrepParams pp;
-        pp.tm_codes = maps.codes;
-        pp.tm_scales = maps.scales;
         pp.M = (int)Mg;
-        pp.N = (int)a.N;
         pp.K = (int)a.K;
         pp.r = (int)a.r;
         pp.KS = pl.KS;
-        pp.C = pl.C;
-        pp.U = pl.U;
-        pp.G = pl.G;
-        pp.pf_units = pl.pf_units;
         pp.x = a.x + m0 * a.K;
         pp.noise = a.noise;
         pp.lora_a = a.lora_a;
-        pp.lora_b = a.lora_b;
         pp.rec = rec;
-        pp.tpart = reinterpret_cast<float4 *>(a.ws + pl.off_tpart);
-        pp.tfull = tfull;
-        pp.ctl = reinterpret_cast<uint32_t *>(a.ws);
         cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(std::max(pl.G, pl.C));
+        cfg.gridDim = dim3(pl.C);
         cfg.blockDim = dim3(kPrepThreads);
         cfg.dynamicSmemBytes = 0;
         cfg.stream = s;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         void *pargs[] = {&pp};
-        err = cudaLaunchKernelExC(&cfg, pl.MP == 8 ? (const void *)prep_kernel<8> : (const void *)prep_kernel<16>,
+        err = cudaLaunchKernelExC(&cfg, pl.MP == 8 ? (const void *)xprep_kernel<8> : (const void *)xprep_kernel<16>,
                                   pargs);
         if (err != cudaSuccess)
             return err;
@@ -1177,12 +983,14 @@ cudaError_t launch_stream_gemm(const GemmArgs &a, cudaStream_t s, const DeviceIn
         p.C = pl.C;
         p.U = pl.U;
         p.KS = pl.KS;
+        p.x = a.x + m0 * a.K;
+        p.noise = a.noise;
+        p.lora_a = a.lora_a;
         p.lora_b = a.lora_b;
         p.lora_scale = a.lora_scale;
         p.tensor_scale = a.tensor_scale;
         p.rec = rec;
         p.rec_bytes = (int)pl.rec;
-        p.tfull = tfull;
         p.bsm = pl.KS > 0 && a.r <= kBsmMaxR && a.r % 8 == 0 ? 1 : 0;
         p.part = reinterpret_cast<float *>(a.ws + pl.off_part);
         p.tcnt = reinterpret_cast<uint32_t *>(a.ws + kCtlBytes);
