@@ -223,10 +223,12 @@ class Workload:
         self.launches_per_step = 2 + 2 + sum(
             per_gemm[nv.gemm_kernel(M, *shape, R_LORA)] * ((M + 15) // 16) for M in MS for shape in (UP, DOWN))
 
-    def op_quantize(self):
+    def op_quantize(self, frozen=False):
         for n in ("up", "down"):
             codes, scales, ts = self.qbuf[n]
-            self.nv.nvfp4_quantize(self.w[n], codes, scales, ts, False, self.ws)
+            if frozen:  # the tensor scale of the resident replica, used as given
+                ts = self.rep[0][n].tensor_scale
+            self.nv.nvfp4_quantize(self.w[n], codes, scales, ts, frozen, self.ws)
 
     def op_gemm(self, M, i):
         R = len(self.rep)
@@ -363,20 +365,22 @@ def run_gpu(args):
     total_ms = max_over_ranks(torch, dist, total_ms, dev, world)
     clocks = sampler.stop()
 
-    # per-operation device times, each operation kind in graphs of its own
-    def op_runs(fn_of_i):
-        if graphs:
-            gs = [capture(torch, lambda i=i: fn_of_i(i)) for i in range(R)]
-            if all(g is not None for g in gs):
-                return [g.replay for g in gs]
-        return [lambda i=i: fn_of_i(i) for i in range(R)]
+    # per-operation device times: each operation kind repeated over the whole
+    # replica ring in one graph (back to back, as the calls of a decode step
+    # run), time per call
+    def op_time(fn_of_i, calls_per_i):
+        seq = lambda: [fn_of_i(i) for i in range(R)]
+        g = capture(torch, seq) if graphs else None
+        run = g.replay if g is not None else seq
+        reps = max(3, args.steps // 4)
+        return time_replays(torch, [run], reps) / (R * calls_per_i)
 
-    reps = max(args.steps, 2 * R)
     kb = {}
-    kb["quantize"] = time_replays(torch, op_runs(lambda i: wl.op_quantize()), reps) / 2
+    kb["quantize"] = op_time(lambda i: wl.op_quantize(), 2)
+    kb["quantize_frozen"] = op_time(lambda i: wl.op_quantize(frozen=True), 2)
     for M in MS:
-        kb[f"gemm_M{M}"] = time_replays(torch, op_runs(lambda i, M=M: wl.op_gemm(M, i)), reps) / 2
-    kb["round_scales"] = time_replays(torch, op_runs(lambda i: wl.op_round()), reps) / 2
+        kb[f"gemm_M{M}"] = op_time(lambda i, M=M: wl.op_gemm(M, i), 2)
+    kb["round_scales"] = op_time(lambda i: wl.op_round(), 2)
     st = nv.nvfp4_get_device_status(wl.ws)
     if st != nv.OK:
         raise RuntimeError(f"device status after timing: {nv.status_string(st)}")
@@ -414,10 +418,11 @@ def run_gpu(args):
         per_kernel[f"gemm_M{M}"] = {"mean_us": round(us, 2), "GB/s": round(b / us / 1e3, 1),
                                     "TFLOP/s": round(f / us / 1e6, 2),
                                     "frac_hbm": round(b / us / 1e3 / peak_hbm, 4)}
-    q_us = kb["quantize"] * 1e3
     qb = sum(quant_bytes(*s) for s in (UP, DOWN)) / 2
-    per_kernel["quantize"] = {"mean_us": round(q_us, 2), "GB/s": round(qb / q_us / 1e3, 1),
-                              "frac_hbm": round(qb / q_us / 1e3 / peak_hbm, 4)}
+    for key in ("quantize", "quantize_frozen"):
+        q_us = kb[key] * 1e3
+        per_kernel[key] = {"mean_us": round(q_us, 2), "GB/s": round(qb / q_us / 1e3, 1),
+                           "frac_hbm": round(qb / q_us / 1e3 / peak_hbm, 4)}
     r_us = kb["round_scales"] * 1e3
     rb = sum(round_bytes(*s) for s in (UP, DOWN)) / 2
     per_kernel["round_scales"] = {"mean_us": round(r_us, 2), "GB/s": round(rb / r_us / 1e3, 1)}
@@ -437,6 +442,12 @@ def run_gpu(args):
         "gpu_launches": wl.launches_per_step * args.steps,
     }
     if rank == 0:
+        if not args.no_configs:
+            line["configs"] = {
+                "single_layer_512x2048": run_single_layer(torch, nv, synth),
+                "qwen2.5-32b-mlp-decode": run_qwen32b(torch, nv, synth, peak_hbm),
+                "qwen2.5-7b-whole-stack-M8": run_whole_stack(torch, nv, synth, peak_hbm),
+            }
         if not args.no_prefill:
             line["prefill"] = run_prefill_case(torch, nv, synth, peak_tf)
         if not args.no_cpu_baseline:
@@ -445,6 +456,140 @@ def run_gpu(args):
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()
+
+
+def graph_time_per_call(torch, seq, ncalls, reps=5):
+    """Device time per call of seq() (ncalls calls) replayed as one CUDA graph."""
+    g = capture(torch, seq)
+    run = g.replay if g is not None else seq
+    run()
+    torch.cuda.synchronize()
+    return time_replays(torch, [run], reps) / ncalls
+
+
+def run_single_layer(torch, nv, synth):
+    """The 512 x 2048 layer, 4 tokens, LoRA r = 16, s = 2, noise sigma 1e-2: its
+    0.59 MB of weights stay in L2, so the call is launch-bound: microseconds
+    per call, no roofline."""
+    c = synth.single_layer_case()
+    dev = lambda b: torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(torch.bfloat16).cuda()
+    q = nv.quantize(dev(c.w))
+    M, K = c.x.shape
+    N = c.w.shape[0]
+    x, a, b = dev(c.x), dev(c.a), dev(c.b)
+    z = torch.from_numpy(c.z).cuda()
+    y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    ws = nv.new_workspace(nv.nvfp4_workspace_bytes(M, N, K, 16))
+    n = 64
+    seq = lambda: [nv.nvfp4_w4a16_lora_gemm(x, q.codes, q.scales, q.tensor_scale, a, b, c.lora_scale, z, y, ws)
+                   for _ in range(n)]
+    ms = graph_time_per_call(torch, seq, n)
+    return {"M": M, "N": N, "K": K, "lora_rank": 16, "us_per_call": round(ms * 1e3, 2),
+            "kernel": nv.gemm_kernel(M, N, K, 16), "timing": f"graph of {n} back-to-back calls"}
+
+
+def _student_t_device(torch, shape, scale, nu, seed):
+    """Seeded Student-t(nu) * scale drawn on the device (normal / sqrt(chi2_nu / nu)),
+    rounded to bf16; nu is an integer here (4)."""
+    g = torch.Generator(device="cuda").manual_seed(seed)
+    zz = torch.randn(shape, generator=g, device="cuda")
+    chi2 = torch.zeros(shape, device="cuda")
+    for _ in range(int(nu)):
+        chi2 += torch.randn(shape, generator=g, device="cuda") ** 2
+    return (zz / torch.sqrt(chi2 / nu) * scale).to(torch.bfloat16)
+
+
+def run_qwen32b(torch, nv, synth, peak_hbm):
+    """Qwen2.5-32B-shaped MLP decode: W 27648 x 5120 and 5120 x 27648 =
+    0.02 Student-t(4), M in {1, 8}, LoRA r = 64, noise sigma 5e-4.  Each
+    projection is quantised into 4 replicas (0.64 GB in all, > 2x L2) and the
+    calls rotate through them, up and down alternating, in one graph."""
+    r, R = 64, 4
+    up, down = synth.QWEN32B_UP, synth.QWEN32B_DOWN
+    dev = lambda b: torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(torch.bfloat16).cuda()
+    ws = nv.new_workspace(max(nv.nvfp4_workspace_bytes(16, *sh, r) for sh in (up, down)))
+    reps, lora, zs = {}, {}, {}
+    for name, sh, seed in (("up", up, 300), ("down", down, 400)):
+        w = _student_t_device(torch, sh, 0.02, 4, seed)
+        reps[name] = [nv.quantize(w, workspace=ws) for _ in range(R)]
+        del w
+        a, b = synth.lora_pair(sh[0], sh[1], r, 0.01, seed + 2)
+        lora[name] = (dev(a), dev(b))
+        zs[name] = torch.from_numpy(synth.noise_vector(sh[1], SIGMA, seed + 3)).cuda()
+    out = {"layers": {"up": list(up), "down": list(down)}, "lora_rank": r, "replicas": R}
+    for M in (1, 8):
+        xs = {n: dev(synth.activations(M, sh[1], 500 + M)) for n, sh in (("up", up), ("down", down))}
+        ys = {n: torch.empty((M, sh[0]), dtype=torch.float32, device="cuda") for n, sh in (("up", up), ("down", down))}
+
+        def seq():
+            for i in range(R):
+                for n in ("up", "down"):
+                    q = reps[n][i]
+                    a, b = lora[n]
+                    nv.nvfp4_w4a16_lora_gemm(xs[n], q.codes, q.scales, q.tensor_scale, a, b, LORA_SCALE, zs[n],
+                                             ys[n], ws)
+        ms = graph_time_per_call(torch, seq, 2 * R)
+        nbytes = sum(gemm_bytes(M, *sh, r) for sh in (up, down)) / 2
+        flops = sum(gemm_flops(M, *sh, r) for sh in (up, down)) / 2
+        out[f"gemm_M{M}"] = {"mean_us": round(ms * 1e3, 2), "GB/s": round(nbytes / ms / 1e6, 1),
+                             "TFLOP/s": round(flops / ms / 1e9, 2),
+                             "frac_hbm": round(nbytes / ms / 1e6 / peak_hbm, 4),
+                             "alg_bytes_per_call": nbytes}
+    st = nv.nvfp4_get_device_status(ws)
+    if st != nv.OK:
+        raise RuntimeError(f"device status after the 32B decode: {nv.status_string(st)}")
+    return out
+
+
+STACK_SHAPES = [("q", 3584, 3584), ("k", 512, 3584), ("v", 512, 3584), ("o", 3584, 3584),
+                ("gate", 18944, 3584), ("up", 18944, 3584), ("down", 3584, 18944)]
+
+
+def run_whole_stack(torch, nv, synth, peak_hbm, layers=28, M=8):
+    """28 Qwen2.5-7B-shaped layers (196 matrices, bf16 ~N(0, 0.02^2) drawn on
+    the device, seed 1000 * layer + matrix), each quantised with its own
+    dynamic tensor scale (3.67 GB of codes and scales), then one decode sweep
+    of the 196 W4A16 GEMMs with the same 8 tokens (no LoRA, no noise), as one
+    graph.  The sweep reads 3.67 GB, far more than L2."""
+    dev = lambda b: torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(torch.bfloat16).cuda()
+    ws = nv.new_workspace(max(nv.nvfp4_workspace_bytes(M, N, K, 0) for _, N, K in STACK_SHAPES))
+    xs = {K: dev(synth.activations(M, K, 70 + K)) for K in (3584, 18944)}
+    gen = torch.Generator(device="cuda")
+    qs, ys = [], []
+    qbytes = 0.0
+    quant_ms = 0.0
+    for layer in range(layers):
+        for j, (name, N, K) in enumerate(STACK_SHAPES):
+            gen.manual_seed(1000 * layer + j)
+            w = (torch.randn((N, K), generator=gen, device="cuda") * 0.02).to(torch.bfloat16)
+            codes = torch.empty((N, K // 2), dtype=torch.uint8, device="cuda")
+            scales = torch.empty((N, K // 16), dtype=torch.uint8, device="cuda")
+            ts = torch.zeros(1, dtype=torch.float32, device="cuda")
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            nv.nvfp4_quantize(w, codes, scales, ts, False, ws)
+            e1.record()
+            torch.cuda.synchronize()
+            quant_ms += e0.elapsed_time(e1)
+            qbytes += quant_bytes(N, K)
+            qs.append((nv.QuantizedWeight(codes, scales, ts), K))
+            ys.append(torch.empty((M, N), dtype=torch.float32, device="cuda"))
+            del w
+
+    def seq():
+        for (q, K), y in zip(qs, ys):
+            nv.nvfp4_w4a16_lora_gemm(xs[K], q.codes, q.scales, q.tensor_scale, None, None, 0.0, None, y, ws)
+    ms = graph_time_per_call(torch, seq, 1, reps=3)
+    st = nv.nvfp4_get_device_status(ws)
+    if st != nv.OK:
+        raise RuntimeError(f"device status after the whole-stack sweep: {nv.status_string(st)}")
+    nbytes = sum(gemm_bytes(M, N, K, 0) for _ in range(layers) for _, N, K in STACK_SHAPES)
+    return {"layers": layers, "matrices": len(qs), "M": M,
+            "sweep_ms": round(ms, 4), "sweep_GB/s": round(nbytes / ms / 1e6, 1),
+            "sweep_frac_hbm": round(nbytes / ms / 1e6 / peak_hbm, 4), "sweep_alg_bytes": nbytes,
+            "quantize_all_ms": round(quant_ms, 3), "quantize_GB/s": round(qbytes / quant_ms / 1e6, 1),
+            "timing": "one graph of the 196 GEMM calls; quantisation timed per matrix (events)"}
 
 
 def run_prefill_case(torch, nv, synth, peak_tf):
@@ -493,13 +638,10 @@ def run_e2e(torch, nv, wl, dev, args):
         for n in ("up", "down"):
             codes, scales, ts = wl.qbuf[n]
             nv.nvfp4_quantize(dev_in[("w", n)], codes, scales, ts, False, wl.ws)
-        R = len(wl.rep)
-        j = 0
-        for M in MS:
+        for M in MS:  # the GEMMs multiply by the weights just quantised
             for n in ("up", "down"):
-                q = wl.rep[(i * 8 + j) % R][n]
-                j += 1
-                nv.nvfp4_w4a16_lora_gemm(dev_in[("x", n, M)], q.codes, q.scales, q.tensor_scale,
+                codes, scales, ts = wl.qbuf[n]
+                nv.nvfp4_w4a16_lora_gemm(dev_in[("x", n, M)], codes, scales, ts,
                                          dev_in[("a", n)], dev_in[("b", n)], LORA_SCALE,
                                          dev_in[("z", n)], wl.y[(n, M)], wl.ws)
         for n in ("up", "down"):
@@ -551,11 +693,19 @@ def oracle_sample_step(oracle, inputs, nthreads):
     return total
 
 
+def nproc():
+    """Cores this process may run on (what `nproc` prints)."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        return os.cpu_count() or 1
+
+
 def cpu_baseline(seconds=15.0):
     import oracle
     from nvfp4_weight_only_02_gb300 import synth
     oracle.build()
-    cores = os.cpu_count() or 1
+    cores = nproc()
     # calibrate on a small sample, then size the sample to about `seconds`
     small = oracle_sample_inputs(synth, 64, 12)
     t0 = time.perf_counter()
@@ -568,6 +718,7 @@ def cpu_baseline(seconds=15.0):
     b = oracle_sample_step(oracle, inputs, cores)
     dt = time.perf_counter() - t0
     return {"value": round(b / dt / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "hardware_concurrency": os.cpu_count(), "nproc": nproc(),
             "seconds": round(dt, 2),
             "sample": f"every step operation on {rows_up} of {UP[0]} up rows and {rows_down} of "
                       f"{DOWN[0]} down rows (all M, same K, r, noise)"}
@@ -580,7 +731,7 @@ def run_reference(args):
     import oracle
     from nvfp4_weight_only_02_gb300 import synth
     oracle.build()
-    cores = os.cpu_count() or 1
+    cores = nproc()
     rows_up, rows_down = 256, 48
     inputs = oracle_sample_inputs(synth, rows_up, rows_down)
     for _ in range(args.warmup):
@@ -603,7 +754,7 @@ def run_reference(args):
         "config": {"workload": WORKLOAD, "layers": {"up": list(UP), "down": list(DOWN)}, "M": list(MS),
                    "lora_rank": R_LORA, "noise_sigma": SIGMA},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
-                         "sample": sample},
+                         "hardware_concurrency": os.cpu_count(), "nproc": nproc(), "sample": sample},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -653,6 +804,19 @@ def run_kernel_case(case, reps):
           f"{nbytes / us / 1e3:.1f} GB/s, {flops / us / 1e6:.1f} TFLOP/s")
 
 
+def free_port():
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        return sk.getsockname()[1]
+
+
+def replica_command(argv, n, port):
+    """The command that runs this benchmark as n single-GPU ranks on 127.0.0.1."""
+    return [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+            "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.abspath(__file__), *argv]
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--kernel-case", default=None,
@@ -665,10 +829,15 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--eager", action="store_true", help="time eager launches instead of CUDA graphs")
     ap.add_argument("--no-prefill", action="store_true", help="skip the 16384-token tensor-core GEMM line")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the single-layer, 32B-decode and whole-stack lines")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ and not args.kernel_case:
+        # N replicas: one process per GPU, started the way the driver does
+        sys.exit(subprocess.call(replica_command(sys.argv[1:], args.gpus, free_port())))
     if args.kernel_case:
         run_kernel_case(args.kernel_case, args.reps)
     elif args.impl == "reference":

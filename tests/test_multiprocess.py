@@ -61,3 +61,13 @@ def test_reference_arm_prints_on_rank0_only(capsys, monkeypatch):
         steps, warmup = 1, 3
     bench.run_reference(Args())
     assert capsys.readouterr().out == ""
+
+
+def test_replica_command_starts_one_rank_per_gpu():
+    """--gpus N without a launcher re-runs the benchmark as N ranks on 127.0.0.1."""
+    cmd = bench.replica_command(["--gpus", "4", "--steps", "5"], 4, 29511)
+    assert cmd[1:4] == ["-m", "torch.distributed.run", "--nnodes=1"]
+    assert "--nproc-per-node=4" in cmd
+    assert cmd[cmd.index("--master-addr") + 1] == "127.0.0.1"
+    assert cmd[cmd.index("--master-port") + 1] == "29511"
+    assert cmd[-4:] == ["--gpus", "4", "--steps", "5"] and cmd[-5].endswith("bench.py")
