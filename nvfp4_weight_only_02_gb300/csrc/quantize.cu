@@ -104,6 +104,37 @@ __device__ __forceinline__ bool fast_quotient_domain(float S)
     return S >= 0x1p-96f && S <= 0x1p96f;
 }
 
+// L2 eviction-priority hints for loads (per instruction; no device setting).
+__device__ __forceinline__ uint64_t l2_policy_evict_last()
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_first()
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+__device__ __forceinline__ uint4 ld_hint_u4(const void *p, uint64_t pol)
+{
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p), "l"(pol));
+    return v;
+}
+
+// Max of the eight bf16 magnitudes of a vector, as magnitude bits (packed pair).
+__device__ __forceinline__ uint32_t absmax_vec2(uint4 v)
+{
+    const uint32_t m = 0x7FFF7FFFu;
+    return __vmaxu2(__vimax3_u16x2(v.x & m, v.y & m, v.z & m), v.w & m);
+}
+
 // Four packed E2M1 bytes from eight signed quotients (element 2i in the low
 // nibble of byte i); round to nearest even, saturating, sign kept (-0 -> 0x8).
 __device__ __forceinline__ uint32_t e2m1x8_pack(const float q[8])
@@ -206,13 +237,18 @@ __global__ void __launch_bounds__(256) quantize_kernel(const uint4 *__restrict__
 
 // ------------------------------------------------------------------ fused dynamic quantise
 // Dynamic mode in one persistent cooperative kernel: pass 1 reads the block's
-// contiguous share of W once for the tensor amax and keeps the last
-// kFusedCacheBlocks 16-element blocks of the share in shared memory; after
-// one grid barrier, pass 2 quantises the share from its end backwards, so it
-// starts with the blocks held in shared memory and continues with those
-// pass 1 read last, which are the ones still in L2.
+// contiguous share of W once for the tensor amax -- consecutive lanes on
+// consecutive 16-byte vectors, six loads in flight per thread -- and keeps
+// the last kFusedCacheBlocks 16-element blocks of the share in shared memory;
+// its other loads ask L2 to keep their lines (evict-last), since pass 2 reads
+// them again.  After one grid barrier, pass 2 quantises the share from its
+// end backwards, one 16-element block per thread and two blocks in flight, so
+// it starts with the blocks held in shared memory and continues with those
+// pass 1 read last, which are the likeliest still to be in L2 (those loads
+// are the last use: evict-first).
 constexpr int kFusedThreads = 1024;
 constexpr int kFusedCacheBlocks = 6144;  // 192 KB of bf16 per block
+constexpr int kFusedInFlight = 6;
 
 __device__ __forceinline__ void quantize_block(uint4 v0, uint4 v1, float s_t, float d, bool d_fast, float rd,
                                                const float *s_S, const float *s_R, uint2 &cw_out,
@@ -257,27 +293,22 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     const int64_t cache_from = max(b0, b1 - (int64_t)kFusedCacheBlocks);
 
     // pass 1: amax of the share; keep its tail in shared memory
+    const uint64_t keep = l2_policy_evict_last(), drop = l2_policy_evict_first();
+    const int64_t v0 = 2 * b0, v1 = 2 * b1, cache_vfrom = 2 * cache_from;
     uint32_t m = 0;
-    int64_t b = b0 + tid;
-    for (; b + kFusedThreads < b1; b += 2 * kFusedThreads) {
-        const uint4 a0 = ld_stream_u4(w + 2 * b), a1 = ld_stream_u4(w + 2 * b + 1);
-        const uint4 c0 = ld_stream_u4(w + 2 * (b + kFusedThreads)), c1 = ld_stream_u4(w + 2 * (b + kFusedThreads) + 1);
-        m = __vmaxu2(m, __vmaxu2(absmax8(a0, a1), absmax8(c0, c1)));
-        if (b >= cache_from) {
-            s_cache[2 * (b - cache_from)] = a0;
-            s_cache[2 * (b - cache_from) + 1] = a1;
+    for (int64_t i = v0 + tid; i < v1; i += (int64_t)kFusedThreads * kFusedInFlight) {
+        uint4 v[kFusedInFlight];
+#pragma unroll
+        for (int k = 0; k < kFusedInFlight; k++) {
+            const int64_t ik = i + (int64_t)k * kFusedThreads;
+            v[k] = ik < v1 ? ld_hint_u4(w + ik, ik >= cache_vfrom ? drop : keep) : make_uint4(0u, 0u, 0u, 0u);
         }
-        if (b + kFusedThreads >= cache_from) {
-            s_cache[2 * (b + kFusedThreads - cache_from)] = c0;
-            s_cache[2 * (b + kFusedThreads - cache_from) + 1] = c1;
-        }
-    }
-    for (; b < b1; b += kFusedThreads) {
-        const uint4 a0 = ld_stream_u4(w + 2 * b), a1 = ld_stream_u4(w + 2 * b + 1);
-        m = __vmaxu2(m, absmax8(a0, a1));
-        if (b >= cache_from) {
-            s_cache[2 * (b - cache_from)] = a0;
-            s_cache[2 * (b - cache_from) + 1] = a1;
+#pragma unroll
+        for (int k = 0; k < kFusedInFlight; k++) {
+            const int64_t ik = i + (int64_t)k * kFusedThreads;
+            m = __vmaxu2(m, absmax_vec2(v[k]));
+            if (ik >= cache_vfrom && ik < v1)
+                s_cache[ik - cache_vfrom] = v[k];
         }
     }
     m = max(m & 0xFFFFu, m >> 16);
@@ -318,21 +349,36 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     const float rd = d_fast ? __frcp_rn(d) : 0.0f;
     __syncthreads();
 
-    // pass 2: from the end of the share backwards
-    for (int64_t bb = b1 - 1 - tid; bb >= b0; bb -= kFusedThreads) {
-        uint4 v0, v1;
+    // pass 2: from the end of the share backwards, two blocks in flight per thread
+    for (int64_t bb = b1 - 1 - tid; bb >= b0; bb -= 2 * kFusedThreads) {
+        const int64_t bc = bb - kFusedThreads;
+        uint4 v0a, v1a, v0b = make_uint4(0u, 0u, 0u, 0u), v1b = v0b;
         if (bb >= cache_from) {
-            v0 = s_cache[2 * (bb - cache_from)];
-            v1 = s_cache[2 * (bb - cache_from) + 1];
+            v0a = s_cache[2 * (bb - cache_from)];
+            v1a = s_cache[2 * (bb - cache_from) + 1];
         } else {
-            v0 = ld_stream_u4(w + 2 * bb);
-            v1 = ld_stream_u4(w + 2 * bb + 1);
+            v0a = ld_hint_u4(w + 2 * bb, drop);
+            v1a = ld_hint_u4(w + 2 * bb + 1, drop);
+        }
+        if (bc >= b0) {
+            if (bc >= cache_from) {
+                v0b = s_cache[2 * (bc - cache_from)];
+                v1b = s_cache[2 * (bc - cache_from) + 1];
+            } else {
+                v0b = ld_hint_u4(w + 2 * bc, drop);
+                v1b = ld_hint_u4(w + 2 * bc + 1, drop);
+            }
         }
         uint2 cw;
         uint32_t e;
-        quantize_block(v0, v1, s_t, d, d_fast, rd, s_S, s_R, cw, e, ctl);
+        quantize_block(v0a, v1a, s_t, d, d_fast, rd, s_S, s_R, cw, e, ctl);
         codes[bb] = cw;
         scales[bb] = (uint8_t)e;
+        if (bc >= b0) {
+            quantize_block(v0b, v1b, s_t, d, d_fast, rd, s_S, s_R, cw, e, ctl);
+            codes[bc] = cw;
+            scales[bc] = (uint8_t)e;
+        }
     }
 
     // the last block out leaves the amax word at zero for the next call
