@@ -113,8 +113,11 @@ nvfp4_status nvfp4_dequantize(const uint8_t *codes, const uint8_t *scales_e4m3,
  * Accumulation is FP32.  M < 64 takes a weight-streaming decode path (per
  * 16 tokens: an activation-preparation kernel, then the GEMM kernel, chained
  * by programmatic dependent launch); M >= 64 takes the tensor-core (tcgen05)
- * prefill kernel, whose workspace holds an f16 copy of v(q) dec(e) (2 N K
- * bytes); nvfp4_gemm_kernel() says which.
+ * prefill kernel, whose workspace holds a bf16 copy of v(q) dec(e) (2 N K
+ * bytes) and of X' (2 M K bytes); nvfp4_gemm_kernel() says which.  Any
+ * finite tensor scale works on both paths, subnormal ones included: where
+ * s / s_t leaves [2^-40, 2^40] the prefill kernel accumulates the LoRA term
+ * apart from the weights' term.
  * workspace: nvfp4_workspace_bytes(M, N, K, r) bytes. */
 nvfp4_status nvfp4_w4a16_lora_gemm(const void *x_bf16, int64_t M, int64_t N, int64_t K,
                                    const uint8_t *codes, const uint8_t *scales_e4m3,

@@ -135,6 +135,63 @@ __device__ __forceinline__ float scale_pow2(float x, int e)
 }
 
 // ---------------------------------------------------------------- memory
+// L2 eviction-priority hints for loads (per instruction; no device setting).
+__device__ __forceinline__ uint64_t l2_policy_evict_last()
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_first()
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+__device__ __forceinline__ uint4 ld_hint_u4(const void *p, uint64_t pol)
+{
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p), "l"(pol));
+    return v;
+}
+
+// 16-byte global -> shared copy that bypasses registers (cp.async); src_bytes
+// 0 writes zeros and reads nothing.  Completion: cp_async_commit groups the
+// copies issued so far, cp_async_wait<n> waits until at most n groups are
+// still in flight.
+__device__ __forceinline__ void cp_async16(void *smem_dst, const void *src, uint32_t src_bytes, uint64_t pol)
+{
+    const uint32_t d = (uint32_t)__cvta_generic_to_shared(smem_dst);
+    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;" ::"r"(d), "l"(src),
+                 "r"(src_bytes), "l"(pol)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+
+template <int N>
+__device__ __forceinline__ void cp_async_wait()
+{
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Programmatic dependent launch: let the next kernel in the stream start its
+// prologue / wait until every prerequisite grid has finished and its memory
+// is visible.
+__device__ __forceinline__ void pdl_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void pdl_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 __device__ __forceinline__ uint4 ld_stream_u4(const void *p)
 {
     uint4 v;

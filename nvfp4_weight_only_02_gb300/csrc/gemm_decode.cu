@@ -69,16 +69,6 @@ __device__ __forceinline__ float bf16_round(float v)
     return __bfloat162float(__float2bfloat16_rn(v));
 }
 
-__device__ __forceinline__ void pdl_launch_dependents()
-{
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-
-__device__ __forceinline__ void pdl_wait()
-{
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-}
-
 // X' f16 layout, in 16-byte chunks: stage s (256 columns), token n, lane
 // slot t (64 columns), chunk q (8 columns), with the chunk index XORed by
 // (4n + t) mod 8 so that the B-fragment loads of a quarter warp hit 8

@@ -6,21 +6,30 @@
 // 16-bit).  With thousands of tokens the product is a dense contraction, so
 // it runs on tcgen05 MMAs with the accumulator in tensor memory.
 //
-// Four kernels per call:
-//   * dequantise W once into f16, v(q) * dec(e) (exact in f16: at most 6
+// Three kernels per call:
+//   * dequantise W once into bf16, v(q) * dec(e) (exact: at most 6
 //     significant bits, 2^-10 <= |value| <= 2688; s_t is applied in the
 //     epilogue), and lay out the LoRA B operand for the tensor core;
-//   * X' = bf16(X z) re-expressed per token as f16 * 2^p_m (the token's
-//     largest |X'| in [2^14, 2^15); exact for every value within 2^28 of it);
-//   * T = X' A^T (fp32, bf16 mma.sync), stored pre-scaled by s / c_m with
-//     c_m = s_t 2^p_m as a hi + lo pair of bf16 (2^-16 relative);
-//   * the GEMM: TMA brings 128 x 64 tiles of X' and 256 x 64 tiles of W into
+//   * the token side, in one pass over X: X'' = bf16(X z) 2^-p_m (bf16,
+//     exact), p_m = 0 unless the token's largest |X'| is outside
+//     [2^-64, 2^32], which keeps every product and partial sum of the GEMM
+//     far inside the FP32 range, and T'' = X'' A^T (fp32, bf16 mma.sync),
+//     stored as a hi + lo pair of bf16 (2^-16 relative), pre-multiplied by
+//     rho = s / s_t when the LoRA term shares the accumulator with the
+//     weights' term (see below);
+//   * the GEMM: TMA brings 128 x 64 tiles of X'' and 256 x 64 tiles of W into
 //     a 4-deep ring (128-byte swizzle); one thread issues tcgen05.mma
-//     kind::f16 (f16 operands) over K, then one or two extra K-steps of bf16
-//     MMAs of [T hi | T lo] against [B | B] into the same TMEM accumulator, so
-//     acc = X' 2^-p W^T + s T B^T / c_m and the epilogue only computes
-//     c_m * acc, converts and stores.  Two 128 x 256 fp32 accumulators in TMEM
-//     (512 columns) let the epilogue of one tile overlap the next tile.
+//     kind::f16 with bf16 operands over K, then one or two extra K-steps of
+//     MMAs of [T'' hi | T'' lo] against [B | B].  Two 128 x 256 fp32
+//     accumulators in TMEM (512 columns).
+// Fused mode (2^-40 <= |s / s_t| <= 2^40, every practical case): the extra
+// K-steps go into the same accumulator, acc = X' 2^-p W^T/s_t + rho T'' B^T,
+// Y = s_t 2^p_m acc, and the epilogue of one tile overlaps the next tile's
+// MMAs.  Split mode (a tensor scale far from s, e.g. weights near 1e-36, where
+// rho T'' would leave the FP32 range): the extra K-steps accumulate T'' B^T in
+// the second TMEM accumulator and the epilogue forms
+// s_t 2^p_m acc_W + s 2^p_m acc_T, each factor applied as mantissa times an
+// exact power of two, so any finite s_t works; one tile at a time.
 // Roles in a block of 6 warps (persistent over 128 x 256 output tiles):
 //   warps 0-3  epilogue (one TMEM lane = one output row per thread);
 //   warp 4     TMA producer;  warp 5  TMEM allocation and MMA issue.
@@ -39,7 +48,7 @@ using namespace sm100;
 
 constexpr int kPfBM = 128;         // tokens per tile
 constexpr int kPfBN = 256;         // weight rows per tile
-constexpr int kPfBK = 64;          // K per stage (128 bytes of f16)
+constexpr int kPfBK = 64;          // K per stage (128 bytes of bf16)
 constexpr int kPfStages = 4;
 constexpr int kPfThreads = 192;
 constexpr int kPfGroupN = 8;       // tile raster: n-tiles per group
@@ -51,82 +60,49 @@ constexpr size_t kPfSmem = 1024 + kPfStages * (kPfABytes + kPfBBytes) + 256;
 struct PrefillParams {
     int M, N, K, ES;          // ES: extra K-steps of 64 for the LoRA term (0, 1 or 2)
     const float *tensor_scale;
-    const float *fac;         // M: 2^p_m
+    float lora_scale;         // s
+    const int *pexp;          // M: p_m
     void *y;
     int y_fp32;
     uint32_t *ctl;
     int mtiles, ntiles;
 };
 
-// c_m = s_t 2^p_m, the factor between the accumulator and Y (1 where it is
-// zero: then either the row of X' or every weight is zero)
-__device__ __forceinline__ float row_factor(float s_t, float fac_m)
+// Whether the LoRA term shares the accumulator with the weights' term, in
+// units of s_t 2^p_m: then T'' is stored times rho = s / s_t, which must keep
+// the products rho T'' B far inside the FP32 range.  s_t = 0 (every weight
+// zero) counts as 1.  NaN or an infinite rho selects the split mode.
+__device__ __forceinline__ bool lora_fused(float s, float s_t)
 {
-    const float c = __fmul_rn(s_t != 0.0f ? s_t : 1.0f, fac_m);
-    return c != 0.0f ? c : 1.0f;
+    if (s == 0.0f)
+        return true;
+    const float rho = fabsf(__fdiv_rn(s, s_t != 0.0f ? s_t : 1.0f));
+    return rho >= 0x1p-40f && rho <= 0x1p40f;
 }
+
+// Multiplies accumulator values by f 2^p (f = m 2^e, m in [0.5, 1)) without
+// forming a subnormal or infinite intermediate: one rounding of m * v, then an
+// exact power of two, which rounds again only where Y itself is subnormal.
+struct RowScale {
+    float c;     // m 2^(e + p) when that is a normal float, else m
+    int ce;      // e + p
+    bool direct;
+    __device__ __forceinline__ void set(float f, int p)
+    {
+        int e;
+        const float m = frexpf(f, &e);
+        ce = e + p;
+        direct = ce >= -125 && ce <= 127;
+        c = direct ? __fmul_rn(m, exp2i(ce)) : m;
+    }
+    __device__ __forceinline__ float apply(float v) const
+    {
+        const float t = __fmul_rn(c, v);
+        return direct ? t : scale_pow2(t, ce);
+    }
+};
 
 // ---------------------------------------------------------------- prologue
-// One warp per token: X' = bf16(X z), its max, and X' 2^-p as f16.
-__global__ void __launch_bounds__(256) prefill_xprime_kernel(const uint16_t *__restrict__ x,
-                                                             const float *__restrict__ z, int M, int K,
-                                                             __half *__restrict__ xh, float *__restrict__ fac)
-{
-    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
-    if (warp >= M)
-        return;
-    const uint16_t *row = x + (size_t)warp * K;
-    auto xprime8 = [&](int k, float (&v)[8]) {
-        const uint4 xb = *reinterpret_cast<const uint4 *>(row + k);
-        const uint32_t w[4] = {xb.x, xb.y, xb.z, xb.w};
-        float zz[8];
-        if (z) {
-            const float4 z0 = *reinterpret_cast<const float4 *>(z + k);
-            const float4 z1 = *reinterpret_cast<const float4 *>(z + k + 4);
-            zz[0] = z0.x; zz[1] = z0.y; zz[2] = z0.z; zz[3] = z0.w;
-            zz[4] = z1.x; zz[5] = z1.y; zz[6] = z1.z; zz[7] = z1.w;
-        }
-#pragma unroll
-        for (int i = 0; i < 8; i++) {
-            float f = bf16_bits_to_f32((w[i / 2] >> (16 * (i & 1))) & 0xFFFFu);
-            if (z)
-                f = __bfloat162float(__float2bfloat16_rn(__fmul_rn(f, zz[i])));
-            v[i] = f;
-        }
-    };
-    float mx = 0.0f;
-    for (int k = lane * 8; k < K; k += 256) {
-        float v[8];
-        xprime8(k, v);
-#pragma unroll
-        for (int i = 0; i < 8; i++)
-            mx = fmaxf(mx, fabsf(v[i]));
-    }
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1)
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-    int pexp = 0;
-    if (mx > 0.0f) {
-        const uint32_t b = __float_as_uint(mx);
-        const int e = (b >> 23) ? (int)(b >> 23) - 127 : (31 - __clz(b)) - 149;
-        pexp = e - 14;
-    }
-    for (int k = lane * 8; k < K; k += 256) {
-        float v[8];
-        xprime8(k, v);
-        uint32_t hw[4];
-#pragma unroll
-        for (int i = 0; i < 4; i++) {
-            __half2 h2 = __halves2half2(__float2half_rn(scale_pow2(v[2 * i], -pexp)),
-                                        __float2half_rn(scale_pow2(v[2 * i + 1], -pexp)));
-            hw[i] = *reinterpret_cast<uint32_t *>(&h2);
-        }
-        *reinterpret_cast<uint4 *>(xh + (size_t)warp * K + k) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-    }
-    if (lane == 0)
-        fac[warp] = exp2i(pexp);
-}
-
 // Column of the LoRA extension operand that holds T'[.][j] (part 0 = hi,
 // 1 = lo): r <= 32 uses one 64-column step [hi | lo], r <= 64 two steps.
 __device__ __forceinline__ int ext_col(int j, int part, int ES)
@@ -134,7 +110,8 @@ __device__ __forceinline__ int ext_col(int j, int part, int ES)
     return ES == 1 ? 32 * part + j : 64 * part + j;
 }
 
-// f16x2 -> bf16x2, exact for the values X' 2^-p (at most 8 significant bits).
+// f16x2 -> bf16x2, exact for values with at most 8 significant bits in the
+// normal range (the dequantised weights v(q) dec(e)).
 __device__ __forceinline__ uint32_t h2_to_bf2(uint32_t h)
 {
     const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&h));
@@ -142,84 +119,302 @@ __device__ __forceinline__ uint32_t h2_to_bf2(uint32_t h)
     return *reinterpret_cast<uint32_t *>(&o);
 }
 
-// The LoRA term in the accumulator's units: T' = s T / c_m = (s / s_t)
-// X'' A^T with X'' = X' 2^-p, the f16 rows the GEMM reads (exact in bf16),
-// written as bf16 hi + lo at the extension columns.  A block takes 64 tokens
-// (one warp per 16, up to 64 LoRA columns) and walks K in steps of 64,
-// staging those columns of X'' and of A in shared memory (the next step's
-// loads are in flight while the current one is multiplied); bf16 mma.sync,
-// FP32 accumulate.  ta (M x 64 ES bf16) must be zero elsewhere.
-constexpr int kLtRows = 64, kLtK = 64, kLtLd = kLtK + 8;  // padded rows: conflict-free fragments
-__global__ void __launch_bounds__(128) prefill_lora_ext_kernel(const __half *__restrict__ xh,
-                                                               const uint16_t *__restrict__ a, int M, int K,
-                                                               int r, int ES, float lora_scale,
-                                                               const float *__restrict__ tensor_scale,
-                                                               uint16_t *__restrict__ ta)
+// A pair of bf16 (even column in the low half) as floats, and back.
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+__device__ __forceinline__ uint32_t pack_bf2_rn(float lo, float hi)
 {
-    __shared__ __align__(16) uint16_t xs[kLtRows * kLtLd];
-    __shared__ __align__(16) uint16_t as[kPfMaxR * kLtLd];
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
-    const int m0 = blockIdx.x * kLtRows;
-    const int njt = (r + 7) / 8;
-    const uint16_t *x16 = reinterpret_cast<const uint16_t *>(xh);
-    // thread tid stages 16-byte pieces i = tid + 128 q: row i / 8, columns 8 (i % 8) ..
-    uint4 xv[4], av[4];
-    auto load = [&](int k0) {
+    uint32_t d;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t mul_bf2(uint32_t a, uint32_t b)
+{
+    uint32_t d;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// Largest |X z| over 8 columns, in FP32 (rounded to bf16 once per token:
+// rounding is monotonic, so that is the largest |X'|).
+__device__ __forceinline__ float absmax8(uint4 xb, const float *__restrict__ z, int k)
+{
+    const uint32_t w[4] = {xb.x, xb.y, xb.z, xb.w};
+    float v[8];
 #pragma unroll
-        for (int q = 0; q < 4; q++) {
-            const int i = tid + 128 * q, row = i >> 3, col = (i & 7) * 8;
-            xv[q] = m0 + row < M ? *reinterpret_cast<const uint4 *>(x16 + (size_t)(m0 + row) * K + k0 + col)
-                                 : make_uint4(0u, 0u, 0u, 0u);
-            av[q] = row < r ? *reinterpret_cast<const uint4 *>(a + (size_t)row * K + k0 + col)
-                            : make_uint4(0u, 0u, 0u, 0u);
+    for (int i = 0; i < 4; i++) {
+        v[2 * i] = bf_lo(w[i]);
+        v[2 * i + 1] = bf_hi(w[i]);
+    }
+    if (z) {
+        const float4 z0 = __ldg(reinterpret_cast<const float4 *>(z + k));
+        const float4 z1 = __ldg(reinterpret_cast<const float4 *>(z + k + 4));
+        const float zz[8] = {z0.x, z0.y, z0.z, z0.w, z1.x, z1.y, z1.z, z1.w};
+#pragma unroll
+        for (int i = 0; i < 8; i++)
+            v[i] = __fmul_rn(v[i], zz[i]);
+    }
+    float m = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; i++)
+        m = fmaxf(m, fabsf(v[i]));
+    return m;
+}
+
+// p_m for a token whose largest |X'| is mx: 0 inside [2^-64, 2^32], where
+// every product and partial sum of both GEMMs stays far inside the FP32
+// range; outside, e - 14 (e = exponent of mx), which puts mx in [2^14, 2^15).
+constexpr float kXpMaxUnscaled = 0x1p32f, kXpMinUnscaled = 0x1p-64f;
+__device__ __forceinline__ int token_pexp(float mx)
+{
+    if (mx <= kXpMaxUnscaled && !(mx > 0.0f && mx < kXpMinUnscaled))
+        return 0;
+    const uint32_t b = __float_as_uint(mx);
+    const int e = (b >> 23) ? (int)(b >> 23) - 127 : (31 - __clz(b)) - 149;
+    return e - 14;  // in [-147, 113]
+}
+
+// 2^-p as a bf16 pair, or 2^127 then 2^(-p - 127) where -p > 127 (y = 0: one
+// factor).
+__device__ __forceinline__ uint2 token_scale_pair(int p)
+{
+    const uint32_t f1 = -p <= 127 ? (uint32_t)(127 - p) : 254u;
+    const uint32_t f2 = -p <= 127 ? 0u : (uint32_t)(-p);
+    return make_uint2(f1 << 7 | f1 << 23, f2 << 7 | f2 << 23);
+}
+
+// The token-side operands of the GEMM, 32 tokens per block (4 warps): K in
+// steps of 64 through a cp.async ring of X and A tiles,
+//   X'' = bf16(X z) 2^-p_m to global memory (the GEMM's A operand) and to a
+//         staging tile, and T'' += X'' A^T with bf16 mma.sync (a warp: 16
+//         tokens x 32 LoRA columns; FP32 accumulate);
+// then T'' times rho = s / s_t (fused mode) or 1 (split mode) as bf16 hi + lo
+// at the extension columns, the zero columns j >= r too.
+// kFix = false: one pass over X with p_m = 0, tracking each token's largest
+//   |X'|; flags[block] = 1 when a token of the block needs p_m != 0.
+// kFix = true: only the flagged blocks run (the others return at once): a
+//   first pass finds each token's largest |X'|, the second applies 2^-p_m (a
+//   packed bf16 multiply, two where 2^-p_m is beyond bf16; exact) and
+//   rewrites the block's X'', p_m and T''.
+constexpr int kXpRows = 32, kXpK = 64, kXpStages = 3, kXpThreads = 128;
+constexpr int kXpLd = kXpK + 8;                       // padded row (elements): conflict-free fragments
+constexpr int kXpXBytes = kXpRows * kXpK * 2;         // raw X tile
+constexpr int kXpABytes = kPfMaxR * kXpLd * 2;        // A tile (padded rows)
+constexpr int kXpStageBytes = kXpXBytes + kXpABytes;
+constexpr size_t kXpSmem = kXpStages * kXpStageBytes + kXpRows * kXpLd * 2 + kXpRows * 8;
+static_assert(kXpSmem <= 48 * 1024, "static dynamic-shared-memory limit");
+
+template <bool kFix>
+__global__ void __launch_bounds__(kXpThreads, 4)
+    prefill_xprep_kernel(const uint16_t *__restrict__ x, const float *__restrict__ z, int M, int K,
+                         const uint16_t *__restrict__ a, int r, int ES, float lora_scale,
+                         const float *__restrict__ tensor_scale, uint16_t *__restrict__ xh,
+                         int *__restrict__ pexp_out, uint16_t *__restrict__ ta, int *__restrict__ flags)
+{
+    extern __shared__ __align__(16) uint8_t xp_smem[];
+    uint16_t *xs = reinterpret_cast<uint16_t *>(xp_smem + kXpStages * kXpStageBytes);  // X'' staging (bf16)
+    uint2 *s_sc = reinterpret_cast<uint2 *>(xp_smem + kXpStages * kXpStageBytes + kXpRows * kXpLd * 2);
+    auto xtile = [&](int st) { return reinterpret_cast<uint16_t *>(xp_smem + st * kXpStageBytes); };
+    auto atile = [&](int st) { return reinterpret_cast<uint16_t *>(xp_smem + st * kXpStageBytes + kXpXBytes); };
+
+    pdl_launch_dependents();  // the next kernel may set itself up while this grid runs
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int m0 = blockIdx.x * kXpRows;
+    const uint64_t keep = l2_policy_evict_last(), drop = l2_policy_evict_first();
+    constexpr uint32_t kOne2 = 0x3F803F80u;  // bf16 pair (1, 1)
+    if (kFix && flags[blockIdx.x] == 0)
+        return;
+
+    if (kFix) {
+        // ---- the largest |X'| of each token (one warp per 8 tokens)
+        for (int rr = 0; rr < kXpRows / 4; rr++) {
+            const int row = warp * (kXpRows / 4) + rr, m = m0 + row;
+            float mx = 0.0f;
+            if (m < M) {
+                const uint16_t *xr = x + (size_t)m * K;
+                for (int k0 = lane * 8; k0 < K; k0 += 256 * 8) {
+                    uint4 xb[8];
+#pragma unroll
+                    for (int u = 0; u < 8; u++) {
+                        const int k = k0 + 256 * u;
+                        xb[u] = k < K ? ld_hint_u4(xr + k, keep) : make_uint4(0u, 0u, 0u, 0u);
+                    }
+#pragma unroll
+                    for (int u = 0; u < 8; u++) {
+                        const int k = k0 + 256 * u;
+                        if (k < K)
+                            mx = fmaxf(mx, absmax8(xb[u], z, k));
+                    }
+                }
+            }
+#pragma unroll
+            for (int off = 16; off >= 1; off >>= 1)
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+            const int pexp = token_pexp(__bfloat162float(__float2bfloat16_rn(mx)));
+            if (lane == 0) {
+                s_sc[row] = pexp != 0 ? token_scale_pair(pexp) : make_uint2(kOne2, 0u);
+                if (m < M)
+                    pexp_out[m] = pexp;
+            }
         }
-    };
-    float c[8][4];
-#pragma unroll
-    for (int jt = 0; jt < 8; jt++)
-        c[jt][0] = c[jt][1] = c[jt][2] = c[jt][3] = 0.0f;
-    load(0);
-    for (int k0 = 0; k0 < K; k0 += kLtK) {
-#pragma unroll
-        for (int q = 0; q < 4; q++) {
-            const int i = tid + 128 * q, row = i >> 3, col = (i & 7) * 8;
-            *reinterpret_cast<uint4 *>(xs + row * kLtLd + col) = xv[q];
-            *reinterpret_cast<uint4 *>(as + row * kLtLd + col) = av[q];
+    } else if (tid < kXpRows) {
+        s_sc[tid] = make_uint2(kOne2, 0u);
+    }
+    // rows r .. 63 of every A tile stay zero (cp.async writes rows < r only)
+    const bool has_lora = ES > 0;
+    if (has_lora) {
+        constexpr int kChunks = kXpLd / 8;  // 16-byte pieces per padded row
+        for (int i = tid; i < kXpStages * (kPfMaxR - r) * kChunks; i += kXpThreads) {
+            const int st = i / ((kPfMaxR - r) * kChunks), rest = i % ((kPfMaxR - r) * kChunks);
+            *reinterpret_cast<uint4 *>(atile(st) + (r + rest / kChunks) * kXpLd + (rest % kChunks) * 8) =
+                make_uint4(0u, 0u, 0u, 0u);
         }
-        __syncthreads();
-        if (k0 + kLtK < K)
-            load(k0 + kLtK);
-        const uint16_t *xr0 = xs + (16 * warp + g) * kLtLd, *xr1 = xr0 + 8 * kLtLd;
+    }
+    __syncthreads();
+
+    const int KS = K / kXpK;
+    auto issue = [&](int ks) {
+        if (ks < KS) {
+            const int st = ks % kXpStages, k0 = ks * kXpK;
+            uint16_t *xt = xtile(st);
 #pragma unroll
-        for (int kk = 0; kk < kLtK; kk += 16) {
-            uint32_t af[4];
-            af[0] = h2_to_bf2(*reinterpret_cast<const uint32_t *>(xr0 + kk + 2 * t));
-            af[1] = h2_to_bf2(*reinterpret_cast<const uint32_t *>(xr1 + kk + 2 * t));
-            af[2] = h2_to_bf2(*reinterpret_cast<const uint32_t *>(xr0 + kk + 2 * t + 8));
-            af[3] = h2_to_bf2(*reinterpret_cast<const uint32_t *>(xr1 + kk + 2 * t + 8));
-#pragma unroll
-            for (int jt = 0; jt < 8; jt++) {
-                if (jt < njt) {
-                    const uint16_t *br = as + (8 * jt + g) * kLtLd + kk + 2 * t;
-                    mma_bf16_16816(c[jt], af, *reinterpret_cast<const uint32_t *>(br),
-                                   *reinterpret_cast<const uint32_t *>(br + 8));
+            for (int q = 0; q < kXpRows * 8 / kXpThreads; q++) {
+                const int i = tid + kXpThreads * q, row = i >> 3, col = (i & 7) * 8;
+                const bool ok = m0 + row < M;
+                cp_async16(xt + row * kXpK + col, x + (size_t)(ok ? m0 + row : 0) * K + k0 + col, ok ? 16u : 0u,
+                           drop);
+            }
+            if (has_lora) {
+                uint16_t *at = atile(st);
+                for (int i = tid; i < r * 8; i += kXpThreads) {
+                    const int row = i >> 3, col = (i & 7) * 8;
+                    cp_async16(at + row * kXpLd + col, a + (size_t)row * K + k0 + col, 16u, keep);
                 }
             }
         }
-        __syncthreads();
+        cp_async_commit();  // possibly empty: keeps one group per step
+    };
+#pragma unroll
+    for (int s = 0; s < kXpStages - 1; s++)
+        issue(s);
+
+    const int g = lane >> 2, t = lane & 3, mt = warp & 1, nq = warp >> 1;
+    const bool mma_warp = has_lora && 32 * nq < r;
+    const int njt = min(4, (r - 32 * nq + 7) / 8);
+    float c[4][4];
+#pragma unroll
+    for (int jt = 0; jt < 4; jt++)
+        c[jt][0] = c[jt][1] = c[jt][2] = c[jt][3] = 0.0f;
+    float rmax[kXpRows * 8 / kXpThreads] = {};  // largest |X z| of this thread's two tokens
+
+    for (int ks = 0; ks < KS; ks++) {
+        cp_async_wait<kXpStages - 2>();
+        __syncthreads();  // tile ks landed for every thread; step ks-1 is done with its buffers
+        issue(ks + kXpStages - 1);
+        const int st = ks % kXpStages, k0 = ks * kXpK;
+#pragma unroll
+        for (int q = 0; q < kXpRows * 8 / kXpThreads; q++) {
+            const int i = tid + kXpThreads * q, row = i >> 3, col = (i & 7) * 8;
+            const int m = m0 + row;
+            const uint4 xb = *reinterpret_cast<const uint4 *>(xtile(st) + row * kXpK + col);
+            uint32_t v[4] = {xb.x, xb.y, xb.z, xb.w};
+            if (z && m < M) {
+                const float4 z0 = __ldg(reinterpret_cast<const float4 *>(z + k0 + col));
+                const float4 z1 = __ldg(reinterpret_cast<const float4 *>(z + k0 + col + 4));
+                const float zz[8] = {z0.x, z0.y, z0.z, z0.w, z1.x, z1.y, z1.z, z1.w};
+#pragma unroll
+                for (int e = 0; e < 4; e++) {
+                    const float lo = __fmul_rn(bf_lo(v[e]), zz[2 * e]), hi = __fmul_rn(bf_hi(v[e]), zz[2 * e + 1]);
+                    if (!kFix)
+                        rmax[q] = fmaxf(rmax[q], fmaxf(fabsf(lo), fabsf(hi)));
+                    v[e] = pack_bf2_rn(lo, hi);
+                }
+            } else if (!kFix) {
+#pragma unroll
+                for (int e = 0; e < 4; e++)
+                    rmax[q] = fmaxf(rmax[q], fmaxf(fabsf(bf_lo(v[e])), fabsf(bf_hi(v[e]))));
+            }
+            if (kFix) {
+                const uint2 sc = s_sc[row];
+                if (sc.x != kOne2) {
+#pragma unroll
+                    for (int e = 0; e < 4; e++) {
+                        v[e] = mul_bf2(v[e], sc.x);
+                        if (sc.y)
+                            v[e] = mul_bf2(v[e], sc.y);
+                    }
+                }
+            }
+            const uint4 o = make_uint4(v[0], v[1], v[2], v[3]);
+            if (m < M)
+                *reinterpret_cast<uint4 *>(xh + (size_t)m * K + k0 + col) = o;
+            *reinterpret_cast<uint4 *>(xs + row * kXpLd + col) = o;
+        }
+        __syncthreads();  // staging tile complete
+        if (mma_warp) {
+            const uint16_t *xr0 = xs + (16 * mt + g) * kXpLd, *xr1 = xr0 + 8 * kXpLd;
+            const uint16_t *at = atile(st);
+#pragma unroll
+            for (int kk = 0; kk < kXpK; kk += 16) {
+                uint32_t af[4];
+                af[0] = *reinterpret_cast<const uint32_t *>(xr0 + kk + 2 * t);
+                af[1] = *reinterpret_cast<const uint32_t *>(xr1 + kk + 2 * t);
+                af[2] = *reinterpret_cast<const uint32_t *>(xr0 + kk + 2 * t + 8);
+                af[3] = *reinterpret_cast<const uint32_t *>(xr1 + kk + 2 * t + 8);
+#pragma unroll
+                for (int jt = 0; jt < 4; jt++) {
+                    if (jt < njt) {
+                        const uint16_t *br = at + (32 * nq + 8 * jt + g) * kXpLd + kk + 2 * t;
+                        mma_bf16_16816(c[jt], af, *reinterpret_cast<const uint32_t *>(br),
+                                       *reinterpret_cast<const uint32_t *>(br + 8));
+                    }
+                }
+            }
+        }
     }
-    const float s_t = *tensor_scale;
-    const float ratio = __fdiv_rn(lora_scale, s_t != 0.0f ? s_t : 1.0f);
-    const int W = 64 * ES;
+    cp_async_wait<0>();
+
+    if (!kFix) {
+        // the 8 threads of a token are 8 consecutive lanes; p_m = 0 here, and a
+        // token that needs another p_m flags the block for the second kernel
+        int *s_need = reinterpret_cast<int *>(xs);  // the staging tile is free now
+        __syncthreads();
+        if (tid == 0)
+            *s_need = 0;
+        __syncthreads();
 #pragma unroll
-    for (int q = 0; q < 4; q++) {
-        const int m = m0 + 16 * warp + g + 8 * (q >> 1);
-        if (m >= M)
-            continue;
+        for (int q = 0; q < kXpRows * 8 / kXpThreads; q++) {
+            float mx = rmax[q];
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+            const int row = (tid + kXpThreads * q) >> 3, m = m0 + row;
+            if ((tid & 7) == 0) {
+                if (token_pexp(__bfloat162float(__float2bfloat16_rn(mx))) != 0)
+                    *s_need = 1;
+                if (m < M)
+                    pexp_out[m] = 0;
+            }
+        }
+        __syncthreads();
+        if (tid == 0)
+            flags[blockIdx.x] = *s_need;
+    }
+
+    // ---- T'' at the extension columns (every column of [0, 32 ES) once)
+    if (has_lora && nq < ES) {
+        const float s_t = *tensor_scale;
+        const float ratio = lora_fused(lora_scale, s_t) ? __fdiv_rn(lora_scale, s_t != 0.0f ? s_t : 1.0f) : 1.0f;
+        const int W = 64 * ES;
 #pragma unroll
-        for (int jt = 0; jt < 8; jt++) {
-            const int j = jt * 8 + 2 * t + (q & 1);
-            if (j < r) {
+        for (int q = 0; q < 4; q++) {
+            const int m = m0 + 16 * mt + g + 8 * (q >> 1);
+            if (m >= M)
+                continue;
+#pragma unroll
+            for (int jt = 0; jt < 4; jt++) {
+                const int j = 32 * nq + 8 * jt + 2 * t + (q & 1);
                 const float tv = __fmul_rn(ratio, c[jt][q]);
                 const __nv_bfloat16 hi = __float2bfloat16_rn(tv);
                 const __nv_bfloat16 lo = __float2bfloat16_rn(tv - __bfloat162float(hi));
@@ -228,31 +423,50 @@ __global__ void __launch_bounds__(128) prefill_lora_ext_kernel(const __half *__r
             }
         }
     }
+    if (!kFix)
+        pdl_wait();  // finish only after the weight kernel it overlapped
 }
 
-// 16 codes (8 bytes) times their block scale -> 16 f16 (two 16-byte chunks).
+// 16 codes (8 bytes) times their block scale -> 16 bf16 (two 16-byte chunks);
+// the product is formed in f16 (exact) and converted.
 __device__ __forceinline__ void dequant16(uint2 c, uint32_t sc2, uint32_t (&o)[8])
 {
     e2m1x8_to_h2x4(c.x, o);
     e2m1x8_to_h2x4(c.y, o + 4);
 #pragma unroll
     for (int i = 0; i < 8; i++)
-        o[i] = hmul2_u32(o[i], sc2);
+        o[i] = h2_to_bf2(hmul2_u32(o[i], sc2));
 }
 
-// deq(W)/s_t = v(q) dec(e) as f16 (N x K), and the LoRA B operand of the
+// deq(W)/s_t = v(q) dec(e) as bf16 (N x K), and the LoRA B operand of the
 // extension steps (N x 64 ES bf16: B at the hi and at the lo columns).
 __global__ void __launch_bounds__(256) prefill_weight_kernel(const uint2 *__restrict__ codes,
                                                              const uint8_t *__restrict__ scales, int64_t nblocks,
                                                              uint4 *__restrict__ wh, const uint16_t *__restrict__ b,
                                                              int N, int r, int ES, uint4 *__restrict__ tb)
 {
+    pdl_launch_dependents();  // the token-side kernel runs beside this one
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nblocks; i += stride) {
-        uint32_t o[8];
-        dequant16(codes[i], e4m3_to_h2_dup(scales[i]), o);
-        wh[2 * i] = make_uint4(o[0], o[1], o[2], o[3]);
-        wh[2 * i + 1] = make_uint4(o[4], o[5], o[6], o[7]);
+    constexpr int kU = 8;  // blocks in flight per thread
+    for (int64_t i0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i0 < nblocks; i0 += kU * stride) {
+        uint2 cv[kU];
+        uint32_t ev[kU];
+#pragma unroll
+        for (int u = 0; u < kU; u++) {
+            const int64_t i = i0 + u * stride;
+            cv[u] = i < nblocks ? ld_stream_u2(codes + i) : make_uint2(0u, 0u);
+            ev[u] = i < nblocks ? ld_stream_u8(scales + i) : 0u;
+        }
+#pragma unroll
+        for (int u = 0; u < kU; u++) {
+            const int64_t i = i0 + u * stride;
+            if (i < nblocks) {
+                uint32_t o[8];
+                dequant16(cv[u], e4m3_to_h2_dup(ev[u]), o);
+                wh[2 * i] = make_uint4(o[0], o[1], o[2], o[3]);
+                wh[2 * i + 1] = make_uint4(o[4], o[5], o[6], o[7]);
+            }
+        }
     }
     if (ES == 0)
         return;
@@ -324,6 +538,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *s_tmem;
+    pdl_wait();  // X'', p_m, T'', W and B from the preparation kernels
 
     const int ntile_total = p.mtiles * p.ntiles;
     const int KB = p.K / kPfBK, KS = KB + p.ES;
@@ -358,15 +573,15 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     } else if (warp == 5) {
         // ---------------- MMA issue
         if (lane == 0) {
-            constexpr uint32_t idesc_h = idesc_f16(kPfBM, kPfBN, 0);  // f16 x f16
-            constexpr uint32_t idesc_b = idesc_f16(kPfBM, kPfBN, 1);  // bf16 x bf16 (LoRA steps)
+            constexpr uint32_t idesc = idesc_f16(kPfBM, kPfBN, 1);  // bf16 x bf16, fp32 accumulate
+            const bool split = p.ES > 0 && !lora_fused(p.lora_scale, *p.tensor_scale);
             uint32_t it = 0, lt = 0;
             for (int tile = blockIdx.x; tile < ntile_total && !*s_abort; tile += gridDim.x, lt++) {
-                const int buf = lt & 1;
-                const uint32_t aph = (lt >> 1) & 1;
+                // split: accumulator 0 takes the weights' term, 1 the LoRA term
+                const int buf = split ? 0 : lt & 1;
+                const uint32_t aph = split ? lt & 1 : (lt >> 1) & 1;
                 if (!mbar_wait(&acc_empty[buf], aph ^ 1)) { fail(); break; }
                 tc_fence_after();
-                const uint32_t d = tmem + buf * kPfBN;
                 bool ok = true;
                 for (int ks = 0; ks < KS; ks++, it++) {
                     const int st = it % kPfStages;
@@ -375,10 +590,12 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                     tc_fence_after();
                     const uint64_t ad = smem_desc_sw128(smem_addr(sA + st * kPfABytes));
                     const uint64_t bd = smem_desc_sw128(smem_addr(sB + st * kPfBBytes));
-                    const uint32_t idesc = ks < KB ? idesc_h : idesc_b;
+                    const bool ext = ks >= KB;
+                    const uint32_t d = tmem + (split && ext ? kPfBN : buf * kPfBN);
+                    const int kk = split && ext ? ks - KB : ks;   // 0: start a fresh accumulation
 #pragma unroll
                     for (int j = 0; j < kPfBK / 16; j++)
-                        mma_f16_ss(d, ad + 2 * j, bd + 2 * j, idesc, (ks | j) != 0);
+                        mma_f16_ss(d, ad + 2 * j, bd + 2 * j, idesc, (kk | j) != 0);
                     mma_commit(&empty[st]);
                 }
                 if (!ok) { fail(); break; }
@@ -389,27 +606,41 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         // ---------------- epilogue: warps 0-3, one accumulator row per thread
         const int row = warp * 32 + lane;
         const float s_t = *p.tensor_scale;
+        const bool split = p.ES > 0 && !lora_fused(p.lora_scale, s_t);
         uint32_t lt = 0;
         for (int tile = blockIdx.x; tile < ntile_total && !*s_abort; tile += gridDim.x, lt++) {
             int mt, nt;
             tile_coords(tile, p.mtiles, p.ntiles, mt, nt);
-            const int buf = lt & 1;
-            const uint32_t aph = (lt >> 1) & 1;
+            const int buf = split ? 0 : lt & 1;
+            const uint32_t aph = split ? lt & 1 : (lt >> 1) & 1;
             if (!mbar_wait(&acc_full[buf], aph)) { fail(); break; }
             tc_fence_after();
             const int m = mt * kPfBM + row;
             const bool mrow = m < p.M;
-            const float cm = mrow ? row_factor(s_t, p.fac[m]) : 0.0f;
+            // Y = s_t 2^p_m acc_W (+ s 2^p_m acc_T in the split mode)
+            RowScale fw, ft;
+            const int pm = mrow ? p.pexp[m] : 0;
+            fw.set(s_t != 0.0f ? s_t : 1.0f, pm);
+            ft.set(p.lora_scale, pm);
             for (int cc = 0; cc < kPfBN / 32; cc++) {
+                const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
                 uint32_t v[32];
-                tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + buf * kPfBN + cc * 32, v);
+                tmem_ld32(lane_base + buf * kPfBN + cc * 32, v);
+                float yv[32];
+                if (split) {
+                    uint32_t u[32];
+                    tmem_ld32(lane_base + kPfBN + cc * 32, u);
+#pragma unroll
+                    for (int i = 0; i < 32; i++)
+                        yv[i] = __fadd_rn(fw.apply(__uint_as_float(v[i])), ft.apply(__uint_as_float(u[i])));
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; i++)
+                        yv[i] = fw.apply(__uint_as_float(v[i]));
+                }
                 const int n0 = nt * kPfBN + cc * 32;
                 if (!mrow || n0 >= p.N)
                     continue;
-                float yv[32];
-#pragma unroll
-                for (int i = 0; i < 32; i++)
-                    yv[i] = __fmul_rn(cm, __uint_as_float(v[i]));
                 if (p.y_fp32) {
                     float *dst = reinterpret_cast<float *>(p.y) + (size_t)m * p.N + n0;
                     if (n0 + 32 <= p.N && (p.N & 3) == 0) {
@@ -500,7 +731,7 @@ cudaError_t encode_tensor_map_2d(CUtensorMap *map, CUtensorMapDataType dt, const
 
 struct PrefillPlan {
     int ES;
-    size_t off_xh, off_fac, off_wh, off_ta, off_tb, total;
+    size_t off_xh, off_pexp, off_flags, off_wh, off_ta, off_tb, total;
 };
 
 static size_t pf_align(size_t v) { return (v + 255) / 256 * 256; }
@@ -512,8 +743,10 @@ static PrefillPlan prefill_plan(int64_t M, int64_t N, int64_t K, int64_t r)
     size_t off = kWsHeaderBytes;
     pl.off_xh = off;
     off = pf_align(off + (size_t)M * K * 2);
-    pl.off_fac = off;
+    pl.off_pexp = off;
     off = pf_align(off + (size_t)M * 4);
+    pl.off_flags = off;
+    off = pf_align(off + (size_t)(M + kXpRows - 1) / kXpRows * 4);
     pl.off_wh = off;
     off = pf_align(off + (size_t)N * K * 2);
     pl.off_ta = off;
@@ -539,30 +772,48 @@ cudaError_t launch_prefill_gemm(const GemmArgs &a, cudaStream_t s, const DeviceI
 {
     const PrefillPlan pl = prefill_plan(a.M, a.N, a.K, a.r);
     const int M = (int)a.M, N = (int)a.N, K = (int)a.K, r = (int)a.r;
-    __half *xh = reinterpret_cast<__half *>(a.ws + pl.off_xh);
-    float *fac = reinterpret_cast<float *>(a.ws + pl.off_fac);
+    uint16_t *xh = reinterpret_cast<uint16_t *>(a.ws + pl.off_xh);
+    int *pexp = reinterpret_cast<int *>(a.ws + pl.off_pexp);
+    int *flags = reinterpret_cast<int *>(a.ws + pl.off_flags);
     uint4 *wh = reinterpret_cast<uint4 *>(a.ws + pl.off_wh);
     uint16_t *ta = reinterpret_cast<uint16_t *>(a.ws + pl.off_ta);
     uint4 *tb = reinterpret_cast<uint4 *>(a.ws + pl.off_tb);
 
     const int64_t nblocks = (int64_t)N * K / 16;
-    const int wgrid = (int)std::min<int64_t>((nblocks + 255) / 256, (int64_t)dev.num_sms * 16);
+    // one block per SM leaves room (registers) for three blocks of the
+    // token-side kernel, which starts beside it (programmatic dependent launch)
+    const int wgrid = (int)std::min<int64_t>((nblocks + 255) / 256, (int64_t)dev.num_sms);
     prefill_weight_kernel<<<wgrid, 256, 0, s>>>(reinterpret_cast<const uint2 *>(a.codes), a.scales, nblocks, wh,
                                                 a.lora_b, N, r, pl.ES, tb);
-    prefill_xprime_kernel<<<(M + 7) / 8, 256, 0, s>>>(a.x, a.noise, M, K, xh, fac);
-    if (pl.ES > 0) {
-        cudaError_t e = cudaMemsetAsync(ta, 0, (size_t)M * 64 * pl.ES * 2, s);
-        if (e != cudaSuccess)
-            return e;
-        prefill_lora_ext_kernel<<<(M + kLtRows - 1) / kLtRows, 128, 0, s>>>(xh, a.lora_a, M, K, r, pl.ES,
-                                                                            a.lora_scale, a.tensor_scale, ta);
-    }
+    // the token side: one pass with p_m = 0, then the blocks holding a token
+    // outside [2^-64, 2^32] again with their p_m (the second grid's other
+    // blocks return at once)
+    const int xgrid = (M + kXpRows - 1) / kXpRows;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t xcfg = {};
+    xcfg.gridDim = dim3(xgrid);
+    xcfg.blockDim = dim3(kXpThreads);
+    xcfg.dynamicSmemBytes = kXpSmem;
+    xcfg.stream = s;
+    xcfg.attrs = attr;
+    xcfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&xcfg, prefill_xprep_kernel<false>, a.x, (const float *)a.noise, M, K,
+                                       a.lora_a, r, pl.ES, a.lora_scale, a.tensor_scale, xh, pexp, ta, flags);
+    if (e != cudaSuccess)
+        return e;
+    prefill_xprep_kernel<true><<<xgrid, kXpThreads, kXpSmem, s>>>(
+        a.x, a.noise, M, K, a.lora_a, r, pl.ES, a.lora_scale, a.tensor_scale, xh, pexp, ta, flags);
+    e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return e;
 
     CUtensorMap tmx, tmw, tma_, tmb;
-    cudaError_t e = encode_tensor_map_2d(&tmx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, xh, (uint64_t)K, (uint64_t)M,
+    e = encode_tensor_map_2d(&tmx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, xh, (uint64_t)K, (uint64_t)M,
                                          (uint64_t)K * 2, kPfBK, kPfBM, CU_TENSOR_MAP_SWIZZLE_128B);
     if (e == cudaSuccess)
-        e = encode_tensor_map_2d(&tmw, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, wh, (uint64_t)K, (uint64_t)N,
+        e = encode_tensor_map_2d(&tmw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, wh, (uint64_t)K, (uint64_t)N,
                                  (uint64_t)K * 2, kPfBK, kPfBN, CU_TENSOR_MAP_SWIZZLE_128B);
     // without LoRA the extension maps are never used: point them at X' and W
     if (e == cudaSuccess)
@@ -584,7 +835,8 @@ cudaError_t launch_prefill_gemm(const GemmArgs &a, cudaStream_t s, const DeviceI
     p.K = K;
     p.ES = pl.ES;
     p.tensor_scale = a.tensor_scale;
-    p.fac = fac;
+    p.lora_scale = a.lora_scale;
+    p.pexp = pexp;
     p.y = a.y;
     p.y_fp32 = a.y_fp32 ? 1 : 0;
     p.ctl = reinterpret_cast<uint32_t *>(a.ws);
@@ -594,8 +846,18 @@ cudaError_t launch_prefill_gemm(const GemmArgs &a, cudaStream_t s, const DeviceI
     if (e != cudaSuccess)
         return e;
     const int tiles = p.mtiles * p.ntiles;
-    const int grid = std::min(tiles, dev.num_sms);
-    prefill_gemm_kernel<<<grid, kPfThreads, kPfSmem, s>>>(tmx, tmw, tma_, tmb, p);
+    // programmatic dependent launch: blocks set up (barriers, TMEM) while the
+    // preparation kernel finishes, then wait for its results
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(std::min(tiles, dev.num_sms));
+    cfg.blockDim = dim3(kPfThreads);
+    cfg.dynamicSmemBytes = kPfSmem;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, prefill_gemm_kernel, tmx, tmw, tma_, tmb, p);
+    if (e != cudaSuccess)
+        return e;
     return cudaGetLastError();
 }
 

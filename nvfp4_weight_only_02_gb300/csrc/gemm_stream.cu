@@ -116,16 +116,6 @@ __host__ __device__ constexpr size_t smem_bytes()  // + 1 KB to align the ring, 
 }
 static_assert(smem_bytes<8>() <= 232448 && smem_bytes<16>() <= 232448, "shared memory");
 
-__device__ __forceinline__ void pdl_launch_dependents()
-{
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-
-__device__ __forceinline__ void pdl_wait()
-{
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-}
-
 __device__ __forceinline__ int owner_of(int u, int U, int G)
 {
     return (int)(((long long)(u + 1) * G - 1) / U);

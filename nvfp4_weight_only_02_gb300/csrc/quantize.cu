@@ -104,30 +104,6 @@ __device__ __forceinline__ bool fast_quotient_domain(float S)
     return S >= 0x1p-96f && S <= 0x1p96f;
 }
 
-// L2 eviction-priority hints for loads (per instruction; no device setting).
-__device__ __forceinline__ uint64_t l2_policy_evict_last()
-{
-    uint64_t pol;
-    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
-    return pol;
-}
-
-__device__ __forceinline__ uint64_t l2_policy_evict_first()
-{
-    uint64_t pol;
-    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
-    return pol;
-}
-
-__device__ __forceinline__ uint4 ld_hint_u4(const void *p, uint64_t pol)
-{
-    uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p), "l"(pol));
-    return v;
-}
-
 // Max of the eight bf16 magnitudes of a vector, as magnitude bits (packed pair).
 __device__ __forceinline__ uint32_t absmax_vec2(uint4 v)
 {

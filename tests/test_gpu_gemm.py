@@ -46,14 +46,14 @@ def _abs_bound(orc, c, codes, scales, st):
     return orc.gemm(ax, ac, scales, st, aa, ab, abs(c.lora_scale), az)
 
 
-def _check(y_gpu, y_ref, absref=None, K=0, r=0):
+def _check(y_gpu, y_ref, absref=None, K=0, r=0, floor=1e-30):
     err = np.abs(y_gpu.astype(np.float64) - y_ref)
     max_rel = err.max() / max(np.abs(y_ref).max(), 1e-300)
     mean_rel = err.sum() / max(np.abs(y_ref).sum(), 1e-300)
     assert max_rel <= MAX_REL, max_rel
     assert mean_rel <= MEAN_REL, mean_rel
     if absref is not None:
-        bound = (K + r + 64) * 2.0 ** -23 * absref + 1e-30
+        bound = (K + r + 64) * 2.0 ** -23 * absref + floor
         worst = (err / bound).max()
         assert worst <= 1.0, worst
     return max_rel, mean_rel
