@@ -67,6 +67,9 @@ def _configure(lib):
     lib.orc_gemm.restype = ctypes.c_int
     lib.orc_gemm.argtypes = [P, i64, i64, i64, P, P, ctypes.c_float, P, P, i64,
                              ctypes.c_float, P, P, ctypes.c_int]
+    lib.orc_gemm_dgrad.restype = ctypes.c_int
+    lib.orc_gemm_dgrad.argtypes = [P, i64, i64, i64, P, P, ctypes.c_float, P, P, i64,
+                                   ctypes.c_float, P, P, ctypes.c_int]
     return lib
 
 
@@ -201,3 +204,27 @@ def gemm(x_bits, codes, scales, s_t, a_bits=None, b_bits=None, lora_scale=0.0, z
     if rc != OK:
         raise ValueError(f"oracle gemm status {rc}")
     return y
+
+
+def gemm_dgrad(dy_bits, codes, scales, s_t, a_bits=None, b_bits=None, lora_scale=0.0, z=None,
+               nthreads=None):
+    """dX (M, K) float64 = (dY deq(W) + s (dY B) A) diag(z): the gradient of
+    gemm() with respect to its input, the bf16 rounding of X' taken as the
+    identity."""
+    dy = _c(dy_bits, np.uint16)
+    codes = _c(codes, np.uint8)
+    scales = _c(scales, np.uint8)
+    M, N = dy.shape
+    K = codes.shape[1] * 2
+    if codes.shape[0] != N:
+        raise ValueError("dY columns must match the weight rows")
+    A = _c(a_bits, np.uint16)
+    B = _c(b_bits, np.uint16)
+    r = 0 if A is None or B is None else A.shape[0]
+    dx = np.zeros((M, K), np.float64)
+    rc = _load().orc_gemm_dgrad(_ptr(dy), M, N, K, _ptr(codes), _ptr(scales),
+                                float(np.float32(s_t)), _ptr(A), _ptr(B), r, float(lora_scale),
+                                _ptr(_c(z, np.float32)), _ptr(dx), nthreads or default_threads())
+    if rc != OK:
+        raise ValueError(f"oracle dgrad status {rc}")
+    return dx

@@ -24,6 +24,9 @@
  *   - Parallel LoRA branch as in QLoRA and noise through the RMSNorm gain
  *     (equivalent to multiplicative weight noise) ("RL with NVFP4 + LoRA",
  *     section "Метод").
+ *   - The layer's input gradient with the quantised weight frozen and only
+ *     the LoRA factors trained (same section): dX = (dY deq(W) + s (dY B) A)
+ *     diag(z), the bf16 rounding of X' taken as the identity.
  *
  * Every encoder is a brute-force nearest search over the enumerated finite
  * grid (ties to the code whose least significant bit is 0); every GEMM is a
@@ -33,7 +36,9 @@
  * Parity pins live in tests/ (test_oracle_*.py): codec round trips against
  * closed forms and library conversions, the grid round trip, the half-step
  * error bound, the 8/9 code share, the scale-only-update invariants, exact
- * rational brute force on tiny GEMMs and exact dyadic cases.
+ * rational brute force on tiny GEMMs and exact dyadic cases; for the input
+ * gradient the exact adjoint identity <dY, Y(X)> = <dX, X> against the
+ * forward, float64 autograd and exact rationals (test_oracle_dgrad.py).
  */
 #include <math.h>
 #include <pthread.h>
@@ -401,6 +406,72 @@ int orc_gemm(const uint16_t *x, int64_t M, int64_t N, int64_t K,
     for_rows(N, nthreads, gemm_row, &c);
     free(xp);
     free(T);
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------ */
+/* Gradient of the same layer with respect to its input, in double     */
+/* ------------------------------------------------------------------ */
+
+/* Only the LoRA factors are trained ("RL with NVFP4 + LoRA", section "Метод":
+ * the quantised weight is frozen, gradients flow through it to the layers
+ * below).  With Y = X' Wd^T + s (X' A^T) B^T and X' = X z, the chain rule
+ * gives dX = (dY Wd + s (dY B) A) diag(z); the bf16 rounding of X' is taken
+ * as the identity (its derivative almost everywhere). */
+struct dgrad_ctx {
+    const uint16_t *dy; /* M x N */
+    int64_t N, K, r;
+    const uint8_t *codes, *scales;
+    double s_t, s;
+    const double *U; /* M x r: dY B */
+    const uint16_t *A;
+    const float *z;
+    double *dx; /* M x K */
+};
+
+static void dgrad_row(void *p, int64_t m)
+{
+    struct dgrad_ctx *c = (struct dgrad_ctx *)p;
+    for (int64_t k = 0; k < c->K; k++) {
+        double acc = 0.0;
+        for (int64_t n = 0; n < c->N; n++) {
+            double d = orc_e2m1_value(code_at(c->codes, c->K, n, k)) *
+                       orc_e4m3_value(c->scales[n * (c->K / 16) + k / 16]) * c->s_t;
+            acc += (double)orc_bf16_to_f32(c->dy[m * c->N + n]) * d;
+        }
+        double lora = 0.0;
+        for (int64_t j = 0; j < c->r; j++)
+            lora += c->U[m * c->r + j] * (double)orc_bf16_to_f32(c->A[j * c->K + k]);
+        double g = acc + c->s * lora;
+        c->dx[m * c->K + k] = c->z ? g * (double)c->z[k] : g;
+    }
+}
+
+/* dX (M x K, double) = (dY deq(W) + s (dY B) A) diag(z).
+ * dy: M x N bf16; z: K floats or NULL (then diag(z) = I); A: r x K bf16 or
+ * NULL; B: N x r bf16 or NULL (either NULL or r == 0 drops the LoRA term). */
+int orc_gemm_dgrad(const uint16_t *dy, int64_t M, int64_t N, int64_t K,
+                   const uint8_t *codes, const uint8_t *scales, float s_t,
+                   const uint16_t *A, const uint16_t *B, int64_t r, float s,
+                   const float *z, double *dx, int nthreads)
+{
+    if (M < 0 || N < 0 || K < 0 || K % 16 != 0 || r < 0)
+        return ORC_BAD_SHAPE;
+    if (!A || !B)
+        r = 0;
+    double *U = (double *)malloc((size_t)(M * r + 1) * sizeof(double));
+    if (!U)
+        return ORC_BAD_SHAPE;
+    for (int64_t m = 0; m < M; m++)
+        for (int64_t j = 0; j < r; j++) {
+            double u = 0.0;
+            for (int64_t n = 0; n < N; n++)
+                u += (double)orc_bf16_to_f32(dy[m * N + n]) * (double)orc_bf16_to_f32(B[n * r + j]);
+            U[m * r + j] = u;
+        }
+    struct dgrad_ctx c = {dy, N, K, r, codes, scales, (double)s_t, (double)s, U, A, z, dx};
+    for_rows(M, nthreads, dgrad_row, &c);
+    free(U);
     return ORC_OK;
 }
 

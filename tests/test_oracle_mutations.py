@@ -12,6 +12,7 @@ import pytest
 
 import oracle
 from tests import test_oracle_codecs as codecs
+from tests import test_oracle_dgrad as dgrad
 from tests import test_oracle_gemm as gemm
 from tests import test_oracle_quantize as quant
 
@@ -33,10 +34,13 @@ MUTATIONS = [
     ("noise ignored", "float p = orc_bf16_to_f32(b) * z[k];", "float p = orc_bf16_to_f32(b);"),
     ("noisy input not rounded to bf16", "b = orc_f32_to_bf16(p);",
      "b = orc_f32_to_bf16(orc_bf16_to_f32(b) * (1.0f + (z[k] - 1.0f) * 0.5f));"),
-    ("LoRA scale dropped", "acc + c->s * lora", "acc + lora"),
+    ("LoRA scale dropped", "c->y[m * c->N + n] = acc + c->s * lora;", "c->y[m * c->N + n] = acc + lora;"),
     ("LoRA B transposed", "c->B[n * c->r + j]", "c->B[j * c->N + n]"),
-    ("wrong block index in GEMM", "c->scales[n * (c->K / 16) + k / 16]", "c->scales[n * (c->K / 16) + k / 32]"),
-    ("tensor scale dropped in GEMM", "* c->s_t;\n            acc", ";\n            acc"),
+    ("wrong block index in GEMM",
+     "c->scales[n * (c->K / 16) + k / 16]) * c->s_t;\n            acc += (double)orc_bf16_to_f32(c->xp",
+     "c->scales[n * (c->K / 16) + k / 32]) * c->s_t;\n            acc += (double)orc_bf16_to_f32(c->xp"),
+    ("tensor scale dropped in GEMM", "* c->s_t;\n            acc += (double)orc_bf16_to_f32(c->xp",
+     ";\n            acc += (double)orc_bf16_to_f32(c->xp"),
     ("dequant drops tensor scale", "float v = vd * s_t;", "float v = vd;"),
     ("scale update divides wrong way", "p / s_t;", "p * s_t;"),
     ("reciprocal instead of division", "float x = orc_bf16_to_f32(row[b * 16 + i]) / S_b;",
@@ -49,7 +53,7 @@ MUTATIONS = [
     ("dequant scales by s_t before the block scale",
      "float vd = (float)(orc_e2m1_value(code_at(codes, K, n, k)) *\n                               orc_e4m3_value(scales[n * (K / 16) + k / 16]));\n            float v = vd * s_t;",
      "float vd = (float)orc_e2m1_value(code_at(codes, K, n, k)) * s_t;\n            float v = vd * (float)orc_e4m3_value(scales[n * (K / 16) + k / 16]);"),
-    ("LoRA term subtracted", "acc + c->s * lora", "acc - c->s * lora"),
+    ("LoRA term subtracted", "c->y[m * c->N + n] = acc + c->s * lora;", "c->y[m * c->N + n] = acc - c->s * lora;"),
     ("GEMM accumulates in float", "        double acc = 0.0;\n        for (int64_t k = 0; k < c->K; k++) {",
      "        float acc = 0.0f;\n        for (int64_t k = 0; k < c->K; k++) {"),
     ("LoRA down-projection in float", "            double t = 0.0;", "            float t = 0.0f;"),
@@ -66,6 +70,22 @@ MUTATIONS = [
     ("array encoder swaps the two encoders",
      "c->out[i] = (uint8_t)(c->which == 0 ? orc_e2m1_encode(c->x[i]) : orc_e4m3_encode_nonneg(c->x[i]));",
      "c->out[i] = (uint8_t)(c->which == 1 ? orc_e2m1_encode(c->x[i]) : orc_e4m3_encode_nonneg(c->x[i]));"),
+    ("dgrad noise dropped", "c->dx[m * c->K + k] = c->z ? g * (double)c->z[k] : g;",
+     "c->dx[m * c->K + k] = g;"),
+    ("dgrad LoRA scale dropped", "double g = acc + c->s * lora;", "double g = acc + lora;"),
+    ("dgrad LoRA term subtracted", "double g = acc + c->s * lora;", "double g = acc - c->s * lora;"),
+    ("dgrad LoRA B read transposed", "(double)orc_bf16_to_f32(B[n * r + j])",
+     "(double)orc_bf16_to_f32(B[j * N + n])"),
+    ("dgrad LoRA A read transposed", "(double)orc_bf16_to_f32(c->A[j * c->K + k])",
+     "(double)orc_bf16_to_f32(c->A[k * c->r + j])"),
+    ("dgrad tensor scale dropped", "* c->s_t;\n            acc += (double)orc_bf16_to_f32(c->dy",
+     ";\n            acc += (double)orc_bf16_to_f32(c->dy"),
+    ("dgrad block index from the wrong column",
+     "c->scales[n * (c->K / 16) + k / 16]) * c->s_t;\n            acc += (double)orc_bf16_to_f32(c->dy",
+     "c->scales[n * (c->K / 16) + k / 32]) * c->s_t;\n            acc += (double)orc_bf16_to_f32(c->dy"),
+    ("dgrad LoRA down-projection in float", "            double u = 0.0;", "            float u = 0.0f;"),
+    ("dgrad uses the first dY row for every row", "acc += (double)orc_bf16_to_f32(c->dy[m * c->N + n]) * d;",
+     "acc += (double)orc_bf16_to_f32(c->dy[n]) * d;"),
     ("array encoder skips the last element of each piece",
      "int64_t lo = r * c->per, hi = lo + c->per < c->n ? lo + c->per : c->n;",
      "int64_t lo = r * c->per, hi = lo + c->per - 1 < c->n ? lo + c->per - 1 : c->n;"),
@@ -95,6 +115,11 @@ PINS = [
     gemm.test_gemm_dyadic_is_exact,
     gemm.test_power_of_two_noise_equals_prescaled_input_and_scaled_weight,
     gemm.test_degenerate_cases,
+    lambda o: dgrad.test_adjoint_identity_exact(o, 3, 16, 64, 4),
+    lambda o: dgrad.test_adjoint_identity_exact(o, 5, 40, 128, 8),
+    lambda o: dgrad.test_matches_float64_autograd(o, True, True),
+    lambda o: dgrad.test_vs_exact_rationals(o, 2, 6, 32, 3),
+    dgrad.test_degenerate_cases,
 ]
 
 
