@@ -127,6 +127,37 @@ nvfp4_status nvfp4_w4a16_lora_gemm(const void *x_bf16, int64_t M, int64_t N, int
                                    void *y, nvfp4_dtype y_dtype,
                                    void *workspace, size_t ws_bytes, void *stream);
 
+/* Input gradient of nvfp4_w4a16_lora_gemm's layer.  The quantised weight is
+ * frozen and only the LoRA factors are trained ("RL with NVFP4 + LoRA"
+ * post, section "Метод"), so the backward pass needs the gradient with
+ * respect to the layer input:
+ *     dX = (dY deq(W) + lora_scale (dY B) A) diag(z),
+ * deq(W) = s_t v(q) dec(e) untransposed (N x K), the bf16 rounding of
+ * X' = X z taken as the identity.
+ *   dy_bf16: M x N (device); dx: M x K, FP32 or bf16 (RNE of the FP32
+ *   result); codes, scales_e4m3, tensor_scale as in nvfp4_w4a16_lora_gemm;
+ *   lora_a_bf16: r x K, lora_b_bf16: N x r (both NULL or r == 0: no LoRA);
+ *   noise_fp32: the forward's z (K floats) or NULL.
+ * Shapes: M >= 1; N and K multiples of 64; r <= 64 (else NVFP4_ERR_SHAPE).
+ * Runs on the tensor-core (tcgen05) kernel of the forward with the roles of
+ * the weight's rows and columns exchanged; its workspace holds a bf16 copy of
+ * (v(q) dec(e))^T (2 N K bytes) and of dY (2 M N bytes).  Accumulation is
+ * FP32; any finite tensor scale works.  Every check runs before anything is
+ * queued.  workspace: nvfp4_dgrad_workspace_bytes(M, N, K, r) bytes, 16-byte
+ * aligned, owned by the caller; calls that share a workspace must not overlap
+ * in time. */
+nvfp4_status nvfp4_w4a16_lora_gemm_dgrad(const void *dy_bf16, int64_t M, int64_t N, int64_t K,
+                                         const uint8_t *codes, const uint8_t *scales_e4m3,
+                                         const float *tensor_scale,
+                                         const void *lora_a_bf16, const void *lora_b_bf16,
+                                         int64_t r, float lora_scale, const float *noise_fp32,
+                                         void *dx, nvfp4_dtype dx_dtype,
+                                         void *workspace, size_t ws_bytes, void *stream);
+
+/* Bytes of workspace needed by nvfp4_w4a16_lora_gemm_dgrad (0 for shapes it
+ * does not take). */
+size_t nvfp4_dgrad_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t r);
+
 /* Scale-QLoRA forward (Scale-QLoRA post, method): the block scales are
  * trainable FP32 parameters (decoded block scales in weight units, N x K/16,
  * as for nvfp4_round_scales) and the codes stay frozen.  Each call rounds the

@@ -26,7 +26,7 @@ EXPORTS = [
     "nvfp4_workspace_bytes", "nvfp4_quantize", "nvfp4_dequantize", "nvfp4_w4a16_lora_gemm",
     "nvfp4_round_scales", "nvfp4_get_device_status", "nvfp4_status_string", "nvfp4_encode_debug",
     "nvfp4_quotient_check", "nvfp4_w4a16_lora_gemm_static", "nvfp4_wait_selftest", "nvfp4_gemm_kernel",
-    "nvfp4_scale_qlora_gemm",
+    "nvfp4_scale_qlora_gemm", "nvfp4_w4a16_lora_gemm_dgrad", "nvfp4_dgrad_workspace_bytes",
 ]
 
 
@@ -71,6 +71,9 @@ def load(build_if_missing: bool = True):
             "nvfp4_gemm_kernel": (ctypes.c_char_p, [i64, i64, i64, i64]),
             "nvfp4_scale_qlora_gemm": (st, [P, i64, i64, i64, P, P, P, P, P, P, i64, ctypes.c_float, P, P,
                                             ctypes.c_int, P, ctypes.c_size_t, P]),
+            "nvfp4_w4a16_lora_gemm_dgrad": (st, [P, i64, i64, i64, P, P, P, P, P, i64, ctypes.c_float, P, P,
+                                                 ctypes.c_int, P, ctypes.c_size_t, P]),
+            "nvfp4_dgrad_workspace_bytes": (ctypes.c_size_t, [i64, i64, i64, i64]),
         }
         for name, (res, args) in sig.items():
             f = getattr(lib, name)
@@ -271,6 +274,51 @@ def dequantize(q: QuantizedWeight, dtype=torch.float32) -> torch.Tensor:
     out = torch.empty(q.shape, dtype=dtype, device=q.codes.device)
     nvfp4_dequantize(q.codes, q.scales, q.tensor_scale, out)
     return out
+
+
+def nvfp4_dgrad_workspace_bytes(M: int, N: int, K: int, r: int) -> int:
+    return int(load().nvfp4_dgrad_workspace_bytes(M, N, K, r))
+
+
+def nvfp4_w4a16_lora_gemm_dgrad(dy: torch.Tensor, codes: torch.Tensor, scales: torch.Tensor,
+                                tensor_scale: torch.Tensor, lora_a, lora_b, lora_scale: float,
+                                noise, dx: torch.Tensor, workspace: torch.Tensor):
+    M, N = dy.shape
+    K = codes.shape[1] * 2
+    _need(dy, torch.bfloat16, (M, N), "dy")
+    _need(codes, torch.uint8, (N, K // 2), "codes")
+    _need(scales, torch.uint8, (N, K // 16), "scales")
+    _need(tensor_scale, torch.float32, (1,), "tensor_scale")
+    r = 0
+    if lora_a is not None:
+        r = lora_a.shape[0]
+        _need(lora_a, torch.bfloat16, (r, K), "lora_a")
+        _need(lora_b, torch.bfloat16, (N, r), "lora_b")
+    if noise is not None:
+        _need(noise, torch.float32, (K,), "noise")
+    if dx.dtype not in (torch.float32, torch.bfloat16):
+        raise ValueError("dx must be float32 or bfloat16")
+    _need(dx, dx.dtype, (M, K), "dx")
+    st = load().nvfp4_w4a16_lora_gemm_dgrad(
+        _ptr(dy), M, N, K, _ptr(codes), _ptr(scales), _ptr(tensor_scale), _ptr(lora_a),
+        _ptr(lora_b), r, float(lora_scale), _ptr(noise), _ptr(dx),
+        OUT_FP32 if dx.dtype == torch.float32 else OUT_BF16, _ptr(workspace), workspace.numel(),
+        _stream())
+    _check(st, "nvfp4_w4a16_lora_gemm_dgrad")
+
+
+def gemm_dgrad(dy, q: "QuantizedWeight", lora_a=None, lora_b=None, lora_scale=0.0, noise=None,
+               out_dtype=torch.float32, workspace=None) -> torch.Tensor:
+    """dX = (dY deq(W) + s (dY B) A) diag(z), the input gradient of gemm()."""
+    M, N = dy.shape
+    K = q.shape[1]
+    r = 0 if lora_a is None else lora_a.shape[0]
+    dx = torch.empty((M, K), dtype=out_dtype, device=dy.device)
+    ws = workspace if workspace is not None else new_workspace(nvfp4_dgrad_workspace_bytes(M, N, K, r),
+                                                              dy.device)
+    nvfp4_w4a16_lora_gemm_dgrad(dy, q.codes, q.scales, q.tensor_scale, lora_a, lora_b, lora_scale, noise,
+                                dx, ws)
+    return dx
 
 
 def gemm(x, q: QuantizedWeight, lora_a=None, lora_b=None, lora_scale=0.0, noise=None,

@@ -185,6 +185,64 @@ nvfp4_status nvfp4_w4a16_lora_gemm(const void *x_bf16, int64_t M, int64_t N, int
     return from_cuda(launch_gemm(a, (cudaStream_t)stream, *dev));
 }
 
+static bool dgrad_shape_ok(int64_t M, int64_t N, int64_t K, int64_t r)
+{
+    return M >= 1 && N >= 64 && K >= 64 && r >= 0 && r <= 64 && M <= (1LL << 31) && N <= (1LL << 30) &&
+           K <= (1LL << 30) && dgrad_supported(M, N, K, r);
+}
+
+size_t nvfp4_dgrad_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t r)
+{
+    if (!dgrad_shape_ok(M, N, K, r))
+        return 0;
+    const size_t g = dgrad_workspace_bytes(M, N, K, r);
+    return g < kCtlBytes ? kCtlBytes : g;
+}
+
+nvfp4_status nvfp4_w4a16_lora_gemm_dgrad(const void *dy_bf16, int64_t M, int64_t N, int64_t K,
+                                         const uint8_t *codes, const uint8_t *scales_e4m3,
+                                         const float *tensor_scale, const void *lora_a_bf16,
+                                         const void *lora_b_bf16, int64_t r, float lora_scale,
+                                         const float *noise_fp32, void *dx, nvfp4_dtype dx_dtype,
+                                         void *workspace, size_t ws_bytes, void *stream)
+{
+    if (!dy_bf16 || !codes || !scales_e4m3 || !tensor_scale || !dx || !workspace)
+        return NVFP4_ERR_INVALID_ARG;
+    if (dx_dtype != NVFP4_OUT_BF16 && dx_dtype != NVFP4_OUT_FP32)
+        return NVFP4_ERR_INVALID_ARG;
+    if (!dgrad_shape_ok(M, N, K, r))
+        return NVFP4_ERR_SHAPE;
+    if (r > 0 && (!lora_a_bf16) != (!lora_b_bf16))
+        return NVFP4_ERR_INVALID_ARG;
+    const bool lora = r > 0 && lora_a_bf16 && lora_b_bf16;
+    if (!aligned16(dy_bf16) || !aligned16(codes) || !aligned16(scales_e4m3) || !aligned16(tensor_scale) ||
+        !aligned16(dx) || !aligned16(workspace) || (noise_fp32 && !aligned16(noise_fp32)) ||
+        (lora && (!aligned16(lora_a_bf16) || !aligned16(lora_b_bf16))))
+        return NVFP4_ERR_ALIGNMENT;
+    NVFP4_TRY_DEVICE(dev);
+    const size_t need = dgrad_workspace_bytes(M, N, K, lora ? r : 0);
+    if (ws_bytes < (need < kCtlBytes ? kCtlBytes : need))
+        return NVFP4_ERR_WORKSPACE;
+    GemmArgs a;
+    a.x = (const uint16_t *)dy_bf16;
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.r = lora ? r : 0;
+    a.codes = codes;
+    a.scales = scales_e4m3;
+    a.tensor_scale = tensor_scale;
+    a.lora_a = lora ? (const uint16_t *)lora_a_bf16 : nullptr;
+    a.lora_b = lora ? (const uint16_t *)lora_b_bf16 : nullptr;
+    a.lora_scale = lora ? lora_scale : 0.0f;
+    a.noise = noise_fp32;
+    a.y = dx;
+    a.y_fp32 = dx_dtype == NVFP4_OUT_FP32;
+    a.ws = (uint8_t *)workspace;
+    a.ws_bytes = ws_bytes;
+    return from_cuda(launch_dgrad_gemm(a, (cudaStream_t)stream, *dev));
+}
+
 const char *nvfp4_gemm_kernel(int64_t M, int64_t N, int64_t K, int64_t r)
 {
     if (M < 1 || N < 1 || K < 16 || K % 16 != 0 || r < 0 || r > 256 || N > (1LL << 30) || K > (1LL << 30))

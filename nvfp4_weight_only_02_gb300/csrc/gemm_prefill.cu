@@ -62,6 +62,7 @@ struct PrefillParams {
     const float *tensor_scale;
     float lora_scale;         // s
     const int *pexp;          // M: p_m
+    const float *colscale;    // N output-column factors (the noise z, for the input gradient) or null
     void *y;
     int y_fp32;
     uint32_t *ctl;
@@ -491,6 +492,79 @@ __global__ void __launch_bounds__(256) prefill_weight_kernel(const uint2 *__rest
     }
 }
 
+// ---------------------------------------------------------------- input gradient
+// dX = (dY deq(W) + s (dY B) A) diag(z) is the same kind of product with the
+// roles exchanged: the contraction runs over the weight's rows n, the output
+// over its columns k.  The GEMM kernel takes its B operand contiguous along
+// the contraction, so the weight side is deq(W)^T / s_t = (v(q) dec(e))^T
+// (K x N bf16), the extension operand is [A^T | A^T] (K x 64 ES) and the
+// token side needs B^T (r x N) as its LoRA factor; z becomes a factor per
+// output column.
+
+// One 64 x 64 tile of deq(W)^T / s_t per block: codes and scales of 64 weight
+// rows staged in shared memory (coalesced 16- and 4-byte loads), dequantised
+// 16 at a time, written transposed into a padded tile, stored as 64 rows of
+// 128 bytes.  N and K are multiples of 64.
+constexpr int kWtTile = 64, kWtLd = kWtTile + 8;
+__global__ void __launch_bounds__(256) dgrad_weight_kernel(const uint8_t *__restrict__ codes,
+                                                           const uint8_t *__restrict__ scales, int N, int K,
+                                                           uint16_t *__restrict__ wt)
+{
+    __shared__ __align__(16) uint8_t s_codes[kWtTile * 32];  // 64 rows x 64 codes
+    __shared__ uint32_t s_scales[kWtTile];                    // 4 block scales per row
+    __shared__ __align__(16) uint16_t tile[kWtTile * kWtLd];  // [k][n]
+    pdl_launch_dependents();  // the token-side kernel runs beside this one
+    const int n0 = blockIdx.x * kWtTile, k0 = blockIdx.y * kWtTile, tid = threadIdx.x;
+    if (tid < 128) {
+        const int row = tid >> 1, half = tid & 1;
+        *reinterpret_cast<uint4 *>(s_codes + row * 32 + half * 16) =
+            ld_stream_u4(codes + (size_t)(n0 + row) * (K / 2) + k0 / 2 + half * 16);
+    } else if (tid < 128 + kWtTile) {
+        const int row = tid - 128;
+        s_scales[row] = ld_stream_u32(scales + (size_t)(n0 + row) * (K / 16) + k0 / 16);
+    }
+    __syncthreads();
+    {
+        const int n = tid & 63, b = tid >> 6;  // weight row, 16-column block
+        uint32_t o[8];
+        dequant16(*reinterpret_cast<const uint2 *>(s_codes + n * 32 + b * 8),
+                  e4m3_to_h2_dup((s_scales[n] >> (8 * b)) & 0xFFu), o);
+#pragma unroll
+        for (int i = 0; i < 8; i++) {
+            tile[(16 * b + 2 * i) * kWtLd + n] = (uint16_t)(o[i] & 0xFFFFu);
+            tile[(16 * b + 2 * i + 1) * kWtLd + n] = (uint16_t)(o[i] >> 16);
+        }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int q = 0; q < 2; q++) {
+        const int i = tid + 256 * q, kr = i >> 3, ch = i & 7;
+        *reinterpret_cast<uint4 *>(wt + (size_t)(k0 + kr) * N + n0 + ch * 8) =
+            *reinterpret_cast<const uint4 *>(tile + kr * kWtLd + ch * 8);
+    }
+}
+
+// [A^T | A^T] at the extension columns (K x 64 ES bf16; zero where j >= r)
+// and B^T (r x N bf16).
+__global__ void __launch_bounds__(256) dgrad_lora_layout_kernel(const uint16_t *__restrict__ a,
+                                                                const uint16_t *__restrict__ b, int N, int K,
+                                                                int r, int ES, uint16_t *__restrict__ tb,
+                                                                uint16_t *__restrict__ bt)
+{
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    const int64_t t0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int W = 64 * ES;
+    for (int64_t i = t0; i < (int64_t)K * W; i += stride) {
+        const int64_t k = i / W;
+        const int c = (int)(i % W), j = ES == 1 ? c % 32 : c % 64;
+        tb[i] = j < r ? a[(int64_t)j * K + k] : (uint16_t)0;
+    }
+    for (int64_t i = t0; i < (int64_t)r * N; i += stride) {
+        const int64_t j = i / N, n = i % N;
+        bt[i] = b[n * r + j];
+    }
+}
+
 // ---------------------------------------------------------------- main kernel
 __device__ __forceinline__ void tile_coords(int t, int mtiles, int ntiles, int &mt, int &nt)
 {
@@ -641,6 +715,11 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                 const int n0 = nt * kPfBN + cc * 32;
                 if (!mrow || n0 >= p.N)
                     continue;
+                if (p.colscale) {
+#pragma unroll
+                    for (int i = 0; i < 32; i++)
+                        yv[i] = __fmul_rn(yv[i], n0 + i < p.N ? __ldg(p.colscale + n0 + i) : 0.0f);
+                }
                 if (p.y_fp32) {
                     float *dst = reinterpret_cast<float *>(p.y) + (size_t)m * p.N + n0;
                     if (n0 + 32 <= p.N && (p.N & 3) == 0) {
@@ -731,63 +810,95 @@ cudaError_t encode_tensor_map_2d(CUtensorMap *map, CUtensorMapDataType dt, const
 
 struct PrefillPlan {
     int ES;
-    size_t off_xh, off_pexp, off_flags, off_wh, off_ta, off_tb, total;
+    size_t off_xh, off_pexp, off_flags, off_wh, off_ta, off_tb, off_bt, total;
 };
 
 static size_t pf_align(size_t v) { return (v + 255) / 256 * 256; }
 
-static PrefillPlan prefill_plan(int64_t M, int64_t N, int64_t K, int64_t r)
+// Workspace of one product Y (M x Nout) = X'' Wop^T + LoRA term with the
+// contraction over Kc: X'' (M x Kc), p_m, block flags, Wop (Nout x Kc), the
+// two extension operands and, for the input gradient, B^T (r x Kc).
+static PrefillPlan prefill_plan(int64_t M, int64_t Nout, int64_t Kc, int64_t r, bool with_bt)
 {
     PrefillPlan pl;
     pl.ES = r == 0 ? 0 : r <= 32 ? 1 : 2;
     size_t off = kWsHeaderBytes;
     pl.off_xh = off;
-    off = pf_align(off + (size_t)M * K * 2);
+    off = pf_align(off + (size_t)M * Kc * 2);
     pl.off_pexp = off;
     off = pf_align(off + (size_t)M * 4);
     pl.off_flags = off;
     off = pf_align(off + (size_t)(M + kXpRows - 1) / kXpRows * 4);
     pl.off_wh = off;
-    off = pf_align(off + (size_t)N * K * 2);
+    off = pf_align(off + (size_t)Nout * Kc * 2);
     pl.off_ta = off;
     off = pf_align(off + (size_t)M * 64 * pl.ES * 2);
     pl.off_tb = off;
-    off = pf_align(off + (size_t)N * 64 * pl.ES * 2);
+    off = pf_align(off + (size_t)Nout * 64 * pl.ES * 2);
+    pl.off_bt = off;
+    if (with_bt)
+        off = pf_align(off + (size_t)r * Kc * 2);
     pl.total = off;
     return pl;
 }
 
+static bool pf_sizes_ok(int64_t M, int64_t Nout, int64_t Kc, int64_t r)
+{
+    return Kc % kPfBK == 0 && r <= kPfMaxR && M <= (1LL << 31) / std::max<int64_t>(Kc, 1) && Nout <= (1LL << 30) &&
+           Nout * Kc <= (1LL << 40);
+}
+
 bool prefill_supported(int64_t M, int64_t N, int64_t K, int64_t r)
 {
-    return M >= kPrefillMinM && K % kPfBK == 0 && r <= kPfMaxR && M <= (1LL << 31) / std::max<int64_t>(K, 1) &&
-           N <= (1LL << 30) && N * K <= (1LL << 40);
+    return M >= kPrefillMinM && pf_sizes_ok(M, N, K, r);
 }
 
 size_t prefill_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t r)
 {
-    return prefill_plan(M, N, K, r).total;
+    return prefill_plan(M, N, K, r, false).total;
 }
 
-cudaError_t launch_prefill_gemm(const GemmArgs &a, cudaStream_t s, const DeviceInfo &dev)
+bool dgrad_supported(int64_t M, int64_t N, int64_t K, int64_t r)
 {
-    const PrefillPlan pl = prefill_plan(a.M, a.N, a.K, a.r);
-    const int M = (int)a.M, N = (int)a.N, K = (int)a.K, r = (int)a.r;
-    uint16_t *xh = reinterpret_cast<uint16_t *>(a.ws + pl.off_xh);
-    int *pexp = reinterpret_cast<int *>(a.ws + pl.off_pexp);
-    int *flags = reinterpret_cast<int *>(a.ws + pl.off_flags);
-    uint4 *wh = reinterpret_cast<uint4 *>(a.ws + pl.off_wh);
-    uint16_t *ta = reinterpret_cast<uint16_t *>(a.ws + pl.off_ta);
-    uint4 *tb = reinterpret_cast<uint4 *>(a.ws + pl.off_tb);
+    return M >= 1 && N % kWtTile == 0 && K % kWtTile == 0 && K <= 64LL * 65535 && pf_sizes_ok(M, K, N, r);
+}
 
-    const int64_t nblocks = (int64_t)N * K / 16;
-    // one block per SM leaves room (registers) for three blocks of the
-    // token-side kernel, which starts beside it (programmatic dependent launch)
-    const int wgrid = (int)std::min<int64_t>((nblocks + 255) / 256, (int64_t)dev.num_sms);
-    prefill_weight_kernel<<<wgrid, 256, 0, s>>>(reinterpret_cast<const uint2 *>(a.codes), a.scales, nblocks, wh,
-                                                a.lora_b, N, r, pl.ES, tb);
-    // the token side: one pass with p_m = 0, then the blocks holding a token
-    // outside [2^-64, 2^32] again with their p_m (the second grid's other
-    // blocks return at once)
+size_t dgrad_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t r)
+{
+    return prefill_plan(M, K, N, r, true).total;
+}
+
+// Everything after the weight-side preparation: the token side (one pass,
+// then the blocks holding a token outside [2^-64, 2^32] again with their p_m;
+// the second grid's other blocks return at once), then the GEMM.  The first
+// token-side grid starts beside the weight-side kernel launched just before
+// it (programmatic dependent launch; that kernel signals at its start, and
+// the token-side grid waits for it before it finishes).
+struct PfRun {
+    int M, Nout, Kc, r;
+    const uint16_t *x;        // M x Kc bf16 (X, or dY for the input gradient)
+    const float *noise;       // Kc input-noise factors of the token side, or null
+    const uint16_t *lora_in;  // r x Kc: the token side's LoRA factor (A, or B^T)
+    float lora_scale;
+    const float *tensor_scale;
+    const float *colscale;    // Nout output-column factors or null
+    void *y;
+    bool y_fp32;
+    uint8_t *ws;
+    PrefillPlan pl;
+};
+
+static cudaError_t run_token_side_and_gemm(const PfRun &q, cudaStream_t s, const DeviceInfo &dev)
+{
+    const PrefillPlan &pl = q.pl;
+    const int M = q.M, N = q.Nout, K = q.Kc, r = q.r;
+    uint16_t *xh = reinterpret_cast<uint16_t *>(q.ws + pl.off_xh);
+    int *pexp = reinterpret_cast<int *>(q.ws + pl.off_pexp);
+    int *flags = reinterpret_cast<int *>(q.ws + pl.off_flags);
+    uint16_t *wh = reinterpret_cast<uint16_t *>(q.ws + pl.off_wh);
+    uint16_t *ta = reinterpret_cast<uint16_t *>(q.ws + pl.off_ta);
+    uint16_t *tb = reinterpret_cast<uint16_t *>(q.ws + pl.off_tb);
+
     const int xgrid = (M + kXpRows - 1) / kXpRows;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -799,23 +910,24 @@ cudaError_t launch_prefill_gemm(const GemmArgs &a, cudaStream_t s, const DeviceI
     xcfg.stream = s;
     xcfg.attrs = attr;
     xcfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&xcfg, prefill_xprep_kernel<false>, a.x, (const float *)a.noise, M, K,
-                                       a.lora_a, r, pl.ES, a.lora_scale, a.tensor_scale, xh, pexp, ta, flags);
+    cudaError_t e = cudaLaunchKernelEx(&xcfg, prefill_xprep_kernel<false>, q.x, q.noise, M, K, q.lora_in, r,
+                                       pl.ES, q.lora_scale, q.tensor_scale, xh, pexp, ta, flags);
     if (e != cudaSuccess)
         return e;
-    prefill_xprep_kernel<true><<<xgrid, kXpThreads, kXpSmem, s>>>(
-        a.x, a.noise, M, K, a.lora_a, r, pl.ES, a.lora_scale, a.tensor_scale, xh, pexp, ta, flags);
+    prefill_xprep_kernel<true><<<xgrid, kXpThreads, kXpSmem, s>>>(q.x, q.noise, M, K, q.lora_in, r, pl.ES,
+                                                                   q.lora_scale, q.tensor_scale, xh, pexp, ta,
+                                                                   flags);
     e = cudaGetLastError();
     if (e != cudaSuccess)
         return e;
 
     CUtensorMap tmx, tmw, tma_, tmb;
     e = encode_tensor_map_2d(&tmx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, xh, (uint64_t)K, (uint64_t)M,
-                                         (uint64_t)K * 2, kPfBK, kPfBM, CU_TENSOR_MAP_SWIZZLE_128B);
+                             (uint64_t)K * 2, kPfBK, kPfBM, CU_TENSOR_MAP_SWIZZLE_128B);
     if (e == cudaSuccess)
         e = encode_tensor_map_2d(&tmw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, wh, (uint64_t)K, (uint64_t)N,
                                  (uint64_t)K * 2, kPfBK, kPfBN, CU_TENSOR_MAP_SWIZZLE_128B);
-    // without LoRA the extension maps are never used: point them at X' and W
+    // without LoRA the extension maps are never used: point them at X'' and W
     if (e == cudaSuccess)
         e = pl.ES > 0 ? encode_tensor_map_2d(&tma_, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, ta, (uint64_t)64 * pl.ES,
                                              (uint64_t)M, (uint64_t)128 * pl.ES, kPfBK, kPfBM,
@@ -834,12 +946,13 @@ cudaError_t launch_prefill_gemm(const GemmArgs &a, cudaStream_t s, const DeviceI
     p.N = N;
     p.K = K;
     p.ES = pl.ES;
-    p.tensor_scale = a.tensor_scale;
-    p.lora_scale = a.lora_scale;
+    p.tensor_scale = q.tensor_scale;
+    p.lora_scale = q.lora_scale;
     p.pexp = pexp;
-    p.y = a.y;
-    p.y_fp32 = a.y_fp32 ? 1 : 0;
-    p.ctl = reinterpret_cast<uint32_t *>(a.ws);
+    p.colscale = q.colscale;
+    p.y = q.y;
+    p.y_fp32 = q.y_fp32 ? 1 : 0;
+    p.ctl = reinterpret_cast<uint32_t *>(q.ws);
     p.mtiles = (M + kPfBM - 1) / kPfBM;
     p.ntiles = (N + kPfBN - 1) / kPfBN;
     e = cudaFuncSetAttribute(prefill_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPfSmem);
@@ -847,7 +960,7 @@ cudaError_t launch_prefill_gemm(const GemmArgs &a, cudaStream_t s, const DeviceI
         return e;
     const int tiles = p.mtiles * p.ntiles;
     // programmatic dependent launch: blocks set up (barriers, TMEM) while the
-    // preparation kernel finishes, then wait for its results
+    // token-side kernel finishes, then wait for its results
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(std::min(tiles, dev.num_sms));
     cfg.blockDim = dim3(kPfThreads);
@@ -859,6 +972,47 @@ cudaError_t launch_prefill_gemm(const GemmArgs &a, cudaStream_t s, const DeviceI
     if (e != cudaSuccess)
         return e;
     return cudaGetLastError();
+}
+
+cudaError_t launch_prefill_gemm(const GemmArgs &a, cudaStream_t s, const DeviceInfo &dev)
+{
+    const PrefillPlan pl = prefill_plan(a.M, a.N, a.K, a.r, false);
+    const int N = (int)a.N, K = (int)a.K, r = (int)a.r;
+    const int64_t nblocks = (int64_t)N * K / 16;
+    // one block per SM leaves room (registers) for three blocks of the
+    // token-side kernel, which starts beside it
+    const int wgrid = (int)std::min<int64_t>((nblocks + 255) / 256, (int64_t)dev.num_sms);
+    prefill_weight_kernel<<<wgrid, 256, 0, s>>>(reinterpret_cast<const uint2 *>(a.codes), a.scales, nblocks,
+                                                reinterpret_cast<uint4 *>(a.ws + pl.off_wh), a.lora_b, N, r, pl.ES,
+                                                reinterpret_cast<uint4 *>(a.ws + pl.off_tb));
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return e;
+    PfRun q = {(int)a.M, N, K, r, a.x, a.noise, a.lora_a, a.lora_scale, a.tensor_scale, nullptr,
+               a.y, a.y_fp32, a.ws, pl};
+    return run_token_side_and_gemm(q, s, dev);
+}
+
+// dX (M x K) from dY (a.x, M x N): the weight rows n are the contraction.
+cudaError_t launch_dgrad_gemm(const GemmArgs &a, cudaStream_t s, const DeviceInfo &dev)
+{
+    const PrefillPlan pl = prefill_plan(a.M, a.K, a.N, a.r, true);
+    const int N = (int)a.N, K = (int)a.K, r = (int)a.r;
+    uint16_t *bt = reinterpret_cast<uint16_t *>(a.ws + pl.off_bt);
+    if (r > 0) {
+        const int64_t work = (int64_t)K * 64 * pl.ES + (int64_t)r * N;
+        const int lgrid = (int)std::min<int64_t>((work + 255) / 256, (int64_t)dev.num_sms * 8);
+        dgrad_lora_layout_kernel<<<lgrid, 256, 0, s>>>(a.lora_a, a.lora_b, N, K, r, pl.ES,
+                                                       reinterpret_cast<uint16_t *>(a.ws + pl.off_tb), bt);
+    }
+    dgrad_weight_kernel<<<dim3(N / kWtTile, K / kWtTile), 256, 0, s>>>(
+        a.codes, a.scales, N, K, reinterpret_cast<uint16_t *>(a.ws + pl.off_wh));
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return e;
+    PfRun q = {(int)a.M, K, N, r, a.x, nullptr, r > 0 ? bt : nullptr, a.lora_scale, a.tensor_scale, a.noise,
+               a.y, a.y_fp32, a.ws, pl};
+    return run_token_side_and_gemm(q, s, dev);
 }
 
 }  // namespace nvfp4

@@ -70,6 +70,13 @@ bool prefill_supported(int64_t M, int64_t N, int64_t K, int64_t r);
 size_t prefill_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t r);
 cudaError_t launch_prefill_gemm(const GemmArgs &a, cudaStream_t s, const DeviceInfo &dev);
 
+// Input gradient dX = (dY deq(W) + s (dY B) A) diag(z) on the same tensor-core
+// kernel (any M >= 1; N and K multiples of 64, r <= 64).  GemmArgs: x = dY
+// (M x N), y = dX (M x K), noise = z (K) or null.
+bool dgrad_supported(int64_t M, int64_t N, int64_t K, int64_t r);
+size_t dgrad_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t r);
+cudaError_t launch_dgrad_gemm(const GemmArgs &a, cudaStream_t s, const DeviceInfo &dev);
+
 // 2-D tiled tensor map (row-major, `row_bytes` between rows, box of
 // box_inner x box_outer elements, zero fill outside) through the driver's
 // encoder, looked up once.

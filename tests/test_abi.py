@@ -88,6 +88,22 @@ def test_host_checks_reject_before_launch(lib):
     st = lib.nvfp4_w4a16_lora_gemm_static(good, 1, 16, 32, good, good, good, good, null, 4, 1.0, null, good, 1,
                                           null)
     assert st in (binding.ERR_INVALID_ARG, binding.ERR_CUDA)  # ERR_CUDA: no device to look the array up on
+    # the input gradient: every host check before the device query
+    dg = lambda dy, dx, ddt, a, b, r, z=null, M=4, N=64, K=128: lib.nvfp4_w4a16_lora_gemm_dgrad(
+        dy, M, N, K, good, good, good, a, b, r, 1.0, z, dx, ddt, good, 1 << 20, null)
+    assert dg(null, good, 1, null, null, 0) == binding.ERR_INVALID_ARG           # no dY
+    assert dg(good, good, 7, null, null, 0) == binding.ERR_INVALID_ARG           # bad output dtype
+    assert dg(good, good, 1, null, null, 0, N=96) == binding.ERR_SHAPE           # N not a multiple of 64
+    assert dg(good, good, 1, null, null, 0, K=80) == binding.ERR_SHAPE           # K not a multiple of 64
+    assert dg(good, good, 1, null, null, 0, M=0) == binding.ERR_SHAPE
+    assert dg(good, good, 1, good, good, 65) == binding.ERR_SHAPE                # rank above 64
+    assert dg(good, good, 1, good, null, 4) == binding.ERR_INVALID_ARG           # half a LoRA pair
+    assert dg(bad_align, good, 1, null, null, 0) == binding.ERR_ALIGNMENT        # dY misaligned
+    assert dg(good, bad_align, 1, null, null, 0) == binding.ERR_ALIGNMENT        # dX misaligned
+    assert dg(good, good, 1, null, null, 0, bad_align) == binding.ERR_ALIGNMENT  # noise misaligned
+    assert dg(good, good, 1, bad_align, good, 4) == binding.ERR_ALIGNMENT        # LoRA A misaligned
+    assert lib.nvfp4_dgrad_workspace_bytes(4, 96, 128, 0) == 0
+    assert lib.nvfp4_dgrad_workspace_bytes(4, 64, 128, 0) > 0
     assert lib.nvfp4_workspace_bytes(1, 16, 30, 0) == 0
     assert lib.nvfp4_gemm_kernel(1, 16, 30, 0) is None
     assert lib.nvfp4_encode_debug(good, 8, 5, good, null) == binding.ERR_INVALID_ARG
