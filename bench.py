@@ -450,6 +450,7 @@ def run_gpu(args):
             }
         if not args.no_prefill:
             line["prefill"] = run_prefill_case(torch, nv, synth, peak_tf)
+            line["dgrad"] = run_dgrad_case(torch, nv, synth, peak_tf)
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(seconds=args.cpu_seconds)
         print(json.dumps(line), flush=True)
@@ -610,6 +611,32 @@ def run_prefill_case(torch, nv, synth, peak_tf):
     f = gemm_flops(M, N, K, R_LORA)
     return {"workload": "16384 x 18944 x 3584 + LoRA r=32, bf16 out", "ms": round(ms, 3),
             "TFLOP/s": round(f / ms / 1e9, 1), "peak_bf16_tflops": peak_tf,
+            "frac": round(f / ms / 1e9 / peak_tf, 4)}
+
+
+def run_dgrad_case(torch, nv, synth, peak_tf):
+    """Input gradient of the same layer for 16384 tokens: dY (16384 x 18944)
+    -> dX (16384 x 3584), LoRA r=32, noise, bf16 out (tensor-core path)."""
+    M, (N, K) = 16384, UP
+    dev = lambda b: torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(torch.bfloat16).cuda()
+    w = dev(synth.normal_weight((N, K), 0.02, 0, outlier_frac=1e-3))
+    q = nv.quantize(w)
+    ws = nv.new_workspace(nv.nvfp4_dgrad_workspace_bytes(M, N, K, R_LORA))
+    a, b = synth.lora_pair(N, K, R_LORA, 0.01, 2)
+    a, b = dev(a), dev(b)
+    z = torch.from_numpy(synth.noise_vector(K, SIGMA, 3)).cuda()
+    dy = dev(synth.activations(M, N, 11, std=1e-3))
+    dx = torch.empty((M, K), dtype=torch.bfloat16, device="cuda")
+    op = lambda: nv.nvfp4_w4a16_lora_gemm_dgrad(dy, q.codes, q.scales, q.tensor_scale, a, b, LORA_SCALE, z,
+                                                dx, ws)
+    op()
+    ms = time_replays(torch, [op], 5)
+    st = nv.nvfp4_get_device_status(ws)
+    if st != nv.OK:
+        raise RuntimeError(nv.status_string(st))
+    f = gemm_flops(M, N, K, R_LORA)
+    return {"workload": "dX 16384 x 3584 from dY 16384 x 18944 (7B up, transposed) + LoRA r=32, bf16 out",
+            "ms": round(ms, 3), "TFLOP/s": round(f / ms / 1e9, 1), "peak_bf16_tflops": peak_tf,
             "frac": round(f / ms / 1e9 / peak_tf, 4)}
 
 
@@ -776,13 +803,23 @@ def run_kernel_case(case, reps):
     dev = lambda b: torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(torch.bfloat16).cuda()
     wb = synth.normal_weight(shape, 0.02, 0, outlier_frac=1e-3, outlier_mult=20.0)
     w = dev(wb)
-    M = int(parts[2][1:]) if kind == "gemm" else (16384 if kind == "prefill" else 0)
-    ws = nv.new_workspace(nv.nvfp4_workspace_bytes(max(M, 1), *shape, R_LORA))
+    M = int(parts[2][1:]) if kind == "gemm" else (16384 if kind in ("prefill", "dgrad") else 0)
+    ws = nv.new_workspace(max(nv.nvfp4_workspace_bytes(max(M, 1), *shape, R_LORA),
+                              nv.nvfp4_dgrad_workspace_bytes(max(M, 1), *shape, R_LORA)))
     q = nv.quantize(w, workspace=ws)
     if kind == "quantize":
         frozen = len(parts) > 2 and parts[2] == "frozen"
         op = lambda: nv.nvfp4_quantize(w, q.codes, q.scales, q.tensor_scale, frozen, ws)
         nbytes, flops = quant_bytes(*shape), 0.0
+    elif kind == "dgrad":
+        a, b = synth.lora_pair(shape[0], shape[1], R_LORA, 0.01, 2)
+        a, b = dev(a), dev(b)
+        z = torch.from_numpy(synth.noise_vector(shape[1], SIGMA, 3)).cuda()
+        dy = dev(synth.activations(M, shape[0], 11, std=1e-3))
+        dx = torch.empty((M, shape[1]), dtype=torch.bfloat16, device="cuda")
+        op = lambda: nv.nvfp4_w4a16_lora_gemm_dgrad(dy, q.codes, q.scales, q.tensor_scale, a, b, LORA_SCALE, z,
+                                                    dx, ws)
+        nbytes, flops = gemm_bytes(M, *shape, R_LORA), gemm_flops(M, *shape, R_LORA)
     else:
         a, b = synth.lora_pair(shape[0], shape[1], R_LORA, 0.01, 2)
         a, b = dev(a), dev(b)

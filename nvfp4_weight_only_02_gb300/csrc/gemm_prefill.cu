@@ -63,6 +63,8 @@ struct PrefillParams {
     float lora_scale;         // s
     const int *pexp;          // M: p_m
     const float *colscale;    // N output-column factors (the noise z, for the input gradient) or null
+    const int *flags;         // per 32 tokens: 1 where X'' had to be rescaled
+    int direct;               // read X (tmap_xd) instead of X'' for tiles without a flag
     void *y;
     int y_fp32;
     uint32_t *ctl;
@@ -198,6 +200,9 @@ __device__ __forceinline__ uint2 token_scale_pair(int p)
 //   first pass finds each token's largest |X'|, the second applies 2^-p_m (a
 //   packed bf16 multiply, two where 2^-p_m is beyond bf16; exact) and
 //   rewrites the block's X'', p_m and T''.
+// direct (no input noise, so X' = X): the first kernel writes no X''; the GEMM
+//   reads X itself, except for 128-token tiles holding a flagged block, whose
+//   X'' the second kernel writes for all four blocks of the tile.
 constexpr int kXpRows = 32, kXpK = 64, kXpStages = 3, kXpThreads = 128;
 constexpr int kXpLd = kXpK + 8;                       // padded row (elements): conflict-free fragments
 constexpr int kXpXBytes = kXpRows * kXpK * 2;         // raw X tile
@@ -205,13 +210,15 @@ constexpr int kXpABytes = kPfMaxR * kXpLd * 2;        // A tile (padded rows)
 constexpr int kXpStageBytes = kXpXBytes + kXpABytes;
 constexpr size_t kXpSmem = kXpStages * kXpStageBytes + kXpRows * kXpLd * 2 + kXpRows * 8;
 static_assert(kXpSmem <= 48 * 1024, "static dynamic-shared-memory limit");
+constexpr int kXpGroup = kPfBM / kXpRows;  // token-side blocks per GEMM row tile
 
 template <bool kFix>
 __global__ void __launch_bounds__(kXpThreads, 4)
     prefill_xprep_kernel(const uint16_t *__restrict__ x, const float *__restrict__ z, int M, int K,
                          const uint16_t *__restrict__ a, int r, int ES, float lora_scale,
                          const float *__restrict__ tensor_scale, uint16_t *__restrict__ xh,
-                         int *__restrict__ pexp_out, uint16_t *__restrict__ ta, int *__restrict__ flags)
+                         int *__restrict__ pexp_out, uint16_t *__restrict__ ta, int *__restrict__ flags,
+                         int direct)
 {
     extern __shared__ __align__(16) uint8_t xp_smem[];
     uint16_t *xs = reinterpret_cast<uint16_t *>(xp_smem + kXpStages * kXpStageBytes);  // X'' staging (bf16)
@@ -224,8 +231,18 @@ __global__ void __launch_bounds__(kXpThreads, 4)
     const int m0 = blockIdx.x * kXpRows;
     const uint64_t keep = l2_policy_evict_last(), drop = l2_policy_evict_first();
     constexpr uint32_t kOne2 = 0x3F803F80u;  // bf16 pair (1, 1)
-    if (kFix && flags[blockIdx.x] == 0)
-        return;
+    if (kFix) {
+        // direct: the GEMM reads X itself except in 128-token tiles holding a
+        // flagged block, so the whole tile's X'' is written here
+        bool need = flags[blockIdx.x] != 0;
+        if (direct) {
+            const int g0 = blockIdx.x & ~(kXpGroup - 1);
+            for (int i = 0; i < kXpGroup && g0 + i < (int)gridDim.x; i++)
+                need = need || flags[g0 + i] != 0;
+        }
+        if (!need)
+            return;
+    }
 
     if (kFix) {
         // ---- the largest |X'| of each token (one warp per 8 tokens)
@@ -348,7 +365,7 @@ __global__ void __launch_bounds__(kXpThreads, 4)
                 }
             }
             const uint4 o = make_uint4(v[0], v[1], v[2], v[3]);
-            if (m < M)
+            if (m < M && (kFix || !direct))
                 *reinterpret_cast<uint4 *>(xh + (size_t)m * K + k0 + col) = o;
             *reinterpret_cast<uint4 *>(xs + row * kXpLd + col) = o;
         }
@@ -576,7 +593,8 @@ __device__ __forceinline__ void tile_coords(int t, int mtiles, int ntiles, int &
 }
 
 __global__ void __launch_bounds__(kPfThreads, 1)
-    prefill_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_w,
+    prefill_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_xd,
+                        const __grid_constant__ CUtensorMap tmap_w,
                         const __grid_constant__ CUtensorMap tmap_ta, const __grid_constant__ CUtensorMap tmap_tb,
                         PrefillParams p)
 {
@@ -629,13 +647,22 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             for (int tile = blockIdx.x; tile < ntile_total && !*s_abort; tile += gridDim.x) {
                 int mt, nt;
                 tile_coords(tile, p.mtiles, p.ntiles, mt, nt);
+                const CUtensorMap *mx = &tmap_x;
+                if (p.direct) {
+                    bool copy = false;
+                    for (int i = 0; i < kXpGroup; i++) {
+                        const int b = mt * kXpGroup + i;
+                        copy = copy || (b * kXpRows < p.M && p.flags[b] != 0);
+                    }
+                    mx = copy ? &tmap_x : &tmap_xd;
+                }
                 for (int ks = 0; ks < KS; ks++, it++) {
                     const int st = it % kPfStages;
                     const uint32_t ph = (it / kPfStages) & 1;
                     if (!mbar_wait(&empty[st], ph ^ 1)) { fail(); break; }
                     mbar_arrive_expect_tx(&full[st], kPfABytes + kPfBBytes);
                     if (ks < KB) {
-                        tma_load_2d(sA + st * kPfABytes, &tmap_x, &full[st], ks * kPfBK, mt * kPfBM);
+                        tma_load_2d(sA + st * kPfABytes, mx, &full[st], ks * kPfBK, mt * kPfBM);
                         tma_load_2d(sB + st * kPfBBytes, &tmap_w, &full[st], ks * kPfBK, nt * kPfBN);
                     } else {
                         tma_load_2d(sA + st * kPfABytes, &tmap_ta, &full[st], (ks - KB) * kPfBK, mt * kPfBM);
@@ -910,20 +937,25 @@ static cudaError_t run_token_side_and_gemm(const PfRun &q, cudaStream_t s, const
     xcfg.stream = s;
     xcfg.attrs = attr;
     xcfg.numAttrs = 1;
+    const int direct = q.noise == nullptr ? 1 : 0;
     cudaError_t e = cudaLaunchKernelEx(&xcfg, prefill_xprep_kernel<false>, q.x, q.noise, M, K, q.lora_in, r,
-                                       pl.ES, q.lora_scale, q.tensor_scale, xh, pexp, ta, flags);
+                                       pl.ES, q.lora_scale, q.tensor_scale, xh, pexp, ta, flags, direct);
     if (e != cudaSuccess)
         return e;
     prefill_xprep_kernel<true><<<xgrid, kXpThreads, kXpSmem, s>>>(q.x, q.noise, M, K, q.lora_in, r, pl.ES,
                                                                    q.lora_scale, q.tensor_scale, xh, pexp, ta,
-                                                                   flags);
+                                                                   flags, direct);
     e = cudaGetLastError();
     if (e != cudaSuccess)
         return e;
 
-    CUtensorMap tmx, tmw, tma_, tmb;
+    CUtensorMap tmx, tmxd, tmw, tma_, tmb;
     e = encode_tensor_map_2d(&tmx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, xh, (uint64_t)K, (uint64_t)M,
                              (uint64_t)K * 2, kPfBK, kPfBM, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (e == cudaSuccess)
+        e = direct ? encode_tensor_map_2d(&tmxd, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, q.x, (uint64_t)K, (uint64_t)M,
+                                          (uint64_t)K * 2, kPfBK, kPfBM, CU_TENSOR_MAP_SWIZZLE_128B)
+                   : (tmxd = tmx, cudaSuccess);
     if (e == cudaSuccess)
         e = encode_tensor_map_2d(&tmw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, wh, (uint64_t)K, (uint64_t)N,
                                  (uint64_t)K * 2, kPfBK, kPfBN, CU_TENSOR_MAP_SWIZZLE_128B);
@@ -950,6 +982,8 @@ static cudaError_t run_token_side_and_gemm(const PfRun &q, cudaStream_t s, const
     p.lora_scale = q.lora_scale;
     p.pexp = pexp;
     p.colscale = q.colscale;
+    p.flags = flags;
+    p.direct = direct;
     p.y = q.y;
     p.y_fp32 = q.y_fp32 ? 1 : 0;
     p.ctl = reinterpret_cast<uint32_t *>(q.ws);
@@ -968,7 +1002,7 @@ static cudaError_t run_token_side_and_gemm(const PfRun &q, cudaStream_t s, const
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, prefill_gemm_kernel, tmx, tmw, tma_, tmb, p);
+    e = cudaLaunchKernelEx(&cfg, prefill_gemm_kernel, tmx, tmxd, tmw, tma_, tmb, p);
     if (e != cudaSuccess)
         return e;
     return cudaGetLastError();

@@ -48,9 +48,10 @@ def test_gemm_with_extreme_tensor_scale(nv, orc, M, N, K, r, w_std, lora):
 ROW_EXP = [None, -120, -70, -40, 0, 20, 40, 100]
 
 
+@pytest.mark.parametrize("noise", [True, False])
 @pytest.mark.parametrize("M,N,K,r", SHAPES)
-def test_gemm_with_extreme_token_magnitudes(nv, orc, M, N, K, r):
-    c = synth.small_case(M, N, K, r, seed=5 * M + K)
+def test_gemm_with_extreme_token_magnitudes(nv, orc, M, N, K, r, noise):
+    c = synth.small_case(M, N, K, r, seed=5 * M + K, with_noise=noise)
     x = synth.bf16_bits_to_f32(c.x).astype(np.float64)
     for i in range(M):
         e = ROW_EXP[i % len(ROW_EXP)]
