@@ -660,6 +660,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_gemm_kernel(const __grid_c
         }
         pdl_wait();
         if (lane == 0) {
+            const uint64_t drop = l2_policy_evict_first();
             // a unit's record: 2^p, T_c and the first M rows of X'
             const uint32_t rbytes = (uint32_t)(kFacBytes + t_bytes(p.KS, MP)) + (uint32_t)p.M * 1024u;
             int q = 0;  // segment
@@ -679,10 +680,13 @@ __global__ void __launch_bounds__(kThreads, 1) stream_gemm_kernel(const __grid_c
                 const bool two = (c + 1) * kChunk <= p.K;  // else a last 256-column chunk
                 uint8_t *st = smem + (size_t)s * stage_bytes<MP>();
                 mbar_arrive_expect_tx(&full[s], (two ? 2 : 1) * kBoxBytes + kScaleBox + rbytes);
-                tma_load_2d(st, &p.tm_codes, &full[s], c * (kChunk / 2), n * kRows);
+                // the weight stream is read once: evict-first, so that the small
+                // reused operands (X, A, B, the records) keep their L2 lines
+                tma_load_2d_hint(st, &p.tm_codes, &full[s], c * (kChunk / 2), n * kRows, drop);
                 if (two)
-                    tma_load_2d(st + kBoxBytes, &p.tm_codes, &full[s], c * (kChunk / 2) + 128, n * kRows);
-                tma_load_2d(st + 2 * kBoxBytes, &p.tm_scales, &full[s], c * (kChunk / 16), n * kRows);
+                    tma_load_2d_hint(st + kBoxBytes, &p.tm_codes, &full[s], c * (kChunk / 2) + 128, n * kRows,
+                                     drop);
+                tma_load_2d_hint(st + 2 * kBoxBytes, &p.tm_scales, &full[s], c * (kChunk / 16), n * kRows, drop);
                 bulk_g2s(st + kXhOff, p.rec + (size_t)c * p.rec_bytes, rbytes, &full[s]);
                 if (p.bsm && (u + 1 == u1 || c + 1 == p.C)) {
                     // the tile's B rows, for the epilogue of the segment this unit ends
