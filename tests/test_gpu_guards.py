@@ -1,8 +1,9 @@
 """Out-of-bounds writes (compute-sanitizer is closed on this machine): every
 output buffer and the workspace sit between guard bytes holding a fixed
 pattern, which must be untouched after each call, on ragged and tiled shapes
-of every kernel family (quantiser both modes, dequantiser, scale update, and
-the GEMM's streaming, register-streaming and tcgen05 paths)."""
+of every kernel family (quantiser both modes, dequantiser, scale update, the
+GEMM's streaming, register-streaming and tcgen05 paths, and the input
+gradient)."""
 import numpy as np
 import pytest
 import torch
@@ -88,4 +89,32 @@ def test_gemm_stays_in_bounds(nv, M, N, K, r):
                                      y.view(dt, (M, N)), ws.view(torch.uint8, (ws.n,)))
         assert nv.nvfp4_get_device_status(ws.view(torch.uint8, (ws.n,))) == nv.OK
         assert y.intact(), "output guard overwritten"
+        assert ws.intact(), "workspace guard overwritten"
+
+
+# M, N, K, r for the input gradient (N, K multiples of 64): ragged tiles of
+# tokens and of output columns, both extension widths, one rescaled token
+DGRAD_CASES = [(1, 64, 64, 0), (5, 128, 320, 8), (130, 192, 640, 40), (200, 320, 1024, 32), (333, 512, 192, 64)]
+
+
+@pytest.mark.parametrize("M,N,K,r", DGRAD_CASES)
+def test_dgrad_stays_in_bounds(nv, M, N, K, r):
+    c = synth.small_case(M, N, K, max(r, 1), seed=3 * M + N + K, with_lora=r > 0, with_noise=True)
+    q = nv.quantize(_dev(c.w))
+    a = _dev(c.a) if r > 0 else None
+    b = _dev(c.b) if r > 0 else None
+    z = torch.from_numpy(c.z).cuda()
+    g = synth.bf16_bits_to_f32(synth.activations(M, N, M + 1))
+    g[M // 2] *= 2.0 ** 50  # one token outside [2^-64, 2^32]: the rescaling kernel runs too
+    dy = _dev(synth.to_bf16_bits(g))
+    need = nv.nvfp4_dgrad_workspace_bytes(M, N, K, r)
+    assert need > 0
+    for dt, es in ((torch.float32, 4), (torch.bfloat16, 2)):
+        dx = Guarded(M * K * es)
+        ws = Guarded((need + 255) // 256 * 256, fill=0)
+        for _ in range(2):  # a second call on the same workspace
+            nv.nvfp4_w4a16_lora_gemm_dgrad(dy, q.codes, q.scales, q.tensor_scale, a, b, c.lora_scale if r else 0.0,
+                                           z, dx.view(dt, (M, K)), ws.view(torch.uint8, (ws.n,)))
+        assert nv.nvfp4_get_device_status(ws.view(torch.uint8, (ws.n,))) == nv.OK
+        assert dx.intact(), "output guard overwritten"
         assert ws.intact(), "workspace guard overwritten"
