@@ -325,26 +325,29 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     const float rd = d_fast ? __frcp_rn(d) : 0.0f;
     __syncthreads();
 
-    // pass 2: from the end of the share backwards, two blocks in flight per thread
-    for (int64_t bb = b1 - 1 - tid; bb >= b0; bb -= 2 * kFusedThreads) {
-        const int64_t bc = bb - kFusedThreads;
-        uint4 v0a, v1a, v0b = make_uint4(0u, 0u, 0u, 0u), v1b = v0b;
-        if (bb >= cache_from) {
-            v0a = s_cache[2 * (bb - cache_from)];
-            v1a = s_cache[2 * (bb - cache_from) + 1];
+    // pass 2: from the end of the share backwards, two blocks per step per
+    // thread; the next step's two blocks are requested before this step's
+    // are quantised (software pipelining: up to four blocks in flight)
+    auto fetch = [&](int64_t b, uint4 &v0, uint4 &v1) {
+        if (b < b0) {
+            v0 = v1 = make_uint4(0u, 0u, 0u, 0u);
+        } else if (b >= cache_from) {
+            v0 = s_cache[2 * (b - cache_from)];
+            v1 = s_cache[2 * (b - cache_from) + 1];
         } else {
-            v0a = ld_hint_u4(w + 2 * bb, drop);
-            v1a = ld_hint_u4(w + 2 * bb + 1, drop);
+            v0 = ld_hint_u4(w + 2 * b, drop);
+            v1 = ld_hint_u4(w + 2 * b + 1, drop);
         }
-        if (bc >= b0) {
-            if (bc >= cache_from) {
-                v0b = s_cache[2 * (bc - cache_from)];
-                v1b = s_cache[2 * (bc - cache_from) + 1];
-            } else {
-                v0b = ld_hint_u4(w + 2 * bc, drop);
-                v1b = ld_hint_u4(w + 2 * bc + 1, drop);
-            }
-        }
+    };
+    int64_t bb = b1 - 1 - tid;
+    uint4 v0a, v1a, v0b, v1b;
+    fetch(bb, v0a, v1a);
+    fetch(bb - kFusedThreads, v0b, v1b);
+    for (; bb >= b0; bb -= 2 * kFusedThreads) {
+        const int64_t bc = bb - kFusedThreads;
+        uint4 n0a, n1a, n0b, n1b;
+        fetch(bb - 2 * kFusedThreads, n0a, n1a);
+        fetch(bc - 2 * kFusedThreads, n0b, n1b);
         uint2 cw;
         uint32_t e;
         quantize_block(v0a, v1a, s_t, d, d_fast, rd, s_S, s_R, cw, e, ctl);
@@ -355,6 +358,10 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
             codes[bc] = cw;
             scales[bc] = (uint8_t)e;
         }
+        v0a = n0a;
+        v1a = n1a;
+        v0b = n0b;
+        v1b = n1b;
     }
 
     // the last block out leaves the amax word at zero for the next call
