@@ -2,10 +2,11 @@
 (q/o 3584x3584, k/v 512x3584, gate/up 18944x3584, down 3584x18944), BF16
 weights ~N(0, 0.02^2) drawn on the device from seeded generators, every one of
 the 196 matrices quantised with its own dynamic tensor scale and multiplied by
-the same 8 tokens.
+the same 8 tokens, with a LoRA pair (r = 32, s = 2) of its own and the
+multiplicative input noise (sigma 5e-4, one vector per input width).
 
 Each matrix is checked against the oracle on sampled rows: the row holding the
-matrix's largest |w| plus three random rows, quantised by the oracle in
+matrix's largest |w| plus seven random rows, quantised by the oracle in
 dynamic mode (so its tensor scale comes from the same amax), must give the
 GPU's tensor scale, codes and block scales bit for bit, and the GPU's GEMM
 outputs for those rows must match the oracle's FP64 GEMM within tolerance.
@@ -25,10 +26,12 @@ SHAPES = [("q", 3584, 3584), ("k", 512, 3584), ("v", 512, 3584), ("o", 3584, 358
 
 
 def test_whole_stack_quantise_and_decode(nv, orc):
-    M = 8
+    M, r, s = 8, 32, 2.0
     xb = {K: synth.activations(M, K, 70 + K) for K in (3584, 18944)}
     xd = {K: torch.from_numpy(b.view(np.int16)).view(torch.bfloat16).cuda() for K, b in xb.items()}
-    ws = nv.new_workspace(max(nv.nvfp4_workspace_bytes(M, N, K, 0) for _, N, K in SHAPES))
+    zh = {K: synth.noise_vector(K, 5e-4, 90 + K) for K in (3584, 18944)}
+    zd = {K: torch.from_numpy(v).cuda() for K, v in zh.items()}
+    ws = nv.new_workspace(max(nv.nvfp4_workspace_bytes(M, N, K, r) for _, N, K in SHAPES))
     gen = torch.Generator(device="cuda")
     pick = np.random.default_rng(2048)
     checked = 0
@@ -36,10 +39,12 @@ def test_whole_stack_quantise_and_decode(nv, orc):
         for j, (name, N, K) in enumerate(SHAPES):
             gen.manual_seed(1000 * layer + j)
             w = (torch.randn((N, K), generator=gen, device="cuda") * 0.02).to(torch.bfloat16)
+            a = (torch.randn((r, K), generator=gen, device="cuda") * 0.01).to(torch.bfloat16)
+            b = (torch.randn((N, r), generator=gen, device="cuda") * 0.01).to(torch.bfloat16)
             q = nv.quantize(w, workspace=ws)
-            y = nv.gemm(xd[K], q, workspace=ws)
+            y = nv.gemm(xd[K], q, a, b, s, zd[K], workspace=ws)
             top = int(torch.argmax(w.abs().float()).item()) // K
-            rows = [top] + [int(r) for r in pick.choice(np.delete(np.arange(N), top), size=3, replace=False)]
+            rows = [top] + [int(i) for i in pick.choice(np.delete(np.arange(N), top), size=7, replace=False)]
             wb = w[rows].view(torch.int16).cpu().numpy().view(np.uint16)
             rc, codes, scales, st = orc.quantize(wb)
             assert rc == orc.OK
@@ -47,9 +52,10 @@ def test_whole_stack_quantise_and_decode(nv, orc):
             assert np.float32(q.tensor_scale.item()) == st, where
             assert np.array_equal(q.codes[rows].cpu().numpy(), codes), where
             assert np.array_equal(q.scales[rows].cpu().numpy(), scales), where
-            ref = orc.gemm(xb[K], codes, scales, st)
+            bits = lambda t: t.view(torch.int16).cpu().numpy().view(np.uint16)
+            ref = orc.gemm(xb[K], codes, scales, st, bits(a), bits(b[rows]), s, zh[K])
             _check(y[:, rows].cpu().numpy(), ref)
             checked += 1
-            del w, q, y
+            del w, a, b, q, y
     assert checked == LAYERS * len(SHAPES)
     assert nv.nvfp4_get_device_status(ws) == nv.OK
