@@ -70,6 +70,8 @@ def _configure(lib):
     lib.orc_gemm_dgrad.restype = ctypes.c_int
     lib.orc_gemm_dgrad.argtypes = [P, i64, i64, i64, P, P, ctypes.c_float, P, P, i64,
                                    ctypes.c_float, P, P, ctypes.c_int]
+    lib.orc_lora_grads.restype = ctypes.c_int
+    lib.orc_lora_grads.argtypes = [P, P, P, i64, i64, i64, P, P, i64, ctypes.c_float, P, P, ctypes.c_int]
     return lib
 
 
@@ -228,3 +230,24 @@ def gemm_dgrad(dy_bits, codes, scales, s_t, a_bits=None, b_bits=None, lora_scale
     if rc != OK:
         raise ValueError(f"oracle dgrad status {rc}")
     return dx
+
+
+def lora_grads(x_bits, dy_bits, a_bits, b_bits, lora_scale, z=None, nthreads=None):
+    """(dA (r, K), dB (N, r)) float64: dA = s (dY B)^T X', dB = s dY^T (X' A^T),
+    X' = bf16(X z)."""
+    x = _c(x_bits, np.uint16)
+    dy = _c(dy_bits, np.uint16)
+    A = _c(a_bits, np.uint16)
+    B = _c(b_bits, np.uint16)
+    M, K = x.shape
+    N = dy.shape[1]
+    r = A.shape[0]
+    if dy.shape[0] != M or A.shape[1] != K or B.shape != (N, r):
+        raise ValueError("shapes do not match")
+    da = np.zeros((r, K), np.float64)
+    db = np.zeros((N, r), np.float64)
+    rc = _load().orc_lora_grads(_ptr(x), _ptr(_c(z, np.float32)), _ptr(dy), M, N, K, _ptr(A), _ptr(B), r,
+                                float(lora_scale), _ptr(da), _ptr(db), nthreads or default_threads())
+    if rc != OK:
+        raise ValueError(f"oracle lora_grads status {rc}")
+    return da, db

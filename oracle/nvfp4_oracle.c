@@ -26,7 +26,8 @@
  *     section "Метод").
  *   - The layer's input gradient with the quantised weight frozen and only
  *     the LoRA factors trained (same section): dX = (dY deq(W) + s (dY B) A)
- *     diag(z), the bf16 rounding of X' taken as the identity.
+ *     diag(z), the bf16 rounding of X' taken as the identity; and the LoRA
+ *     factors' gradients dB = s dY^T (X' A^T), dA = s (dY B)^T X'.
  *
  * Every encoder is a brute-force nearest search over the enumerated finite
  * grid (ties to the code whose least significant bit is 0); every GEMM is a
@@ -38,7 +39,9 @@
  * error bound, the 8/9 code share, the scale-only-update invariants, exact
  * rational brute force on tiny GEMMs and exact dyadic cases; for the input
  * gradient the exact adjoint identity <dY, Y(X)> = <dX, X> against the
- * forward, float64 autograd and exact rationals (test_oracle_dgrad.py).
+ * forward, float64 autograd and exact rationals (test_oracle_dgrad.py); for
+ * the LoRA gradients the forward's exact linearity in A and in B, float64
+ * autograd and exact rationals (test_oracle_lora_grads.py).
  */
 #include <math.h>
 #include <pthread.h>
@@ -471,6 +474,82 @@ int orc_gemm_dgrad(const uint16_t *dy, int64_t M, int64_t N, int64_t K,
         }
     struct dgrad_ctx c = {dy, N, K, r, codes, scales, (double)s_t, (double)s, U, A, z, dx};
     for_rows(M, nthreads, dgrad_row, &c);
+    free(U);
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------ */
+/* Gradients of the LoRA factors, in double                            */
+/* ------------------------------------------------------------------ */
+
+/* The trained parameters are A and B ("RL with NVFP4 + LoRA", section
+ * "Метод").  With T = X' A^T and the LoRA term s T B^T of Y:
+ *   dB = s dY^T T          (N x r),
+ *   dA = s (dY B)^T X'     (r x K),
+ * X' = bf16(X z) as in the forward. */
+struct lgrad_ctx {
+    const uint16_t *xp, *dy;
+    int64_t M, N, K, r;
+    double s;
+    const double *T, *U; /* M x r each */
+    double *da, *db;
+};
+
+static void lgrad_b_row(void *p, int64_t n)
+{
+    struct lgrad_ctx *c = (struct lgrad_ctx *)p;
+    for (int64_t j = 0; j < c->r; j++) {
+        double acc = 0.0;
+        for (int64_t m = 0; m < c->M; m++)
+            acc += (double)orc_bf16_to_f32(c->dy[m * c->N + n]) * c->T[m * c->r + j];
+        c->db[n * c->r + j] = c->s * acc;
+    }
+}
+
+static void lgrad_a_row(void *p, int64_t j)
+{
+    struct lgrad_ctx *c = (struct lgrad_ctx *)p;
+    for (int64_t k = 0; k < c->K; k++) {
+        double acc = 0.0;
+        for (int64_t m = 0; m < c->M; m++)
+            acc += c->U[m * c->r + j] * (double)orc_bf16_to_f32(c->xp[m * c->K + k]);
+        c->da[j * c->K + k] = c->s * acc;
+    }
+}
+
+/* da: r x K, db: N x r (double).  x: M x K bf16, z: K floats or NULL, dy:
+ * M x N bf16, A: r x K bf16, B: N x r bf16. */
+int orc_lora_grads(const uint16_t *x, const float *z, const uint16_t *dy, int64_t M, int64_t N, int64_t K,
+                   const uint16_t *A, const uint16_t *B, int64_t r, float s, double *da, double *db,
+                   int nthreads)
+{
+    if (M < 0 || N < 0 || K < 0 || r < 1 || !A || !B)
+        return ORC_BAD_SHAPE;
+    uint16_t *xp = (uint16_t *)malloc((size_t)(M * K + 1) * 2);
+    double *T = (double *)malloc((size_t)(M * r + 1) * sizeof(double));
+    double *U = (double *)malloc((size_t)(M * r + 1) * sizeof(double));
+    if (!xp || !T || !U) {
+        free(xp);
+        free(T);
+        free(U);
+        return ORC_BAD_SHAPE;
+    }
+    orc_noisy_input(x, z, M, K, xp);
+    for (int64_t m = 0; m < M; m++)
+        for (int64_t j = 0; j < r; j++) {
+            double t = 0.0, u = 0.0;
+            for (int64_t k = 0; k < K; k++)
+                t += (double)orc_bf16_to_f32(xp[m * K + k]) * (double)orc_bf16_to_f32(A[j * K + k]);
+            for (int64_t n = 0; n < N; n++)
+                u += (double)orc_bf16_to_f32(dy[m * N + n]) * (double)orc_bf16_to_f32(B[n * r + j]);
+            T[m * r + j] = t;
+            U[m * r + j] = u;
+        }
+    struct lgrad_ctx c = {xp, dy, M, N, K, r, (double)s, T, U, da, db};
+    for_rows(N, nthreads, lgrad_b_row, &c);
+    for_rows(r, nthreads, lgrad_a_row, &c);
+    free(xp);
+    free(T);
     free(U);
     return ORC_OK;
 }

@@ -14,6 +14,7 @@ import oracle
 from tests import test_oracle_codecs as codecs
 from tests import test_oracle_dgrad as dgrad
 from tests import test_oracle_gemm as gemm
+from tests import test_oracle_lora_grads as lgrads
 from tests import test_oracle_quantize as quant
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "nvfp4_oracle.c")
@@ -47,8 +48,9 @@ MUTATIONS = [
      "float x = orc_bf16_to_f32(row[b * 16 + i]) * (1.0f / S_b);"),
     ("zero block scale not special-cased", "if (S_b != 0.0f) {", "if (1) {"),
     ("tensor amax without abs", "float v = fabsf(orc_bf16_to_f32(w[i]));", "float v = orc_bf16_to_f32(w[i]);"),
-    ("LoRA branch without noise", "t += (double)orc_bf16_to_f32(xp[m * K + k])",
-     "t += (double)orc_bf16_to_f32(x[m * K + k])"),
+    ("LoRA branch without noise",
+     "t += (double)orc_bf16_to_f32(xp[m * K + k]) * (double)orc_bf16_to_f32(A[j * K + k]);\n            T[m * r + j] = t;",
+     "t += (double)orc_bf16_to_f32(x[m * K + k]) * (double)orc_bf16_to_f32(A[j * K + k]);\n            T[m * r + j] = t;"),
     ("frozen scale ignored", "    if (given) {\n        s_t = *st_io;", "    if (0) {\n        s_t = *st_io;"),
     ("dequant scales by s_t before the block scale",
      "float vd = (float)(orc_e2m1_value(code_at(codes, K, n, k)) *\n                               orc_e4m3_value(scales[n * (K / 16) + k / 16]));\n            float v = vd * s_t;",
@@ -59,7 +61,9 @@ MUTATIONS = [
     ("LoRA down-projection in float", "            double t = 0.0;", "            float t = 0.0f;"),
     ("negative scale parameter not zeroed", "(s_t == 0.0f || p <= 0.0f) ? 0.0f : p / s_t",
      "(s_t == 0.0f) ? 0.0f : fabsf(p) / s_t"),
-    ("LoRA A read transposed", "(double)orc_bf16_to_f32(A[j * K + k])", "(double)orc_bf16_to_f32(A[k * r + j])"),
+    ("LoRA A read transposed",
+     "(double)orc_bf16_to_f32(A[j * K + k]);\n            T[m * r + j] = t;",
+     "(double)orc_bf16_to_f32(A[k * r + j]);\n            T[m * r + j] = t;"),
     ("block amax over half the block", "        float a_b = 0.0f;\n        for (int i = 0; i < 16; i++) {",
      "        float a_b = 0.0f;\n        for (int i = 0; i < 8; i++) {"),
     ("LoRA scale on the base term", "c->y[m * c->N + n] = acc + c->s * lora;", "c->y[m * c->N + n] = c->s * acc + lora;"),
@@ -74,8 +78,8 @@ MUTATIONS = [
      "c->dx[m * c->K + k] = g;"),
     ("dgrad LoRA scale dropped", "double g = acc + c->s * lora;", "double g = acc + lora;"),
     ("dgrad LoRA term subtracted", "double g = acc + c->s * lora;", "double g = acc - c->s * lora;"),
-    ("dgrad LoRA B read transposed", "(double)orc_bf16_to_f32(B[n * r + j])",
-     "(double)orc_bf16_to_f32(B[j * N + n])"),
+    ("dgrad LoRA B read transposed", "(double)orc_bf16_to_f32(B[n * r + j]);\n            U[m * r + j] = u;",
+     "(double)orc_bf16_to_f32(B[j * N + n]);\n            U[m * r + j] = u;"),
     ("dgrad LoRA A read transposed", "(double)orc_bf16_to_f32(c->A[j * c->K + k])",
      "(double)orc_bf16_to_f32(c->A[k * c->r + j])"),
     ("dgrad tensor scale dropped", "* c->s_t;\n            acc += (double)orc_bf16_to_f32(c->dy",
@@ -86,6 +90,20 @@ MUTATIONS = [
     ("dgrad LoRA down-projection in float", "            double u = 0.0;", "            float u = 0.0f;"),
     ("dgrad uses the first dY row for every row", "acc += (double)orc_bf16_to_f32(c->dy[m * c->N + n]) * d;",
      "acc += (double)orc_bf16_to_f32(c->dy[n]) * d;"),
+    ("dB scale dropped", "c->db[n * c->r + j] = c->s * acc;", "c->db[n * c->r + j] = acc;"),
+    ("dA scale dropped", "c->da[j * c->K + k] = c->s * acc;", "c->da[j * c->K + k] = acc;"),
+    ("dB from U instead of T", "* c->T[m * c->r + j];", "* c->U[m * c->r + j];"),
+    ("dA from T instead of U", "acc += c->U[m * c->r + j] * (double)orc_bf16_to_f32(c->xp",
+     "acc += c->T[m * c->r + j] * (double)orc_bf16_to_f32(c->xp"),
+    ("dB written transposed", "c->db[n * c->r + j] = c->s * acc;", "c->db[j * c->N + n] = c->s * acc;"),
+    ("LoRA gradients without noise",
+     "    orc_noisy_input(x, z, M, K, xp);\n    for (int64_t m = 0; m < M; m++)\n        for (int64_t j = 0; j < r; j++) {\n            double t = 0.0, u = 0.0;",
+     "    orc_noisy_input(x, NULL, M, K, xp);\n    for (int64_t m = 0; m < M; m++)\n        for (int64_t j = 0; j < r; j++) {\n            double t = 0.0, u = 0.0;"),
+    ("U with B read transposed", "(double)orc_bf16_to_f32(B[n * r + j]);\n            T[m * r + j] = t;",
+     "(double)orc_bf16_to_f32(B[j * N + n]);\n            T[m * r + j] = t;"),
+    ("T of the gradients with A read transposed",
+     "(double)orc_bf16_to_f32(A[j * K + k]);\n            for (int64_t n = 0; n < N; n++)",
+     "(double)orc_bf16_to_f32(A[k * r + j]);\n            for (int64_t n = 0; n < N; n++)"),
     ("array encoder skips the last element of each piece",
      "int64_t lo = r * c->per, hi = lo + c->per < c->n ? lo + c->per : c->n;",
      "int64_t lo = r * c->per, hi = lo + c->per - 1 < c->n ? lo + c->per - 1 : c->n;"),
@@ -120,6 +138,10 @@ PINS = [
     lambda o: dgrad.test_matches_float64_autograd(o, True, True),
     lambda o: dgrad.test_vs_exact_rationals(o, 2, 6, 32, 3),
     dgrad.test_degenerate_cases,
+    lambda o: lgrads.test_linear_in_each_factor_exact(o, 3, 16, 64, 4),
+    lambda o: lgrads.test_matches_float64_autograd(o, True),
+    lgrads.test_vs_exact_rationals,
+    lgrads.test_degenerate_cases,
 ]
 
 
