@@ -451,6 +451,7 @@ def run_gpu(args):
         if not args.no_prefill:
             line["prefill"] = run_prefill_case(torch, nv, synth, peak_tf)
             line["dgrad"] = run_dgrad_case(torch, nv, synth, peak_tf)
+            line["lora_grads"] = run_lora_grads_case(torch, nv, synth, peak_hbm)
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(seconds=args.cpu_seconds)
         print(json.dumps(line), flush=True)
@@ -640,6 +641,29 @@ def run_dgrad_case(torch, nv, synth, peak_tf):
             "frac": round(f / ms / 1e9 / peak_tf, 4)}
 
 
+def run_lora_grads_case(torch, nv, synth, peak_hbm):
+    """LoRA factor gradients for 16384 tokens of the 7B up shape: dA (32 x 3584)
+    and dB (18944 x 32) from X, z, dY, A, B.  HBM-bound: the algorithmic bytes
+    are one read of X and of dY (and of A, B) plus the two outputs."""
+    M, (N, K) = 16384, UP
+    dev = lambda b: torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(torch.bfloat16).cuda()
+    a, b = synth.lora_pair(N, K, R_LORA, 0.01, 2)
+    a, b = dev(a), dev(b)
+    z = torch.from_numpy(synth.noise_vector(K, SIGMA, 3)).cuda()
+    x = dev(synth.activations(M, K, 10))
+    dy = dev(synth.activations(M, N, 11, std=1e-3))
+    ga = torch.empty((R_LORA, K), dtype=torch.float32, device="cuda")
+    gb = torch.empty((N, R_LORA), dtype=torch.float32, device="cuda")
+    ws = nv.new_workspace(nv.nvfp4_lora_grads_workspace_bytes(M, N, K, R_LORA))
+    op = lambda: nv.nvfp4_lora_grads(x, z, dy, a, b, LORA_SCALE, ga, gb, ws)
+    op()
+    ms = time_replays(torch, [op], 5)
+    nbytes = 2.0 * M * (K + N) + 2.0 * R_LORA * (K + N) + 4.0 * K + 4.0 * R_LORA * (K + N)
+    return {"workload": "dA 32 x 3584, dB 18944 x 32 from X 16384 x 3584 (noise) and dY 16384 x 18944",
+            "ms": round(ms, 3), "GB/s": round(nbytes / ms / 1e6, 1), "peak_hbm_gbs": peak_hbm,
+            "frac": round(nbytes / ms / 1e6 / peak_hbm, 4)}
+
+
 def run_e2e(torch, nv, wl, dev, args):
     """Public-API step with host buffers: pinned inputs copied in, outputs back."""
     t = torch
@@ -803,7 +827,7 @@ def run_kernel_case(case, reps):
     dev = lambda b: torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(torch.bfloat16).cuda()
     wb = synth.normal_weight(shape, 0.02, 0, outlier_frac=1e-3, outlier_mult=20.0)
     w = dev(wb)
-    M = int(parts[2][1:]) if kind == "gemm" else (16384 if kind in ("prefill", "dgrad") else 0)
+    M = int(parts[2][1:]) if kind == "gemm" else (16384 if kind in ("prefill", "dgrad", "loragrads") else 0)
     ws = nv.new_workspace(max(nv.nvfp4_workspace_bytes(max(M, 1), *shape, R_LORA),
                               nv.nvfp4_dgrad_workspace_bytes(max(M, 1), *shape, R_LORA)))
     q = nv.quantize(w, workspace=ws)
@@ -811,6 +835,17 @@ def run_kernel_case(case, reps):
         frozen = len(parts) > 2 and parts[2] == "frozen"
         op = lambda: nv.nvfp4_quantize(w, q.codes, q.scales, q.tensor_scale, frozen, ws)
         nbytes, flops = quant_bytes(*shape), 0.0
+    elif kind == "loragrads":
+        a, b = synth.lora_pair(shape[0], shape[1], R_LORA, 0.01, 2)
+        a, b = dev(a), dev(b)
+        z = torch.from_numpy(synth.noise_vector(shape[1], SIGMA, 3)).cuda()
+        x = dev(synth.activations(M, shape[1], 10))
+        dy = dev(synth.activations(M, shape[0], 11, std=1e-3))
+        ga = torch.empty((R_LORA, shape[1]), dtype=torch.float32, device="cuda")
+        gb = torch.empty((shape[0], R_LORA), dtype=torch.float32, device="cuda")
+        ws = nv.new_workspace(nv.nvfp4_lora_grads_workspace_bytes(M, *shape, R_LORA))
+        op = lambda: nv.nvfp4_lora_grads(x, z, dy, a, b, LORA_SCALE, ga, gb, ws)
+        nbytes, flops = 2.0 * M * (shape[0] + shape[1]), 0.0
     elif kind == "dgrad":
         a, b = synth.lora_pair(shape[0], shape[1], R_LORA, 0.01, 2)
         a, b = dev(a), dev(b)

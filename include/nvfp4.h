@@ -158,7 +158,33 @@ nvfp4_status nvfp4_w4a16_lora_gemm_dgrad(const void *dy_bf16, int64_t M, int64_t
  * does not take). */
 size_t nvfp4_dgrad_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t r);
 
-/* Scale-QLoRA forward (Scale-QLoRA post, method): the block scales are
+/* Gradients of the LoRA factors of nvfp4_w4a16_lora_gemm's layer, the
+ * parameters the RL post trains on a frozen NVFP4 weight ("RL with NVFP4 +
+ * LoRA", section "Метод"):
+ *     grad_b = lora_scale dY^T (X' A^T)      (N x r, FP32),
+ *     grad_a = lora_scale (dY B)^T X'        (r x K, FP32),
+ * X' = bf16(X z) as in the forward.
+ *   x_bf16: M x K, noise_fp32: K floats or NULL, dy_bf16: M x N (device);
+ *   lora_a_bf16: r x K, lora_b_bf16: N x r; grad_a, grad_b: device FP32,
+ *   overwritten (not accumulated).
+ * Shapes: M >= 1; N and K multiples of 64; 1 <= r <= 64 (else
+ * NVFP4_ERR_SHAPE).  The token sums run in FP32 on the tensor cores with the
+ * (X' A^T) and (dY B) rows as bf16 hi + lo pairs; the token ranges' partial sums are
+ * added in a fixed order, so results do not depend on scheduling.  Every
+ * check runs before anything is queued.  workspace:
+ * nvfp4_lora_grads_workspace_bytes(M, N, K, r) bytes, 16-byte aligned, owned
+ * by the caller; calls that share a workspace must not overlap in time. */
+nvfp4_status nvfp4_lora_grads(const void *x_bf16, const float *noise_fp32, const void *dy_bf16,
+                              int64_t M, int64_t N, int64_t K,
+                              const void *lora_a_bf16, const void *lora_b_bf16, int64_t r,
+                              float lora_scale, float *grad_a, float *grad_b,
+                              void *workspace, size_t ws_bytes, void *stream);
+
+/* Bytes of workspace needed by nvfp4_lora_grads (0 for shapes it does not
+ * take). */
+size_t nvfp4_lora_grads_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t r);
+
+/* Scale-QLoRA forward/* Scale-QLoRA forward (Scale-QLoRA post, method): the block scales are
  * trainable FP32 parameters (decoded block scales in weight units, N x K/16,
  * as for nvfp4_round_scales) and the codes stay frozen.  Each call rounds the
  * parameters to E4M3 against *tensor_scale into scales_e4m3 (exactly

@@ -27,6 +27,7 @@ EXPORTS = [
     "nvfp4_round_scales", "nvfp4_get_device_status", "nvfp4_status_string", "nvfp4_encode_debug",
     "nvfp4_quotient_check", "nvfp4_w4a16_lora_gemm_static", "nvfp4_wait_selftest", "nvfp4_gemm_kernel",
     "nvfp4_scale_qlora_gemm", "nvfp4_w4a16_lora_gemm_dgrad", "nvfp4_dgrad_workspace_bytes",
+    "nvfp4_lora_grads", "nvfp4_lora_grads_workspace_bytes",
 ]
 
 
@@ -74,6 +75,9 @@ def load(build_if_missing: bool = True):
             "nvfp4_w4a16_lora_gemm_dgrad": (st, [P, i64, i64, i64, P, P, P, P, P, i64, ctypes.c_float, P, P,
                                                  ctypes.c_int, P, ctypes.c_size_t, P]),
             "nvfp4_dgrad_workspace_bytes": (ctypes.c_size_t, [i64, i64, i64, i64]),
+            "nvfp4_lora_grads": (st, [P, P, P, i64, i64, i64, P, P, i64, ctypes.c_float, P, P, P, ctypes.c_size_t,
+                                      P]),
+            "nvfp4_lora_grads_workspace_bytes": (ctypes.c_size_t, [i64, i64, i64, i64]),
         }
         for name, (res, args) in sig.items():
             f = getattr(lib, name)
@@ -319,6 +323,42 @@ def gemm_dgrad(dy, q: "QuantizedWeight", lora_a=None, lora_b=None, lora_scale=0.
     nvfp4_w4a16_lora_gemm_dgrad(dy, q.codes, q.scales, q.tensor_scale, lora_a, lora_b, lora_scale, noise,
                                 dx, ws)
     return dx
+
+
+def nvfp4_lora_grads_workspace_bytes(M: int, N: int, K: int, r: int) -> int:
+    return int(load().nvfp4_lora_grads_workspace_bytes(M, N, K, r))
+
+
+def nvfp4_lora_grads(x: torch.Tensor, noise, dy: torch.Tensor, lora_a: torch.Tensor, lora_b: torch.Tensor,
+                     lora_scale: float, grad_a: torch.Tensor, grad_b: torch.Tensor, workspace: torch.Tensor):
+    M, K = x.shape
+    N = dy.shape[1]
+    r = lora_a.shape[0]
+    _need(x, torch.bfloat16, (M, K), "x")
+    _need(dy, torch.bfloat16, (M, N), "dy")
+    _need(lora_a, torch.bfloat16, (r, K), "lora_a")
+    _need(lora_b, torch.bfloat16, (N, r), "lora_b")
+    _need(grad_a, torch.float32, (r, K), "grad_a")
+    _need(grad_b, torch.float32, (N, r), "grad_b")
+    if noise is not None:
+        _need(noise, torch.float32, (K,), "noise")
+    st = load().nvfp4_lora_grads(_ptr(x), _ptr(noise), _ptr(dy), M, N, K, _ptr(lora_a), _ptr(lora_b), r,
+                                 float(lora_scale), _ptr(grad_a), _ptr(grad_b), _ptr(workspace),
+                                 workspace.numel(), _stream())
+    _check(st, "nvfp4_lora_grads")
+
+
+def lora_grads(x, dy, lora_a, lora_b, lora_scale, noise=None, workspace=None):
+    """(dA (r, K), dB (N, r)) float32: dA = s (dY B)^T X', dB = s dY^T (X' A^T)."""
+    M, K = x.shape
+    N = dy.shape[1]
+    r = lora_a.shape[0]
+    ga = torch.empty((r, K), dtype=torch.float32, device=x.device)
+    gb = torch.empty((N, r), dtype=torch.float32, device=x.device)
+    ws = workspace if workspace is not None else new_workspace(nvfp4_lora_grads_workspace_bytes(M, N, K, r),
+                                                              x.device)
+    nvfp4_lora_grads(x, noise, dy, lora_a, lora_b, lora_scale, ga, gb, ws)
+    return ga, gb
 
 
 def gemm(x, q: QuantizedWeight, lora_a=None, lora_b=None, lora_scale=0.0, noise=None,

@@ -243,6 +243,47 @@ nvfp4_status nvfp4_w4a16_lora_gemm_dgrad(const void *dy_bf16, int64_t M, int64_t
     return from_cuda(launch_dgrad_gemm(a, (cudaStream_t)stream, *dev));
 }
 
+size_t nvfp4_lora_grads_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t r)
+{
+    if (!lora_grads_supported(M, N, K, r))
+        return 0;
+    const size_t g = lora_grads_workspace_bytes(M, N, K, r);
+    return g < kCtlBytes ? kCtlBytes : g;
+}
+
+nvfp4_status nvfp4_lora_grads(const void *x_bf16, const float *noise_fp32, const void *dy_bf16, int64_t M,
+                              int64_t N, int64_t K, const void *lora_a_bf16, const void *lora_b_bf16, int64_t r,
+                              float lora_scale, float *grad_a, float *grad_b, void *workspace, size_t ws_bytes,
+                              void *stream)
+{
+    if (!x_bf16 || !dy_bf16 || !lora_a_bf16 || !lora_b_bf16 || !grad_a || !grad_b || !workspace)
+        return NVFP4_ERR_INVALID_ARG;
+    if (!lora_grads_supported(M, N, K, r))
+        return NVFP4_ERR_SHAPE;
+    if (!aligned16(x_bf16) || !aligned16(dy_bf16) || !aligned16(lora_a_bf16) || !aligned16(lora_b_bf16) ||
+        !aligned16(grad_a) || !aligned16(grad_b) || !aligned16(workspace) || (noise_fp32 && !aligned16(noise_fp32)))
+        return NVFP4_ERR_ALIGNMENT;
+    NVFP4_TRY_DEVICE(dev);
+    const size_t need = lora_grads_workspace_bytes(M, N, K, r);
+    if (ws_bytes < (need < kCtlBytes ? kCtlBytes : need))
+        return NVFP4_ERR_WORKSPACE;
+    LoraGradArgs a;
+    a.x = (const uint16_t *)x_bf16;
+    a.dy = (const uint16_t *)dy_bf16;
+    a.noise = noise_fp32;
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.r = r;
+    a.lora_a = (const uint16_t *)lora_a_bf16;
+    a.lora_b = (const uint16_t *)lora_b_bf16;
+    a.lora_scale = lora_scale;
+    a.grad_a = grad_a;
+    a.grad_b = grad_b;
+    a.ws = (uint8_t *)workspace;
+    return from_cuda(launch_lora_grads(a, (cudaStream_t)stream, *dev));
+}
+
 const char *nvfp4_gemm_kernel(int64_t M, int64_t N, int64_t K, int64_t r)
 {
     if (M < 1 || N < 1 || K < 16 || K % 16 != 0 || r < 0 || r > 256 || N > (1LL << 30) || K > (1LL << 30))

@@ -218,7 +218,7 @@ __global__ void __launch_bounds__(kXpThreads, 4)
                          const uint16_t *__restrict__ a, int r, int ES, float lora_scale,
                          const float *__restrict__ tensor_scale, uint16_t *__restrict__ xh,
                          int *__restrict__ pexp_out, uint16_t *__restrict__ ta, int *__restrict__ flags,
-                         int direct)
+                         int direct, float *__restrict__ t_out)
 {
     extern __shared__ __align__(16) uint8_t xp_smem[];
     uint16_t *xs = reinterpret_cast<uint16_t *>(xp_smem + kXpStages * kXpStageBytes);  // X'' staging (bf16)
@@ -365,7 +365,7 @@ __global__ void __launch_bounds__(kXpThreads, 4)
                 }
             }
             const uint4 o = make_uint4(v[0], v[1], v[2], v[3]);
-            if (m < M && (kFix || !direct))
+            if (m < M && (kFix || !direct) && xh)
                 *reinterpret_cast<uint4 *>(xh + (size_t)m * K + k0 + col) = o;
             *reinterpret_cast<uint4 *>(xs + row * kXpLd + col) = o;
         }
@@ -420,8 +420,24 @@ __global__ void __launch_bounds__(kXpThreads, 4)
             flags[blockIdx.x] = *s_need;
     }
 
+    // ---- T'' in fp32 (M x r, in units of 2^p_m), for the LoRA gradients
+    if (t_out && has_lora && nq < ES) {
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+            const int m = m0 + 16 * mt + g + 8 * (q >> 1);
+            if (m >= M)
+                continue;
+#pragma unroll
+            for (int jt = 0; jt < 4; jt++) {
+                const int j = 32 * nq + 8 * jt + 2 * t + (q & 1);
+                if (j < r)
+                    t_out[(size_t)m * r + j] = c[jt][q];
+            }
+        }
+    }
+
     // ---- T'' at the extension columns (every column of [0, 32 ES) once)
-    if (has_lora && nq < ES) {
+    if (has_lora && nq < ES && ta) {
         const float s_t = *tensor_scale;
         const float ratio = lora_fused(lora_scale, s_t) ? __fdiv_rn(lora_scale, s_t != 0.0f ? s_t : 1.0f) : 1.0f;
         const int W = 64 * ES;
@@ -561,8 +577,8 @@ __global__ void __launch_bounds__(256) dgrad_weight_kernel(const uint8_t *__rest
     }
 }
 
-// [A^T | A^T] at the extension columns (K x 64 ES bf16; zero where j >= r)
-// and B^T (r x N bf16).
+// [A^T | A^T] at the extension columns (K x 64 ES bf16; zero where j >= r;
+// skipped when tb is null) and B^T (r x N bf16).
 __global__ void __launch_bounds__(256) dgrad_lora_layout_kernel(const uint16_t *__restrict__ a,
                                                                 const uint16_t *__restrict__ b, int N, int K,
                                                                 int r, int ES, uint16_t *__restrict__ tb,
@@ -571,7 +587,7 @@ __global__ void __launch_bounds__(256) dgrad_lora_layout_kernel(const uint16_t *
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     const int64_t t0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int W = 64 * ES;
-    for (int64_t i = t0; i < (int64_t)K * W; i += stride) {
+    for (int64_t i = t0; tb && i < (int64_t)K * W; i += stride) {
         const int64_t k = i / W;
         const int c = (int)(i % W), j = ES == 1 ? c % 32 : c % 64;
         tb[i] = j < r ? a[(int64_t)j * K + k] : (uint16_t)0;
@@ -579,6 +595,173 @@ __global__ void __launch_bounds__(256) dgrad_lora_layout_kernel(const uint16_t *
     for (int64_t i = t0; i < (int64_t)r * N; i += stride) {
         const int64_t j = i / N, n = i % N;
         bt[i] = b[n * r + j];
+    }
+}
+
+// ---------------------------------------------------------------- LoRA gradients
+// dB = s dY^T T and dA = s (dY B)^T X' are products whose contraction runs over
+// the tokens: Out[p][j] = sum_m G[m][p] H[m][j] with G bf16 (M x P: dY, or
+// X'' for dA) and H fp32 (M x r: T'', or U''), each row of H scaled by
+// 2^(pe1[m] + pe2[m]) (the token-side kernel's p_m).
+// lora_hprep_kernel writes the scaled H once as bf16 hi + lo (2^-16
+// relative), transposed to [j][m] so that the MMA's B fragments are 32-bit
+// loads.  lora_reduce_kernel: a block takes 128 columns p and one range of
+// tokens (split-M; the ranges' sums are added in a fixed order by the third
+// kernel); 64-token tiles of G (64 x 128) and of H (r x 64, hi and lo) come
+// through a 3-stage cp.async ring, and bf16 mma.sync accumulates G^T H in
+// FP32 (A fragments transposed by ldmatrix; a warp owns 32 columns p x all
+// of r).
+constexpr int kRdP = 128, kRdM = 64, kRdStages = 3, kRdThreads = 128;
+constexpr int kRdLdG = kRdP + 8;  // G tile [m][p], padded (elements)
+constexpr int kRdLdH = kRdM + 8;  // H tile [j][m], padded (elements): conflict-free B fragments
+constexpr int kRdGBytes = kRdM * kRdLdG * 2;
+constexpr int kRdHBytes = kPfMaxR * kRdLdH * 2;  // one of hi, lo
+constexpr int kRdStageBytes = kRdGBytes + 2 * kRdHBytes;
+constexpr size_t kRdSmem = (size_t)kRdStages * kRdStageBytes;
+
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t (&r)[4], const void *p)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(smem_addr(p)));
+}
+
+// hhi, hlo: r x Mp (Mp = M rounded up to kRdM, zero past M).
+__global__ void __launch_bounds__(256) lora_hprep_kernel(const float *__restrict__ H, int M, int Mp, int r,
+                                                         const int *__restrict__ pe1, const int *__restrict__ pe2,
+                                                         uint16_t *__restrict__ hhi, uint16_t *__restrict__ hlo)
+{
+    const int64_t n = (int64_t)r * Mp;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        const int j = (int)(i / Mp), m = (int)(i % Mp);
+        float v = 0.0f;
+        if (m < M)
+            v = scale_pow2(H[(size_t)m * r + j], pe1[m] + (pe2 ? pe2[m] : 0));
+        const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+        const __nv_bfloat16 lo = __float2bfloat16_rn(v - __bfloat162float(hi));
+        hhi[i] = *reinterpret_cast<const uint16_t *>(&hi);
+        hlo[i] = *reinterpret_cast<const uint16_t *>(&lo);
+    }
+}
+
+__global__ void __launch_bounds__(kRdThreads, 2) lora_reduce_kernel(const uint16_t *__restrict__ G, int M, int P,
+                                                                    const uint16_t *__restrict__ hhi,
+                                                                    const uint16_t *__restrict__ hlo, int Mp, int r,
+                                                                    int msplit, float *__restrict__ part)
+{
+    extern __shared__ __align__(16) uint8_t rd_smem[];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
+    const int p0 = blockIdx.x * kRdP, split = blockIdx.y;
+    const int mb = split * msplit, me = min(M, mb + msplit);
+    const int nchunks = (me - mb + kRdM - 1) / kRdM;
+    const uint64_t drop = l2_policy_evict_first(), keep = l2_policy_evict_last();
+    auto gtile = [&](int st) { return reinterpret_cast<uint16_t *>(rd_smem + st * kRdStageBytes); };
+    auto htile = [&](int st, int part_) {
+        return reinterpret_cast<uint16_t *>(rd_smem + st * kRdStageBytes + kRdGBytes + part_ * kRdHBytes);
+    };
+    // rows r .. 63 of every H tile stay zero (the copies fill rows < r only)
+    constexpr int kHChunks = kRdLdH / 8;
+    for (int i = tid; i < kRdStages * 2 * (kPfMaxR - r) * kHChunks; i += kRdThreads) {
+        const int per = (kPfMaxR - r) * kHChunks, sp = i / per, rest = i % per;
+        *reinterpret_cast<uint4 *>(htile(sp >> 1, sp & 1) + (r + rest / kHChunks) * kRdLdH + (rest % kHChunks) * 8) =
+            make_uint4(0u, 0u, 0u, 0u);
+    }
+
+    auto issue = [&](int ci) {
+        if (ci < nchunks) {
+            const int st = ci % kRdStages, mc = mb + ci * kRdM;
+            uint16_t *gd = gtile(st);
+#pragma unroll
+            for (int q = 0; q < kRdM * (kRdP / 8) / kRdThreads; q++) {
+                const int i = tid + kRdThreads * q, row = i / (kRdP / 8), col = (i % (kRdP / 8)) * 8;
+                const int m = mc + row;
+                const bool ok = m < me && p0 + col < P;  // the last tile may hold 64 columns
+                cp_async16(gd + row * kRdLdG + col, G + (ok ? (size_t)m * P + p0 + col : 0), ok ? 16u : 0u, drop);
+            }
+            // H rows j < r, tokens mc .. mc + 63: splits are whole 64-token tiles
+            // and the H buffers are zero from M to Mp, so nothing crosses a split
+            for (int i = tid; i < 2 * r * (kRdM / 8); i += kRdThreads) {
+                const int part_ = i / (r * (kRdM / 8)), rest = i % (r * (kRdM / 8));
+                const int j = rest / (kRdM / 8), col = (rest % (kRdM / 8)) * 8;
+                cp_async16(htile(st, part_) + j * kRdLdH + col, (part_ ? hlo : hhi) + (size_t)j * Mp + mc + col, 16u,
+                           keep);
+            }
+        }
+        cp_async_commit();
+    };
+    __syncthreads();
+#pragma unroll
+    for (int s = 0; s < kRdStages - 1; s++)
+        issue(s);
+
+    float acc[2][8][4];
+#pragma unroll
+    for (int pt = 0; pt < 2; pt++)
+#pragma unroll
+        for (int jt = 0; jt < 8; jt++)
+            acc[pt][jt][0] = acc[pt][jt][1] = acc[pt][jt][2] = acc[pt][jt][3] = 0.0f;
+    const int njt = (r + 7) / 8;
+
+    for (int ci = 0; ci < nchunks; ci++) {
+        cp_async_wait<kRdStages - 2>();
+        __syncthreads();  // tile ci landed for every thread; chunk ci-1 is done with its buffers
+        issue(ci + kRdStages - 1);
+        const int st = ci % kRdStages;
+        const uint16_t *gt = gtile(st), *hh = htile(st, 0), *hl = htile(st, 1);
+#pragma unroll
+        for (int kk = 0; kk < kRdM; kk += 16) {
+            uint32_t af[2][4];
+            {
+                const int i = lane >> 3, rr = lane & 7;
+#pragma unroll
+                for (int pt = 0; pt < 2; pt++)
+                    ldmatrix_x4_trans(af[pt], gt + (kk + (i >> 1) * 8 + rr) * kRdLdG + 32 * warp + 16 * pt +
+                                                  (i & 1) * 8);
+            }
+#pragma unroll
+            for (int jt = 0; jt < 8; jt++) {
+                if (jt < njt) {
+                    const int hb = (8 * jt + g) * kRdLdH + kk + 2 * t;
+                    const uint32_t b0h = *reinterpret_cast<const uint32_t *>(hh + hb);
+                    const uint32_t b1h = *reinterpret_cast<const uint32_t *>(hh + hb + 8);
+                    const uint32_t b0l = *reinterpret_cast<const uint32_t *>(hl + hb);
+                    const uint32_t b1l = *reinterpret_cast<const uint32_t *>(hl + hb + 8);
+#pragma unroll
+                    for (int pt = 0; pt < 2; pt++) {
+                        mma_bf16_16816(acc[pt][jt], af[pt], b0h, b1h);
+                        mma_bf16_16816(acc[pt][jt], af[pt], b0l, b1l);
+                    }
+                }
+            }
+        }
+    }
+    cp_async_wait<0>();
+    // rows p = p0 + 32 warp + 16 pt + g (+8), columns j = 8 jt + 2t (+1)
+    float *out = part + (size_t)split * P * r;
+#pragma unroll
+    for (int pt = 0; pt < 2; pt++)
+#pragma unroll
+        for (int jt = 0; jt < 8; jt++)
+#pragma unroll
+            for (int q = 0; q < 4; q++) {
+                const int p = p0 + 32 * warp + 16 * pt + g + 8 * (q >> 1), j = 8 * jt + 2 * t + (q & 1);
+                if (j < r && p < P)
+                    out[(size_t)p * r + j] = acc[pt][jt][q];
+            }
+}
+
+// out = s * (sum of the splits' partial sums, in split order); dA is stored
+// transposed (r x P), dB as computed (P x r).
+__global__ void __launch_bounds__(256) lora_sum_kernel(const float *__restrict__ part, int splits, int P, int r,
+                                                       float s, float *__restrict__ out, int transposed)
+{
+    const int64_t n = (int64_t)P * r;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        float v = 0.0f;
+        for (int k = 0; k < splits; k++)
+            v += part[(size_t)k * n + i];
+        const int64_t p = i / r, j = i % r;
+        out[transposed ? j * P + p : i] = __fmul_rn(s, v);
     }
 }
 
@@ -939,12 +1122,12 @@ static cudaError_t run_token_side_and_gemm(const PfRun &q, cudaStream_t s, const
     xcfg.numAttrs = 1;
     const int direct = q.noise == nullptr ? 1 : 0;
     cudaError_t e = cudaLaunchKernelEx(&xcfg, prefill_xprep_kernel<false>, q.x, q.noise, M, K, q.lora_in, r,
-                                       pl.ES, q.lora_scale, q.tensor_scale, xh, pexp, ta, flags, direct);
+                                       pl.ES, q.lora_scale, q.tensor_scale, xh, pexp, ta, flags, direct, nullptr);
     if (e != cudaSuccess)
         return e;
     prefill_xprep_kernel<true><<<xgrid, kXpThreads, kXpSmem, s>>>(q.x, q.noise, M, K, q.lora_in, r, pl.ES,
                                                                    q.lora_scale, q.tensor_scale, xh, pexp, ta,
-                                                                   flags, direct);
+                                                                   flags, direct, nullptr);
     e = cudaGetLastError();
     if (e != cudaSuccess)
         return e;
@@ -1047,6 +1230,116 @@ cudaError_t launch_dgrad_gemm(const GemmArgs &a, cudaStream_t s, const DeviceInf
     PfRun q = {(int)a.M, K, N, r, a.x, nullptr, r > 0 ? bt : nullptr, a.lora_scale, a.tensor_scale, a.noise,
                a.y, a.y_fp32, a.ws, pl};
     return run_token_side_and_gemm(q, s, dev);
+}
+
+// ---------------------------------------------------------------- LoRA gradients, host
+// Workspace: X'' (M x K), p_m and block flags for X and for dY, T'' and U''
+// (M x r fp32), B^T (r x N), and the partial sums of the token splits.
+constexpr int kLgTargetBlocks = 304;  // reduction blocks per product: at most one wave at two per SM
+
+struct LgPlan {
+    int ES, sb, sa, msb, msa, Mp;
+    size_t off_xh, off_px, off_fx, off_t, off_pd, off_fd, off_u, off_bt, off_hhi, off_hlo, off_part, total;
+};
+
+// tokens per split: a multiple of kRdM giving about kLgTargetBlocks blocks
+static int lg_msplit(int64_t M, int64_t P)
+{
+    const int64_t ptiles = (P + kRdP - 1) / kRdP;
+    const int64_t want = std::max<int64_t>(1, kLgTargetBlocks / ptiles);
+    const int64_t per = (M + want - 1) / want;
+    return (int)std::max<int64_t>(kRdM, (per + kRdM - 1) / kRdM * kRdM);
+}
+
+static LgPlan lg_plan(int64_t M, int64_t N, int64_t K, int64_t r)
+{
+    LgPlan pl;
+    pl.ES = r <= 32 ? 1 : 2;
+    pl.msb = lg_msplit(M, N);
+    pl.msa = lg_msplit(M, K);
+    pl.sb = (int)((M + pl.msb - 1) / pl.msb);
+    pl.sa = (int)((M + pl.msa - 1) / pl.msa);
+    const size_t nblk = (size_t)(M + kXpRows - 1) / kXpRows;
+    size_t off = kWsHeaderBytes;
+    pl.off_xh = off;
+    off = pf_align(off + (size_t)M * K * 2);
+    pl.off_px = off;
+    off = pf_align(off + (size_t)M * 4);
+    pl.off_fx = off;
+    off = pf_align(off + nblk * 4);
+    pl.off_t = off;
+    off = pf_align(off + (size_t)M * r * 4);
+    pl.off_pd = off;
+    off = pf_align(off + (size_t)M * 4);
+    pl.off_fd = off;
+    off = pf_align(off + nblk * 4);
+    pl.off_u = off;
+    off = pf_align(off + (size_t)M * r * 4);
+    pl.off_bt = off;
+    off = pf_align(off + (size_t)r * N * 2);
+    pl.Mp = (int)((M + kRdM - 1) / kRdM * kRdM);
+    pl.off_hhi = off;
+    off = pf_align(off + (size_t)r * pl.Mp * 2);
+    pl.off_hlo = off;
+    off = pf_align(off + (size_t)r * pl.Mp * 2);
+    pl.off_part = off;
+    off = pf_align(off + std::max((size_t)pl.sb * N, (size_t)pl.sa * K) * r * 4);
+    pl.total = off;
+    return pl;
+}
+
+bool lora_grads_supported(int64_t M, int64_t N, int64_t K, int64_t r)
+{
+    return M >= 1 && r >= 1 && r <= kPfMaxR && N % 64 == 0 && K % 64 == 0 && N <= (1LL << 30) &&
+           K <= (1LL << 30) && M <= (1LL << 31) / std::max(N, K);
+}
+
+size_t lora_grads_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t r)
+{
+    return lg_plan(M, N, K, r).total;
+}
+
+cudaError_t launch_lora_grads(const LoraGradArgs &a, cudaStream_t s, const DeviceInfo &dev)
+{
+    const LgPlan pl = lg_plan(a.M, a.N, a.K, a.r);
+    const int M = (int)a.M, N = (int)a.N, K = (int)a.K, r = (int)a.r;
+    uint16_t *xh = reinterpret_cast<uint16_t *>(a.ws + pl.off_xh);
+    int *px = reinterpret_cast<int *>(a.ws + pl.off_px), *fx = reinterpret_cast<int *>(a.ws + pl.off_fx);
+    int *pd = reinterpret_cast<int *>(a.ws + pl.off_pd), *fd = reinterpret_cast<int *>(a.ws + pl.off_fd);
+    float *tt = reinterpret_cast<float *>(a.ws + pl.off_t), *uu = reinterpret_cast<float *>(a.ws + pl.off_u);
+    uint16_t *bt = reinterpret_cast<uint16_t *>(a.ws + pl.off_bt);
+    float *part = reinterpret_cast<float *>(a.ws + pl.off_part);
+
+    const int64_t lwork = (int64_t)r * N;
+    dgrad_lora_layout_kernel<<<(int)std::min<int64_t>((lwork + 255) / 256, (int64_t)dev.num_sms * 8), 256, 0, s>>>(
+        a.lora_a, a.lora_b, N, K, r, pl.ES, nullptr, bt);
+    // T'' = X'' A^T with X'' kept (the operand of dA), then U'' = dY B
+    const int xgrid = (M + kXpRows - 1) / kXpRows;
+    prefill_xprep_kernel<false><<<xgrid, kXpThreads, kXpSmem, s>>>(a.x, a.noise, M, K, a.lora_a, r, pl.ES, 0.0f,
+                                                                    nullptr, xh, px, nullptr, fx, 0, tt);
+    prefill_xprep_kernel<true><<<xgrid, kXpThreads, kXpSmem, s>>>(a.x, a.noise, M, K, a.lora_a, r, pl.ES, 0.0f,
+                                                                   nullptr, xh, px, nullptr, fx, 0, tt);
+    prefill_xprep_kernel<false><<<xgrid, kXpThreads, kXpSmem, s>>>(a.dy, nullptr, M, N, bt, r, pl.ES, 0.0f, nullptr,
+                                                                    nullptr, pd, nullptr, fd, 1, uu);
+    prefill_xprep_kernel<true><<<xgrid, kXpThreads, kXpSmem, s>>>(a.dy, nullptr, M, N, bt, r, pl.ES, 0.0f, nullptr,
+                                                                   nullptr, pd, nullptr, fd, 1, uu);
+    // dB = s dY^T T, dA = s U^T X'
+    uint16_t *hhi = reinterpret_cast<uint16_t *>(a.ws + pl.off_hhi), *hlo = reinterpret_cast<uint16_t *>(a.ws + pl.off_hlo);
+    cudaError_t e = cudaFuncSetAttribute(lora_reduce_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRdSmem);
+    if (e != cudaSuccess)
+        return e;
+    const int hgrid = (int)std::min<int64_t>(((int64_t)r * pl.Mp + 255) / 256, (int64_t)dev.num_sms * 8);
+    const int sgrid_b = (int)std::min<int64_t>(((int64_t)N * r + 255) / 256, (int64_t)dev.num_sms * 8);
+    const int sgrid_a = (int)std::min<int64_t>(((int64_t)K * r + 255) / 256, (int64_t)dev.num_sms * 8);
+    lora_hprep_kernel<<<hgrid, 256, 0, s>>>(tt, M, pl.Mp, r, px, nullptr, hhi, hlo);
+    lora_reduce_kernel<<<dim3((N + kRdP - 1) / kRdP, pl.sb), kRdThreads, kRdSmem, s>>>(a.dy, M, N, hhi, hlo, pl.Mp, r,
+                                                                                      pl.msb, part);
+    lora_sum_kernel<<<sgrid_b, 256, 0, s>>>(part, pl.sb, N, r, a.lora_scale, a.grad_b, 0);
+    lora_hprep_kernel<<<hgrid, 256, 0, s>>>(uu, M, pl.Mp, r, pd, px, hhi, hlo);
+    lora_reduce_kernel<<<dim3((K + kRdP - 1) / kRdP, pl.sa), kRdThreads, kRdSmem, s>>>(xh, M, K, hhi, hlo, pl.Mp, r,
+                                                                                      pl.msa, part);
+    lora_sum_kernel<<<sgrid_a, 256, 0, s>>>(part, pl.sa, K, r, a.lora_scale, a.grad_a, 1);
+    return cudaGetLastError();
 }
 
 }  // namespace nvfp4

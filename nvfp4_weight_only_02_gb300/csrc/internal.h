@@ -77,6 +77,21 @@ bool dgrad_supported(int64_t M, int64_t N, int64_t K, int64_t r);
 size_t dgrad_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t r);
 cudaError_t launch_dgrad_gemm(const GemmArgs &a, cudaStream_t s, const DeviceInfo &dev);
 
+// LoRA factor gradients dA = s (dY B)^T X' (r x K) and dB = s dY^T (X' A^T)
+// (N x r), FP32 (1 <= r <= 64; N and K multiples of 64; any M >= 1).
+struct LoraGradArgs {
+    const uint16_t *x, *dy;       // M x K, M x N bf16
+    const float *noise;           // K or null
+    int64_t M, N, K, r;
+    const uint16_t *lora_a, *lora_b;
+    float lora_scale;
+    float *grad_a, *grad_b;       // r x K, N x r
+    uint8_t *ws;
+};
+bool lora_grads_supported(int64_t M, int64_t N, int64_t K, int64_t r);
+size_t lora_grads_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t r);
+cudaError_t launch_lora_grads(const LoraGradArgs &a, cudaStream_t s, const DeviceInfo &dev);
+
 // 2-D tiled tensor map (row-major, `row_bytes` between rows, box of
 // box_inner x box_outer elements, zero fill outside) through the driver's
 // encoder, looked up once.

@@ -102,6 +102,21 @@ def test_host_checks_reject_before_launch(lib):
     assert dg(good, bad_align, 1, null, null, 0) == binding.ERR_ALIGNMENT        # dX misaligned
     assert dg(good, good, 1, null, null, 0, bad_align) == binding.ERR_ALIGNMENT  # noise misaligned
     assert dg(good, good, 1, bad_align, good, 4) == binding.ERR_ALIGNMENT        # LoRA A misaligned
+    # the LoRA gradients
+    lg = lambda x, dy, a, b, ga, gb, z=null, M=4, N=64, K=128, r=8: lib.nvfp4_lora_grads(
+        x, z, dy, M, N, K, a, b, r, 1.0, ga, gb, good, 1 << 20, null)
+    assert lg(null, good, good, good, good, good) == binding.ERR_INVALID_ARG
+    assert lg(good, good, good, null, good, good) == binding.ERR_INVALID_ARG     # no B
+    assert lg(good, good, good, good, good, null) == binding.ERR_INVALID_ARG     # no dB output
+    assert lg(good, good, good, good, good, good, r=0) == binding.ERR_SHAPE
+    assert lg(good, good, good, good, good, good, r=65) == binding.ERR_SHAPE
+    assert lg(good, good, good, good, good, good, N=96) == binding.ERR_SHAPE
+    assert lg(good, good, good, good, good, good, K=80) == binding.ERR_SHAPE
+    assert lg(bad_align, good, good, good, good, good) == binding.ERR_ALIGNMENT
+    assert lg(good, good, good, good, bad_align, good) == binding.ERR_ALIGNMENT  # dA misaligned
+    assert lg(good, good, good, good, good, good, bad_align) == binding.ERR_ALIGNMENT
+    assert lib.nvfp4_lora_grads_workspace_bytes(4, 64, 128, 0) == 0
+    assert lib.nvfp4_lora_grads_workspace_bytes(4, 64, 128, 8) > 0
     assert lib.nvfp4_dgrad_workspace_bytes(4, 96, 128, 0) == 0
     assert lib.nvfp4_dgrad_workspace_bytes(4, 64, 128, 0) > 0
     assert lib.nvfp4_workspace_bytes(1, 16, 30, 0) == 0

@@ -118,3 +118,21 @@ def test_dgrad_stays_in_bounds(nv, M, N, K, r):
         assert nv.nvfp4_get_device_status(ws.view(torch.uint8, (ws.n,))) == nv.OK
         assert dx.intact(), "output guard overwritten"
         assert ws.intact(), "workspace guard overwritten"
+
+
+@pytest.mark.parametrize("M,N,K,r", [(1, 64, 64, 1), (70, 192, 320, 40), (333, 512, 192, 64)])
+def test_lora_grads_stay_in_bounds(nv, M, N, K, r):
+    c = synth.small_case(M, N, K, r, seed=5 * M + N + K)
+    g = synth.bf16_bits_to_f32(synth.activations(M, N, M + 2))
+    g[M // 2] *= 2.0 ** 50  # a rescaled token
+    dy = _dev(synth.to_bf16_bits(g))
+    need = nv.nvfp4_lora_grads_workspace_bytes(M, N, K, r)
+    assert need > 0
+    ga, gb = Guarded(r * K * 4), Guarded(N * r * 4)
+    ws = Guarded((need + 255) // 256 * 256, fill=0)
+    for _ in range(2):
+        nv.nvfp4_lora_grads(_dev(c.x), torch.from_numpy(c.z).cuda(), dy, _dev(c.a), _dev(c.b), c.lora_scale,
+                            ga.view(torch.float32, (r, K)), gb.view(torch.float32, (N, r)),
+                            ws.view(torch.uint8, (ws.n,)))
+    assert ga.intact() and gb.intact(), "output guard overwritten"
+    assert ws.intact(), "workspace guard overwritten"
