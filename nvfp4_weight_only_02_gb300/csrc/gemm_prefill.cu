@@ -777,8 +777,8 @@ __device__ __forceinline__ void tile_coords(int t, int mtiles, int ntiles, int &
 
 __global__ void __launch_bounds__(kPfThreads, 1)
     prefill_gemm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_xd,
-                        const __grid_constant__ CUtensorMap tmap_w,
-                        const __grid_constant__ CUtensorMap tmap_ta, const __grid_constant__ CUtensorMap tmap_tb,
+                        const __grid_constant__ CUtensorMap tmap_wh,
+                        const __grid_constant__ CUtensorMap tmap_ta, const __grid_constant__ CUtensorMap tmap_tbh,
                         PrefillParams p)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -796,7 +796,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < kPfStages; s++) {
             mbar_init(&full[s], 1);   // TMA producer (with tx bytes)
-            mbar_init(&empty[s], 1);  // tcgen05.commit
+            mbar_init(&empty[s], 2);  // tcgen05.commit of both CTAs of the pair
         }
         for (int b = 0; b < 2; b++) {
             mbar_init(&acc_full[b], 1);
@@ -813,9 +813,13 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *s_tmem;
-    pdl_wait();  // X'', p_m, T'', W and B from the preparation kernels
+    cluster_sync();  // the peer's barriers are initialised before any copy targets them
+    pdl_wait();      // X'', p_m, T'', W and B from the preparation kernels
 
-    const int ntile_total = p.mtiles * p.ntiles;
+    // CTA pairs (clusters of 2) take pairs of row tiles that share a weight
+    // tile: each CTA copies half of the B tile and multicasts it to both
+    const int crank = (int)cluster_ctarank(), cid = (int)cluster_id_x(), ncl = (int)cluster_count_x();
+    const int mpairs = (p.mtiles + 1) / 2, npairs = mpairs * p.ntiles;
     const int KB = p.K / kPfBK, KS = KB + p.ES;
 
     auto fail = [&]() {
@@ -827,9 +831,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         // ---------------- TMA producer: X' and W tiles, then the LoRA extension
         if (lane == 0) {
             uint32_t it = 0;
-            for (int tile = blockIdx.x; tile < ntile_total && !*s_abort; tile += gridDim.x) {
-                int mt, nt;
-                tile_coords(tile, p.mtiles, p.ntiles, mt, nt);
+            for (int pt = cid; pt < npairs && !*s_abort; pt += ncl) {
+                int mp, nt;
+                tile_coords(pt, mpairs, p.ntiles, mp, nt);
+                const int mt = 2 * mp + crank;
                 const CUtensorMap *mx = &tmap_x;
                 if (p.direct) {
                     bool copy = false;
@@ -844,14 +849,24 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                     const uint32_t ph = (it / kPfStages) & 1;
                     if (!mbar_wait(&empty[st], ph ^ 1)) { fail(); break; }
                     mbar_arrive_expect_tx(&full[st], kPfABytes + kPfBBytes);
+                    // the stage is free in both CTAs (empty counts both commits)
+                    uint8_t *bh = sB + st * kPfBBytes + crank * (kPfBBytes / 2);
+                    const int by = nt * kPfBN + crank * (kPfBN / 2);
                     if (ks < KB) {
                         tma_load_2d(sA + st * kPfABytes, mx, &full[st], ks * kPfBK, mt * kPfBM);
-                        tma_load_2d(sB + st * kPfBBytes, &tmap_w, &full[st], ks * kPfBK, nt * kPfBN);
+                        tma_load_2d_mc(bh, &tmap_wh, &full[st], ks * kPfBK, by, 3);
                     } else {
                         tma_load_2d(sA + st * kPfABytes, &tmap_ta, &full[st], (ks - KB) * kPfBK, mt * kPfBM);
-                        tma_load_2d(sB + st * kPfBBytes, &tmap_tb, &full[st], (ks - KB) * kPfBK, nt * kPfBN);
+                        tma_load_2d_mc(bh, &tmap_tbh, &full[st], (ks - KB) * kPfBK, by, 3);
                     }
                 }
+            }
+            // every stage released by both CTAs before leaving: the peer's
+            // last commits must not arrive after this CTA has exited
+            for (int k = 0; k < kPfStages && !*s_abort; k++) {
+                const uint32_t i2 = it + k;
+                if (i2 >= (uint32_t)kPfStages && !mbar_wait(&empty[i2 % kPfStages], ((i2 / kPfStages) & 1) ^ 1))
+                    fail();
             }
         }
     } else if (warp == 5) {
@@ -860,7 +875,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             constexpr uint32_t idesc = idesc_f16(kPfBM, kPfBN, 1);  // bf16 x bf16, fp32 accumulate
             const bool split = p.ES > 0 && !lora_fused(p.lora_scale, *p.tensor_scale);
             uint32_t it = 0, lt = 0;
-            for (int tile = blockIdx.x; tile < ntile_total && !*s_abort; tile += gridDim.x, lt++) {
+            for (int pt = cid; pt < npairs && !*s_abort; pt += ncl, lt++) {
                 // split: accumulator 0 takes the weights' term, 1 the LoRA term
                 const int buf = split ? 0 : lt & 1;
                 const uint32_t aph = split ? lt & 1 : (lt >> 1) & 1;
@@ -880,7 +895,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 #pragma unroll
                     for (int j = 0; j < kPfBK / 16; j++)
                         mma_f16_ss(d, ad + 2 * j, bd + 2 * j, idesc, (kk | j) != 0);
-                    mma_commit(&empty[st]);
+                    mma_commit_mc(&empty[st], 3);
                 }
                 if (!ok) { fail(); break; }
                 mma_commit(&acc_full[buf]);
@@ -892,9 +907,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         const float s_t = *p.tensor_scale;
         const bool split = p.ES > 0 && !lora_fused(p.lora_scale, s_t);
         uint32_t lt = 0;
-        for (int tile = blockIdx.x; tile < ntile_total && !*s_abort; tile += gridDim.x, lt++) {
-            int mt, nt;
-            tile_coords(tile, p.mtiles, p.ntiles, mt, nt);
+        for (int pt = cid; pt < npairs && !*s_abort; pt += ncl, lt++) {
+            int mp, nt;
+            tile_coords(pt, mpairs, p.ntiles, mp, nt);
+            const int mt = 2 * mp + crank;
             const int buf = split ? 0 : lt & 1;
             const uint32_t aph = split ? lt & 1 : (lt >> 1) & 1;
             if (!mbar_wait(&acc_full[buf], aph)) { fail(); break; }
@@ -973,6 +989,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 
     tc_fence_before();
     __syncthreads();
+    cluster_sync();  // neither CTA leaves while the other may still copy into it
     if (warp == 5) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
@@ -1141,7 +1158,7 @@ static cudaError_t run_token_side_and_gemm(const PfRun &q, cudaStream_t s, const
                    : (tmxd = tmx, cudaSuccess);
     if (e == cudaSuccess)
         e = encode_tensor_map_2d(&tmw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, wh, (uint64_t)K, (uint64_t)N,
-                                 (uint64_t)K * 2, kPfBK, kPfBN, CU_TENSOR_MAP_SWIZZLE_128B);
+                                 (uint64_t)K * 2, kPfBK, kPfBN / 2, CU_TENSOR_MAP_SWIZZLE_128B);
     // without LoRA the extension maps are never used: point them at X'' and W
     if (e == cudaSuccess)
         e = pl.ES > 0 ? encode_tensor_map_2d(&tma_, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, ta, (uint64_t)64 * pl.ES,
@@ -1150,7 +1167,7 @@ static cudaError_t run_token_side_and_gemm(const PfRun &q, cudaStream_t s, const
                       : (tma_ = tmx, cudaSuccess);
     if (e == cudaSuccess)
         e = pl.ES > 0 ? encode_tensor_map_2d(&tmb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, tb, (uint64_t)64 * pl.ES,
-                                             (uint64_t)N, (uint64_t)128 * pl.ES, kPfBK, kPfBN,
+                                             (uint64_t)N, (uint64_t)128 * pl.ES, kPfBK, kPfBN / 2,
                                              CU_TENSOR_MAP_SWIZZLE_128B)
                       : (tmb = tmw, cudaSuccess);
     if (e != cudaSuccess)
@@ -1175,16 +1192,23 @@ static cudaError_t run_token_side_and_gemm(const PfRun &q, cudaStream_t s, const
     e = cudaFuncSetAttribute(prefill_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPfSmem);
     if (e != cudaSuccess)
         return e;
-    const int tiles = p.mtiles * p.ntiles;
-    // programmatic dependent launch: blocks set up (barriers, TMEM) while the
-    // token-side kernel finishes, then wait for its results
+    // clusters of 2 CTAs over pairs of row tiles (they share each weight
+    // tile); programmatic dependent launch: blocks set up (barriers, TMEM)
+    // while the token-side kernel finishes, then wait for its results
+    const int pairs = (p.mtiles + 1) / 2 * p.ntiles;
+    cudaLaunchAttribute gattr[2];
+    gattr[0] = attr[0];
+    gattr[1].id = cudaLaunchAttributeClusterDimension;
+    gattr[1].val.clusterDim.x = 2;
+    gattr[1].val.clusterDim.y = 1;
+    gattr[1].val.clusterDim.z = 1;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(std::min(tiles, dev.num_sms));
+    cfg.gridDim = dim3(2 * std::min(pairs, dev.num_sms / 2));
     cfg.blockDim = dim3(kPfThreads);
     cfg.dynamicSmemBytes = kPfSmem;
     cfg.stream = s;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.attrs = gattr;
+    cfg.numAttrs = 2;
     e = cudaLaunchKernelEx(&cfg, prefill_gemm_kernel, tmx, tmxd, tmw, tma_, tmb, p);
     if (e != cudaSuccess)
         return e;
