@@ -127,6 +127,58 @@ nvfp4_status nvfp4_w4a16_lora_gemm(const void *x_bf16, int64_t M, int64_t N, int
                                    void *y, nvfp4_dtype y_dtype,
                                    void *workspace, size_t ws_bytes, void *stream);
 
+/* One entry of nvfp4_w4a16_lora_gemm_list.  Each field means what the
+ * argument of nvfp4_w4a16_lora_gemm with the same name means (device
+ * pointers); the struct array itself is in host memory and is read before the
+ * call returns. */
+typedef struct nvfp4_projection {
+    const void *x_bf16;          /* M x K bf16 (entries may share one X)   */
+    const uint8_t *codes;        /* N x K/2 bytes                          */
+    const uint8_t *scales_e4m3;  /* N x K/16 bytes                         */
+    const float *tensor_scale;   /* 1 float                                */
+    const void *lora_a_bf16;     /* r x K bf16; ignored when r == 0        */
+    const void *lora_b_bf16;     /* N x r bf16; ignored when r == 0        */
+    const float *noise_fp32;     /* K floats or NULL (then X' = X)         */
+    void *y;                     /* M x N of the call's y_dtype            */
+    int64_t N, K;
+    float lora_scale;
+} nvfp4_projection;
+
+/* Bytes of workspace for nvfp4_w4a16_lora_gemm_list with these entries (host
+ * array of `count`); 0 when the host checks of that call would fail. */
+size_t nvfp4_gemm_list_workspace_bytes(const nvfp4_projection *list, int count, int64_t M, int64_t r);
+
+/* Several independent projections of the same token count in one call: for
+ * every entry i,
+ *     y_i = s_t,i X'_i deq(W_i)^T + lora_scale_i (X'_i A_i^T) B_i^T,
+ *     X'_i = bf16(X_i * z_i),
+ * the layer of nvfp4_w4a16_lora_gemm ("RL with NVFP4 + LoRA" post, section
+ * "Метод"), on the weight-streaming decode path of that call (rollouts are
+ * memory-bound on the weights: same post, section "Эксперименты").  This is
+ * the shape of a decoder layer's projections that read one input (q, k and v;
+ * gate and up), or of any batch of independent GEMMs.
+ * One activation-preparation launch serves all entries, then one streaming
+ * launch moves every entry's weight bytes back to back, so the fixed cost of
+ * a call (the dependency chain from the preparation kernel, filling the
+ * ring, the last tile's epilogue) is paid once per launch instead of once per
+ * projection.  Entries go 16 at a time into a launch (fewer if their
+ * 128-row tiles exceed 4096); M > 16 runs in groups of 16 tokens.
+ * Each y_i agrees with nvfp4_w4a16_lora_gemm's result for that entry to
+ * FP32 summation order (the split of K over blocks can differ); a one-entry
+ * list computes exactly what nvfp4_w4a16_lora_gemm computes for M < 64.
+ * Requirements (checked on the host before anything is launched):
+ *   list != NULL, 1 <= count <= 65536 (else NVFP4_ERR_INVALID_ARG /
+ *   NVFP4_ERR_SHAPE); 1 <= M <= 2^31, 0 <= r <= 64; per entry: 256 <= K
+ *   <= 2^30 and K % 256 == 0, 1 <= N <= 524288 (NVFP4_ERR_SHAPE); x, codes,
+ *   scales, tensor_scale and y non-null, and A and B non-null when r > 0
+ *   (NVFP4_ERR_INVALID_ARG); every pointer 16-byte aligned
+ *   (NVFP4_ERR_ALIGNMENT).
+ * No y_i may overlap another entry's y or any input of the list.
+ * workspace: nvfp4_gemm_list_workspace_bytes(list, count, M, r) bytes. */
+nvfp4_status nvfp4_w4a16_lora_gemm_list(const nvfp4_projection *list, int count, int64_t M, int64_t r,
+                                        nvfp4_dtype y_dtype, void *workspace, size_t ws_bytes,
+                                        void *stream);
+
 /* Input gradient of nvfp4_w4a16_lora_gemm's layer.  The quantised weight is
  * frozen and only the LoRA factors are trained ("RL with NVFP4 + LoRA"
  * post, section "Метод"), so the backward pass needs the gradient with

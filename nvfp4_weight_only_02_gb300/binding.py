@@ -27,8 +27,17 @@ EXPORTS = [
     "nvfp4_round_scales", "nvfp4_get_device_status", "nvfp4_status_string", "nvfp4_encode_debug",
     "nvfp4_quotient_check", "nvfp4_w4a16_lora_gemm_static", "nvfp4_wait_selftest", "nvfp4_gemm_kernel",
     "nvfp4_scale_qlora_gemm", "nvfp4_w4a16_lora_gemm_dgrad", "nvfp4_dgrad_workspace_bytes",
-    "nvfp4_lora_grads", "nvfp4_lora_grads_workspace_bytes",
+    "nvfp4_lora_grads", "nvfp4_lora_grads_workspace_bytes", "nvfp4_gemm_list_workspace_bytes",
+    "nvfp4_w4a16_lora_gemm_list",
 ]
+
+
+class Projection(ctypes.Structure):
+    """struct nvfp4_projection (one entry of nvfp4_w4a16_lora_gemm_list)."""
+    _fields_ = [("x_bf16", ctypes.c_void_p), ("codes", ctypes.c_void_p), ("scales_e4m3", ctypes.c_void_p),
+                ("tensor_scale", ctypes.c_void_p), ("lora_a_bf16", ctypes.c_void_p),
+                ("lora_b_bf16", ctypes.c_void_p), ("noise_fp32", ctypes.c_void_p), ("y", ctypes.c_void_p),
+                ("N", ctypes.c_int64), ("K", ctypes.c_int64), ("lora_scale", ctypes.c_float)]
 
 
 class NVFP4Error(RuntimeError):
@@ -78,6 +87,8 @@ def load(build_if_missing: bool = True):
             "nvfp4_lora_grads": (st, [P, P, P, i64, i64, i64, P, P, i64, ctypes.c_float, P, P, P, ctypes.c_size_t,
                                       P]),
             "nvfp4_lora_grads_workspace_bytes": (ctypes.c_size_t, [i64, i64, i64, i64]),
+            "nvfp4_gemm_list_workspace_bytes": (ctypes.c_size_t, [P, ctypes.c_int, i64, i64]),
+            "nvfp4_w4a16_lora_gemm_list": (st, [P, ctypes.c_int, i64, i64, ctypes.c_int, P, ctypes.c_size_t, P]),
         }
         for name, (res, args) in sig.items():
             f = getattr(lib, name)
@@ -190,6 +201,50 @@ def nvfp4_w4a16_lora_gemm(x: torch.Tensor, codes: torch.Tensor, scales: torch.Te
         OUT_FP32 if y.dtype == torch.float32 else OUT_BF16, _ptr(workspace), workspace.numel(),
         _stream())
     _check(st, "nvfp4_w4a16_lora_gemm")
+
+
+def _projection_array(entries):
+    """entries: (x, codes, scales, tensor_scale, lora_a, lora_b, lora_scale, noise, y) tuples of CUDA
+    tensors (lora_a, lora_b, noise may be None).  Returns (ctypes array, M, r, y dtype code)."""
+    if len(entries) == 0:
+        raise ValueError("empty projection list")
+    M = entries[0][0].shape[0]
+    r = 0 if entries[0][4] is None else entries[0][4].shape[0]
+    ydt = entries[0][8].dtype
+    if ydt not in (torch.float32, torch.bfloat16):
+        raise ValueError("y must be float32 or bfloat16")
+    arr = (Projection * len(entries))()
+    for i, (x, codes, scales, ts, a, b, s, z, y) in enumerate(entries):
+        K = x.shape[1]
+        N = codes.shape[0]
+        _need(x, torch.bfloat16, (M, K), f"x[{i}]")
+        _need(codes, torch.uint8, (N, K // 2), f"codes[{i}]")
+        _need(scales, torch.uint8, (N, K // 16), f"scales[{i}]")
+        _need(ts, torch.float32, (1,), f"tensor_scale[{i}]")
+        if (a is None) != (r == 0):
+            raise ValueError("every entry of a list has the same LoRA rank")
+        if a is not None:
+            _need(a, torch.bfloat16, (r, K), f"lora_a[{i}]")
+            _need(b, torch.bfloat16, (N, r), f"lora_b[{i}]")
+        if z is not None:
+            _need(z, torch.float32, (K,), f"noise[{i}]")
+        _need(y, ydt, (M, N), f"y[{i}]")
+        arr[i] = Projection(_ptr(x), _ptr(codes), _ptr(scales), _ptr(ts), _ptr(a), _ptr(b), _ptr(z), _ptr(y),
+                            N, K, float(s))
+    return arr, M, r, OUT_FP32 if ydt == torch.float32 else OUT_BF16
+
+
+def nvfp4_gemm_list_workspace_bytes(entries) -> int:
+    arr, M, r, _ = _projection_array(entries)
+    return int(load().nvfp4_gemm_list_workspace_bytes(arr, len(entries), M, r))
+
+
+def nvfp4_w4a16_lora_gemm_list(entries, workspace: torch.Tensor):
+    """Independent projections of one token count in one call (see _projection_array for an entry)."""
+    arr, M, r, ydt = _projection_array(entries)
+    st = load().nvfp4_w4a16_lora_gemm_list(arr, len(entries), M, r, ydt, _ptr(workspace), workspace.numel(),
+                                           _stream())
+    _check(st, "nvfp4_w4a16_lora_gemm_list")
 
 
 def nvfp4_round_scales(scale_param: torch.Tensor, tensor_scale: torch.Tensor,
@@ -359,6 +414,19 @@ def lora_grads(x, dy, lora_a, lora_b, lora_scale, noise=None, workspace=None):
                                                               x.device)
     nvfp4_lora_grads(x, noise, dy, lora_a, lora_b, lora_scale, ga, gb, ws)
     return ga, gb
+
+
+def gemm_list(items, out_dtype=torch.float32, workspace=None):
+    """items: (x, q, lora_a, lora_b, lora_scale, noise) tuples (q a QuantizedWeight; lora_a, lora_b,
+    noise may be None).  Returns the list of outputs, each M x N."""
+    entries = []
+    for x, q, a, b, s, z in items:
+        y = torch.empty((x.shape[0], q.shape[0]), dtype=out_dtype, device=x.device)
+        entries.append((x, q.codes, q.scales, q.tensor_scale, a, b, s, z, y))
+    ws = workspace if workspace is not None else new_workspace(nvfp4_gemm_list_workspace_bytes(entries),
+                                                              entries[0][0].device)
+    nvfp4_w4a16_lora_gemm_list(entries, ws)
+    return [e[8] for e in entries]
 
 
 def gemm(x, q: QuantizedWeight, lora_a=None, lora_b=None, lora_scale=0.0, noise=None,

@@ -2,6 +2,7 @@
 // checks on the host, then launches on the caller's stream.  Nothing here
 // computes; no entry point allocates device memory.
 #include <mutex>
+#include <vector>
 
 #include "common.cuh"
 #include "internal.h"
@@ -183,6 +184,87 @@ nvfp4_status nvfp4_w4a16_lora_gemm(const void *x_bf16, int64_t M, int64_t N, int
     if (st != NVFP4_OK)
         return st;
     return from_cuda(launch_gemm(a, (cudaStream_t)stream, *dev));
+}
+
+// Host checks of a list call, in the order the header states; fills args
+// (workspace fields left empty).
+static nvfp4_status list_checks(const nvfp4_projection *list, int count, int64_t M, int64_t r, bool y_fp32,
+                                std::vector<GemmArgs> &args)
+{
+    if (!list)
+        return NVFP4_ERR_INVALID_ARG;
+    if (count < 1 || count > 65536 || M < 1 || M > (1LL << 31) || r < 0 || r > 64)
+        return NVFP4_ERR_SHAPE;
+    args.resize((size_t)count);
+    for (int i = 0; i < count; i++) {
+        const nvfp4_projection &e = list[i];
+        if (e.N < 1 || e.N > 524288 || e.K < 256 || e.K % 256 != 0 || e.K > (1LL << 30))
+            return NVFP4_ERR_SHAPE;
+        if (!e.x_bf16 || !e.codes || !e.scales_e4m3 || !e.tensor_scale || !e.y ||
+            (r > 0 && (!e.lora_a_bf16 || !e.lora_b_bf16)))
+            return NVFP4_ERR_INVALID_ARG;
+        if (!aligned16(e.x_bf16) || !aligned16(e.codes) || !aligned16(e.scales_e4m3) ||
+            !aligned16(e.tensor_scale) || !aligned16(e.y) || (e.noise_fp32 && !aligned16(e.noise_fp32)) ||
+            (r > 0 && (!aligned16(e.lora_a_bf16) || !aligned16(e.lora_b_bf16))))
+            return NVFP4_ERR_ALIGNMENT;
+        GemmArgs &a = args[(size_t)i];
+        a.x = (const uint16_t *)e.x_bf16;
+        a.M = M;
+        a.N = e.N;
+        a.K = e.K;
+        a.r = r;
+        a.codes = e.codes;
+        a.scales = e.scales_e4m3;
+        a.tensor_scale = e.tensor_scale;
+        a.lora_a = r > 0 ? (const uint16_t *)e.lora_a_bf16 : nullptr;
+        a.lora_b = r > 0 ? (const uint16_t *)e.lora_b_bf16 : nullptr;
+        a.lora_scale = r > 0 ? e.lora_scale : 0.0f;
+        a.noise = e.noise_fp32;
+        a.y = e.y;
+        a.y_fp32 = y_fp32;
+        a.ws = nullptr;
+        a.ws_bytes = 0;
+    }
+    return NVFP4_OK;
+}
+
+size_t nvfp4_gemm_list_workspace_bytes(const nvfp4_projection *list, int count, int64_t M, int64_t r)
+{
+    std::vector<GemmArgs> args;
+    if (list_checks(list, count, M, r, false, args) != NVFP4_OK)
+        return 0;
+    nvfp4_status st;
+    const DeviceInfo *dev = device_info(&st);
+    if (!dev)
+        return 0;
+    const size_t g = stream_list_workspace_bytes(args.data(), count, *dev);
+    return g == 0 ? 0 : g < kCtlBytes ? kCtlBytes : g;
+}
+
+nvfp4_status nvfp4_w4a16_lora_gemm_list(const nvfp4_projection *list, int count, int64_t M, int64_t r,
+                                        nvfp4_dtype y_dtype, void *workspace, size_t ws_bytes, void *stream)
+{
+    if (y_dtype != NVFP4_OUT_BF16 && y_dtype != NVFP4_OUT_FP32)
+        return NVFP4_ERR_INVALID_ARG;
+    std::vector<GemmArgs> args;
+    const nvfp4_status cs = list_checks(list, count, M, r, y_dtype == NVFP4_OUT_FP32, args);
+    if (cs != NVFP4_OK)
+        return cs;
+    if (!workspace)
+        return NVFP4_ERR_INVALID_ARG;
+    if (!aligned16(workspace))
+        return NVFP4_ERR_ALIGNMENT;
+    NVFP4_TRY_DEVICE(dev);
+    const size_t need = stream_list_workspace_bytes(args.data(), count, *dev);
+    if (need == 0)
+        return NVFP4_ERR_UNSUPPORTED_DEVICE;
+    if (ws_bytes < need)
+        return NVFP4_ERR_WORKSPACE;
+    for (GemmArgs &a : args) {
+        a.ws = (uint8_t *)workspace;
+        a.ws_bytes = ws_bytes;
+    }
+    return from_cuda(launch_stream_list(args.data(), count, (cudaStream_t)stream, *dev));
 }
 
 static bool dgrad_shape_ok(int64_t M, int64_t N, int64_t K, int64_t r)

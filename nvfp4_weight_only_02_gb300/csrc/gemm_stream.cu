@@ -45,6 +45,7 @@
 //    for the last block to arrive, which adds the shares in block order
 //    (results do not depend on arrival order).
 #include <algorithm>
+#include <cstring>
 #include <mutex>
 #include <unordered_map>
 
@@ -134,6 +135,20 @@ __host__ __device__ __forceinline__ int xh_unit(int m, int ux)
     return ux ^ (((m & 1) << 2) | ((ux >> 3) & 3));
 }
 
+// Byte offset of 16-byte unit ux (columns 8ux .. 8ux+7 of the chunk; ux =
+// 32h + 8t + j) of token m in a chunk record's X' rows.  Tokens come in pairs
+// of 2 KB; inside a pair, the units that the 8 lanes (m & 1, t) of a quarter
+// warp read for one k-step pair j are 128 contiguous bytes, so a consumer
+// lane reads every unit of a stage at one base address plus constant offsets
+// (j * 128, and 8192 per eight tokens).
+__host__ __device__ __forceinline__ int xrec_off(int m, int ux)
+{
+    return (m >> 1) * 2048 + (ux >> 5) * 1024 + (ux & 7) * 128 + (((m & 1) << 2) | ((ux >> 3) & 3)) * 16;
+}
+
+// X' bytes of a record copied into a stage: whole token pairs.
+__host__ __device__ __forceinline__ int xrec_bytes(int M) { return (M + 1) / 2 * 2048; }
+
 __device__ __forceinline__ float bf16_round(float v) { return __bfloat162float(__float2bfloat16_rn(v)); }
 
 __device__ __forceinline__ uint32_t bf16x2_bits(float a, float b)
@@ -143,33 +158,59 @@ __device__ __forceinline__ uint32_t bf16x2_bits(float a, float b)
 }
 
 
-struct Params {
-    CUtensorMap tm_codes;   // codes, N x K/2 bytes: boxes of 128 x 128, 128B swizzle
-    CUtensorMap tm_scales;  // scales, N x K/16 bytes: boxes of 128 x 32
-    int M, N, K, r, C, U, KS;  // KS: LoRA k-steps (1, 2 or 4; 0 without LoRA)
-    const uint16_t *x;         // M x K bf16 (this token group)
-    const float *noise;        // K floats or null
-    const uint16_t *lora_a;    // r x K bf16
-    const uint16_t *lora_b;    // N x r bf16
-    float lora_scale;
+// One projection of a launch: its weight maps, LoRA up factor and output,
+// and where its units, tile counters and chunk records start in the launch.
+struct Proj {
+    CUtensorMap tm_codes;       // codes, N x K/2 bytes: boxes of 128 x 128, 128B swizzle
+    CUtensorMap tm_scales;      // scales, N x K/16 bytes: boxes of 128 x 32
+    const uint16_t *lora_b;     // N x r bf16
     const float *tensor_scale;
-    const uint8_t *rec;        // [C] chunk records: 2^p per token | T_c | X' rows
+    void *y;                    // M x N (this token group)
+    float lora_scale;
+    int N, K, C;                // C: 512-column chunks
+    int ubeg, tbeg, cbeg;       // first unit, tile counter and chunk record
+};
+
+// A launch: up to NP projections with the same token count and LoRA rank,
+// their units concatenated in list order and split evenly over the blocks.
+template <int NP>
+struct Params {
+    Proj proj[NP];
+    int count;                  // projections in this launch
+    int M, r, U, KS;            // U: units of all projections; KS: LoRA k-steps (1, 2, 4; 0 without LoRA)
+    const uint8_t *rec;         // chunk records: 2^p per token | T_c | X' rows
     int rec_bytes;
-    int bsm;                   // 1: the producer stages each tile's B rows in shared memory
-    float *part;               // [G][2][8][32][MP/2]: tile shares left for the last block
-    uint32_t *tcnt;            // tile arrival counters
+    int bsm;                    // 1: the producer stages each tile's B rows in shared memory
+    float *part;                // [G][2][8][32][MP/2]: tile shares left for the last block
+    uint32_t *tcnt;             // tile arrival counters
     uint32_t *ctl;
-    void *y;
     int y_fp32;
 };
 
+// Projection of unit u (units of a launch are in list order).
+template <int NP>
+__device__ __forceinline__ int proj_of_unit(const Params<NP> &p, int u)
+{
+    int j = 0;
+#pragma unroll
+    for (int k = 1; k < NP; k++)
+        if (k < p.count && u >= p.proj[k].ubeg)
+            j = k;
+    return j;
+}
+
 // ---------------------------------------------------------------- xprep kernel
-struct PrepParams {
-    int M, K, r, KS;
+struct PrepProj {
     const uint16_t *x;       // M x K bf16
     const float *noise;      // K floats or null
     const uint16_t *lora_a;  // r x K bf16
-    uint8_t *rec;            // [C] records of rec_bytes(KS, MP)
+    int K, cbeg;             // cbeg: this projection's first chunk record
+};
+template <int NP>
+struct PrepParams {
+    PrepProj proj[NP];
+    int count, M, r, KS;
+    uint8_t *rec;            // chunk records of rec_bytes(KS, MP)
 };
 
 // Block c: warp m < M forms X' of token m (lane l: columns 16l .. 16l+15 of
@@ -181,42 +222,49 @@ struct PrepParams {
 // conflict-free 16-byte units.  Warps split (8-column n-tile of T, half,
 // k-step pairs); one warp per n-tile sums the parts in fixed order and
 // stores them in the layout the epilogue loads as B fragments.
-template <int MP>
-__global__ void __launch_bounds__(kPrepThreads, 1) xprep_kernel(const __grid_constant__ PrepParams p)
+template <int MP, int NP>
+__global__ void __launch_bounds__(kPrepThreads, 1) xprep_kernel(const __grid_constant__ PrepParams<NP> p)
 {
     constexpr int NT = MP / 8;
     __shared__ __align__(16) uint8_t xb[MP * 1024];
     __shared__ float4 scratch[kCWarps * 32];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-    const int c = blockIdx.x;
+    int pj = 0;  // the projection of this block's chunk
+#pragma unroll
+    for (int k = 1; k < NP; k++)
+        if (k < p.count && (int)blockIdx.x >= p.proj[k].cbeg)
+            pj = k;
+    const PrepProj &pr = p.proj[pj];
+    const int K = pr.K;
+    const int c = (int)blockIdx.x - pr.cbeg;
     const int kbase = c * kChunk;
-    const int halves = kbase + kChunk <= p.K ? 2 : 1;
-    const uint32_t cbytes = (uint32_t)min(kChunk, p.K - kbase) * 2u;
+    const int halves = kbase + kChunk <= K ? 2 : 1;
+    const uint32_t cbytes = (uint32_t)min(kChunk, K - kbase) * 2u;
     // the chunk's activations, noise and A rows into L2 while the previous kernel finishes
     if (warp < p.M && lane == 0)
-        bulk_prefetch_l2(p.x + (size_t)warp * p.K + kbase, cbytes);
-    if (warp == kCWarps - 1 && lane == 0 && p.noise)
-        bulk_prefetch_l2(p.noise + kbase, 2 * cbytes);
+        bulk_prefetch_l2(pr.x + (size_t)warp * K + kbase, cbytes);
+    if (warp == kCWarps - 1 && lane == 0 && pr.noise)
+        bulk_prefetch_l2(pr.noise + kbase, 2 * cbytes);
     if (p.KS > 0 && lane == 0)
         for (int j = warp; j < p.r; j += kCWarps)
-            bulk_prefetch_l2(p.lora_a + (size_t)j * p.K + kbase, cbytes);
+            bulk_prefetch_l2(pr.lora_a + (size_t)j * K + kbase, cbytes);
     pdl_launch_dependents();  // the GEMM's blocks may start prefetching weights
     pdl_wait();
 
-    uint8_t *rec = p.rec + (size_t)c * rec_bytes(p.KS, MP);
+    uint8_t *rec = p.rec + (size_t)(pr.cbeg + c) * rec_bytes(p.KS, MP);
     float *fac = reinterpret_cast<float *>(rec);
     float4 *trec = reinterpret_cast<float4 *>(rec + kFacBytes);
     uint8_t *xrec = rec + kFacBytes + t_bytes(p.KS, MP);
     const int k0 = kbase + lane * 16;
-    const bool conv = warp < p.M, kin = conv && k0 < p.K;
+    const bool conv = warp < p.M, kin = conv && k0 < K;
     uint4 xa = make_uint4(0u, 0u, 0u, 0u), xc = xa;
     float4 z4[4];
     if (kin) {
-        const uint4 *xs = reinterpret_cast<const uint4 *>(p.x + (size_t)warp * p.K + k0);
+        const uint4 *xs = reinterpret_cast<const uint4 *>(pr.x + (size_t)warp * K + k0);
         xa = __ldcg(xs);
         xc = __ldcg(xs + 1);
-        if (p.noise) {
-            const float4 *zs = reinterpret_cast<const float4 *>(p.noise + k0);
+        if (pr.noise) {
+            const float4 *zs = reinterpret_cast<const float4 *>(pr.noise + k0);
 #pragma unroll
             for (int q = 0; q < 4; q++)
                 z4[q] = __ldcg(zs + q);
@@ -230,7 +278,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1) xprep_kernel(const __grid_con
     const int jt = unit / halves, hh = unit % halves;
     const int npairs = 8 / wpu;                // k-step pairs per warp
     const int jrow = jt * 8 + g;
-    const uint16_t *arow = p.lora_a + (size_t)min(jrow, max(p.r - 1, 0)) * p.K + kbase + 256 * hh + 64 * t;
+    const uint16_t *arow = pr.lora_a + (size_t)min(jrow, max(p.r - 1, 0)) * K + kbase + 256 * hh + 64 * t;
     uint4 af[8];
     if (p.KS > 0) {
 #pragma unroll
@@ -247,7 +295,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1) xprep_kernel(const __grid_con
 #pragma unroll
         for (int i = 0; i < 16; i++) {
             float f = bf16_bits_to_f32((xw[i / 2] >> (16 * (i & 1))) & 0xFFFFu);
-            if (kin && p.noise) {
+            if (kin && pr.noise) {
                 const float4 zq = z4[i / 4];
                 const float z = (i & 3) == 0 ? zq.x : (i & 3) == 1 ? zq.y : (i & 3) == 2 ? zq.z : zq.w;
                 f = bf16_round(__fmul_rn(f, z));
@@ -275,14 +323,19 @@ __global__ void __launch_bounds__(kPrepThreads, 1) xprep_kernel(const __grid_con
                 hw[i] = *reinterpret_cast<uint32_t *>(&h2);
                 bw[i] = bf16x2_bits(lo, hi);  // exact: lo, hi are bf16 values
             }
-            const int off = 16 * xh_unit(warp, 2 * lane + u2);
-            *reinterpret_cast<uint4 *>(xrec + warp * 1024 + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-            *reinterpret_cast<uint4 *>(xb + warp * 1024 + off) = make_uint4(bw[0], bw[1], bw[2], bw[3]);
+            *reinterpret_cast<uint4 *>(xrec + xrec_off(warp, 2 * lane + u2)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            *reinterpret_cast<uint4 *>(xb + warp * 1024 + 16 * xh_unit(warp, 2 * lane + u2)) =
+                make_uint4(bw[0], bw[1], bw[2], bw[3]);
         }
         if (lane == 0)
             fac[warp] = exp2i(pexp);
     } else if (warp < MP && lane == 0) {
         fac[warp] = 0.0f;  // tokens past M: their MMA columns are zero
+    }
+    if ((p.M & 1) && warp == p.M) {  // the other half of the last token pair: zeros
+#pragma unroll
+        for (int u2 = 0; u2 < 2; u2++)
+            *reinterpret_cast<uint4 *>(xrec + xrec_off(warp, 2 * lane + u2)) = make_uint4(0u, 0u, 0u, 0u);
     }
     if (p.KS == 0)
         return;
@@ -348,8 +401,10 @@ __device__ __forceinline__ uint32_t word_of(const uint4 &v, int i)
 // 256*h + 64*t .. +63.  k-step 2j+e uses columns 64t + 8j + 4e .. +3: code
 // bytes 2e, 2e+1 of word j, scale byte j/2, X' unit j (words 2e, 2e+1).
 // Code box h holds 128-byte rows whose 16-byte chunk c sits at c ^ (row % 8).
+// Token slots past M hold zeros (xprep writes the odd token pair's other half;
+// the rest of the stage's X' rows are zeroed once), so every slot is read.
 template <int MP>
-__device__ __forceinline__ void compute_unit(const uint8_t *st, int xoff, int mt, int h, int g, int t, int M,
+__device__ __forceinline__ void compute_unit(const uint8_t *st, int xoff, int mt, int h, int g, int t,
                                              float (&acc)[MP / 8][4])
 {
     constexpr int NT = MP / 8;
@@ -369,8 +424,8 @@ __device__ __forceinline__ void compute_unit(const uint8_t *st, int xoff, int mt
     uint32_t s0[4], s1[4];
     e4m3x4_to_h2dup(sw0, s0);
     e4m3x4_to_h2dup(sw1, s1);
-    const int key = ((g & 1) << 2) | t;
-    const uint8_t *xrow = xb + h * 512 + t * 128;
+    // unit 32h + 8t + j of token g + 8nt (see xrec_off)
+    const uint8_t *xl = xb + (g >> 1) * 2048 + h * 1024 + (((g & 1) << 2) | t) * 16;
     // CS independent accumulator sets (by k-step) keep four MMA chains in flight
     constexpr int CS = 4 / NT;
     float cur[CS][NT][4];
@@ -385,11 +440,8 @@ __device__ __forceinline__ void compute_unit(const uint8_t *st, int xoff, int mt
     for (int j = 0; j < 8; j++) {
         uint4 xf[NT];
 #pragma unroll
-        for (int nt = 0; nt < NT; nt++) {
-            const int tok = g + 8 * nt;
-            xf[nt] = tok < M ? *reinterpret_cast<const uint4 *>(xrow + tok * 1024 + 16 * (j ^ key))
-                             : make_uint4(0u, 0u, 0u, 0u);
-        }
+        for (int nt = 0; nt < NT; nt++)
+            xf[nt] = *reinterpret_cast<const uint4 *>(xl + nt * 8192 + j * 128);
         const uint32_t w0 = word_of(j < 4 ? c00 : c01, j & 3);
         const uint32_t w1 = word_of(j < 4 ? c10 : c11, j & 3);
         uint32_t r0[4], r1[4];
@@ -428,30 +480,30 @@ __device__ __forceinline__ void compute_unit(const uint8_t *st, int xoff, int mt
 }
 
 // Two LoRA B entries (row R, columns j, j+1) as a bf16 pair; zero outside.
-__device__ __forceinline__ uint32_t lora_pair(const Params &p, int R, int j)
+__device__ __forceinline__ uint32_t lora_pair(const Proj &pj, int r, int R, int j)
 {
-    if (R >= p.N || j >= p.r)
+    if (R >= pj.N || j >= r)
         return 0u;
-    const uint16_t *row = p.lora_b + (size_t)R * p.r;
-    if ((p.r & 1) == 0)
+    const uint16_t *row = pj.lora_b + (size_t)R * r;
+    if ((r & 1) == 0)
         return __ldcg(reinterpret_cast<const uint32_t *>(row + j));
     const uint32_t lo = __ldcg(row + j);
-    const uint32_t hi = j + 1 < p.r ? (uint32_t)__ldcg(row + j + 1) : 0u;
+    const uint32_t hi = j + 1 < r ? (uint32_t)__ldcg(row + j + 1) : 0u;
     return lo | (hi << 16);
 }
 
 // The same from a tile's B rows staged in shared memory (bs: row R - 128 n).
-__device__ __forceinline__ uint32_t lora_pair_s(const Params &p, const uint16_t *bs, int n, int R, int j)
+__device__ __forceinline__ uint32_t lora_pair_s(const Proj &pj, int r, const uint16_t *bs, int n, int R, int j)
 {
-    if (R >= p.N || j >= p.r)
+    if (R >= pj.N || j >= r)
         return 0u;
-    return *reinterpret_cast<const uint32_t *>(bs + (size_t)(R - n * kRows) * p.r + j);
+    return *reinterpret_cast<const uint32_t *>(bs + (size_t)(R - n * kRows) * r + j);
 }
 
 // The block's share of tile n for half-0 warp mt: s_t * acc + s * T_R B^T
 // (B rows from bs in shared memory, or from global memory when bs is null).
 template <int MP>
-__device__ __forceinline__ void tile_share(const Params &p, int n, int mt, int lane, float s_t,
+__device__ __forceinline__ void tile_share(const Proj &pj, int r, int KS, int n, int mt, int lane, float s_t,
                                            const float (&acc)[MP / 8][4], const float4 *tr, const uint16_t *bs,
                                            float (&out)[MP / 8][4])
 {
@@ -466,18 +518,18 @@ __device__ __forceinline__ void tile_share(const Params &p, int n, int mt, int l
             cl[nt][q] = 0.0f;
 #pragma unroll
     for (int ks = 0; ks < kMaxKS; ks++) {
-        if (ks < p.KS) {
+        if (ks < KS) {
             uint32_t a[4];
             if (bs) {
-                a[0] = lora_pair_s(p, bs, n, R0, 16 * ks + 2 * t);
-                a[1] = lora_pair_s(p, bs, n, R1, 16 * ks + 2 * t);
-                a[2] = lora_pair_s(p, bs, n, R0, 16 * ks + 8 + 2 * t);
-                a[3] = lora_pair_s(p, bs, n, R1, 16 * ks + 8 + 2 * t);
+                a[0] = lora_pair_s(pj, r, bs, n, R0, 16 * ks + 2 * t);
+                a[1] = lora_pair_s(pj, r, bs, n, R1, 16 * ks + 2 * t);
+                a[2] = lora_pair_s(pj, r, bs, n, R0, 16 * ks + 8 + 2 * t);
+                a[3] = lora_pair_s(pj, r, bs, n, R1, 16 * ks + 8 + 2 * t);
             } else {
-                a[0] = lora_pair(p, R0, 16 * ks + 2 * t);
-                a[1] = lora_pair(p, R1, 16 * ks + 2 * t);
-                a[2] = lora_pair(p, R0, 16 * ks + 8 + 2 * t);
-                a[3] = lora_pair(p, R1, 16 * ks + 8 + 2 * t);
+                a[0] = lora_pair(pj, r, R0, 16 * ks + 2 * t);
+                a[1] = lora_pair(pj, r, R1, 16 * ks + 2 * t);
+                a[2] = lora_pair(pj, r, R0, 16 * ks + 8 + 2 * t);
+                a[3] = lora_pair(pj, r, R1, 16 * ks + 8 + 2 * t);
             }
 #pragma unroll
             for (int nt = 0; nt < NT; nt++) {
@@ -495,11 +547,12 @@ __device__ __forceinline__ void tile_share(const Params &p, int n, int mt, int l
     for (int nt = 0; nt < NT; nt++)
 #pragma unroll
         for (int q = 0; q < 4; q++)
-            out[nt][q] = __fmaf_rn(s_t, acc[nt][q], p.lora_scale * cl[nt][q]);
+            out[nt][q] = __fmaf_rn(s_t, acc[nt][q], pj.lora_scale * cl[nt][q]);
 }
 
 template <int MP>
-__device__ __forceinline__ void store_tile(const Params &p, int n, int mt, int lane, const float (&y)[MP / 8][4])
+__device__ __forceinline__ void store_tile(const Proj &pj, int M, int y_fp32, int n, int mt, int lane,
+                                           const float (&y)[MP / 8][4])
 {
     constexpr int NT = MP / 8;
     const int g = lane >> 2, t = lane & 3;
@@ -510,19 +563,22 @@ __device__ __forceinline__ void store_tile(const Params &p, int n, int mt, int l
         for (int q = 0; q < 4; q++) {
             const int R = R0 + 8 * (q >> 1);
             const int tok = 8 * nt + 2 * t + (q & 1);
-            if (tok < p.M && R < p.N) {
-                const size_t o = (size_t)tok * p.N + R;
-                if (p.y_fp32)
-                    reinterpret_cast<float *>(p.y)[o] = y[nt][q];
+            if (tok < M && R < pj.N) {
+                const size_t o = (size_t)tok * pj.N + R;
+                if (y_fp32)
+                    reinterpret_cast<float *>(pj.y)[o] = y[nt][q];
                 else
-                    reinterpret_cast<__nv_bfloat16 *>(p.y)[o] = __float2bfloat16_rn(y[nt][q]);
+                    reinterpret_cast<__nv_bfloat16 *>(pj.y)[o] = __float2bfloat16_rn(y[nt][q]);
             }
         }
 }
 
-// End of the block's segment of tile n (consumer warp mt, half h).
-template <int MP>
-__device__ __forceinline__ void finish_segment(const Params &p, int n, int u0, int mt, int h, int lane,
+// End of the block's segment of tile n of projection j (consumer warp mt,
+// half h).  The tile's units are ubeg + n C .. + C - 1 of the launch; a block
+// whose range starts inside the tile leaves its share in slot 0, the block
+// whose range ends in it (having started earlier) in slot 1.
+template <int MP, int NP>
+__device__ __forceinline__ void finish_segment(const Params<NP> &p, int j, int n, int u0, int mt, int h, int lane,
                                                float (&acc)[MP / 8][4], const float4 *tr, const uint16_t *bs,
                                                float *red, int buf, volatile uint32_t *s_flag, float s_t)
 {
@@ -544,12 +600,15 @@ __device__ __forceinline__ void finish_segment(const Params &p, int n, int u0, i
             acc[nt][2] += v.z;
             acc[nt][3] += v.w;
         }
+        const Proj &pj = p.proj[j];
         float y[NT][4];
-        tile_share<MP>(p, n, mt, lane, s_t, acc, tr, bs, y);
-        const int first = owner_of(n * p.C, p.U, G), last = owner_of(n * p.C + p.C - 1, p.U, G);
+        tile_share<MP>(pj, p.r, p.KS, n, mt, lane, s_t, acc, tr, bs, y);
+        const int tu0 = pj.ubeg + n * pj.C;  // the tile's first unit in the launch
+        const int first = owner_of(tu0, p.U, G), last = owner_of(tu0 + pj.C - 1, p.U, G);
+        uint32_t *cnt = p.tcnt + pj.tbeg + n;
         bool finish = true;
         if (last > first) {
-            const int slot = (u0 / p.C == n) ? 0 : 1;
+            const int slot = u0 >= tu0 ? 0 : 1;
             float4 *dst = reinterpret_cast<float4 *>(p.part) + ((((size_t)b * 2 + slot) * 8 + mt) * 32 + lane) * NT;
 #pragma unroll
             for (int nt = 0; nt < NT; nt++)
@@ -557,7 +616,7 @@ __device__ __forceinline__ void finish_segment(const Params &p, int n, int u0, i
             named_sync(kBarGroup, 256);
             if (mt == 0 && lane == 0) {
                 __threadfence();
-                *s_flag = atomicAdd(&p.tcnt[n], 1u) == (uint32_t)(last - first);
+                *s_flag = atomicAdd(cnt, 1u) == (uint32_t)(last - first);
             }
             named_sync(kBarGroup, 256);
             finish = *s_flag != 0;
@@ -576,7 +635,7 @@ __device__ __forceinline__ void finish_segment(const Params &p, int n, int u0, i
 #pragma unroll
                     for (int k = 0; k < KB; k++) {
                         const int bb = bb0 + k;
-                        const int sl = (range_begin(bb, p.U, G) / p.C == n) ? 0 : 1;
+                        const int sl = range_begin(bb, p.U, G) >= tu0 ? 0 : 1;
                         const float4 *src = reinterpret_cast<const float4 *>(p.part) +
                                             ((((size_t)bb * 2 + sl) * 8 + mt) * 32 + lane) * NT;
 #pragma unroll
@@ -601,11 +660,11 @@ __device__ __forceinline__ void finish_segment(const Params &p, int n, int u0, i
                     for (int q = 0; q < 4; q++)
                         y[nt][q] = tot[nt][q];
                 if (mt == 0 && lane == 0)
-                    p.tcnt[n] = 0;
+                    *cnt = 0;
             }
         }
         if (finish)
-            store_tile<MP>(p, n, mt, lane, y);
+            store_tile<MP>(pj, p.M, p.y_fp32, n, mt, lane, y);
     }
 #pragma unroll
     for (int nt = 0; nt < NT; nt++)
@@ -614,8 +673,8 @@ __device__ __forceinline__ void finish_segment(const Params &p, int n, int u0, i
             acc[nt][q] = 0.0f;
 }
 
-template <int MP>
-__global__ void __launch_bounds__(kThreads, 1) stream_gemm_kernel(const __grid_constant__ Params p)
+template <int MP, int NP>
+__global__ void __launch_bounds__(kThreads, 1) stream_gemm_kernel(const __grid_constant__ Params<NP> p)
 {
     constexpr int NT = MP / 8;
     constexpr int S = n_stages<MP>();
@@ -651,19 +710,23 @@ __global__ void __launch_bounds__(kThreads, 1) stream_gemm_kernel(const __grid_c
         if (lane == 0) {
             // the weights of the first units into L2 while xprep runs
             for (int u = u0; u < min(u1, u0 + kPrefetchUnits); u++) {
-                const int n = u / p.C, c = u - n * p.C;
-                tma_prefetch_2d(&p.tm_codes, c * (kChunk / 2), n * kRows);
-                if ((c + 1) * kChunk <= p.K)
-                    tma_prefetch_2d(&p.tm_codes, c * (kChunk / 2) + 128, n * kRows);
-                tma_prefetch_2d(&p.tm_scales, c * (kChunk / 16), n * kRows);
+                const Proj &pj = p.proj[proj_of_unit(p, u)];
+                const int n = (u - pj.ubeg) / pj.C, c = u - pj.ubeg - n * pj.C;
+                tma_prefetch_2d(&pj.tm_codes, c * (kChunk / 2), n * kRows);
+                if ((c + 1) * kChunk <= pj.K)
+                    tma_prefetch_2d(&pj.tm_codes, c * (kChunk / 2) + 128, n * kRows);
+                tma_prefetch_2d(&pj.tm_scales, c * (kChunk / 16), n * kRows);
             }
         }
         pdl_wait();
         if (lane == 0) {
             const uint64_t drop = l2_policy_evict_first();
             // a unit's record: 2^p, T_c and the first M rows of X'
-            const uint32_t rbytes = (uint32_t)(kFacBytes + t_bytes(p.KS, MP)) + (uint32_t)p.M * 1024u;
-            int q = 0;  // segment
+            const uint32_t rbytes = (uint32_t)(kFacBytes + t_bytes(p.KS, MP)) + (uint32_t)xrec_bytes(p.M);
+            int q = 0;                     // segment
+            // projection, tile and chunk of unit u, advanced unit by unit
+            int j = proj_of_unit(p, u0);
+            int n = (u0 - p.proj[j].ubeg) / p.proj[j].C, c = u0 - p.proj[j].ubeg - n * p.proj[j].C;
             for (int i = 0; i < u1 - u0; i++) {
                 const int u = u0 + i, s = i % S;
                 // the first unit alone: its stage lands before the other stages
@@ -676,28 +739,38 @@ __global__ void __launch_bounds__(kThreads, 1) stream_gemm_kernel(const __grid_c
                     record_timeout_tiles(p.ctl);
                     break;  // stop copying; consumers time out and wind down
                 }
-                const int n = u / p.C, c = u - n * p.C;
-                const bool two = (c + 1) * kChunk <= p.K;  // else a last 256-column chunk
+                const Proj &pj = p.proj[j];
+                const bool two = (c + 1) * kChunk <= pj.K;  // else a last 256-column chunk
                 uint8_t *st = smem + (size_t)s * stage_bytes<MP>();
                 mbar_arrive_expect_tx(&full[s], (two ? 2 : 1) * kBoxBytes + kScaleBox + rbytes);
                 // the weight stream is read once: evict-first, so that the small
                 // reused operands (X, A, B, the records) keep their L2 lines
-                tma_load_2d_hint(st, &p.tm_codes, &full[s], c * (kChunk / 2), n * kRows, drop);
+                tma_load_2d_hint(st, &pj.tm_codes, &full[s], c * (kChunk / 2), n * kRows, drop);
                 if (two)
-                    tma_load_2d_hint(st + kBoxBytes, &p.tm_codes, &full[s], c * (kChunk / 2) + 128, n * kRows,
+                    tma_load_2d_hint(st + kBoxBytes, &pj.tm_codes, &full[s], c * (kChunk / 2) + 128, n * kRows,
                                      drop);
-                tma_load_2d_hint(st + 2 * kBoxBytes, &p.tm_scales, &full[s], c * (kChunk / 16), n * kRows, drop);
-                bulk_g2s(st + kXhOff, p.rec + (size_t)c * p.rec_bytes, rbytes, &full[s]);
-                if (p.bsm && (u + 1 == u1 || c + 1 == p.C)) {
+                tma_load_2d_hint(st + 2 * kBoxBytes, &pj.tm_scales, &full[s], c * (kChunk / 16), n * kRows, drop);
+                bulk_g2s(st + kXhOff, p.rec + (size_t)(pj.cbeg + c) * p.rec_bytes, rbytes, &full[s]);
+                if (p.bsm && (u + 1 == u1 || c + 1 == pj.C)) {
                     // the tile's B rows, for the epilogue of the segment this unit ends
                     if (q >= 2 && !mbar_wait(&bempty[q & 1], ((q >> 1) + 1) & 1)) {
                         record_timeout_tiles(p.ctl);
                         break;
                     }
-                    const uint32_t bbytes = (uint32_t)min(kRows, p.N - n * kRows) * (uint32_t)p.r * 2u;
+                    const uint32_t bbytes = (uint32_t)min(kRows, pj.N - n * kRows) * (uint32_t)p.r * 2u;
                     mbar_arrive_expect_tx(&bfull[q & 1], bbytes);
-                    bulk_g2s(bbuf + (q & 1) * (kBBytes / 2), p.lora_b + (size_t)n * kRows * p.r, bbytes, &bfull[q & 1]);
+                    bulk_g2s(bbuf + (q & 1) * (kBBytes / 2), pj.lora_b + (size_t)n * kRows * p.r, bbytes,
+                             &bfull[q & 1]);
                     q++;
+                }
+                if (++c == pj.C) {
+                    c = 0;
+                    if (j + 1 < p.count && u + 1 >= p.proj[j + 1].ubeg) {
+                        j++;
+                        n = 0;
+                    } else {
+                        n++;
+                    }
                 }
             }
         }
@@ -707,8 +780,20 @@ __global__ void __launch_bounds__(kThreads, 1) stream_gemm_kernel(const __grid_c
         // ---------------- consumer warps
         pdl_wait();
         const int mt = warp & 7, h = warp >> 3, g = lane >> 2, t = lane & 3;
-        const float s_t = __ldcg(p.tensor_scale);
         const int xoff = (int)(kXhOff + kFacBytes + t_bytes(p.KS, MP));
+        {
+            // token slots the record copies never reach: zeros, once (the copies
+            // write the stage only below xoff + xrec_bytes(M))
+            const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+            for (int s = 0; s < S; s++)
+                for (int o = xrec_bytes(p.M) + 16 * (int)threadIdx.x; o < MP * 1024; o += 16 * kCWarps * 32)
+                    *reinterpret_cast<uint4 *>(smem + (size_t)s * stage_bytes<MP>() + xoff + o) = zero;
+            named_sync(kBarConsumers, kCWarps * 32);
+        }
+        // projection, tile and chunk of unit u, advanced unit by unit
+        int j = proj_of_unit(p, u0);
+        int n = (u0 - p.proj[j].ubeg) / p.proj[j].C, c = u0 - p.proj[j].ubeg - n * p.proj[j].C;
+        float s_t = __ldcg(p.proj[j].tensor_scale);
         float acc[NT][4];
 #pragma unroll
         for (int nt = 0; nt < NT; nt++)
@@ -726,10 +811,10 @@ __global__ void __launch_bounds__(kThreads, 1) stream_gemm_kernel(const __grid_c
                 if (lane == 0)
                     record_timeout_tiles(p.ctl);
             }
-            const int n = u / p.C, c = u - n * p.C;
+            const Proj &pj = p.proj[j];
             const uint8_t *st = smem + (size_t)s * stage_bytes<MP>();
-            if (h == 0 || (c + 1) * kChunk <= p.K)
-                compute_unit<MP>(st, xoff, mt, h, g, t, p.M, acc);
+            if (h == 0 || (c + 1) * kChunk <= pj.K)
+                compute_unit<MP>(st, xoff, mt, h, g, t, acc);
             if (h == 1) {  // T of this chunk into the segment's sum (element mt*32 + lane, ...)
                 const float4 *ts = reinterpret_cast<const float4 *>(st + kXhOff + kFacBytes);
                 float4 *ta = tacc + buf * (kMaxKS * NT * 32);
@@ -753,20 +838,30 @@ __global__ void __launch_bounds__(kThreads, 1) stream_gemm_kernel(const __grid_c
                 mbar_arrive(&empty[s]);
             if (u + 1 == u1)
                 pdl_launch_dependents();
-            if (u + 1 == u1 || c + 1 == p.C) {
+            if (u + 1 == u1 || c + 1 == pj.C) {
                 if (p.bsm && ok && !mbar_wait(&bfull[buf], (q >> 1) & 1)) {
                     ok = false;
                     if (lane == 0)
                         record_timeout_tiles(p.ctl);
                 }
-                finish_segment<MP>(p, n, u0, mt, h, lane, acc, tacc + buf * (kMaxKS * NT * 32),
-                                   p.bsm ? bbuf + buf * (kBBytes / 2) : nullptr, red, buf, s_flag, s_t);
+                finish_segment<MP, NP>(p, j, n, u0, mt, h, lane, acc, tacc + buf * (kMaxKS * NT * 32),
+                                       p.bsm ? bbuf + buf * (kBBytes / 2) : nullptr, red, buf, s_flag, s_t);
                 __syncwarp();
                 if (p.bsm && lane == 0)
                     mbar_arrive(&bempty[buf]);
                 buf ^= 1;
                 q++;
                 seg_start = true;
+            }
+            if (++c == pj.C) {  // the next tile; a tile never spans two projections
+                c = 0;
+                if (NP > 1 && j + 1 < p.count && u + 1 >= p.proj[j + 1].ubeg) {
+                    j++;
+                    n = 0;
+                    s_t = __ldcg(p.proj[j].tensor_scale);
+                } else {
+                    n++;
+                }
             }
         }
     } else {
@@ -775,33 +870,53 @@ __global__ void __launch_bounds__(kThreads, 1) stream_gemm_kernel(const __grid_c
 }
 
 // ================================================================ host side
+constexpr int kListMax = 16;  // projections per launch of the list kernels
+
+// One launch: the projections' units, tile counters and chunk records in list
+// order, and the workspace layout.
 struct Plan {
-    int MP, C, tiles, U, G, KS;
+    int MP, KS, count, U, G, tiles, chunks;
+    int C[kListMax], ubeg[kListMax], tbeg[kListMax], cbeg[kListMax];
     size_t rec, off_rec, off_part, total;
 };
 
 static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-static bool make_plan(int64_t M, int64_t N, int64_t K, int64_t r, const DeviceInfo &dev, Plan &pl)
+static bool make_plan(int64_t M, const int64_t *N, const int64_t *K, int count, int64_t r, const DeviceInfo &dev,
+                      Plan &pl)
 {
-    if (!dev.stream_ok || K % 256 != 0 || M < 1 || M > 16 || r < 0 || r > kMaxR)
+    if (!dev.stream_ok || count < 1 || count > kListMax || M < 1 || M > 16 || r < 0 || r > kMaxR)
         return false;
     pl.MP = M <= 8 ? 8 : 16;
-    pl.C = (int)((K + kChunk - 1) / kChunk);
-    pl.tiles = (int)((N + kRows - 1) / kRows);
-    if (pl.tiles > kTileCounters || pl.C > (1 << 20) || (long long)pl.tiles * pl.C > (1LL << 30))
-        return false;
-    pl.U = pl.tiles * pl.C;
-    pl.G = std::min(dev.num_sms, pl.U);
-    // as many tiles as SMs, give or take 10 %: one whole tile per block, so
-    // no tile needs a cross-block hand-over at the end
-    if (pl.tiles <= dev.num_sms && pl.tiles * 10 >= dev.num_sms * 9)
-        pl.G = pl.tiles;
     pl.KS = r == 0 ? 0 : r <= 16 ? 1 : r <= 32 ? 2 : 4;
+    pl.count = count;
+    long long U = 0, T = 0, CS = 0;
+    for (int i = 0; i < count; i++) {
+        if (K[i] < 256 || K[i] % 256 != 0 || K[i] > (1LL << 30) || N[i] < 1 || N[i] > (1LL << 30))
+            return false;
+        const long long C = (K[i] + kChunk - 1) / kChunk, tl = (N[i] + kRows - 1) / kRows;
+        pl.C[i] = (int)C;
+        pl.ubeg[i] = (int)std::min(U, 1LL << 30);
+        pl.tbeg[i] = (int)std::min(T, (long long)kTileCounters);
+        pl.cbeg[i] = (int)std::min(CS, 1LL << 30);
+        U += tl * C;
+        T += tl;
+        CS += C;
+        if (T > kTileCounters || U > (1LL << 30))
+            return false;
+    }
+    pl.U = (int)U;
+    pl.tiles = (int)T;
+    pl.chunks = (int)CS;
+    pl.G = (int)std::min<long long>(dev.num_sms, U);
+    // one projection with as many tiles as SMs, give or take 10 %: one whole
+    // tile per block, so no tile needs a cross-block hand-over at the end
+    if (count == 1 && pl.tiles <= dev.num_sms && pl.tiles * 10 >= dev.num_sms * 9)
+        pl.G = pl.tiles;
     size_t off = kWsHeaderBytes;
     pl.rec = rec_bytes(pl.KS, pl.MP);
     pl.off_rec = off;
-    off = align_up(off + (size_t)pl.C * pl.rec, 256);
+    off = align_up(off + (size_t)pl.chunks * pl.rec, 256);
     pl.off_part = off;
     off = align_up(off + (size_t)pl.G * 2 * kRows * pl.MP * 4, 256);
     pl.total = off;
@@ -826,6 +941,7 @@ struct PlanKeyHash {
 static std::mutex g_plan_mu;
 static std::unordered_map<PlanKey, Plan, PlanKeyHash> g_plans;
 
+// The plan of a single projection, cached by shape.
 static bool cached_plan(int64_t M, int64_t N, int64_t K, int64_t r, const DeviceInfo &dev, Plan &pl)
 {
     const PlanKey key{dev.device, M <= 8 ? 8 : 16, N, K, r};
@@ -837,13 +953,42 @@ static bool cached_plan(int64_t M, int64_t N, int64_t K, int64_t r, const Device
             return true;
         }
     }
-    if (!make_plan(M, N, K, r, dev, pl))
+    if (!make_plan(M, &N, &K, 1, r, dev, pl))
         return false;
     std::lock_guard<std::mutex> lk(g_plan_mu);
     if (g_plans.size() > 4096)
         g_plans.clear();
     g_plans[key] = pl;
     return true;
+}
+
+// The plan of list[i0 .. i0 + n) for a token group of Mg.
+static bool list_plan(const GemmArgs *list, int i0, int n, int64_t Mg, const DeviceInfo &dev, Plan &pl)
+{
+    if (n == 1)
+        return cached_plan(Mg, list[i0].N, list[i0].K, list[i0].r, dev, pl);
+    int64_t N[kListMax], K[kListMax];
+    for (int i = 0; i < n; i++) {
+        N[i] = list[i0 + i].N;
+        K[i] = list[i0 + i].K;
+    }
+    return make_plan(Mg, N, K, n, list[i0].r, dev, pl);
+}
+
+// Length of the launch that starts at list[i0]: as many projections as fit
+// in kListMax and in the tile counters.
+static int launch_length(const GemmArgs *list, int i0, int count)
+{
+    long long tiles = 0;
+    int n = 0;
+    while (i0 + n < count && n < kListMax) {
+        const long long tl = (list[i0 + n].N + kRows - 1) / kRows;
+        if (n > 0 && tiles + tl > kTileCounters)
+            break;
+        tiles += tl;
+        n++;
+    }
+    return n;
 }
 
 // Tensor maps of one weight (codes, scales), cached by address and shape.
@@ -899,19 +1044,19 @@ static cudaError_t weight_maps(const GemmArgs &a, MapPair &mp)
 void query_stream_occupancy(DeviceInfo &dev)
 {
     using namespace stream;
-    int b8 = 0, b16 = 0;
-    if (cudaFuncSetAttribute(stream_gemm_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem_bytes<8>()) != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b8, stream_gemm_kernel<8>, kThreads, smem_bytes<8>()) !=
-            cudaSuccess)
-        b8 = 0;
-    if (cudaFuncSetAttribute(stream_gemm_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem_bytes<16>()) != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b16, stream_gemm_kernel<16>, kThreads, smem_bytes<16>()) !=
-            cudaSuccess)
-        b16 = 0;
+    auto blocks = [](const void *fn, size_t smem) {
+        int nb = 0;
+        if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, fn, kThreads, smem) != cudaSuccess)
+            nb = 0;
+        return nb;
+    };
+    const int b8 = blocks((const void *)stream_gemm_kernel<8, 1>, smem_bytes<8>());
+    const int b16 = blocks((const void *)stream_gemm_kernel<16, 1>, smem_bytes<16>());
+    const int l8 = blocks((const void *)stream_gemm_kernel<8, kListMax>, smem_bytes<8>());
+    const int l16 = blocks((const void *)stream_gemm_kernel<16, kListMax>, smem_bytes<16>());
     cudaGetLastError();
-    dev.stream_ok = b8 >= 1 && b16 >= 1;
+    dev.stream_ok = b8 >= 1 && b16 >= 1 && l8 >= 1 && l16 >= 1;
 }
 
 bool stream_supported(int64_t N, int64_t K, int64_t r, const DeviceInfo &dev)
@@ -929,78 +1074,135 @@ size_t stream_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t r, const 
     return pl.total;
 }
 
-cudaError_t launch_stream_gemm(const GemmArgs &a, cudaStream_t s, const DeviceInfo &dev)
+size_t stream_list_workspace_bytes(const GemmArgs *list, int count, const DeviceInfo &dev)
 {
     using namespace stream;
-    MapPair maps;
-    cudaError_t err = weight_maps(a, maps);
+    if (count < 1)
+        return 0;
+    const int64_t Mg = std::min<int64_t>(list[0].M, 16);
+    size_t need = 0;
+    for (int i0 = 0; i0 < count;) {
+        const int n = launch_length(list, i0, count);
+        // token groups of 16 (M > 16) reuse the workspace one after another
+        Plan pl;
+        if (!list_plan(list, i0, n, Mg, dev, pl))
+            return 0;
+        need = std::max(need, pl.total);
+        i0 += n;
+    }
+    return need;
+}
+
+namespace stream {
+
+// One launch pair (xprep, GEMM) for list[i0 .. i0 + n), tokens m0 .. m0 + Mg.
+template <int MP, int NP>
+static cudaError_t launch_group(const GemmArgs *list, int i0, int n, int64_t m0, int64_t Mg, const Plan &pl,
+                                cudaStream_t s, cudaLaunchAttribute *attr)
+{
+    const GemmArgs &a0 = list[i0];
+    uint8_t *rec = a0.ws + pl.off_rec;
+    PrepParams<NP> pp;
+    Params<NP> p;
+    std::memset(&pp, 0, sizeof(pp));
+    std::memset(&p, 0, sizeof(p));
+    for (int i = 0; i < n; i++) {
+        const GemmArgs &a = list[i0 + i];
+        MapPair maps;
+        cudaError_t err = weight_maps(a, maps);
+        if (err != cudaSuccess)
+            return err;
+        pp.proj[i].x = a.x + m0 * a.K;
+        pp.proj[i].noise = a.noise;
+        pp.proj[i].lora_a = a.lora_a;
+        pp.proj[i].K = (int)a.K;
+        pp.proj[i].cbeg = pl.cbeg[i];
+        Proj &pj = p.proj[i];
+        pj.tm_codes = maps.codes;
+        pj.tm_scales = maps.scales;
+        pj.lora_b = a.lora_b;
+        pj.tensor_scale = a.tensor_scale;
+        pj.y = a.y_fp32 ? (void *)((float *)a.y + m0 * a.N) : (void *)((uint16_t *)a.y + m0 * a.N);
+        pj.lora_scale = a.lora_scale;
+        pj.N = (int)a.N;
+        pj.K = (int)a.K;
+        pj.C = pl.C[i];
+        pj.ubeg = pl.ubeg[i];
+        pj.tbeg = pl.tbeg[i];
+        pj.cbeg = pl.cbeg[i];
+    }
+    pp.count = n;
+    pp.M = (int)Mg;
+    pp.r = (int)a0.r;
+    pp.KS = pl.KS;
+    pp.rec = rec;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(pl.chunks);
+    cfg.blockDim = dim3(kPrepThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    void *pargs[] = {&pp};
+    cudaError_t err = cudaLaunchKernelExC(&cfg, (const void *)xprep_kernel<MP, NP>, pargs);
     if (err != cudaSuccess)
         return err;
+
+    p.count = n;
+    p.M = (int)Mg;
+    p.r = (int)a0.r;
+    p.U = pl.U;
+    p.KS = pl.KS;
+    p.rec = rec;
+    p.rec_bytes = (int)pl.rec;
+    p.bsm = pl.KS > 0 && a0.r <= kBsmMaxR && a0.r % 8 == 0 ? 1 : 0;
+    p.part = reinterpret_cast<float *>(a0.ws + pl.off_part);
+    p.tcnt = reinterpret_cast<uint32_t *>(a0.ws + kCtlBytes);
+    p.ctl = reinterpret_cast<uint32_t *>(a0.ws);
+    p.y_fp32 = a0.y_fp32 ? 1 : 0;
+    cfg.gridDim = dim3(pl.G);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem_bytes<MP>();
+    void *args[] = {&p};
+    return cudaLaunchKernelExC(&cfg, (const void *)stream_gemm_kernel<MP, NP>, args);
+}
+
+}  // namespace stream
+
+cudaError_t launch_stream_list(const GemmArgs *list, int count, cudaStream_t s, const DeviceInfo &dev)
+{
+    using namespace stream;
+    if (count < 1)
+        return cudaErrorInvalidValue;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
-    for (int64_t m0 = 0; m0 < a.M; m0 += 16) {
-        const int64_t Mg = std::min<int64_t>(16, a.M - m0);
-        Plan pl;
-        if (!cached_plan(Mg, a.N, a.K, a.r, dev, pl))
-            return cudaErrorInvalidConfiguration;
-        uint8_t *rec = a.ws + pl.off_rec;
-        PrepParams pp;
-        pp.M = (int)Mg;
-        pp.K = (int)a.K;
-        pp.r = (int)a.r;
-        pp.KS = pl.KS;
-        pp.x = a.x + m0 * a.K;
-        pp.noise = a.noise;
-        pp.lora_a = a.lora_a;
-        pp.rec = rec;
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(pl.C);
-        cfg.blockDim = dim3(kPrepThreads);
-        cfg.dynamicSmemBytes = 0;
-        cfg.stream = s;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        void *pargs[] = {&pp};
-        err = cudaLaunchKernelExC(&cfg, pl.MP == 8 ? (const void *)xprep_kernel<8> : (const void *)xprep_kernel<16>,
-                                  pargs);
-        if (err != cudaSuccess)
-            return err;
-
-        Params p;
-        p.tm_codes = maps.codes;
-        p.tm_scales = maps.scales;
-        p.M = (int)Mg;
-        p.N = (int)a.N;
-        p.K = (int)a.K;
-        p.r = (int)a.r;
-        p.C = pl.C;
-        p.U = pl.U;
-        p.KS = pl.KS;
-        p.x = a.x + m0 * a.K;
-        p.noise = a.noise;
-        p.lora_a = a.lora_a;
-        p.lora_b = a.lora_b;
-        p.lora_scale = a.lora_scale;
-        p.tensor_scale = a.tensor_scale;
-        p.rec = rec;
-        p.rec_bytes = (int)pl.rec;
-        p.bsm = pl.KS > 0 && a.r <= kBsmMaxR && a.r % 8 == 0 ? 1 : 0;
-        p.part = reinterpret_cast<float *>(a.ws + pl.off_part);
-        p.tcnt = reinterpret_cast<uint32_t *>(a.ws + kCtlBytes);
-        p.ctl = reinterpret_cast<uint32_t *>(a.ws);
-        p.y = a.y_fp32 ? (void *)((float *)a.y + m0 * a.N) : (void *)((uint16_t *)a.y + m0 * a.N);
-        p.y_fp32 = a.y_fp32 ? 1 : 0;
-        cfg.gridDim = dim3(pl.G);
-        cfg.blockDim = dim3(kThreads);
-        cfg.dynamicSmemBytes = pl.MP == 8 ? smem_bytes<8>() : smem_bytes<16>();
-        void *args[] = {&p};
-        err = cudaLaunchKernelExC(
-            &cfg, pl.MP == 8 ? (const void *)stream_gemm_kernel<8> : (const void *)stream_gemm_kernel<16>, args);
-        if (err != cudaSuccess)
-            return err;
+    const int64_t M = list[0].M;
+    for (int i0 = 0; i0 < count;) {
+        const int n = launch_length(list, i0, count);
+        for (int64_t m0 = 0; m0 < M; m0 += 16) {
+            const int64_t Mg = std::min<int64_t>(16, M - m0);
+            Plan pl;
+            if (!list_plan(list, i0, n, Mg, dev, pl))
+                return cudaErrorInvalidConfiguration;
+            cudaError_t err;
+            if (n == 1)
+                err = pl.MP == 8 ? launch_group<8, 1>(list, i0, n, m0, Mg, pl, s, attr)
+                                 : launch_group<16, 1>(list, i0, n, m0, Mg, pl, s, attr);
+            else
+                err = pl.MP == 8 ? launch_group<8, kListMax>(list, i0, n, m0, Mg, pl, s, attr)
+                                 : launch_group<16, kListMax>(list, i0, n, m0, Mg, pl, s, attr);
+            if (err != cudaSuccess)
+                return err;
+        }
+        i0 += n;
     }
     return cudaSuccess;
+}
+
+cudaError_t launch_stream_gemm(const GemmArgs &a, cudaStream_t s, const DeviceInfo &dev)
+{
+    return launch_stream_list(&a, 1, s, dev);
 }
 
 }  // namespace nvfp4

@@ -63,6 +63,13 @@ void query_stream_occupancy(DeviceInfo &dev);
 bool stream_supported(int64_t N, int64_t K, int64_t r, const DeviceInfo &dev);
 size_t stream_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t r, const DeviceInfo &dev);
 cudaError_t launch_stream_gemm(const GemmArgs &a, cudaStream_t s, const DeviceInfo &dev);
+// A list of projections with the same M, r and output type (list[0] gives
+// them and the workspace) in launches of up to 16 projections: one
+// activation-preparation launch and one streaming launch over all their
+// units.  0 / cudaErrorInvalidConfiguration when a projection does not fit
+// the streaming kernel.
+size_t stream_list_workspace_bytes(const GemmArgs *list, int count, const DeviceInfo &dev);
+cudaError_t launch_stream_list(const GemmArgs *list, int count, cudaStream_t s, const DeviceInfo &dev);
 
 // Tensor-core (tcgen05) path for many tokens; smaller M uses the decode kernel.
 constexpr int64_t kPrefillMinM = 64;

@@ -125,6 +125,46 @@ def test_host_checks_reject_before_launch(lib):
     assert lib.nvfp4_quotient_check(0, (1 << 23) + 1, good, null) == binding.ERR_INVALID_ARG
 
 
+def test_list_host_checks_reject_before_launch(lib):
+    P = ctypes.c_void_p
+    good, bad = 4096, 4096 + 4
+
+    def entry(x=good, codes=good, scales=good, ts=good, a=good, b=good, z=None, y=good, N=64, K=512):
+        return binding.Projection(P(x) if x else None, P(codes) if codes else None, P(scales) if scales else None,
+                                  P(ts) if ts else None, P(a) if a else None, P(b) if b else None,
+                                  P(z) if z else None, P(y) if y else None, N, K, 2.0)
+
+    def call(entries, M=4, r=8, ydt=1, ws=good, count=None):
+        arr = (binding.Projection * max(1, len(entries)))(*entries)
+        n = len(entries) if count is None else count
+        return lib.nvfp4_w4a16_lora_gemm_list(arr, n, M, r, ydt, P(ws) if ws else None, 1 << 30, None)
+
+    ok2 = [entry(), entry(N=3584, K=18944)]
+    assert lib.nvfp4_w4a16_lora_gemm_list(None, 1, 4, 8, 1, P(good), 1 << 30, None) == binding.ERR_INVALID_ARG
+    assert call(ok2, count=0) == binding.ERR_SHAPE
+    assert call(ok2, count=65537) == binding.ERR_SHAPE
+    assert call(ok2, M=0) == binding.ERR_SHAPE
+    assert call(ok2, r=65) == binding.ERR_SHAPE
+    assert call(ok2, ydt=7) == binding.ERR_INVALID_ARG
+    assert call([entry(), entry(K=528)]) == binding.ERR_SHAPE           # K not a multiple of 256
+    assert call([entry(K=0)]) == binding.ERR_SHAPE
+    assert call([entry(), entry(N=0)]) == binding.ERR_SHAPE
+    assert call([entry(N=524289)]) == binding.ERR_SHAPE                 # more tiles than the counters
+    assert call([entry(), entry(codes=0)]) == binding.ERR_INVALID_ARG
+    assert call([entry(b=0)]) == binding.ERR_INVALID_ARG                # half a LoRA pair with r > 0
+    assert call([entry(a=0, b=0)], r=0) != binding.ERR_INVALID_ARG      # r = 0: A and B are ignored
+    assert call([entry(x=bad)]) == binding.ERR_ALIGNMENT
+    assert call([entry(), entry(y=bad)]) == binding.ERR_ALIGNMENT
+    assert call([entry(z=bad)]) == binding.ERR_ALIGNMENT
+    assert call([entry(a=bad)]) == binding.ERR_ALIGNMENT
+    assert call(ok2, ws=0) == binding.ERR_INVALID_ARG
+    assert call(ok2, ws=bad) == binding.ERR_ALIGNMENT
+    # every check passed: the next step is the device query (no GPU here)
+    assert call(ok2) in (binding.ERR_CUDA, binding.ERR_UNSUPPORTED_DEVICE)
+    arr = (binding.Projection * 2)(entry(), entry(K=528))
+    assert lib.nvfp4_gemm_list_workspace_bytes(arr, 2, 4, 8) == 0
+
+
 def test_library_does_not_link_the_oracle():
     # the product library and the oracle share no code: no oracle symbol in it
     out = os.popen(f"nm -D --defined-only {build.LIB}").read()
