@@ -200,10 +200,17 @@ class Workload:
             for M in MS:
                 self.x[(name, M)] = to_dev(synth.activations(M, shape[1], seed + 10 + M))
         self.ws = nv.new_workspace(max(nv.nvfp4_workspace_bytes(16, *s, R_LORA) for s in (UP, DOWN)), dev)
+        # outputs and workspace of the projection lists (8 up + 8 down per list)
+        self.ylist = {(n, M, k): t.empty((M, (UP if n == "up" else DOWN)[0]), dtype=t.float32, device=dev)
+                      for n in ("up", "down") for M in MS for k in range(8)}
         # replicas of the quantised weights for the GEMMs
         self.rep = []
         for i in range(replicas):
             self.rep.append({n: nv.quantize(self.w[n], workspace=self.ws) for n in ("up", "down")})
+        q0 = self.rep[0]
+        ents = [(self.x[(n, 16)], q0[n].codes, q0[n].scales, q0[n].tensor_scale, *self.lora[n], LORA_SCALE,
+                 self.z[n], self.ylist[(n, 16, k)]) for k in range(8) for n in ("up", "down")]
+        self.wsl = nv.new_workspace(nv.nvfp4_gemm_list_workspace_bytes(ents), dev)
         self.y = {(n, M): t.empty((M, (UP if n == "up" else DOWN)[0]), dtype=t.float32, device=dev)
                   for n in ("up", "down") for M in MS}
         # trained block-scale parameters for the scale-only update
@@ -237,6 +244,19 @@ class Workload:
             a, b = self.lora[n]
             self.nv.nvfp4_w4a16_lora_gemm(self.x[(n, M)], q.codes, q.scales, q.tensor_scale, a, b,
                                           LORA_SCALE, self.z[n], self.y[(n, M)], self.ws)
+
+    def op_gemm_list(self, M, i, L=16):
+        """One projection list: the up and down weights of L/2 consecutive
+        replicas from replica i on (independent projections, one token count)."""
+        R = len(self.rep)
+        ents = []
+        for k in range(L // 2):
+            for n in ("up", "down"):
+                q = self.rep[(i + k) % R][n]
+                a, b = self.lora[n]
+                ents.append((self.x[(n, M)], q.codes, q.scales, q.tensor_scale, a, b, LORA_SCALE, self.z[n],
+                             self.ylist[(n, M, k)]))
+        self.nv.nvfp4_w4a16_lora_gemm_list(ents, self.wsl)
 
     def op_round(self):
         for n in ("up", "down"):
@@ -380,6 +400,8 @@ def run_gpu(args):
     kb["quantize_frozen"] = op_time(lambda i: wl.op_quantize(frozen=True), 2)
     for M in MS:
         kb[f"gemm_M{M}"] = op_time(lambda i, M=M: wl.op_gemm(M, i), 2)
+    for M in MS:
+        kb[f"gemm_list_M{M}"] = op_time(lambda i, M=M: wl.op_gemm_list(M, i), 16)
     kb["round_scales"] = op_time(lambda i: wl.op_round(), 2)
     st = nv.nvfp4_get_device_status(wl.ws)
     if st != nv.OK:
@@ -418,6 +440,12 @@ def run_gpu(args):
         per_kernel[f"gemm_M{M}"] = {"mean_us": round(us, 2), "GB/s": round(b / us / 1e3, 1),
                                     "TFLOP/s": round(f / us / 1e6, 2),
                                     "frac_hbm": round(b / us / 1e3 / peak_hbm, 4)}
+    for M in MS:  # per projection, inside lists of 16 (nvfp4_w4a16_lora_gemm_list)
+        b = sum(gemm_bytes(M, *s, R_LORA) for s in (UP, DOWN)) / 2
+        us = kb[f"gemm_list_M{M}"] * 1e3
+        per_kernel[f"gemm_list_M{M}"] = {"mean_us_per_projection": round(us, 2), "GB/s": round(b / us / 1e3, 1),
+                                         "frac_hbm": round(b / us / 1e3 / peak_hbm, 4),
+                                         "projections_per_call": 16}
     qb = sum(quant_bytes(*s) for s in (UP, DOWN)) / 2
     for key in ("quantize", "quantize_frozen"):
         q_us = kb[key] * 1e3
@@ -537,6 +565,18 @@ def run_qwen32b(torch, nv, synth, peak_hbm):
                              "TFLOP/s": round(flops / ms / 1e9, 2),
                              "frac_hbm": round(nbytes / ms / 1e6 / peak_hbm, 4),
                              "alg_bytes_per_call": nbytes}
+        # the same 8 projections as one list call
+        yl = {(n, i): torch.empty_like(ys[n]) for n in ("up", "down") for i in range(R)}  # no shared outputs
+        ents = [(xs[n], reps[n][i].codes, reps[n][i].scales, reps[n][i].tensor_scale, *lora[n], LORA_SCALE, zs[n],
+                 yl[(n, i)]) for i in range(R) for n in ("up", "down")]
+        wsl = nv.new_workspace(nv.nvfp4_gemm_list_workspace_bytes(ents))
+        ms_l = graph_time_per_call(torch, lambda: nv.nvfp4_w4a16_lora_gemm_list(ents, wsl), 2 * R)
+        out[f"gemm_list_M{M}"] = {"mean_us_per_projection": round(ms_l * 1e3, 2),
+                                  "GB/s": round(nbytes / ms_l / 1e6, 1),
+                                  "frac_hbm": round(nbytes / ms_l / 1e6 / peak_hbm, 4),
+                                  "projections_per_call": 2 * R}
+        if nv.nvfp4_get_device_status(wsl) != nv.OK:
+            raise RuntimeError("device status after the 32B list")
     st = nv.nvfp4_get_device_status(ws)
     if st != nv.OK:
         raise RuntimeError(f"device status after the 32B decode: {nv.status_string(st)}")
@@ -586,12 +626,38 @@ def run_whole_stack(torch, nv, synth, peak_hbm, layers=28, M=8):
     st = nv.nvfp4_get_device_status(ws)
     if st != nv.OK:
         raise RuntimeError(f"device status after the whole-stack sweep: {nv.status_string(st)}")
+
+    # the same sweep grouped as a decoder layer's dependencies allow: q, k and
+    # v read one input, so do gate and up; o and down wait for their inputs
+    groups = [("q", "k", "v"), ("o",), ("gate", "up"), ("down",)]
+    names = [n for n, _, _ in STACK_SHAPES]
+    lists = []
+    for layer in range(layers):
+        for grp in groups:
+            ents = []
+            for n in grp:
+                (q, K), y = qs[layer * len(STACK_SHAPES) + names.index(n)], ys[layer * len(STACK_SHAPES) + names.index(n)]
+                ents.append((xs[K], q.codes, q.scales, q.tensor_scale, None, None, 0.0, None, y))
+            lists.append(ents)
+    wsl = nv.new_workspace(max(nv.nvfp4_gemm_list_workspace_bytes(e) for e in lists))
+
+    def seq_lists():
+        for ents in lists:
+            nv.nvfp4_w4a16_lora_gemm_list(ents, wsl)
+    ms_l = graph_time_per_call(torch, seq_lists, 1, reps=3)
+    st = nv.nvfp4_get_device_status(wsl)
+    if st != nv.OK:
+        raise RuntimeError(f"device status after the layer-list sweep: {nv.status_string(st)}")
     nbytes = sum(gemm_bytes(M, N, K, 0) for _ in range(layers) for _, N, K in STACK_SHAPES)
     return {"layers": layers, "matrices": len(qs), "M": M,
             "sweep_ms": round(ms, 4), "sweep_GB/s": round(nbytes / ms / 1e6, 1),
             "sweep_frac_hbm": round(nbytes / ms / 1e6 / peak_hbm, 4), "sweep_alg_bytes": nbytes,
+            "layer_lists_ms": round(ms_l, 4), "layer_lists_GB/s": round(nbytes / ms_l / 1e6, 1),
+            "layer_lists_frac_hbm": round(nbytes / ms_l / 1e6 / peak_hbm, 4),
+            "layer_lists": "per layer [q, k, v], [o], [gate, up], [down]: 112 list calls",
             "quantize_all_ms": round(quant_ms, 3), "quantize_GB/s": round(qbytes / quant_ms / 1e6, 1),
-            "timing": "one graph of the 196 GEMM calls; quantisation timed per matrix (events)"}
+            "timing": "one graph of the 196 GEMM calls (and one of the 112 list calls); quantisation timed "
+                      "per matrix (events)"}
 
 
 def run_prefill_case(torch, nv, synth, peak_tf):

@@ -426,16 +426,10 @@ __device__ __forceinline__ void compute_unit(const uint8_t *st, int xoff, int mt
     e4m3x4_to_h2dup(sw1, s1);
     // unit 32h + 8t + j of token g + 8nt (see xrec_off)
     const uint8_t *xl = xb + (g >> 1) * 2048 + h * 1024 + (((g & 1) << 2) | t) * 16;
-    // CS independent accumulator sets (by k-step) keep four MMA chains in flight
-    constexpr int CS = 4 / NT;
+    // CS independent accumulator sets (by k-step) per 8-token n-tile; the
+    // first MMA of each chain starts from C = 0
+    constexpr int CS = 2;
     float cur[CS][NT][4];
-#pragma unroll
-    for (int c = 0; c < CS; c++)
-#pragma unroll
-        for (int nt = 0; nt < NT; nt++)
-#pragma unroll
-            for (int q = 0; q < 4; q++)
-                cur[c][nt][q] = 0.0f;
 #pragma unroll
     for (int j = 0; j < 8; j++) {
         uint4 xf[NT];
@@ -454,15 +448,23 @@ __device__ __forceinline__ void compute_unit(const uint8_t *st, int xoff, int mt
         a[2] = hmul2_u32(r0[1], sa);
         a[3] = hmul2_u32(r1[1], sc);
 #pragma unroll
-        for (int nt = 0; nt < NT; nt++)
-            mma_f16_16816(cur[(2 * j) % CS][nt], a, xf[nt].x, xf[nt].y);
+        for (int nt = 0; nt < NT; nt++) {
+            if (2 * j < CS)
+                mma_f16_16816_z(cur[(2 * j) % CS][nt], a, xf[nt].x, xf[nt].y);
+            else
+                mma_f16_16816(cur[(2 * j) % CS][nt], a, xf[nt].x, xf[nt].y);
+        }
         a[0] = hmul2_u32(r0[2], sa);
         a[1] = hmul2_u32(r1[2], sc);
         a[2] = hmul2_u32(r0[3], sa);
         a[3] = hmul2_u32(r1[3], sc);
 #pragma unroll
-        for (int nt = 0; nt < NT; nt++)
-            mma_f16_16816(cur[(2 * j + 1) % CS][nt], a, xf[nt].z, xf[nt].w);
+        for (int nt = 0; nt < NT; nt++) {
+            if (2 * j + 1 < CS)
+                mma_f16_16816_z(cur[(2 * j + 1) % CS][nt], a, xf[nt].z, xf[nt].w);
+            else
+                mma_f16_16816(cur[(2 * j + 1) % CS][nt], a, xf[nt].z, xf[nt].w);
+        }
     }
 #pragma unroll
     for (int nt = 0; nt < NT; nt++) {
@@ -470,8 +472,7 @@ __device__ __forceinline__ void compute_unit(const uint8_t *st, int xoff, int mt
         float v[4];
 #pragma unroll
         for (int q = 0; q < 4; q++)
-            v[q] = CS == 4 ? (cur[0][nt][q] + cur[1][nt][q]) + (cur[2 % CS][nt][q] + cur[3 % CS][nt][q])
-                           : cur[0][nt][q] + cur[1 % CS][nt][q];
+            v[q] = cur[0][nt][q] + cur[1][nt][q];
         acc[nt][0] = __fmaf_rn(v[0], f.x, acc[nt][0]);
         acc[nt][1] = __fmaf_rn(v[1], f.y, acc[nt][1]);
         acc[nt][2] = __fmaf_rn(v[2], f.x, acc[nt][2]);
