@@ -886,6 +886,8 @@ def run_kernel_case(case, reps):
     from nvfp4_weight_only_02_gb300 import binding as nv
     from nvfp4_weight_only_02_gb300 import synth
     nv.load()
+    if case.startswith("list_M"):  # one projection list: 8 up + 8 down replicas, r = 32, noise
+        return run_list_case(torch, nv, synth, int(case[6:]), reps)
     parts = case.split("_")
     kind = parts[0]
     which = parts[1] if len(parts) > 1 else "up"
@@ -940,6 +942,38 @@ def run_kernel_case(case, reps):
         raise RuntimeError(nv.status_string(st))
     print(f"kernel case {case}: {reps} reps, graph {us:.2f} us/call (eager {us_eager:.2f}), "
           f"{nbytes / us / 1e3:.1f} GB/s, {flops / us / 1e6:.1f} TFLOP/s")
+
+
+def run_list_case(torch, nv, synth, M, reps, R=8):
+    """Kernel case for ncu: one nvfp4_w4a16_lora_gemm_list call over 8 up and 8
+    down replicas of the 7B MLP weights (0.61 GB, > 4x L2), repeated."""
+    dev = lambda b: torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(torch.bfloat16).cuda()
+    ws = nv.new_workspace(max(nv.nvfp4_workspace_bytes(16, *sh, R_LORA) for sh in (UP, DOWN)))
+    ents = []
+    for name, sh, seed in (("up", UP, 0), ("down", DOWN, 100)):
+        w = dev(synth.normal_weight(sh, 0.02, seed, outlier_frac=1e-3, outlier_mult=20.0))
+        a, b = synth.lora_pair(sh[0], sh[1], R_LORA, 0.01, seed + 2)
+        a, b = dev(a), dev(b)
+        z = torch.from_numpy(synth.noise_vector(sh[1], SIGMA, seed + 3)).cuda()
+        x = dev(synth.activations(M, sh[1], seed + 10 + M))
+        for _ in range(R):
+            q = nv.quantize(w, workspace=ws)
+            ents.append((x, q.codes, q.scales, q.tensor_scale, a, b, LORA_SCALE, z,
+                         torch.empty((M, sh[0]), dtype=torch.float32, device="cuda")))
+        del w
+    ents = [ents[(k % 2) * R + k // 2] for k in range(2 * R)]  # up, down alternating
+    wsl = nv.new_workspace(nv.nvfp4_gemm_list_workspace_bytes(ents))
+    op = lambda: nv.nvfp4_w4a16_lora_gemm_list(ents, wsl)
+    op()
+    torch.cuda.synchronize()
+    us_eager = time_replays(torch, [op], reps) * 1e3
+    g = capture(torch, op)
+    us = time_replays(torch, [g.replay], reps) * 1e3 if g is not None else us_eager
+    if nv.nvfp4_get_device_status(wsl) != nv.OK:
+        raise RuntimeError("device status after the list case")
+    nbytes = sum(gemm_bytes(M, *sh, R_LORA) for sh in (UP, DOWN)) * R
+    print(f"kernel case list_M{M}: {reps} reps, graph {us:.2f} us/call (eager {us_eager:.2f}), "
+          f"{2 * R} projections, {us / (2 * R):.2f} us/projection, {nbytes / us / 1e3:.1f} GB/s")
 
 
 def free_port():
