@@ -325,27 +325,43 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     const float rd = d_fast ? __frcp_rn(d) : 0.0f;
     __syncthreads();
 
-    // pass 2: from the end of the share backwards, two blocks per step per
-    // thread; the next step's two blocks are requested before this step's
-    // are quantised (software pipelining: up to four blocks in flight)
+    // pass 2, from the end of the share backwards.  First the tail kept in
+    // shared memory (kFusedCacheBlocks is a whole number of strides, so each
+    // thread's last cached block is followed by block cache_from - 1 - tid),
+    // two blocks per step per thread.
+    int64_t bb = b1 - 1 - tid;
+    for (; bb >= cache_from; bb -= 2 * kFusedThreads) {
+        const int64_t bc = bb - kFusedThreads;
+        uint2 cw;
+        uint32_t e;
+        quantize_block(s_cache[2 * (bb - cache_from)], s_cache[2 * (bb - cache_from) + 1], s_t, d, d_fast, rd,
+                       s_S, s_R, cw, e, ctl);
+        codes[bb] = cw;
+        scales[bb] = (uint8_t)e;
+        if (bc >= cache_from) {
+            quantize_block(s_cache[2 * (bc - cache_from)], s_cache[2 * (bc - cache_from) + 1], s_t, d, d_fast,
+                           rd, s_S, s_R, cw, e, ctl);
+            codes[bc] = cw;
+            scales[bc] = (uint8_t)e;
+        }
+    }
+    // Then the rest of the share from L2 and DRAM (read once: evict-first), two
+    // blocks per step per thread; the next step's two blocks are requested
+    // before this step's are quantised (up to four blocks in flight).  A block
+    // before b0 is neither loaded nor quantised.
+    bb = cache_from - 1 - tid;
     auto fetch = [&](int64_t b, uint4 &v0, uint4 &v1) {
-        if (b < b0) {
-            v0 = v1 = make_uint4(0u, 0u, 0u, 0u);
-        } else if (b >= cache_from) {
-            v0 = s_cache[2 * (b - cache_from)];
-            v1 = s_cache[2 * (b - cache_from) + 1];
-        } else {
+        if (b >= b0) {
             v0 = ld_hint_u4(w + 2 * b, drop);
             v1 = ld_hint_u4(w + 2 * b + 1, drop);
         }
     };
-    int64_t bb = b1 - 1 - tid;
-    uint4 v0a, v1a, v0b, v1b;
+    uint4 v0a = make_uint4(0u, 0u, 0u, 0u), v1a = v0a, v0b = v0a, v1b = v0a;
+    uint4 n0a = v0a, n1a = v0a, n0b = v0a, n1b = v0a;
     fetch(bb, v0a, v1a);
     fetch(bb - kFusedThreads, v0b, v1b);
     for (; bb >= b0; bb -= 2 * kFusedThreads) {
         const int64_t bc = bb - kFusedThreads;
-        uint4 n0a, n1a, n0b, n1b;
         fetch(bb - 2 * kFusedThreads, n0a, n1a);
         fetch(bc - 2 * kFusedThreads, n0b, n1b);
         uint2 cw;
