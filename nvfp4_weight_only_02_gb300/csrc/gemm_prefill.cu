@@ -51,7 +51,7 @@ constexpr int kPfBN = 256;         // weight rows per tile
 constexpr int kPfBK = 64;          // K per stage (128 bytes of bf16)
 constexpr int kPfStages = 4;
 constexpr int kPfThreads = 192;
-constexpr int kPfGroupN = 8;       // tile raster: n-tiles per group
+constexpr int kPfGroupN = 16;      // tile raster: n-tiles per group (W rows kept in L2 while X'' streams)
 constexpr int kPfMaxR = 64;
 constexpr uint32_t kPfABytes = kPfBM * kPfBK * 2;  // 16 KB
 constexpr uint32_t kPfBBytes = kPfBN * kPfBK * 2;  // 32 KB
