@@ -648,6 +648,20 @@ def run_whole_stack(torch, nv, synth, peak_hbm, layers=28, M=8):
     st = nv.nvfp4_get_device_status(wsl)
     if st != nv.OK:
         raise RuntimeError(f"device status after the layer-list sweep: {nv.status_string(st)}")
+
+    # the sweep as it is defined here (196 GEMMs on synthetic inputs that do not
+    # depend on one another): lists of 16 in sweep order
+    flat = [e for ents in lists for e in ents]
+    chunks = [flat[i:i + 16] for i in range(0, len(flat), 16)]
+    ws16 = nv.new_workspace(max(nv.nvfp4_gemm_list_workspace_bytes(c) for c in chunks))
+
+    def seq_16():
+        for c in chunks:
+            nv.nvfp4_w4a16_lora_gemm_list(c, ws16)
+    ms_16 = graph_time_per_call(torch, seq_16, 1, reps=3)
+    st = nv.nvfp4_get_device_status(ws16)
+    if st != nv.OK:
+        raise RuntimeError(f"device status after the 16-list sweep: {nv.status_string(st)}")
     nbytes = sum(gemm_bytes(M, N, K, 0) for _ in range(layers) for _, N, K in STACK_SHAPES)
     return {"layers": layers, "matrices": len(qs), "M": M,
             "sweep_ms": round(ms, 4), "sweep_GB/s": round(nbytes / ms / 1e6, 1),
@@ -655,9 +669,23 @@ def run_whole_stack(torch, nv, synth, peak_hbm, layers=28, M=8):
             "layer_lists_ms": round(ms_l, 4), "layer_lists_GB/s": round(nbytes / ms_l / 1e6, 1),
             "layer_lists_frac_hbm": round(nbytes / ms_l / 1e6 / peak_hbm, 4),
             "layer_lists": "per layer [q, k, v], [o], [gate, up], [down]: 112 list calls",
+            "lists16_ms": round(ms_16, 4), "lists16_GB/s": round(nbytes / ms_16 / 1e6, 1),
+            "lists16_frac_hbm": round(nbytes / ms_16 / 1e6 / peak_hbm, 4),
+            "lists16": "the 196 independent GEMMs of the sweep as 13 list calls of up to 16, in sweep order",
             "quantize_all_ms": round(quant_ms, 3), "quantize_GB/s": round(qbytes / quant_ms / 1e6, 1),
-            "timing": "one graph of the 196 GEMM calls (and one of the 112 list calls); quantisation timed "
-                      "per matrix (events)"}
+            "timing": "one graph each of the 196 GEMM calls, the 112 layer-list calls and the 13 16-lists; "
+                      "quantisation timed per matrix (events)"}
+
+
+def timed_op(torch, op, reps=10):
+    """Device ms per call of op(), as CUDA-graph replays like every other line
+    (eager launches when capture is not possible), and how it was timed."""
+    op()
+    torch.cuda.synchronize()
+    g = capture(torch, op)
+    if g is None:
+        return time_replays(torch, [op], reps), f"eager, {reps} calls"
+    return time_replays(torch, [g.replay], reps), f"CUDA-graph replays, {reps} calls"
 
 
 def run_prefill_case(torch, nv, synth, peak_tf):
@@ -673,12 +701,11 @@ def run_prefill_case(torch, nv, synth, peak_tf):
     x = dev(synth.activations(M, K, 10))
     y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
     op = lambda: nv.nvfp4_w4a16_lora_gemm(x, q.codes, q.scales, q.tensor_scale, a, b, LORA_SCALE, z, y, ws)
-    op()
-    ms = time_replays(torch, [op], 5)
+    ms, timing = timed_op(torch, op)
     f = gemm_flops(M, N, K, R_LORA)
     return {"workload": "16384 x 18944 x 3584 + LoRA r=32, bf16 out", "ms": round(ms, 3),
             "TFLOP/s": round(f / ms / 1e9, 1), "peak_bf16_tflops": peak_tf,
-            "frac": round(f / ms / 1e9 / peak_tf, 4)}
+            "frac": round(f / ms / 1e9 / peak_tf, 4), "timing": timing}
 
 
 def run_dgrad_case(torch, nv, synth, peak_tf):
@@ -696,15 +723,14 @@ def run_dgrad_case(torch, nv, synth, peak_tf):
     dx = torch.empty((M, K), dtype=torch.bfloat16, device="cuda")
     op = lambda: nv.nvfp4_w4a16_lora_gemm_dgrad(dy, q.codes, q.scales, q.tensor_scale, a, b, LORA_SCALE, z,
                                                 dx, ws)
-    op()
-    ms = time_replays(torch, [op], 5)
+    ms, timing = timed_op(torch, op)
     st = nv.nvfp4_get_device_status(ws)
     if st != nv.OK:
         raise RuntimeError(nv.status_string(st))
     f = gemm_flops(M, N, K, R_LORA)
     return {"workload": "dX 16384 x 3584 from dY 16384 x 18944 (7B up, transposed) + LoRA r=32, bf16 out",
             "ms": round(ms, 3), "TFLOP/s": round(f / ms / 1e9, 1), "peak_bf16_tflops": peak_tf,
-            "frac": round(f / ms / 1e9 / peak_tf, 4)}
+            "frac": round(f / ms / 1e9 / peak_tf, 4), "timing": timing}
 
 
 def run_lora_grads_case(torch, nv, synth, peak_hbm):
@@ -722,12 +748,11 @@ def run_lora_grads_case(torch, nv, synth, peak_hbm):
     gb = torch.empty((N, R_LORA), dtype=torch.float32, device="cuda")
     ws = nv.new_workspace(nv.nvfp4_lora_grads_workspace_bytes(M, N, K, R_LORA))
     op = lambda: nv.nvfp4_lora_grads(x, z, dy, a, b, LORA_SCALE, ga, gb, ws)
-    op()
-    ms = time_replays(torch, [op], 5)
+    ms, timing = timed_op(torch, op)
     nbytes = 2.0 * M * (K + N) + 2.0 * R_LORA * (K + N) + 4.0 * K + 4.0 * R_LORA * (K + N)
     return {"workload": "dA 32 x 3584, dB 18944 x 32 from X 16384 x 3584 (noise) and dY 16384 x 18944",
             "ms": round(ms, 3), "GB/s": round(nbytes / ms / 1e6, 1), "peak_hbm_gbs": peak_hbm,
-            "frac": round(nbytes / ms / 1e6 / peak_hbm, 4)}
+            "frac": round(nbytes / ms / 1e6 / peak_hbm, 4), "timing": timing}
 
 
 def run_e2e(torch, nv, wl, dev, args):
