@@ -236,7 +236,7 @@ nvfp4_status nvfp4_lora_grads(const void *x_bf16, const float *noise_fp32, const
  * take). */
 size_t nvfp4_lora_grads_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t r);
 
-/* Scale-QLoRA forward/* Scale-QLoRA forward (Scale-QLoRA post, method): the block scales are
+/* Scale-QLoRA forward (Scale-QLoRA post, method): the block scales are
  * trainable FP32 parameters (decoded block scales in weight units, N x K/16,
  * as for nvfp4_round_scales) and the codes stay frozen.  Each call rounds the
  * parameters to E4M3 against *tensor_scale into scales_e4m3 (exactly
