@@ -59,3 +59,58 @@ def test_whole_stack_quantise_and_decode(nv, orc):
             del w, a, b, q, y
     assert checked == LAYERS * len(SHAPES)
     assert nv.nvfp4_get_device_status(ws) == nv.OK
+
+
+def test_whole_stack_as_projection_lists(nv, orc):
+    """The same 196 matrices run three ways: single calls, lists grouped per
+    layer as a decoder's dependencies allow ([q, k, v], [o], [gate, up],
+    [down]) and lists of 16 in sweep order.  Every list output equals the
+    single call's to FP32 summation order (only the split of K over blocks
+    differs), and on sampled rows of every seventh matrix the list outputs
+    match the oracle within tolerance."""
+    M, r, s = 8, 32, 2.0
+    xb = {K: synth.activations(M, K, 170 + K) for K in (3584, 18944)}
+    xd = {K: torch.from_numpy(b.view(np.int16)).view(torch.bfloat16).cuda() for K, b in xb.items()}
+    zh = {K: synth.noise_vector(K, 5e-4, 190 + K) for K in (3584, 18944)}
+    zd = {K: torch.from_numpy(v).cuda() for K, v in zh.items()}
+    ws = nv.new_workspace(max(nv.nvfp4_workspace_bytes(M, N, K, r) for _, N, K in SHAPES))
+    gen = torch.Generator(device="cuda")
+    pick = np.random.default_rng(4096)
+    bits = lambda t: t.view(torch.int16).cpu().numpy().view(np.uint16)
+    items, samples = [], {}
+    for layer in range(LAYERS):
+        for j, (name, N, K) in enumerate(SHAPES):
+            gen.manual_seed(5000 * layer + j)
+            w = (torch.randn((N, K), generator=gen, device="cuda") * 0.02).to(torch.bfloat16)
+            a = (torch.randn((r, K), generator=gen, device="cuda") * 0.01).to(torch.bfloat16)
+            b = (torch.randn((N, r), generator=gen, device="cuda") * 0.01).to(torch.bfloat16)
+            q = nv.quantize(w, workspace=ws)
+            idx = len(items)
+            if idx % 7 == 0:
+                top = int(torch.argmax(w.abs().float()).item()) // K
+                rows = [top] + [int(i) for i in pick.choice(np.delete(np.arange(N), top), size=7, replace=False)]
+                samples[idx] = (rows, bits(w[rows]), bits(a), bits(b[rows]))
+            items.append((xd[K], q, a, b, s, zd[K]))
+            del w
+    singles = [nv.gemm(*it, workspace=ws) for it in items]
+    names = [n for n, _, _ in SHAPES]
+    groups = [("q", "k", "v"), ("o",), ("gate", "up"), ("down",)]
+    layer_lists = [[layer * len(SHAPES) + names.index(n) for n in grp] for layer in range(LAYERS) for grp in groups]
+    flat = list(range(len(items)))
+    sixteen = [flat[i:i + 16] for i in range(0, len(flat), 16)]
+    for plan in (layer_lists, sixteen):
+        outs = [None] * len(items)
+        for ids in plan:
+            for i, y in zip(ids, nv.gemm_list([items[i] for i in ids])):
+                outs[i] = y
+        torch.cuda.synchronize()
+        for i, (y, y1) in enumerate(zip(outs, singles)):
+            d = (y - y1).abs().max().item() / max(y1.abs().max().item(), 1e-30)
+            assert d <= 1e-5, (i, d)
+            if i in samples:
+                rows, wb, ab, bb = samples[i]
+                K = items[i][0].shape[1]
+                rc, codes, scales, st = orc.quantize(wb)
+                assert rc == orc.OK
+                _check(y[:, rows].cpu().numpy(), orc.gemm(xb[K], codes, scales, st, ab, bb, s, zh[K]))
+    assert nv.nvfp4_get_device_status(ws) == nv.OK
