@@ -171,3 +171,29 @@ def test_library_does_not_link_the_oracle():
     assert "orc_" not in out
     exported = set(re.findall(r"\b(nvfp4_[a-z0-9_]+)\b", out))
     assert exported == set(_declared())
+
+
+def test_projection_struct_layout_matches_the_header(tmp_path):
+    # the ctypes mirror of struct nvfp4_projection has the C layout of the header
+    import shutil
+    import subprocess
+    if shutil.which("gcc") is None:
+        pytest.skip("gcc not found")
+    src = tmp_path / "layout.c"
+    src.write_text('#include <stdio.h>\n#include <stddef.h>\n#include "nvfp4.h"\n'
+                   'int main(void) { printf("%zu", sizeof(nvfp4_projection));\n'
+                   '  const size_t o[] = {offsetof(nvfp4_projection, x_bf16), offsetof(nvfp4_projection, codes),\n'
+                   '    offsetof(nvfp4_projection, scales_e4m3), offsetof(nvfp4_projection, tensor_scale),\n'
+                   '    offsetof(nvfp4_projection, lora_a_bf16), offsetof(nvfp4_projection, lora_b_bf16),\n'
+                   '    offsetof(nvfp4_projection, noise_fp32), offsetof(nvfp4_projection, y),\n'
+                   '    offsetof(nvfp4_projection, N), offsetof(nvfp4_projection, K),\n'
+                   '    offsetof(nvfp4_projection, lora_scale)};\n'
+                   '  for (int i = 0; i < 11; i++) printf(" %zu", o[i]);\n  return 0; }\n')
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-I", os.path.dirname(HEADER), str(src), "-o", str(exe)], check=True)
+    got = [int(v) for v in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()]
+    P = binding.Projection
+    names = ["x_bf16", "codes", "scales_e4m3", "tensor_scale", "lora_a_bf16", "lora_b_bf16", "noise_fp32", "y",
+             "N", "K", "lora_scale"]
+    assert [f[0] for f in P._fields_] == names
+    assert got == [ctypes.sizeof(P)] + [getattr(P, n).offset for n in names]
