@@ -200,16 +200,16 @@ class Workload:
             for M in MS:
                 self.x[(name, M)] = to_dev(synth.activations(M, shape[1], seed + 10 + M))
         self.ws = nv.new_workspace(max(nv.nvfp4_workspace_bytes(16, *s, R_LORA) for s in (UP, DOWN)), dev)
-        # outputs and workspace of the projection lists (8 up + 8 down per list)
+        # outputs and workspace of the projection lists (16 up + 16 down per list)
         self.ylist = {(n, M, k): t.empty((M, (UP if n == "up" else DOWN)[0]), dtype=t.float32, device=dev)
-                      for n in ("up", "down") for M in MS for k in range(8)}
+                      for n in ("up", "down") for M in MS for k in range(16)}
         # replicas of the quantised weights for the GEMMs
         self.rep = []
         for i in range(replicas):
             self.rep.append({n: nv.quantize(self.w[n], workspace=self.ws) for n in ("up", "down")})
         q0 = self.rep[0]
         ents = [(self.x[(n, 16)], q0[n].codes, q0[n].scales, q0[n].tensor_scale, *self.lora[n], LORA_SCALE,
-                 self.z[n], self.ylist[(n, 16, k)]) for k in range(8) for n in ("up", "down")]
+                 self.z[n], self.ylist[(n, 16, k)]) for k in range(16) for n in ("up", "down")]
         self.wsl = nv.new_workspace(nv.nvfp4_gemm_list_workspace_bytes(ents), dev)
         self.y = {(n, M): t.empty((M, (UP if n == "up" else DOWN)[0]), dtype=t.float32, device=dev)
                   for n in ("up", "down") for M in MS}
@@ -245,7 +245,7 @@ class Workload:
             self.nv.nvfp4_w4a16_lora_gemm(self.x[(n, M)], q.codes, q.scales, q.tensor_scale, a, b,
                                           LORA_SCALE, self.z[n], self.y[(n, M)], self.ws)
 
-    def op_gemm_list(self, M, i, L=16):
+    def op_gemm_list(self, M, i, L=32):
         """One projection list: the up and down weights of L/2 consecutive
         replicas from replica i on (independent projections, one token count)."""
         R = len(self.rep)
@@ -401,7 +401,7 @@ def run_gpu(args):
     for M in MS:
         kb[f"gemm_M{M}"] = op_time(lambda i, M=M: wl.op_gemm(M, i), 2)
     for M in MS:
-        kb[f"gemm_list_M{M}"] = op_time(lambda i, M=M: wl.op_gemm_list(M, i), 16)
+        kb[f"gemm_list_M{M}"] = op_time(lambda i, M=M: wl.op_gemm_list(M, i), 32)
     kb["round_scales"] = op_time(lambda i: wl.op_round(), 2)
     st = nv.nvfp4_get_device_status(wl.ws)
     if st != nv.OK:
@@ -440,12 +440,12 @@ def run_gpu(args):
         per_kernel[f"gemm_M{M}"] = {"mean_us": round(us, 2), "GB/s": round(b / us / 1e3, 1),
                                     "TFLOP/s": round(f / us / 1e6, 2),
                                     "frac_hbm": round(b / us / 1e3 / peak_hbm, 4)}
-    for M in MS:  # per projection, inside lists of 16 (nvfp4_w4a16_lora_gemm_list)
+    for M in MS:  # per projection, inside lists of 32 (nvfp4_w4a16_lora_gemm_list)
         b = sum(gemm_bytes(M, *s, R_LORA) for s in (UP, DOWN)) / 2
         us = kb[f"gemm_list_M{M}"] * 1e3
         per_kernel[f"gemm_list_M{M}"] = {"mean_us_per_projection": round(us, 2), "GB/s": round(b / us / 1e3, 1),
                                          "frac_hbm": round(b / us / 1e3 / peak_hbm, 4),
-                                         "projections_per_call": 16}
+                                         "projections_per_call": 32}
     qb = sum(quant_bytes(*s) for s in (UP, DOWN)) / 2
     for key in ("quantize", "quantize_frozen"):
         q_us = kb[key] * 1e3
@@ -650,18 +650,18 @@ def run_whole_stack(torch, nv, synth, peak_hbm, layers=28, M=8):
         raise RuntimeError(f"device status after the layer-list sweep: {nv.status_string(st)}")
 
     # the sweep as it is defined here (196 GEMMs on synthetic inputs that do not
-    # depend on one another): lists of 16 in sweep order
+    # depend on one another): lists of 32 in sweep order
     flat = [e for ents in lists for e in ents]
-    chunks = [flat[i:i + 16] for i in range(0, len(flat), 16)]
-    ws16 = nv.new_workspace(max(nv.nvfp4_gemm_list_workspace_bytes(c) for c in chunks))
+    chunks = [flat[i:i + 32] for i in range(0, len(flat), 32)]
+    ws32 = nv.new_workspace(max(nv.nvfp4_gemm_list_workspace_bytes(c) for c in chunks))
 
-    def seq_16():
+    def seq_32():
         for c in chunks:
-            nv.nvfp4_w4a16_lora_gemm_list(c, ws16)
-    ms_16 = graph_time_per_call(torch, seq_16, 1, reps=3)
-    st = nv.nvfp4_get_device_status(ws16)
+            nv.nvfp4_w4a16_lora_gemm_list(c, ws32)
+    ms_32 = graph_time_per_call(torch, seq_32, 1, reps=3)
+    st = nv.nvfp4_get_device_status(ws32)
     if st != nv.OK:
-        raise RuntimeError(f"device status after the 16-list sweep: {nv.status_string(st)}")
+        raise RuntimeError(f"device status after the 32-list sweep: {nv.status_string(st)}")
     nbytes = sum(gemm_bytes(M, N, K, 0) for _ in range(layers) for _, N, K in STACK_SHAPES)
     return {"layers": layers, "matrices": len(qs), "M": M,
             "sweep_ms": round(ms, 4), "sweep_GB/s": round(nbytes / ms / 1e6, 1),
@@ -669,11 +669,11 @@ def run_whole_stack(torch, nv, synth, peak_hbm, layers=28, M=8):
             "layer_lists_ms": round(ms_l, 4), "layer_lists_GB/s": round(nbytes / ms_l / 1e6, 1),
             "layer_lists_frac_hbm": round(nbytes / ms_l / 1e6 / peak_hbm, 4),
             "layer_lists": "per layer [q, k, v], [o], [gate, up], [down]: 112 list calls",
-            "lists16_ms": round(ms_16, 4), "lists16_GB/s": round(nbytes / ms_16 / 1e6, 1),
-            "lists16_frac_hbm": round(nbytes / ms_16 / 1e6 / peak_hbm, 4),
-            "lists16": "the 196 independent GEMMs of the sweep as 13 list calls of up to 16, in sweep order",
+            "lists32_ms": round(ms_32, 4), "lists32_GB/s": round(nbytes / ms_32 / 1e6, 1),
+            "lists32_frac_hbm": round(nbytes / ms_32 / 1e6 / peak_hbm, 4),
+            "lists32": "the 196 independent GEMMs of the sweep as 7 list calls of up to 32, in sweep order",
             "quantize_all_ms": round(quant_ms, 3), "quantize_GB/s": round(qbytes / quant_ms / 1e6, 1),
-            "timing": "one graph each of the 196 GEMM calls, the 112 layer-list calls and the 13 16-lists; "
+            "timing": "one graph each of the 196 GEMM calls, the 112 layer-list calls and the 7 32-lists; "
                       "quantisation timed per matrix (events)"}
 
 

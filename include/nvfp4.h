@@ -161,7 +161,7 @@ size_t nvfp4_gemm_list_workspace_bytes(const nvfp4_projection *list, int count, 
  * launch moves every entry's weight bytes back to back, so the fixed cost of
  * a call (the dependency chain from the preparation kernel, filling the
  * ring, the last tile's epilogue) is paid once per launch instead of once per
- * projection.  Entries go 16 at a time into a launch (fewer if their
+ * projection.  Entries go 32 at a time into a launch (fewer if their
  * 128-row tiles exceed 4096); M > 16 runs in groups of 16 tokens.
  * Each y_i agrees with nvfp4_w4a16_lora_gemm's result for that entry to
  * FP32 summation order (the split of K over blocks can differ); a one-entry

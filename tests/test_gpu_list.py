@@ -84,12 +84,21 @@ def test_one_entry_list_equals_single_call(nv, orc, M, N, K, r):
 
 
 def test_long_list_with_shared_inputs(nv, orc):
-    # 20 entries: two launches (16 + 4); entries of the same K read one X
+    # 20 entries: one launch of the 32-entry kernel; entries of the same K read one X
     shapes = [(128 + 64 * (i % 5), 256 * (1 + i % 3)) for i in range(20)]
     items, cases = _make(nv, orc, shapes, 6, 16, seed=500, shared_x=True, noise_every=3)
     ys = nv.gemm_list(items)
     torch.cuda.synchronize()
     _check_all(orc, ys, cases, 16)
+
+
+def test_list_longer_than_a_launch(nv, orc):
+    # 40 entries: two launches (32 + 8), the second with the 16-entry kernel
+    shapes = [(64 + 32 * (i % 7), 256 * (1 + i % 2)) for i in range(40)]
+    items, cases = _make(nv, orc, shapes, 3, 8, seed=700, shared_x=True, noise_every=4)
+    ys = nv.gemm_list(items)
+    torch.cuda.synchronize()
+    _check_all(orc, ys, cases, 8)
 
 
 def test_list_split_by_tile_counters(nv, orc):
