@@ -200,16 +200,16 @@ class Workload:
             for M in MS:
                 self.x[(name, M)] = to_dev(synth.activations(M, shape[1], seed + 10 + M))
         self.ws = nv.new_workspace(max(nv.nvfp4_workspace_bytes(16, *s, R_LORA) for s in (UP, DOWN)), dev)
-        # outputs and workspace of the projection lists (16 up + 16 down per list)
+        # outputs and workspace of the projection lists (32 up + 32 down per list)
         self.ylist = {(n, M, k): t.empty((M, (UP if n == "up" else DOWN)[0]), dtype=t.float32, device=dev)
-                      for n in ("up", "down") for M in MS for k in range(16)}
+                      for n in ("up", "down") for M in MS for k in range(32)}
         # replicas of the quantised weights for the GEMMs
         self.rep = []
         for i in range(replicas):
             self.rep.append({n: nv.quantize(self.w[n], workspace=self.ws) for n in ("up", "down")})
         q0 = self.rep[0]
         ents = [(self.x[(n, 16)], q0[n].codes, q0[n].scales, q0[n].tensor_scale, *self.lora[n], LORA_SCALE,
-                 self.z[n], self.ylist[(n, 16, k)]) for k in range(16) for n in ("up", "down")]
+                 self.z[n], self.ylist[(n, 16, k)]) for k in range(32) for n in ("up", "down")]
         self.wsl = nv.new_workspace(nv.nvfp4_gemm_list_workspace_bytes(ents), dev)
         self.y = {(n, M): t.empty((M, (UP if n == "up" else DOWN)[0]), dtype=t.float32, device=dev)
                   for n in ("up", "down") for M in MS}
@@ -245,7 +245,7 @@ class Workload:
             self.nv.nvfp4_w4a16_lora_gemm(self.x[(n, M)], q.codes, q.scales, q.tensor_scale, a, b,
                                           LORA_SCALE, self.z[n], self.y[(n, M)], self.ws)
 
-    def op_gemm_list(self, M, i, L=32):
+    def op_gemm_list(self, M, i, L=64):
         """One projection list: the up and down weights of L/2 consecutive
         replicas from replica i on (independent projections, one token count)."""
         R = len(self.rep)
@@ -401,7 +401,7 @@ def run_gpu(args):
     for M in MS:
         kb[f"gemm_M{M}"] = op_time(lambda i, M=M: wl.op_gemm(M, i), 2)
     for M in MS:
-        kb[f"gemm_list_M{M}"] = op_time(lambda i, M=M: wl.op_gemm_list(M, i), 32)
+        kb[f"gemm_list_M{M}"] = op_time(lambda i, M=M: wl.op_gemm_list(M, i), 64)
     kb["round_scales"] = op_time(lambda i: wl.op_round(), 2)
     st = nv.nvfp4_get_device_status(wl.ws)
     if st != nv.OK:
@@ -440,12 +440,12 @@ def run_gpu(args):
         per_kernel[f"gemm_M{M}"] = {"mean_us": round(us, 2), "GB/s": round(b / us / 1e3, 1),
                                     "TFLOP/s": round(f / us / 1e6, 2),
                                     "frac_hbm": round(b / us / 1e3 / peak_hbm, 4)}
-    for M in MS:  # per projection, inside lists of 32 (nvfp4_w4a16_lora_gemm_list)
+    for M in MS:  # per projection, inside lists of 64 (nvfp4_w4a16_lora_gemm_list)
         b = sum(gemm_bytes(M, *s, R_LORA) for s in (UP, DOWN)) / 2
         us = kb[f"gemm_list_M{M}"] * 1e3
         per_kernel[f"gemm_list_M{M}"] = {"mean_us_per_projection": round(us, 2), "GB/s": round(b / us / 1e3, 1),
                                          "frac_hbm": round(b / us / 1e3 / peak_hbm, 4),
-                                         "projections_per_call": 32}
+                                         "projections_per_call": 64}
     qb = sum(quant_bytes(*s) for s in (UP, DOWN)) / 2
     for key in ("quantize", "quantize_frozen"):
         q_us = kb[key] * 1e3
@@ -650,18 +650,22 @@ def run_whole_stack(torch, nv, synth, peak_hbm, layers=28, M=8):
         raise RuntimeError(f"device status after the layer-list sweep: {nv.status_string(st)}")
 
     # the sweep as it is defined here (196 GEMMs on synthetic inputs that do not
-    # depend on one another): lists of 32 in sweep order
+    # depend on one another): lists of 32, then of 64, in sweep order
     flat = [e for ents in lists for e in ents]
-    chunks = [flat[i:i + 32] for i in range(0, len(flat), 32)]
-    ws32 = nv.new_workspace(max(nv.nvfp4_gemm_list_workspace_bytes(c) for c in chunks))
+    ms_chunked = {}
+    for L in (32, 64):
+        chunks = [flat[i:i + L] for i in range(0, len(flat), L)]
+        wsc = nv.new_workspace(max(nv.nvfp4_gemm_list_workspace_bytes(c) for c in chunks))
 
-    def seq_32():
-        for c in chunks:
-            nv.nvfp4_w4a16_lora_gemm_list(c, ws32)
-    ms_32 = graph_time_per_call(torch, seq_32, 1, reps=3)
-    st = nv.nvfp4_get_device_status(ws32)
-    if st != nv.OK:
-        raise RuntimeError(f"device status after the 32-list sweep: {nv.status_string(st)}")
+        def seq_chunks(chunks=chunks, wsc=wsc):
+            for c in chunks:
+                nv.nvfp4_w4a16_lora_gemm_list(c, wsc)
+        ms_chunked[L] = graph_time_per_call(torch, seq_chunks, 1, reps=3)
+        st = nv.nvfp4_get_device_status(wsc)
+        if st != nv.OK:
+            raise RuntimeError(f"device status after the {L}-list sweep: {nv.status_string(st)}")
+        del wsc
+    ms_32, ms_64 = ms_chunked[32], ms_chunked[64]
     nbytes = sum(gemm_bytes(M, N, K, 0) for _ in range(layers) for _, N, K in STACK_SHAPES)
     return {"layers": layers, "matrices": len(qs), "M": M,
             "sweep_ms": round(ms, 4), "sweep_GB/s": round(nbytes / ms / 1e6, 1),
@@ -672,8 +676,12 @@ def run_whole_stack(torch, nv, synth, peak_hbm, layers=28, M=8):
             "lists32_ms": round(ms_32, 4), "lists32_GB/s": round(nbytes / ms_32 / 1e6, 1),
             "lists32_frac_hbm": round(nbytes / ms_32 / 1e6 / peak_hbm, 4),
             "lists32": "the 196 independent GEMMs of the sweep as 7 list calls of up to 32, in sweep order",
+            "lists64_ms": round(ms_64, 4), "lists64_GB/s": round(nbytes / ms_64 / 1e6, 1),
+            "lists64_frac_hbm": round(nbytes / ms_64 / 1e6 / peak_hbm, 4),
+            "lists64": "the same as 4 list calls of up to 64",
             "quantize_all_ms": round(quant_ms, 3), "quantize_GB/s": round(qbytes / quant_ms / 1e6, 1),
-            "timing": "one graph each of the 196 GEMM calls, the 112 layer-list calls and the 7 32-lists; "
+            "timing": "one graph each of the 196 GEMM calls, the 112 layer-list calls, the 7 32-lists and "
+                      "the 4 64-lists; "
                       "quantisation timed per matrix (events)"}
 
 

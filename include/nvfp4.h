@@ -161,15 +161,15 @@ size_t nvfp4_gemm_list_workspace_bytes(const nvfp4_projection *list, int count, 
  * launch moves every entry's weight bytes back to back, so the fixed cost of
  * a call (the dependency chain from the preparation kernel, filling the
  * ring, the last tile's epilogue) is paid once per launch instead of once per
- * projection.  Entries go 32 at a time into a launch (fewer if their
- * 128-row tiles exceed 4096); M > 16 runs in groups of 16 tokens.
+ * projection.  Entries go 64 at a time into a launch (fewer if their
+ * 128-row tiles exceed 8192); M > 16 runs in groups of 16 tokens.
  * Each y_i agrees with nvfp4_w4a16_lora_gemm's result for that entry to
  * FP32 summation order (the split of K over blocks can differ); a one-entry
  * list computes exactly what nvfp4_w4a16_lora_gemm computes for M < 64.
  * Requirements (checked on the host before anything is launched):
  *   list != NULL, 1 <= count <= 65536 (else NVFP4_ERR_INVALID_ARG /
  *   NVFP4_ERR_SHAPE); 1 <= M <= 2^31, 0 <= r <= 64; per entry: 256 <= K
- *   <= 2^30 and K % 256 == 0, 1 <= N <= 524288 (NVFP4_ERR_SHAPE); x, codes,
+ *   <= 2^30 and K % 256 == 0, 1 <= N <= 1048576 (NVFP4_ERR_SHAPE); x, codes,
  *   scales, tensor_scale and y non-null, and A and B non-null when r > 0
  *   (NVFP4_ERR_INVALID_ARG); every pointer 16-byte aligned
  *   (NVFP4_ERR_ALIGNMENT).

@@ -198,7 +198,7 @@ static nvfp4_status list_checks(const nvfp4_projection *list, int count, int64_t
     args.resize((size_t)count);
     for (int i = 0; i < count; i++) {
         const nvfp4_projection &e = list[i];
-        if (e.N < 1 || e.N > 524288 || e.K < 256 || e.K % 256 != 0 || e.K > (1LL << 30))
+        if (e.N < 1 || e.N > 1048576 || e.K < 256 || e.K % 256 != 0 || e.K > (1LL << 30))
             return NVFP4_ERR_SHAPE;
         if (!e.x_bf16 || !e.codes || !e.scales_e4m3 || !e.tensor_scale || !e.y ||
             (r > 0 && (!e.lora_a_bf16 || !e.lora_b_bf16)))

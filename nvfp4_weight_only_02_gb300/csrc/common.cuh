@@ -35,7 +35,7 @@ constexpr uint32_t kTilesDirty = 0x7D17u;
 // counters before it returns).  Per-call scratch starts after them.
 // The words count arrivals per output tile (decode GEMMs: the last block to
 // arrive at a tile adds up the shares of the others).
-constexpr int kTileCounters = 4096;
+constexpr int kTileCounters = 8192;
 constexpr size_t kWsHeaderBytes = kCtlBytes + 4 * (size_t)kTileCounters;
 
 // Spin limit of every device-side wait: about a second of polling, after

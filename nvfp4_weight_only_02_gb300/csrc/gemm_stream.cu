@@ -871,8 +871,10 @@ __global__ void __launch_bounds__(kThreads, 1) stream_gemm_kernel(const __grid_c
 }
 
 // ================================================================ host side
-constexpr int kListMax = 32;  // projections per launch of the list kernels
-constexpr int kListMid = 16;  // shorter lists take an instantiation with a smaller parameter block
+constexpr int kListMax = 64;    // projections per launch of the list kernels
+constexpr int kListMid = 32;    // shorter lists take an instantiation with a smaller parameter block
+constexpr int kListSmall = 16;
+static_assert(sizeof(Params<kListMax>) <= 32764, "kernel parameters");
 
 // One launch: the projections' units, tile counters and chunk records in list
 // order, and the workspace layout.
@@ -1059,8 +1061,10 @@ void query_stream_occupancy(DeviceInfo &dev)
     const int l16 = blocks((const void *)stream_gemm_kernel<16, kListMax>, smem_bytes<16>());
     const int m8 = blocks((const void *)stream_gemm_kernel<8, kListMid>, smem_bytes<8>());
     const int m16 = blocks((const void *)stream_gemm_kernel<16, kListMid>, smem_bytes<16>());
+    const int s8 = blocks((const void *)stream_gemm_kernel<8, kListSmall>, smem_bytes<8>());
+    const int s16 = blocks((const void *)stream_gemm_kernel<16, kListSmall>, smem_bytes<16>());
     cudaGetLastError();
-    dev.stream_ok = b8 >= 1 && b16 >= 1 && l8 >= 1 && l16 >= 1 && m8 >= 1 && m16 >= 1;
+    dev.stream_ok = b8 >= 1 && b16 >= 1 && l8 >= 1 && l16 >= 1 && m8 >= 1 && m16 >= 1 && s8 >= 1 && s16 >= 1;
 }
 
 bool stream_supported(int64_t N, int64_t K, int64_t r, const DeviceInfo &dev)
@@ -1195,6 +1199,9 @@ cudaError_t launch_stream_list(const GemmArgs *list, int count, cudaStream_t s, 
             if (n == 1)
                 err = pl.MP == 8 ? launch_group<8, 1>(list, i0, n, m0, Mg, pl, s, attr)
                                  : launch_group<16, 1>(list, i0, n, m0, Mg, pl, s, attr);
+            else if (n <= kListSmall)
+                err = pl.MP == 8 ? launch_group<8, kListSmall>(list, i0, n, m0, Mg, pl, s, attr)
+                                 : launch_group<16, kListSmall>(list, i0, n, m0, Mg, pl, s, attr);
             else if (n <= kListMid)
                 err = pl.MP == 8 ? launch_group<8, kListMid>(list, i0, n, m0, Mg, pl, s, attr)
                                  : launch_group<16, kListMid>(list, i0, n, m0, Mg, pl, s, attr);

@@ -64,7 +64,7 @@ bool stream_supported(int64_t N, int64_t K, int64_t r, const DeviceInfo &dev);
 size_t stream_workspace_bytes(int64_t M, int64_t N, int64_t K, int64_t r, const DeviceInfo &dev);
 cudaError_t launch_stream_gemm(const GemmArgs &a, cudaStream_t s, const DeviceInfo &dev);
 // A list of projections with the same M, r and output type (list[0] gives
-// them and the workspace) in launches of up to 32 projections: one
+// them and the workspace) in launches of up to 64 projections: one
 // activation-preparation launch and one streaming launch over all their
 // units.  0 / cudaErrorInvalidConfiguration when a projection does not fit
 // the streaming kernel.

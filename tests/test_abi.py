@@ -149,7 +149,7 @@ def test_list_host_checks_reject_before_launch(lib):
     assert call([entry(), entry(K=528)]) == binding.ERR_SHAPE           # K not a multiple of 256
     assert call([entry(K=0)]) == binding.ERR_SHAPE
     assert call([entry(), entry(N=0)]) == binding.ERR_SHAPE
-    assert call([entry(N=524289)]) == binding.ERR_SHAPE                 # more tiles than the counters
+    assert call([entry(N=1048577)]) == binding.ERR_SHAPE                # more tiles than the counters
     assert call([entry(), entry(codes=0)]) == binding.ERR_INVALID_ARG
     assert call([entry(b=0)]) == binding.ERR_INVALID_ARG                # half a LoRA pair with r > 0
     assert call([entry(a=0, b=0)], r=0) != binding.ERR_INVALID_ARG      # r = 0: A and B are ignored

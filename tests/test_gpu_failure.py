@@ -41,10 +41,10 @@ def test_timeout_with_tile_counters_leaves_workspace_reusable(nv, orc):
     ws = nv.new_workspace(nv.nvfp4_workspace_bytes(M, N, K, 16))
     nv.nvfp4_wait_selftest(ws, 2)
     torch.cuda.synchronize()
-    words = ws[:256 + 4 * 4096].view(torch.int32).cpu().numpy()
+    words = ws[:256 + 4 * 8192].view(torch.int32).cpu().numpy()
     assert (words[64:] != 0).sum() == 4          # four tile counters left counted
     assert nv.nvfp4_get_device_status(ws) == nv.ERR_TIMEOUT
-    words = ws[:256 + 4 * 4096].view(torch.int32).cpu().numpy()
+    words = ws[:256 + 4 * 8192].view(torch.int32).cpu().numpy()
     assert not words.any()                        # control block and counters all zero again
     dev = lambda b: torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(torch.bfloat16).cuda()
     q = nv.quantize(dev(c.w))

@@ -93,8 +93,9 @@ def test_long_list_with_shared_inputs(nv, orc):
 
 
 def test_list_longer_than_a_launch(nv, orc):
-    # 40 entries: two launches (32 + 8), the second with the 16-entry kernel
-    shapes = [(64 + 32 * (i % 7), 256 * (1 + i % 2)) for i in range(40)]
+    # 72 entries: two launches (64 + 8), the second with the 16-entry kernel;
+    # a 40-entry list takes the 64-entry kernel
+    shapes = [(64 + 32 * (i % 7), 256 * (1 + i % 2)) for i in range(72)]
     items, cases = _make(nv, orc, shapes, 3, 8, seed=700, shared_x=True, noise_every=4)
     ys = nv.gemm_list(items)
     torch.cuda.synchronize()
@@ -102,9 +103,9 @@ def test_list_longer_than_a_launch(nv, orc):
 
 
 def test_list_split_by_tile_counters(nv, orc):
-    # three entries of 1563 tiles each: more than the 4096 tile counters of
+    # three entries of 3125 tiles each: more than the 8192 tile counters of
     # one launch, so the host splits them 2 + 1
-    items, cases = _make(nv, orc, [(200000, 256), (200000, 256), (200000, 256)], 2, 0, seed=900)
+    items, cases = _make(nv, orc, [(400000, 256), (400000, 256), (400000, 256)], 2, 0, seed=900)
     ys = nv.gemm_list(items)
     torch.cuda.synchronize()
     _check_all(orc, ys, cases, 0)
@@ -160,4 +161,4 @@ def test_list_stays_in_bounds(nv, orc):
         assert all(g.intact() for g in outs), "output guard overwritten"
         assert ws.intact(), "workspace guard overwritten"
         # the tile counters are back at zero for the next call
-        assert not ws.view(torch.uint8, (ws.n,))[256:256 + 4 * 4096].any()
+        assert not ws.view(torch.uint8, (ws.n,))[256:256 + 4 * 8192].any()

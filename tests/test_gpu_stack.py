@@ -64,7 +64,7 @@ def test_whole_stack_quantise_and_decode(nv, orc):
 def test_whole_stack_as_projection_lists(nv, orc):
     """The same 196 matrices run three ways: single calls, lists grouped per
     layer as a decoder's dependencies allow ([q, k, v], [o], [gate, up],
-    [down]) and lists of 32 in sweep order.  Every list output equals the
+    [down]) and lists of 64 in sweep order.  Every list output equals the
     single call's to FP32 summation order (only the split of K over blocks
     differs), and on sampled rows of every seventh matrix the list outputs
     match the oracle within tolerance."""
@@ -97,7 +97,7 @@ def test_whole_stack_as_projection_lists(nv, orc):
     groups = [("q", "k", "v"), ("o",), ("gate", "up"), ("down",)]
     layer_lists = [[layer * len(SHAPES) + names.index(n) for n in grp] for layer in range(LAYERS) for grp in groups]
     flat = list(range(len(items)))
-    longest = [flat[i:i + 32] for i in range(0, len(flat), 32)]
+    longest = [flat[i:i + 64] for i in range(0, len(flat), 64)]
     for plan in (layer_lists, longest):
         outs = [None] * len(items)
         for ids in plan:
