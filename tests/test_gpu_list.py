@@ -102,6 +102,17 @@ def test_list_longer_than_a_launch(nv, orc):
     _check_all(orc, ys, cases, 8)
 
 
+@pytest.mark.parametrize("n", [16, 17, 32, 33, 64, 65])
+def test_list_length_boundaries(nv, orc, n):
+    # the host takes the 16-, 32- or 64-entry kernel, the smallest that holds
+    # the launch; 65 entries are a launch of 64 and a one-projection remainder
+    shapes = [(64 + 16 * (i % 5), 256 * (1 + i % 3)) for i in range(n)]
+    items, cases = _make(nv, orc, shapes, 2, 4, seed=1300 + n, shared_x=True, noise_every=5)
+    ys = nv.gemm_list(items)
+    torch.cuda.synchronize()
+    _check_all(orc, ys, cases, 4)
+
+
 def test_list_split_by_tile_counters(nv, orc):
     # three entries of 3125 tiles each: more than the 8192 tile counters of
     # one launch, so the host splits them 2 + 1
