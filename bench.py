@@ -951,6 +951,8 @@ def run_kernel_case(case, reps):
     nv.load()
     if case.startswith("list_M"):  # one projection list: 8 up + 8 down replicas, r = 32, noise
         return run_list_case(torch, nv, synth, int(case[6:]), reps)
+    if case.startswith("list64_M"):  # one launch of the longest list: 32 up + 32 down replicas
+        return run_list_case(torch, nv, synth, int(case[8:]), reps, R=32)
     parts = case.split("_")
     kind = parts[0]
     which = parts[1] if len(parts) > 1 else "up"
@@ -1008,8 +1010,8 @@ def run_kernel_case(case, reps):
 
 
 def run_list_case(torch, nv, synth, M, reps, R=8):
-    """Kernel case for ncu: one nvfp4_w4a16_lora_gemm_list call over 8 up and 8
-    down replicas of the 7B MLP weights (0.61 GB, > 4x L2), repeated."""
+    """Kernel case for ncu: one nvfp4_w4a16_lora_gemm_list call over R up and R
+    down replicas of the 7B MLP weights (R = 8: 0.61 GB, > 4x L2), repeated."""
     dev = lambda b: torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(torch.bfloat16).cuda()
     ws = nv.new_workspace(max(nv.nvfp4_workspace_bytes(16, *sh, R_LORA) for sh in (UP, DOWN)))
     ents = []

@@ -222,8 +222,11 @@ struct PrepParams {
 // conflict-free 16-byte units.  Warps split (8-column n-tile of T, half,
 // k-step pairs); one warp per n-tile sums the parts in fixed order and
 // stores them in the layout the epilogue loads as B fragments.
-template <int MP, int NP>
-__global__ void __launch_bounds__(kPrepThreads, 1) xprep_kernel(const __grid_constant__ PrepParams<NP> p)
+// OCC = 2 (64 registers, two blocks per SM) for launches with more chunks
+// than SMs: the waves of blocks overlap.  A launch of one wave runs faster
+// with OCC = 1, whose blocks keep more loads in flight.
+template <int MP, int NP, int OCC>
+__global__ void __launch_bounds__(kPrepThreads, OCC) xprep_kernel(const __grid_constant__ PrepParams<NP> p)
 {
     constexpr int NT = MP / 8;
     __shared__ __align__(16) uint8_t xb[MP * 1024];
@@ -1106,7 +1109,7 @@ namespace stream {
 // One launch pair (xprep, GEMM) for list[i0 .. i0 + n), tokens m0 .. m0 + Mg.
 template <int MP, int NP>
 static cudaError_t launch_group(const GemmArgs *list, int i0, int n, int64_t m0, int64_t Mg, const Plan &pl,
-                                cudaStream_t s, cudaLaunchAttribute *attr)
+                                cudaStream_t s, cudaLaunchAttribute *attr, int num_sms)
 {
     const GemmArgs &a0 = list[i0];
     uint8_t *rec = a0.ws + pl.off_rec;
@@ -1152,7 +1155,9 @@ static cudaError_t launch_group(const GemmArgs *list, int i0, int n, int64_t m0,
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     void *pargs[] = {&pp};
-    cudaError_t err = cudaLaunchKernelExC(&cfg, (const void *)xprep_kernel<MP, NP>, pargs);
+    const void *prep = pl.chunks > num_sms ? (const void *)xprep_kernel<MP, NP, 2>
+                                                : (const void *)xprep_kernel<MP, NP, 1>;
+    cudaError_t err = cudaLaunchKernelExC(&cfg, prep, pargs);
     if (err != cudaSuccess)
         return err;
 
@@ -1197,17 +1202,17 @@ cudaError_t launch_stream_list(const GemmArgs *list, int count, cudaStream_t s, 
             // the kernel parameters are copied in full at each launch: the
             // smallest instantiation that holds the list
             if (n == 1)
-                err = pl.MP == 8 ? launch_group<8, 1>(list, i0, n, m0, Mg, pl, s, attr)
-                                 : launch_group<16, 1>(list, i0, n, m0, Mg, pl, s, attr);
+                err = pl.MP == 8 ? launch_group<8, 1>(list, i0, n, m0, Mg, pl, s, attr, dev.num_sms)
+                                 : launch_group<16, 1>(list, i0, n, m0, Mg, pl, s, attr, dev.num_sms);
             else if (n <= kListSmall)
-                err = pl.MP == 8 ? launch_group<8, kListSmall>(list, i0, n, m0, Mg, pl, s, attr)
-                                 : launch_group<16, kListSmall>(list, i0, n, m0, Mg, pl, s, attr);
+                err = pl.MP == 8 ? launch_group<8, kListSmall>(list, i0, n, m0, Mg, pl, s, attr, dev.num_sms)
+                                 : launch_group<16, kListSmall>(list, i0, n, m0, Mg, pl, s, attr, dev.num_sms);
             else if (n <= kListMid)
-                err = pl.MP == 8 ? launch_group<8, kListMid>(list, i0, n, m0, Mg, pl, s, attr)
-                                 : launch_group<16, kListMid>(list, i0, n, m0, Mg, pl, s, attr);
+                err = pl.MP == 8 ? launch_group<8, kListMid>(list, i0, n, m0, Mg, pl, s, attr, dev.num_sms)
+                                 : launch_group<16, kListMid>(list, i0, n, m0, Mg, pl, s, attr, dev.num_sms);
             else
-                err = pl.MP == 8 ? launch_group<8, kListMax>(list, i0, n, m0, Mg, pl, s, attr)
-                                 : launch_group<16, kListMax>(list, i0, n, m0, Mg, pl, s, attr);
+                err = pl.MP == 8 ? launch_group<8, kListMax>(list, i0, n, m0, Mg, pl, s, attr, dev.num_sms)
+                                 : launch_group<16, kListMax>(list, i0, n, m0, Mg, pl, s, attr, dev.num_sms);
             if (err != cudaSuccess)
                 return err;
         }

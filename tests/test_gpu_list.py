@@ -113,6 +113,16 @@ def test_list_length_boundaries(nv, orc, n):
     _check_all(orc, ys, cases, 4)
 
 
+@pytest.mark.parametrize("shapes", [[(128 + 32 * i, 16384) for i in range(5)], [(64, 81920)]])
+def test_more_chunk_records_than_sms(nv, orc, shapes):
+    # 160 chunks of 512 columns in one launch: the preparation kernel runs
+    # with two blocks per SM (a list, then a single projection)
+    items, cases = _make(nv, orc, shapes, 3, 8, seed=1500 + len(shapes), shared_x=True, noise_every=2)
+    ys = nv.gemm_list(items)
+    torch.cuda.synchronize()
+    _check_all(orc, ys, cases, 8)
+
+
 def test_list_split_by_tile_counters(nv, orc):
     # three entries of 3125 tiles each: more than the 8192 tile counters of
     # one launch, so the host splits them 2 + 1
