@@ -1037,7 +1037,8 @@ def run_list_case(torch, nv, synth, M, reps, R=8):
     if nv.nvfp4_get_device_status(wsl) != nv.OK:
         raise RuntimeError("device status after the list case")
     nbytes = sum(gemm_bytes(M, *sh, R_LORA) for sh in (UP, DOWN)) * R
-    print(f"kernel case list_M{M}: {reps} reps, graph {us:.2f} us/call (eager {us_eager:.2f}), "
+    name = f"list_M{M}" if R == 8 else f"list{2 * R}_M{M}"
+    print(f"kernel case {name}: {reps} reps, graph {us:.2f} us/call (eager {us_eager:.2f}), "
           f"{2 * R} projections, {us / (2 * R):.2f} us/projection, {nbytes / us / 1e3:.1f} GB/s")
 
 
